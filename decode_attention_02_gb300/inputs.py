@@ -1,0 +1,233 @@
+"""Seeded synthetic inputs for MFA decode attention.
+
+This module only draws and lays out data; it holds none of the attention
+arithmetic.  The same generator feeds the CPU oracle (tests) and the CUDA path
+(tests, benchmark, smoke run), so both sides see identical bytes.
+
+Workload shapes follow the Step-3 MFA decode step (paperlayer.ai/abs/2507.19427v1,
+section 5 "Model-System Co-design"): 64 query heads of width 256 attend over one
+shared K head and one shared V head; the printed arithmetic intensity (128 with
+8-bit KV) and effective rank (16,384) fix H=64 and d=256.  The KV cache is paged
+with 64-token pages.
+
+Recipe (fixed seeds, numpy PCG64 via ``default_rng``), in draw order:
+  1. lengths: given, or uniform integers in [lo, hi] inclusive;
+  2. physical page order: identity ("contiguous") or ``rng.permutation``;
+  3. q ~ N(0,1) fp32 [B, H, d];
+  4. K pool ~ N(0,1) fp32 [num_blocks, page, d], drawn in chunks of
+     ``_CHUNK_BLOCKS`` pages; optionally each scalar K element is multiplied
+     by ``k_spike_mult`` with independent probability ``k_spike_frac``
+     (uniform draw right after each chunk's normals);
+  5. V pool ~ N(0,1) fp32, same chunking, no spikes.
+Storage: bf16 by round-to-nearest-even, or FP8 e4m3 with one fp32 scale per
+token row (absmax/448, 1 for an all-zero row), codes = e4m3(RNE(x/scale))
+after clamping to +-448.  Unused page slots and unused physical pages are
+filled with NaN when ``poison`` is set, so any read of them shows up.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+NUM_Q_HEADS = 64
+HEAD_DIM = 256
+PAGE_SIZE = 64
+_CHUNK_BLOCKS = 512
+BF16_NAN_BITS = 0x7FC0
+E4M3_NAN_CODE = 0x7F
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    lens: Optional[Sequence[int]] = None        # explicit lengths, or None to draw
+    len_range: Optional[tuple] = None           # (lo, hi) inclusive when drawn
+    kv_dtype: str = "bf16"                      # "bf16" | "fp8_e4m3"
+    layout: str = "shuffled"                    # "shuffled" | "contiguous"
+    seed: int = 0
+    k_spike_frac: float = 0.0
+    k_spike_mult: float = 20.0
+    extra_blocks: int = 0
+    poison: bool = True
+    num_q_heads: int = NUM_Q_HEADS
+    head_dim: int = HEAD_DIM
+    page_size: int = PAGE_SIZE
+    softmax_scale: Optional[float] = None       # None -> 1/sqrt(head_dim)
+
+    def scale(self) -> float:
+        if self.softmax_scale is not None:
+            return float(self.softmax_scale)
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+# The five decode workloads, plus the FP8 versions of the 4K and long shapes.
+WORKLOADS = {
+    "tiny_b1_l512_bf16": Workload(
+        "tiny_b1_l512_bf16", batch=1, lens=(512,), layout="contiguous", seed=0),
+    "b32_l4096_bf16": Workload(
+        "b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=1),
+    "ragged_b128_l1024_8192_bf16": Workload(
+        "ragged_b128_l1024_8192_bf16", batch=128, len_range=(1024, 8192), seed=2,
+        k_spike_frac=0.01, k_spike_mult=20.0),
+    "b128_l4096_fp8": Workload(
+        "b128_l4096_fp8", batch=128, lens=(4096,) * 128, kv_dtype="fp8_e4m3", seed=3),
+    "long_b4_l131072_bf16": Workload(
+        "long_b4_l131072_bf16", batch=4, lens=(131072, 131072, 65536, 16384), seed=4),
+    "b32_l4096_fp8": Workload(
+        "b32_l4096_fp8", batch=32, lens=(4096,) * 32, kv_dtype="fp8_e4m3", seed=5),
+    "long_b4_l131072_fp8": Workload(
+        "long_b4_l131072_fp8", batch=4, lens=(131072, 131072, 65536, 16384),
+        kv_dtype="fp8_e4m3", seed=6),
+}
+
+
+@dataclasses.dataclass
+class Case:
+    """Host tensors of one decode step (all torch CPU tensors, contiguous)."""
+    workload: Workload
+    q: torch.Tensor             # bf16 [B, H, d]
+    k_cache: torch.Tensor       # bf16 [nb, page, d] or uint8 e4m3 codes
+    v_cache: torch.Tensor
+    k_scale: Optional[torch.Tensor]   # fp32 [nb, page] (FP8 only)
+    v_scale: Optional[torch.Tensor]
+    block_table: torch.Tensor   # int32 [B, max_pages], -1 where unused
+    seq_lens: torch.Tensor      # int32 [B]
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_pages(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+def _pages(length: int, page: int) -> int:
+    return (length + page - 1) // page
+
+
+def _draw_pool(rng, nb, page, d, spike_frac, spike_mult):
+    out = np.empty((nb, page, d), dtype=np.float32)
+    for c0 in range(0, nb, _CHUNK_BLOCKS):
+        c1 = min(nb, c0 + _CHUNK_BLOCKS)
+        x = rng.standard_normal((c1 - c0, page, d), dtype=np.float32)
+        if spike_frac > 0.0:
+            mask = rng.random((c1 - c0, page, d), dtype=np.float32) < np.float32(spike_frac)
+            x[mask] *= np.float32(spike_mult)
+        out[c0:c1] = x
+    return out
+
+
+def _to_bf16(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(x).to(torch.bfloat16)
+
+
+def _to_e4m3(x: np.ndarray):
+    """Per-token-row FP8 storage: codes (uint8) and fp32 scales absmax/448."""
+    absmax = np.abs(x).max(axis=-1)
+    scale = (absmax.astype(np.float32) / np.float32(448.0)).astype(np.float32)
+    scale[absmax == 0] = np.float32(1.0)
+    y = np.clip(x / scale[..., None], np.float32(-448.0), np.float32(448.0)).astype(np.float32)
+    codes = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, torch.from_numpy(scale)
+
+
+def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case:
+    """Draw one decode step's inputs for workload ``w`` (deterministic in w.seed)."""
+    rng = np.random.default_rng(w.seed)
+    B, H, d, page = w.batch, w.num_q_heads, w.head_dim, w.page_size
+    if lens_override is not None:
+        lens = np.asarray(lens_override, dtype=np.int64)
+    elif w.lens is not None:
+        lens = np.asarray(w.lens, dtype=np.int64)
+    else:
+        lo, hi = w.len_range
+        lens = rng.integers(lo, hi + 1, size=B)
+    assert lens.shape == (B,) and (lens >= 0).all()
+    npages = [_pages(int(L), page) for L in lens]
+    total = int(sum(npages))
+    nb = max(1, total + w.extra_blocks)
+    max_pages = max(1, max(npages) if npages else 1)
+
+    if w.layout == "contiguous":
+        perm = np.arange(nb, dtype=np.int64)
+    else:
+        perm = rng.permutation(nb)
+
+    q = rng.standard_normal((B, H, d), dtype=np.float32)
+    kf = _draw_pool(rng, nb, page, d, w.k_spike_frac, w.k_spike_mult)
+    vf = _draw_pool(rng, nb, page, d, 0.0, 1.0)
+
+    table = np.full((B, max_pages), -1, dtype=np.int32)
+    used = np.zeros(nb, dtype=bool)
+    # (block, first unused slot) of each sequence's last page
+    tails = []
+    pos = 0
+    for b in range(B):
+        for p in range(npages[b]):
+            blk = int(perm[pos]); pos += 1
+            table[b, p] = blk
+            used[blk] = True
+        if npages[b]:
+            rem = int(lens[b]) - page * (npages[b] - 1)
+            if rem < page:
+                tails.append((int(table[b, npages[b] - 1]), rem))
+
+    if w.kv_dtype == "bf16":
+        k_cache, v_cache = _to_bf16(kf), _to_bf16(vf)
+        k_scale = v_scale = None
+        if w.poison:
+            kb, vb = k_cache.view(torch.int16), v_cache.view(torch.int16)
+            nan = torch.tensor(BF16_NAN_BITS, dtype=torch.int16)
+            for blk, rem in tails:
+                kb[blk, rem:] = nan
+                vb[blk, rem:] = nan
+            unused = torch.from_numpy(np.nonzero(~used)[0])
+            if unused.numel():
+                kb[unused] = nan
+                vb[unused] = nan
+    elif w.kv_dtype == "fp8_e4m3":
+        k_cache, k_scale = _to_e4m3(kf)
+        v_cache, v_scale = _to_e4m3(vf)
+        if w.poison:
+            for blk, rem in tails:
+                k_cache[blk, rem:] = E4M3_NAN_CODE
+                v_cache[blk, rem:] = E4M3_NAN_CODE
+                k_scale[blk, rem:] = float("nan")
+                v_scale[blk, rem:] = float("nan")
+            unused = torch.from_numpy(np.nonzero(~used)[0])
+            if unused.numel():
+                k_cache[unused] = E4M3_NAN_CODE
+                v_cache[unused] = E4M3_NAN_CODE
+                k_scale[unused] = float("nan")
+                v_scale[unused] = float("nan")
+    else:
+        raise ValueError(f"unknown kv_dtype {w.kv_dtype!r}")
+
+    return Case(
+        workload=w,
+        q=_to_bf16(q).contiguous(),
+        k_cache=k_cache.contiguous(),
+        v_cache=v_cache.contiguous(),
+        k_scale=None if k_scale is None else k_scale.contiguous(),
+        v_scale=None if v_scale is None else v_scale.contiguous(),
+        block_table=torch.from_numpy(table).contiguous(),
+        seq_lens=torch.from_numpy(lens.astype(np.int32)).contiguous(),
+    )
+
+
+def small(name: str, batch: int, lens: Sequence[int], kv_dtype: str = "bf16", seed: int = 100,
+          layout: str = "shuffled", extra_blocks: int = 2, k_spike_frac: float = 0.0,
+          softmax_scale: Optional[float] = None, num_q_heads: int = NUM_Q_HEADS,
+          head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE) -> Case:
+    """A small poisoned case for parity tests (explicit lengths)."""
+    w = Workload(name, batch=batch, lens=tuple(int(x) for x in lens), kv_dtype=kv_dtype,
+                 layout=layout, seed=seed, extra_blocks=extra_blocks,
+                 k_spike_frac=k_spike_frac, softmax_scale=softmax_scale,
+                 num_q_heads=num_q_heads, head_dim=head_dim, page_size=page_size)
+    return generate(w)

@@ -1,0 +1,143 @@
+"""CPU oracle for MFA decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its cpu_baseline
+leg and its reference arm) may import this package.  The product path
+(``decode_attention_02_gb300``) never imports it and shares no code with it.
+
+``mfa_oracle.c`` is the plain fp64 definition of softmax(q K^T * scale) V over
+the paged cache (Step-3, paperlayer.ai/abs/2507.19427v1, sections 2 and 5);
+this module compiles it with gcc and calls it through ctypes.
+
+Pins (tests/test_oracle.py): torch SDPA in float64 on a dense gather done by
+numpy indexing, scipy logsumexp for lse, the two-token logistic closed form,
+L=1 -> v_0, constant K -> mean of V, key-shift and block-permutation
+invariance, convex hull, split/merge identity, and every e4m3 code against
+torch.float8_e4m3fn.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mfa_oracle.c")
+_LIB = os.path.join(_HERE, "libmfa_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable flags: same results on x86_64 and aarch64)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+                               "-fno-fast-math", "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load_library(path: str):
+    """Load a compiled oracle library and declare its signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.mfa_oracle_decode.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P,
+                                      ctypes.c_double, P, P, I]
+    lib.mfa_oracle_decode.restype = I
+    lib.mfa_oracle_combine.argtypes = [I, ctypes.c_long, I, P, P, P, P]
+    lib.mfa_oracle_combine.restype = I
+    lib.mfa_oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.mfa_oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.mfa_oracle_num_cpus.argtypes = []
+    lib.mfa_oracle_num_cpus.restype = I
+    return lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = load_library(_LIB)
+    return _lib
+
+
+def num_cpus() -> int:
+    return int(_load().mfa_oracle_num_cpus())
+
+
+def e4m3_to_double(code: int, lib=None) -> float:
+    return float((lib or _load()).mfa_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def _np(t):
+    """Contiguous numpy view of a torch CPU tensor (bf16 viewed as uint16)."""
+    import torch
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        t = t.contiguous().numpy()
+    return np.ascontiguousarray(t)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
+           softmax_scale: Optional[float] = None, batch_slice: Optional[slice] = None,
+           lib=None):
+    """Oracle decode of ``case`` -> (out float64 [B,H,d], lse float64 [B,H]).
+
+    ``t_begin``/``t_end`` (int sequences of length B) restrict each sequence to
+    a token range; ``batch_slice`` restricts the batch (for bounded samples).
+    ``lib`` selects another compiled copy of the oracle (mutation tests).
+    """
+    w = case.workload
+    q = _np(case.q)
+    table = _np(case.block_table).astype(np.int32)
+    lens = _np(case.seq_lens).astype(np.int32)
+    if batch_slice is not None:
+        q, table, lens = q[batch_slice], table[batch_slice], lens[batch_slice]
+        q, table, lens = (np.ascontiguousarray(x) for x in (q, table, lens))
+        if t_begin is not None:
+            t_begin = np.asarray(t_begin)[batch_slice]
+        if t_end is not None:
+            t_end = np.asarray(t_end)[batch_slice]
+    B, H, d = q.shape
+    kc, vc = _np(case.k_cache), _np(case.v_cache)
+    ks, vs = _np(case.k_scale), _np(case.v_scale)
+    if ks is not None:
+        ks, vs = ks.astype(np.float32), vs.astype(np.float32)
+    tb = None if t_begin is None else np.ascontiguousarray(np.asarray(t_begin, dtype=np.int32))
+    te = None if t_end is None else np.ascontiguousarray(np.asarray(t_end, dtype=np.int32))
+    out = np.zeros((B, H, d), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    scale = w.scale() if softmax_scale is None else float(softmax_scale)
+    rc = (lib or _load()).mfa_oracle_decode(
+        B, H, d, w.page_size, table.shape[1], 1 if w.kv_dtype == "fp8_e4m3" else 0,
+        _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(table), _ptr(lens),
+        _ptr(tb), _ptr(te), scale, _ptr(out), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"mfa_oracle_decode failed with code {rc}")
+    return out, lse
+
+
+def combine(part_o: np.ndarray, part_lse: np.ndarray):
+    """Log-sum-exp merge. part_o [S, ..., d], part_lse [S, ...] -> (out [..., d], lse [...])."""
+    part_o = np.ascontiguousarray(part_o, dtype=np.float64)
+    part_lse = np.ascontiguousarray(part_lse, dtype=np.float64)
+    S = part_o.shape[0]
+    d = part_o.shape[-1]
+    rest = part_lse.shape[1:]
+    R = int(np.prod(rest)) if rest else 1
+    out = np.zeros(rest + (d,), dtype=np.float64)
+    lse = np.zeros(rest, dtype=np.float64)
+    rc = _load().mfa_oracle_combine(S, R, d, _ptr(part_o), _ptr(part_lse), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"mfa_oracle_combine failed with code {rc}")
+    return out, lse
