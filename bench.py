@@ -1,0 +1,458 @@
+"""Benchmark of the MFA decode step on GB300 (one JSON line on rank 0).
+
+A step is one pass of the whole hot path -- decode kernel plus log-sum-exp
+combine -- over one batch of synthetic decode inputs.  The default workload is
+B=32 sequences of 4096 tokens, bf16 KV, 64 query heads of width 256 over one
+shared K/V head in 64-token pages whose physical order is a seeded permutation.
+
+value      : KV-cache bytes read per second over the timed steps (GB/s), inputs
+             resident in HBM; several input copies rotate so that each step reads
+             KV that is not in L2.
+e2e        : the same metric through the public Python API with the per-step
+             inputs (q, block table, lengths) copied from pinned host memory and
+             the outputs (out, lse) copied back, inside the timed region; the KV
+             cache stays resident (it is the attention instance's state).
+roofline   : the decode kernel alone, algorithmic bytes per launch / its mean
+             CUDA-event duration, against the measured HBM copy bandwidth.
+cpu_baseline: the fp64 CPU oracle on a bounded sample of the same workload.
+
+--impl reference times the oracle itself (the reference arm) on the same
+workload, each step a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "b32_l4096_bf16"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ------------------------------------------------------------------ accounting
+
+def kv_bytes_per_token(kv_dtype: str) -> int:
+    """K and V rows of one token: 2*256 elements (+ two fp32 scales for e4m3)."""
+    return 2 * 256 * 2 if kv_dtype == "bf16" else 2 * 256 * 1 + 2 * 4
+
+
+def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64) -> dict:
+    """HBM bytes one decode step must move: every cached K/V row once, q and out once,
+    the used block-table entries, the lengths and the lse."""
+    tokens = int(sum(lens))
+    pages = int(sum((L + page - 1) // page for L in lens))
+    B = len(lens)
+    kv = tokens * kv_bytes_per_token(kv_dtype)
+    other = B * (H * d * 2) * 2 + pages * 4 + B * 4 + B * H * 4
+    return {"kv": kv, "total": kv + other}
+
+
+def algorithmic_flops(lens, H: int = 64, d: int = 256) -> int:
+    """2*H*d for q.K^T plus 2*H*d for P.V per cached token (softmax not counted)."""
+    return int(sum(lens)) * 4 * H * d
+
+
+def intensity_per_token(kv_dtype: str, H: int = 64, d: int = 256, kv_heads_bytes: float = None) -> float:
+    """FLOPs per KV byte of the decode step, per token (8-bit KV without scales: 4Hd/2d = 2H)."""
+    b = kv_bytes_per_token(kv_dtype) if kv_heads_bytes is None else kv_heads_bytes
+    return 4 * H * d / b
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "decode_attention_02_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"mfa_decode_kernel_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != source_digest():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch_full_workload"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, windows):
+        samples = []
+        for t, line in self.lines:
+            if not any(a <= t <= b for a, b in windows):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                samples.append(dict(sm=float(parts[1]), smax=float(parts[2]),
+                                    reasons={"hw_slowdown": parts[5], "hw_thermal_slowdown": parts[6],
+                                             "sw_thermal_slowdown": parts[7], "sw_power_cap": parts[8]}))
+            except ValueError:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        reasons = sorted({k for s in samples for k, v in s["reasons"].items() if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s["sm"] for s in samples),
+                "sm_max_mhz": max(s["smax"] for s in samples), "reasons": reasons, "samples": len(samples)}
+
+
+# ------------------------------------------------------------------ arms
+
+def cpu_oracle_sample(case, target_s: float = 10.0, nthreads: int = 0):
+    """Time the oracle on a bounded batch slice (about target_s seconds of work)."""
+    import oracle
+    lens = case.seq_lens.tolist()
+    order = [b for b in range(len(lens)) if lens[b] > 0]
+    t0 = time.perf_counter()
+    oracle.decode(case, batch_slice=slice(order[0], order[0] + 1), nthreads=nthreads)
+    t1 = time.perf_counter() - t0
+    k = max(1, min(len(lens), int(target_s / max(t1, 1e-3))))
+    t0 = time.perf_counter()
+    oracle.decode(case, batch_slice=slice(0, k), nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"]
+    return kv / dt / 1e9, dt, k
+
+
+def run_reference(args, case, rank: int, world: int):
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    cores = oracle.num_cpus()
+    lens = case.seq_lens.tolist()
+    # bounded sample per step: enough sequences for ~1-3 s of oracle work on all cores
+    t0 = time.perf_counter()
+    oracle.decode(case, batch_slice=slice(0, 1))
+    t1 = time.perf_counter() - t0
+    k = max(1, min(len(lens), int(2.0 / max(t1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle.decode(case, batch_slice=slice(0, 1))
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(case, batch_slice=slice(0, k))
+        times.append(time.perf_counter() - t0)
+    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"]
+    total = sum(times)
+    value = kv * args.steps / total / 1e9
+    sample = f"{k} of {len(lens)} sequences per step ({sum(lens[:k])} tokens), fp64, all {cores} cores"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(case),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+METRIC = "MFA decode-attention KV GB/s and TFLOP/s at 1 GB300; % of HBM/tensor roofline"
+
+
+def workload_config(case, extra=None):
+    w = case.workload
+    lens = case.seq_lens.tolist()
+    cfg = {"workload": w.name, "batch": len(lens), "total_tokens": int(sum(lens)),
+           "min_len": int(min(lens)), "max_len": int(max(lens)), "num_q_heads": w.num_q_heads,
+           "head_dim": w.head_dim, "kv_heads": 1, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+           "softmax_scale": w.scale(), "parallelism": "replica per GPU"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def run_native(args, case, rank: int, world: int):
+    import torch
+    import decode_attention_02_gb300 as mfa
+    from decode_attention_02_gb300 import build
+
+    build.build_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = case.workload
+    lens = case.seq_lens.tolist()
+    kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    B = len(lens)
+    acct = algorithmic_bytes(lens, w.kv_dtype)
+    flops = algorithmic_flops(lens)
+
+    # rotating input copies: consecutive steps never find their KV in L2
+    set_bytes = case.k_cache.numel() * case.k_cache.element_size() * 2
+    nsets = 1 + max(1, math.ceil(2 * L2_BYTES / max(set_bytes, 1)))
+    sets = []
+    for _ in range(nsets):
+        sets.append(dict(
+            q=case.q.to(dev), k=case.k_cache.to(dev), v=case.v_cache.to(dev),
+            ks=None if case.k_scale is None else case.k_scale.to(dev),
+            vs=None if case.v_scale is None else case.v_scale.to(dev),
+            table=case.block_table.to(dev), lens=case.seq_lens.to(dev)))
+    out = torch.empty(B, 64, 256, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, 64, dtype=torch.float32, device=dev)
+    dec = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
+                      host_seq_lens=lens, device=dev)
+    dec_only = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
+                           host_seq_lens=lens, flags=mfa.MFA_PLAN_NO_COMBINE, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    G = dec.plan.num_ctas
+    launches_per_step = 1 + (1 if G > 1 else 0)
+
+    def step(i, d=dec):
+        s = sets[i % nsets]
+        mfa.mfa_decode_run(d.plan, d.problem, s["q"], s["k"], s["v"], s["ks"], s["vs"], s["table"], s["lens"],
+                           out, lse, d.workspace, None)
+
+    # status word of this exact launch configuration must stay clear
+    step(0)
+    torch.cuda.synchronize()
+    status = mfa.mfa_read_device_status(dec.workspace)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+    windows = []
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # --- timed steps (decode + combine), replayed from a CUDA graph of exactly K steps
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(args.steps):
+            step(i)
+    graph.replay()   # untimed: first replay uploads the graph
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start = time.time()
+    e0.record(stream)
+    graph.replay()
+    e1.record(stream)
+    barrier()
+    windows.append((t_start, time.time()))
+    ms_total = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+
+    # --- decode kernel alone: per-launch CUDA events, queued behind a GPU sleep so
+    #     the launches run back to back whatever the host-side cost of enqueueing them
+    nk = max(min(args.steps, 400), 50)
+    for i in range(3):
+        step(i, dec_only)
+    barrier()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+    t_start = time.time()
+    torch.cuda._sleep(int(2e7))
+    for i in range(nk):
+        evs[i][0].record(stream)
+        step(i, dec_only)
+        evs[i][1].record(stream)
+    barrier()
+    windows.append((t_start, time.time()))
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_mean_ms = sum(kern_ms) / len(kern_ms)
+
+    # --- end to end through the public API: host inputs in, host outputs out
+    q_h = case.q.pin_memory()
+    table_h = case.block_table.pin_memory()
+    lens_h = case.seq_lens.pin_memory()
+    out_h = torch.empty(B, 64, 256, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(B, 64, dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(sets[0]["q"])
+    table_d = torch.empty_like(sets[0]["table"])
+    lens_d = torch.empty_like(sets[0]["lens"])
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, table_h, lens_h))
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h))
+
+    def e2e_step(i):
+        s = sets[i % nsets]
+        q_d.copy_(q_h, non_blocking=True)
+        table_d.copy_(table_h, non_blocking=True)
+        lens_d.copy_(lens_h, non_blocking=True)
+        dec(q_d, s["k"], s["v"], table_d, lens_d, k_scale=s["ks"], v_scale=s["vs"], out=out, lse=lse)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier()
+    t_start = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    barrier()
+    windows.append((t_start, time.time()))
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    # keep sampling clocks until the windows hold enough samples
+    clocks = sampler.summary(windows)
+    if clocks["samples"] < 5:
+        t_start = time.time()
+        i = 0
+        while time.time() - t_start < 0.6:
+            graph.replay()
+            torch.cuda.synchronize()
+        windows.append((t_start, time.time()))
+        time.sleep(0.1)
+        clocks = sampler.summary(windows)
+        clocks["window"] = "timed regions plus 0.6 s of identical steps"
+    sampler.stop()
+
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+    kv_gbs = acct["kv"] * world / (ms_step * 1e-3) / 1e9
+    achieved = acct["total"] / (kern_mean_ms * 1e-3) / 1e9
+    tflops = flops * world / (ms_step * 1e-3) / 1e12
+    t_hbm = acct["total"] / (hbm_peak * 1e9)
+    t_tc = flops / (bf16_peak * 1e12)
+    result = {
+        "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV, bf16 MMA",
+        "data": "synthetic",
+        "config": workload_config(case, {"l2": f"{nsets} rotating input copies ({nsets * set_bytes / 1e6:.0f} MB "
+                                               f"of KV) so no step reads KV left in L2 by the previous one",
+                                         "num_ctas": G}),
+        "tflops": tflops,
+        "hbm_roofline_frac": (t_hbm / (ms_step * 1e-3)),
+        "tensor_roofline_frac": (t_tc / (ms_step * 1e-3)),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": profiled_traffic(w.name),
+                     "kernel": "mfa_decode_kernel", "mean_launch_ms": kern_mean_ms,
+                     "algorithmic_bytes_per_launch": acct["total"], "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": acct["kv"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from decode_attention_02_gb300 import inputs
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    case = inputs.generate(inputs.WORKLOADS[args.workload])
+
+    if args.impl == "reference":
+        res = run_reference(args, case, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    res = run_native(args, case, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            import oracle
+            oracle.build()
+            v, dt, k = cpu_oracle_sample(case)
+            res["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": oracle.num_cpus(), "kind": "oracle",
+                                   "sample": f"{k} of {len(case.seq_lens)} sequences, fp64, {dt:.1f} s"}
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,222 @@
+"""MFA decode attention for GB300 (sm_103a).
+
+Thin ctypes binding over ``libmfa.so`` (CUDA kernels + C ABI, see include/mfa.h).
+Every step of the decode runs in the library's kernels; this module only
+marshals arguments.  PyTorch supplies device memory and the current stream.
+
+The operation is Step-3's MFA decode step (paperlayer.ai/abs/2507.19427v1,
+section 2 "Step-3 Model Card" and section 5 "Model-System Co-design"): 64 query
+heads of width 256 over one shared K head and one shared V head held in a paged
+KV cache of 64-token pages, out = softmax(q K^T * scale) V and its log-sum-exp.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmfa.so")
+
+MFA_OK = 0
+MFA_ERR_INVALID_ARG = 1
+MFA_ERR_UNSUPPORTED = 2
+MFA_ERR_WORKSPACE = 3
+MFA_ERR_CUDA = 4
+MFA_ERR_DEVICE_CHECK = 5
+
+MFA_KV_BF16 = 0
+MFA_KV_FP8_E4M3 = 1
+
+MFA_DEV_TIMEOUT = 0x1
+MFA_DEV_BAD_BLOCK = 0x2
+MFA_DEV_BAD_LENGTH = 0x4
+MFA_DEV_SCHEDULE = 0x8
+
+MFA_PLAN_CHECK = 0x1
+MFA_PLAN_NO_COMBINE = 0x2
+
+NUM_Q_HEADS = 64
+HEAD_DIM = 256
+PAGE_SIZE = 64
+
+# Every symbol include/mfa.h declares.
+EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
+                    "mfa_status_string", "mfa_abi_version")
+
+
+class MfaProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("max_pages_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+class MfaPlan(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("tile_tokens", ctypes.c_int32),
+                ("max_tiles_per_cta", ctypes.c_int32), ("num_partials", ctypes.c_int32),
+                ("batch", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("num_sms", ctypes.c_int32),
+                ("total_tiles", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64)]
+
+
+class MfaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmfa.so; raises if it has not been built (no fallback path exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with decode_attention_02_gb300.build.build_library()")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    lib.mfa_decode_plan.argtypes = [ctypes.POINTER(MfaProblem), P, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_uint32, ctypes.POINTER(MfaPlan)]
+    lib.mfa_decode_plan.restype = ctypes.c_int
+    lib.mfa_decode_run.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P, P, P, P, P,
+                                   P, P, P, ctypes.c_uint64, P]
+    lib.mfa_decode_run.restype = ctypes.c_int
+    lib.mfa_combine.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, ctypes.c_uint64, P, P,
+                                P, P]
+    lib.mfa_combine.restype = ctypes.c_int
+    lib.mfa_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, P]
+    lib.mfa_read_device_status.restype = ctypes.c_int
+    lib.mfa_status_string.argtypes = [ctypes.c_int]
+    lib.mfa_status_string.restype = ctypes.c_char_p
+    lib.mfa_abi_version.argtypes = []
+    lib.mfa_abi_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().mfa_status_string(int(status)).decode()
+    except ImportError:
+        return "library not loaded"
+
+
+def _check(status: int, where: str):
+    if status != MFA_OK:
+        raise MfaError(status, where)
+
+
+def _ptr(x) -> Optional[int]:
+    """Device pointer of a torch tensor (must be CUDA and contiguous), an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _nbytes(x) -> int:
+    return x.numel() * x.element_size()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_problem(batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
+                 softmax_scale: float = HEAD_DIM ** -0.5, num_q_heads: int = NUM_Q_HEADS,
+                 head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE) -> MfaProblem:
+    return MfaProblem(batch, num_q_heads, head_dim, page_size, max_pages_per_seq, num_blocks, kv_dtype,
+                      softmax_scale)
+
+
+def mfa_decode_plan(problem: MfaProblem, host_seq_lens: Optional[Sequence[int]] = None, max_seq_len: int = 0,
+                    num_sms: int = 0, force_ctas: int = 0, flags: int = 0) -> MfaPlan:
+    lib = load_library()
+    plan = MfaPlan()
+    lens_arr = None
+    if host_seq_lens is not None:
+        vals = [int(v) for v in host_seq_lens]
+        lens_arr = (ctypes.c_int32 * max(1, len(vals)))(*vals)
+    st = lib.mfa_decode_plan(ctypes.byref(problem), lens_arr, int(max_seq_len), int(num_sms), int(force_ctas),
+                             int(flags), ctypes.byref(plan))
+    _check(st, "mfa_decode_plan")
+    return plan
+
+
+def mfa_decode_run(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_scale, v_scale, block_table,
+                   seq_lens, out, lse, workspace, stream=None, workspace_bytes: Optional[int] = None) -> None:
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    st = lib.mfa_decode_run(ctypes.byref(plan), ctypes.byref(problem), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out),
+                            _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "mfa_decode_run")
+
+
+def mfa_combine(plan: MfaPlan, problem: MfaProblem, workspace, seq_lens, out, lse, stream=None,
+                workspace_bytes: Optional[int] = None) -> None:
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    st = lib.mfa_combine(ctypes.byref(plan), ctypes.byref(problem), _ptr(workspace), int(workspace_bytes),
+                         _ptr(seq_lens), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "mfa_combine")
+
+
+def mfa_read_device_status(workspace, clear: bool = True, stream=None) -> int:
+    lib = load_library()
+    word = ctypes.c_uint32(0)
+    st = lib.mfa_read_device_status(_ptr(workspace), ctypes.byref(word), 1 if clear else 0, _stream(stream))
+    _check(st, "mfa_read_device_status")
+    return int(word.value)
+
+
+def workspace_layout(plan: MfaPlan):
+    """Byte offsets of (partial O, partial lse) inside the workspace (see include/mfa.h)."""
+    o_off = 256
+    lse_off = (o_off + plan.num_partials * NUM_Q_HEADS * HEAD_DIM * 4 + 255) // 256 * 256
+    return o_off, lse_off
+
+
+class Decoder:
+    """Plan + workspace for one batch shape; ``__call__`` enqueues a decode step.
+
+    Device buffers come from PyTorch's allocator; the step itself is
+    ``mfa_decode_run`` (decode kernel + combine kernel).
+    """
+
+    def __init__(self, batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
+                 softmax_scale: float = HEAD_DIM ** -0.5, host_seq_lens=None, max_seq_len: int = 0,
+                 force_ctas: int = 0, flags: int = 0, device=None):
+        import torch
+        self.problem = make_problem(batch, max_pages_per_seq, num_blocks, kv_dtype, softmax_scale)
+        if host_seq_lens is None and max_seq_len == 0:
+            max_seq_len = max_pages_per_seq * PAGE_SIZE
+        self.plan = mfa_decode_plan(self.problem, host_seq_lens, max_seq_len, 0, force_ctas, flags)
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.workspace = torch.zeros(int(self.plan.workspace_bytes), dtype=torch.uint8, device=self.device)
+
+    def __call__(self, q, k_cache, v_cache, block_table, seq_lens, k_scale=None, v_scale=None, out=None,
+                 lse=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((self.problem.batch, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+        if lse is None:
+            lse = torch.empty((self.problem.batch, NUM_Q_HEADS), dtype=torch.float32, device=q.device)
+        mfa_decode_run(self.plan, self.problem, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                       out, lse, self.workspace, stream)
+        return out, lse

@@ -1,0 +1,1050 @@
+// MFA decode attention for GB300 (sm_103a): split-KV decode kernel, log-sum-exp
+// combine kernel, and the C ABI declared in include/mfa.h.
+//
+// The step (Step-3, paperlayer.ai/abs/2507.19427v1, sections 2 and 5): 64 query
+// heads of width 256 attend over ONE shared K head and ONE shared V head in a
+// paged cache, so every KV page is a dense [64 x 256] . [256 x tokens] contraction
+// shared by all heads.  Section 4 states the cost model: the larger of compute and
+// KV-memory access.  At 64 FLOP/B (bf16 KV) the step is HBM-bound on GB300, so the
+// design streams each KV byte exactly once per step:
+//
+//  * One CTA per SM (persistent).  CTA g owns tiles [floor(gW/G), floor((g+1)W/G))
+//    of the batch's W 128-token tiles laid end to end, so the load is even for any
+//    length mix; a sequence cut by a CTA boundary yields partial results that the
+//    combine kernel merges (split-KV with a log-sum-exp merge).
+//  * Each CTA holds all 64 heads of its sequence, so K and V are read once.
+//  * Warp 0 streams K/V pages with TMA (3-D tensor maps over the page pool; the
+//    block table supplies the page coordinate) into a 10-slot, 16 KB/slot ring.
+//  * Warp 1 issues tcgen05 MMAs in the transposed form, which fills the M=128
+//    datapath: S^T[128 tokens x 64 heads] = K_tile . Q^T and
+//    O^T[256 d x 64 heads] += V^T . P^T (two M=128 halves), fp32 accumulators in
+//    tensor memory (S double-buffered, O double-buffered across sequences).
+//  * Warps 2-5 (one thread per tensor-memory lane = token) run the online softmax
+//    in fp32.  The running max is lazy: a head's reference max moves only when a
+//    score exceeds it by 2^8, so the common tile needs no cross-thread reduction;
+//    row sums accumulate per thread and are reduced once per sequence.
+//  * The ragged last page is loaded with its valid rows shifted to the end of the
+//    box (negative row start; TMA fills the rest with zeros), so NaN or stale data
+//    in unused page slots never enters an MMA.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "mfa.h"
+#include "ptx.cuh"
+
+namespace mfa {
+
+constexpr int kH = 64;             // query heads
+constexpr int kD = 256;            // head width
+constexpr int kPage = 64;          // tokens per KV page
+constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
+constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kSoftmaxThreads = 128;
+constexpr int kNumSlots = 10;
+constexpr int kSlotBytes = 16384;
+constexpr int kMaxTilesPerCta = 128;
+constexpr int kMaxSeg = kMaxTilesPerCta;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr int kOffQ = 0;                                     // 4 x [64 heads x 128 B]
+constexpr int kOffP = 32768;                                 // [128 tokens x 128 B]
+constexpr int kOffRing = 49152;                              // kNumSlots x 16 KB
+constexpr int kOffBar = kOffRing + kNumSlots * kSlotBytes;  // mbarriers
+constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..11] scan
+constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
+constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
+constexpr int kOffRed = kOffAlpha + 256;      // float[4][64] cross-warp reduction scratch
+constexpr int kOffLinv = kOffRed + 1024;      // float[64]  1 / row sum
+constexpr int kOffSeg = kOffLinv + 256;       // int4[kMaxSeg] {b, first tile, end tile, L}
+constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
+constexpr int kOffTileBlk = kOffSegN0 + 4 * kMaxSeg;    // int2[kMaxTilesPerCta] page ids
+constexpr int kSmemUsed = kOffTileBlk + 8 * kMaxTilesPerCta;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+enum Bar : int {
+  kBarFull = 0,
+  kBarEmpty = kBarFull + kNumSlots,
+  kBarQFull = kBarEmpty + kNumSlots,
+  kBarQEmpty,
+  kBarSFull,   // 2
+  kBarSEmpty = kBarSFull + 2,
+  kBarPFull = kBarSEmpty + 2,
+  kBarPvDone,
+  kBarOFull,   // 2
+  kBarOEmpty = kBarOFull + 2,
+  kBarDrain = kBarOEmpty + 2,
+  kBarCount
+};
+static_assert(kBarCount * 8 <= 512, "barrier area");
+
+// Tensor-memory columns.
+constexpr uint32_t kTmemS = 0;     // S^T buffers: [0,64) and [64,128)
+constexpr uint32_t kTmemO = 128;   // O^T buffer k, half hh: 128 + 128k + 64hh
+constexpr uint32_t kTmemL = 384;   // per-lane row-sum partials, 64 heads
+
+struct DecodeParams {
+  CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
+  CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256], box {64, 64, 1}, 128B swizzle
+  CUtensorMap tm_v;
+  const float* k_scale;
+  const float* v_scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  unsigned int* status;
+  int batch;
+  int max_pages;
+  int num_blocks;
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* seq_lens;
+  __nv_bfloat16* out;
+  float* lse;
+  int batch;
+  int max_pages;
+  int num_ctas;
+};
+
+// ------------------------------------------------------------------ helpers
+
+// tcgen05 shared-memory matrix descriptor: start, leading/stride byte offsets,
+// descriptor version 1 (bits 46..47), 128-byte swizzle (bits 61..63 = 2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// tcgen05 instruction descriptor for kind::f16: fp32 D, bf16 or f16 A/B,
+// K-major (0) or MN-major (1) operands, N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn, bool b_mn, int m, int n) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ int clamp_len(int L, int cap, bool& bad) {
+  if (L < 0) { bad = true; return 0; }
+  if (L > cap) { bad = true; return cap; }
+  return L;
+}
+
+__device__ __forceinline__ int tiles_of(int L) { return (L + kTile - 1) / kTile; }
+
+// Bounded wait on an mbarrier phase.  Returns false after kWaitLimitNs, or at
+// once when another role has raised the CTA's abort flag.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const bool ok = wait_slow(bar, parity, abort_flag, kWaitLimitNs);
+  if (!ok && abort_flag != nullptr) *abort_flag = 1;
+  return ok;
+}
+
+// Block-wide (kThreads) inclusive scan of one int per thread; also returns the total.
+__device__ __forceinline__ int block_incl_scan(int v, int* scratch, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) scratch[warp] = v;
+  __syncthreads();
+  int before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int x = scratch[w];
+    before += (w < warp) ? x : 0;
+    tot += x;
+  }
+  __syncthreads();
+  total = tot;
+  return v + before;
+}
+
+// Reduce 64 per-thread values across the 32 lanes of a warp by halving exchanges;
+// lane l ends with the results for heads 2l and 2l+1.
+template <bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], float& r0, float& r1) {
+  const int lane = threadIdx.x & 31;
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool hi = lane & 16;
+    const float keep = hi ? v[i + 32] : v[i], send = hi ? v[i] : v[i + 32];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool hi = lane & 8;
+    const float keep = hi ? v[i + 16] : v[i], send = hi ? v[i] : v[i + 16];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 4;
+    const float keep = hi ? v[i + 8] : v[i], send = hi ? v[i] : v[i + 8];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 2;
+    const float keep = hi ? v[i + 4] : v[i], send = hi ? v[i] : v[i + 4];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 1;
+    const float keep = hi ? v[i + 2] : v[i], send = hi ? v[i] : v[i + 2];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+  }
+  r0 = v[0];
+  r1 = v[1];
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 64 consecutive TMEM columns of this thread's lane, as two 32-register halves.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  tmem_ld32(taddr, a);
+  tmem_ld32(taddr + 32, b);
+  tmem_ld_wait(a);
+  tmem_ld_wait(b);
+}
+#define SV(h) ((h) < 32 ? sa[(h)] : sb[(h) - 32])
+
+// Warp-uniform bounded wait (all lanes poll; the warp agrees on the outcome).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = wait_bar(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------ decode kernel
+
+__global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+  volatile int* abort_flag = misc + 1;
+  int4* seg = reinterpret_cast<int4*>(smem + kOffSeg);
+  int* seg_n0 = reinterpret_cast<int*>(smem + kOffSegN0);
+  int2* tile_blk = reinterpret_cast<int2*>(smem + kOffTileBlk);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
+
+  // ---------------- set-up: barriers, tensor memory
+  if (tid == 0) {
+    for (int i = 0; i < kNumSlots; ++i) {
+      mbar_init(bar(kBarFull + i), 1);
+      mbar_init(bar(kBarEmpty + i), 1);
+    }
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarSFull + i), 1);
+      mbar_init(bar(kBarSEmpty + i), kSoftmaxThreads);
+      mbar_init(bar(kBarOFull + i), 1);
+      mbar_init(bar(kBarOEmpty + i), kSoftmaxThreads);
+    }
+    mbar_init(bar(kBarPFull), kSoftmaxThreads);
+    mbar_init(bar(kBarPvDone), 1);
+    mbar_init(bar(kBarDrain), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sbase + kOffMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 32 * 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+
+  // ---------------- schedule: this CTA's tile range and its per-sequence segments
+  const int cap = p.max_pages * kPage;
+  {
+    int* scratch = misc + 4;
+    bool bad = false;
+    int loc = 0;
+    for (int b = tid; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
+    if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
+    int W = 0;
+    block_incl_scan(loc, scratch, W);
+    const int G = gridDim.x, g = blockIdx.x;
+    const int t0 = static_cast<int>((static_cast<long long>(g) * W) / G);
+    const int t1 = static_cast<int>((static_cast<long long>(g + 1) * W) / G);
+    int nseg = 0;
+    if (t1 - t0 > kMaxTilesPerCta) {
+      if (tid == 0) atomicOr(p.status, MFA_DEV_SCHEDULE);
+    } else {
+      int carry = 0;
+      for (int c0 = 0; c0 < p.batch && carry < t1; c0 += kThreads) {
+        const int b = c0 + tid;
+        bool dummy = false;
+        const int L = (b < p.batch) ? clamp_len(p.seq_lens[b], cap, dummy) : 0;
+        const int T = tiles_of(L);
+        int tot = 0, ftot = 0;
+        const int incl = block_incl_scan(T, scratch, tot) + carry;
+        const int excl = incl - T;
+        const int f = (T > 0 && excl < t1 && incl > t0) ? 1 : 0;
+        const int fidx = nseg + block_incl_scan(f, scratch, ftot) - f;
+        if (f) {
+          const int lo = max(t0, excl), hi = min(t1, incl);
+          seg[fidx] = make_int4(b, lo - excl, hi - excl, L);
+          seg_n0[fidx] = lo - t0;
+        }
+        carry += tot;
+        nseg += ftot;
+      }
+    }
+    if (tid == 0) {
+      misc[2] = nseg;
+      misc[3] = (nseg > 0) ? (t1 - t0) : 0;
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = static_cast<uint32_t>(misc[0]);
+  const int nseg = misc[2];
+  const int ntiles = misc[3];
+
+  if (warp == 0) {
+    // ---------------- producer: page ids, then TMA loads of Q, K, V
+    bool bad_blk = false;
+    for (int s = 0; s < nseg; ++s) {
+      const int4 sg = seg[s];
+      const int32_t* row = p.block_table + static_cast<size_t>(sg.x) * p.max_pages;
+      for (int j = sg.y + lane; j < sg.z; j += 32) {
+        const int b0 = row[2 * j];
+        const int b1 = (kPage * (2 * j + 1) < sg.w) ? row[2 * j + 1] : 0;
+        if (b0 < 0 || b0 >= p.num_blocks || b1 < 0 || b1 >= p.num_blocks) bad_blk = true;
+        tile_blk[seg_n0[s] + j - sg.y] = make_int2(b0, b1);
+      }
+    }
+    if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
+    __syncwarp();
+    if (lane == 0 && ntiles > 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      uint32_t u = 0;       // ring uses issued
+      int nq = 0;           // Q loads issued
+      int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
+      bool ok = true;
+      for (int n = 0; n <= ntiles && ok; ++n) {
+        if (n < ntiles) {
+          const int4 sg = seg[sk];
+          if (jk == sg.y) {
+            if (sk > 0) ok = wait_bar(bar(kBarQEmpty), (sk - 1) & 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(kBarQFull), kH * kD * 2);
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(sbase + kOffQ + c * 8192, &p.tm_q, bar(kBarQFull), 64 * c, kH * sg.x);
+            ++nq;
+          }
+          const int2 bk = tile_blk[n];
+          const int r0 = min(kPage, sg.w - kTile * jk);
+          const int r1 = min(kPage, sg.w - kTile * jk - kPage);
+          for (int c = 0; c < 4; ++c, ++u) {
+            const uint32_t slot = u % kNumSlots;
+            ok = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
+            if (!ok) break;
+            const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
+            mbar_arrive_expect_tx(bar(kBarFull + slot), r1 > 0 ? 16384 : 8192);
+            tma_load_3d_hint(dst, &p.tm_k, bar(kBarFull + slot), 64 * c, r0 - kPage, bk.x, pol);
+            if (r1 > 0)
+              tma_load_3d_hint(dst + 8192, &p.tm_k, bar(kBarFull + slot), 64 * c, r1 - kPage, bk.y, pol);
+          }
+          if (!ok) break;
+          if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
+        }
+        if (n >= 1) {
+          const int4 sg = seg[sv];
+          const int2 bk = tile_blk[n - 1];
+          const int rr0 = min(kPage, sg.w - kTile * jv);
+          const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
+          for (int pg = 0; pg < 2 && ok; ++pg) {
+            const int r = pg ? rr1 : rr0;
+            const int blk = pg ? bk.y : bk.x;
+            for (int hh = 0; hh < 2; ++hh, ++u) {
+              const uint32_t slot = u % kNumSlots;
+              ok = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
+              if (!ok) break;
+              const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
+              if (r > 0) {
+                mbar_arrive_expect_tx(bar(kBarFull + slot), 16384);
+                tma_load_3d_hint(dst, &p.tm_v, bar(kBarFull + slot), 128 * hh, r - kPage, blk, pol);
+                tma_load_3d_hint(dst + 8192, &p.tm_v, bar(kBarFull + slot), 128 * hh + 64, r - kPage, blk, pol);
+              } else {
+                mbar_arrive(bar(kBarFull + slot));
+              }
+            }
+          }
+          if (!ok) break;
+          if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
+        }
+      }
+      if (!ok) {
+        atomicOr(p.status, MFA_DEV_TIMEOUT);
+        // let every copy already issued land before the CTA can exit
+        const uint32_t first = (u > kNumSlots) ? u - kNumSlots : 0;
+        for (uint32_t v = first; v < u; ++v)
+          wait_slow(bar(kBarFull + v % kNumSlots), (v / kNumSlots) & 1, nullptr, kDrainLimitNs);
+        if (nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdescQK = idesc_f16(true, false, false, 128, 64);
+      constexpr uint32_t kIdescPV = idesc_f16(true, true, true, 128, 64);
+      uint32_t u = 0;
+      int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
+      bool ok = true;
+      for (int n = 0; n <= ntiles && ok; ++n) {
+        if (n < ntiles) {
+          const int4 sg = seg[sk];
+          const bool first = (jk == sg.y), last = (jk == sg.z - 1);
+          if (first) ok = wait_bar(bar(kBarQFull), sk & 1, abort_flag);
+          if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + kTmemS + 64u * (n & 1);
+          for (int c = 0; c < 4; ++c, ++u) {
+            const uint32_t slot = u % kNumSlots;
+            ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
+            const uint32_t b0 = sbase + kOffQ + c * 8192;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_f16_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
+                          kIdescQK, (c | kk) != 0);
+            umma_commit(bar(kBarEmpty + slot));
+          }
+          if (!ok) break;
+          umma_commit(bar(kBarSFull + (n & 1)));
+          if (last) umma_commit(bar(kBarQEmpty));
+          if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
+        }
+        if (n >= 1) {
+          const int m = n - 1;
+          const int4 sg = seg[sv];
+          const bool first = (jv == sg.y), last = (jv == sg.z - 1);
+          const int kb = sv & 1;
+          ok = wait_bar(bar(kBarPFull), m & 1, abort_flag);
+          if (ok && first && sv >= 2) ok = wait_bar(bar(kBarOEmpty + kb), ((sv >> 1) - 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const int rr0 = min(kPage, sg.w - kTile * jv);
+          const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
+          for (int pg = 0; pg < 2 && ok; ++pg) {
+            const int r = pg ? rr1 : rr0;
+            for (int hh = 0; hh < 2; ++hh, ++u) {
+              const uint32_t slot = u % kNumSlots;
+              ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              if (r > 0) {
+                const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
+                const uint32_t b0 = sbase + kOffP + pg * 8192;
+                const uint32_t d_tmem = tmem + kTmemO + 128u * kb + 64u * hh;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  umma_f16_ss(d_tmem, smem_desc(a0 + 2048 * kk, 8192, 1024),
+                              smem_desc(b0 + 2048 * kk, 1024, 1024), kIdescPV,
+                              !(first && pg == 0 && kk == 0));
+              }
+              umma_commit(bar(kBarEmpty + slot));
+            }
+          }
+          if (!ok) break;
+          umma_commit(bar(kBarPvDone));
+          if (last) umma_commit(bar(kBarOFull + kb));
+          if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
+        }
+      }
+      if (!ok) atomicOr(p.status, MFA_DEV_TIMEOUT);
+      // every MMA must be complete before tensor memory is released
+      umma_commit(bar(kBarDrain));
+      wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
+    }
+  } else {
+    // ---------------- softmax + epilogue (128 threads, one per TMEM lane)
+    const int t128 = tid - 64;
+    const int wq = warp & 3;                       // TMEM lane quarter of this warp
+    const int row = wq * 32 + lane;                // token row of a tile / d within an O half
+    const int sw = warp - 2;                       // 0..3
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    float* m_ref = reinterpret_cast<float*>(smem + kOffMref);
+    float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    float* linv = reinterpret_cast<float*>(smem + kOffLinv);
+    const float c = p.scale_log2;
+
+    // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
+    for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+      bool dummy = false;
+      if (clamp_len(p.seq_lens[b], cap, dummy) != 0) continue;
+      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(b) * kH * kD);
+      for (int i = t128; i < kH * kD * 2 / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr && t128 < kH) p.lse[b * kH + t128] = -INFINITY;
+    }
+
+    bool aborted = false;
+    int n = 0;
+    const uint32_t l_tmem = tmem + kTmemL + lane_base;   // this thread's 64 row-sum partials
+    for (int s = 0; s < nseg; ++s) {
+      const int4 sg = seg[s];
+      const int b = sg.x, L = sg.w, kb = s & 1;
+      const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
+      const int slot_p = b + static_cast<int>(blockIdx.x);
+      if (t128 < kH) m_ref[t128] = -INFINITY;
+      named_bar_sync(1, kSoftmaxThreads);
+      bool stop = false;
+      for (int j = sg.y; j < sg.z; ++j, ++n) {
+        const bool first = (j == sg.y);
+        const uint32_t s_tmem = tmem + kTmemS + 64u * (n & 1) + lane_base;
+        const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
+        // --- PV of the previous tile must be done before P or O are touched
+        const bool okPV = (n == 0) ? true : wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
+        aborted = aborted || !okS || !okPV;
+        // --- validity of this thread's row (the last page's rows sit at the end of the box)
+        const int pg = row >> 6, i = row & 63;
+        const int rp = min(kPage, L - kTile * j - kPage * pg);
+        const bool valid = okS && rp > 0 && i >= kPage - rp;
+        // --- does any score of this row exceed its head's reference max by > 2^8?
+        bool need = false;
+        if (okS) {
+          tc_fence_after();
+          uint32_t sa[32], sb[32];
+          tmem_ld64(s_tmem, sa, sb);
+#pragma unroll
+          for (int h = 0; h < 64; h += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h);
+            need |= (fmaf(__uint_as_float(SV(h + 0)), c, -m4.x) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(SV(h + 1)), c, -m4.y) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(SV(h + 2)), c, -m4.z) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(SV(h + 3)), c, -m4.w) > kRescaleThreshold);
+          }
+          need = need && valid;
+        }
+        if (named_bar_or(1, kSoftmaxThreads, need || aborted || *abort_flag)) {
+          if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) { stop = true; break; }
+          // --- rare path: new reference max for heads whose scores jumped by > 2^8
+          {
+            uint32_t sa[32], sb[32];
+            tmem_ld64(s_tmem, sa, sb);
+            float mv[64];
+#pragma unroll
+            for (int h = 0; h < 64; ++h) mv[h] = valid ? __uint_as_float(SV(h)) * c : -INFINITY;
+            float r0, r1;
+            warp_reduce_scatter64<true>(mv, r0, r1);
+            red[sw * 64 + 2 * lane] = r0;
+            red[sw * 64 + 2 * lane + 1] = r1;
+          }
+          named_bar_sync(1, kSoftmaxThreads);
+          if (t128 < kH) {
+            const float mt = fmaxf(fmaxf(red[t128], red[64 + t128]), fmaxf(red[128 + t128], red[192 + t128]));
+            const float mo = m_ref[t128];
+            float a = 1.f;
+            if (mt > mo + kRescaleThreshold) {
+              a = exp2f(mo - mt);
+              m_ref[t128] = mt;
+            }
+            alpha_s[t128] = a;
+          }
+          named_bar_sync(1, kSoftmaxThreads);
+          if (!first) {
+            // row-sum partials and O^T rows (d = row, 128 + row) times alpha per head column
+            for (int k3 = 0; k3 < 3; ++k3) {
+              uint32_t oa[32], ob[32];
+              const uint32_t ta = (k3 == 2) ? l_tmem : tmem + kTmemO + 128u * kb + 64u * k3 + lane_base;
+              tmem_ld64(ta, oa, ob);
+#pragma unroll
+              for (int h = 0; h < 32; ++h) {
+                oa[h] = __float_as_uint(__uint_as_float(oa[h]) * alpha_s[h]);
+                ob[h] = __float_as_uint(__uint_as_float(ob[h]) * alpha_s[h + 32]);
+              }
+              tmem_st32(ta, oa);
+              tmem_st32(ta + 32, ob);
+            }
+            tmem_st_wait();
+          }
+        }
+        // --- probabilities, row sums, P^T row (bf16, 128B-swizzled) for the PV MMA
+        uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sv[32], lv[32];
+          tmem_ld32(s_tmem + 32 * half, sv);
+          if (!first) tmem_ld32(l_tmem + 32 * half, lv);
+          tmem_ld_wait(sv);
+          if (!first) {
+            tmem_ld_wait(lv);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) lv[e] = 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int hl = 8 * q + 2 * e, h = 32 * half + hl;
+              const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h);
+              const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
+              const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
+              lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + p0);
+              lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + p1);
+              pk[e] = pack_bf16(p0, p1);
+            }
+            const int chunk = 4 * half + q;
+            *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          tmem_st32(l_tmem + 32 * half, lv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarSEmpty + (n & 1)));
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarPFull));
+      }
+      if (stop) break;
+
+      // ---------------- epilogue of sequence b's segment
+      {
+        uint32_t la[32], lb[32];
+        tmem_ld64(l_tmem, la, lb);
+        float lsum[64];
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          lsum[h] = __uint_as_float(la[h]);
+          lsum[h + 32] = __uint_as_float(lb[h]);
+        }
+        float r0, r1;
+        warp_reduce_scatter64<false>(lsum, r0, r1);
+        red[sw * 64 + 2 * lane] = r0;
+        red[sw * 64 + 2 * lane + 1] = r1;
+      }
+      named_bar_sync(1, kSoftmaxThreads);
+      if (t128 < kH) {
+        const float l = (red[t128] + red[64 + t128]) + (red[128 + t128] + red[192 + t128]);
+        linv[t128] = 1.f / l;
+        const float lse_v = (m_ref[t128] + log2f(l)) * 0.69314718055994531f;
+        if (whole) {
+          if (p.lse != nullptr) p.lse[b * kH + t128] = lse_v;
+        } else {
+          p.part_lse[static_cast<size_t>(slot_p) * kH + t128] = lse_v;
+        }
+      }
+      named_bar_sync(1, kSoftmaxThreads);
+      const bool okO = wait_warp(bar(kBarOFull + kb), (s >> 1) & 1, abort_flag);
+      aborted = aborted || !okO;
+      if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) break;
+      tc_fence_after();
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t oa[32], ob[32];
+        tmem_ld64(tmem + kTmemO + 128u * kb + 64u * hh + lane_base, oa, ob);
+        const int d = 128 * hh + row;
+        if (whole) {
+          __nv_bfloat16* dst = p.out + static_cast<size_t>(b) * kH * kD + d;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            dst[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * linv[h]);
+            dst[(h + 32) * kD] = __float2bfloat16_rn(__uint_as_float(ob[h]) * linv[h + 32]);
+          }
+        } else {
+          float* dst = p.part_o + static_cast<size_t>(slot_p) * kH * kD + d;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            dst[h * kD] = __uint_as_float(oa[h]) * linv[h];
+            dst[(h + 32) * kD] = __uint_as_float(ob[h]) * linv[h + 32];
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarOEmpty + kb));
+      named_bar_sync(1, kSoftmaxThreads);
+    }
+    if (aborted && t128 == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
+  }
+
+  // ---------------- teardown
+  grid_dep_launch();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ combine kernel
+
+__device__ __forceinline__ int cta_of_tile(long long t, long long W, long long G) {
+  // largest g with floor(g*W/G) <= t
+  return static_cast<int>(((t + 1) * G + W - 1) / W - 1);
+}
+
+constexpr int kCombineThreads = 256;
+constexpr int kCombineHeadsPerCta = 8;
+
+__global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
+  grid_dep_wait();
+  __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
+  const int b = blockIdx.x, hg = blockIdx.y;
+  const int cap = p.max_pages * kPage;
+  int before = 0, total = 0;
+  for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
+    bool dummy = false;
+    const int T = tiles_of(clamp_len(p.seq_lens[i], cap, dummy));
+    total += T;
+    before += (i < b) ? T : 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red_b[threadIdx.x >> 5] = before;
+    red_t[threadIdx.x >> 5] = total;
+  }
+  __syncthreads();
+  before = 0;
+  total = 0;
+  for (int w = 0; w < kCombineThreads / 32; ++w) {
+    before += red_b[w];
+    total += red_t[w];
+  }
+  bool dummy = false;
+  const int Tb = tiles_of(clamp_len(p.seq_lens[b], cap, dummy));
+  if (Tb == 0) return;
+  const int g0 = cta_of_tile(before, total, p.num_ctas);
+  const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
+  if (g0 == g1) return;  // written whole by the decode kernel
+  const int d = threadIdx.x;
+  for (int hh = 0; hh < kCombineHeadsPerCta; ++hh) {
+    const int h = hg * kCombineHeadsPerCta + hh;
+    float M = -INFINITY;
+    for (int g = g0; g <= g1; ++g) M = fmaxf(M, p.part_lse[static_cast<size_t>(b + g) * kH + h]);
+    float sum = 0.f, acc = 0.f;
+    for (int g = g0; g <= g1; ++g) {
+      const size_t slot = static_cast<size_t>(b + g);
+      const float w = expf(p.part_lse[slot * kH + h] - M);
+      sum += w;
+      acc = fmaf(w, p.part_o[(slot * kH + h) * kD + d], acc);
+    }
+    p.out[(static_cast<size_t>(b) * kH + h) * kD + d] = __float2bfloat16_rn(acc / sum);
+    if (d == 0 && p.lse != nullptr) p.lse[b * kH + h] = M + logf(sum);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr uint64_t kWsHeader = 256;
+
+static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+static uint64_t partial_o_offset() { return kWsHeader; }
+static uint64_t partial_lse_offset(int num_partials) {
+  return align_up(kWsHeader + static_cast<uint64_t>(num_partials) * kH * kD * 4, 256);
+}
+static uint64_t workspace_bytes_for(int num_partials) {
+  return align_up(partial_lse_offset(num_partials) + static_cast<uint64_t>(num_partials) * kH * 4, 256);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static mfa_status check_problem(const mfa_problem* pr) {
+  if (pr == nullptr) return MFA_ERR_INVALID_ARG;
+  if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
+  if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;
+  if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
+  if (pr->num_q_heads != kH || pr->head_dim != kD || pr->page_size != kPage) return MFA_ERR_UNSUPPORTED;
+  if (pr->kv_dtype != MFA_KV_BF16) return MFA_ERR_UNSUPPORTED;  // e4m3 path not in this build yet
+  if (static_cast<long long>(pr->max_pages_per_seq) * kPage > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
+  if (static_cast<long long>(pr->batch) * kH > INT_MAX) return MFA_ERR_INVALID_ARG;
+  return MFA_OK;
+}
+
+static mfa_status check_plan(const mfa_plan* pl, const mfa_problem* pr) {
+  if (pl == nullptr) return MFA_ERR_INVALID_ARG;
+  if (pl->batch != pr->batch || pl->kv_dtype != pr->kv_dtype) return MFA_ERR_INVALID_ARG;
+  if (pl->num_ctas < 1 || pl->num_partials != pr->batch + pl->num_ctas - 1) return MFA_ERR_INVALID_ARG;
+  if (pl->workspace_bytes != workspace_bytes_for(pl->num_partials)) return MFA_ERR_INVALID_ARG;
+  return MFA_OK;
+}
+
+static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const void* q, const void* k,
+                              const void* v) {
+  auto enc = encode_fn();
+  if (enc == nullptr) return MFA_ERR_CUDA;
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr->batch) * kH};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MFA_ERR_CUDA;
+  }
+  const void* pools[2] = {k, v};
+  CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
+  for (int i = 0; i < 2; ++i) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
+                          static_cast<cuuint64_t>(pr->num_blocks)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(kD) * 2 * kPage};
+    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MFA_ERR_CUDA;
+  }
+  return MFA_OK;
+}
+
+static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, const void* workspace,
+                                 const int32_t* seq_lens, void* out, float* lse, cudaStream_t stream,
+                                 bool dependent) {
+  CombineParams cp;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  cp.part_o = reinterpret_cast<const float*>(ws + partial_o_offset());
+  cp.part_lse = reinterpret_cast<const float*>(ws + partial_lse_offset(pl->num_partials));
+  cp.seq_lens = seq_lens;
+  cp.out = static_cast<__nv_bfloat16*>(out);
+  cp.lse = lse;
+  cp.batch = pr->batch;
+  cp.max_pages = pr->max_pages_per_seq;
+  cp.num_ctas = pl->num_ctas;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH / kCombineHeadsPerCta, 1);
+  cfg.blockDim = dim3(kCombineThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, mfa_combine_kernel, cp) != cudaSuccess) return MFA_ERR_CUDA;
+  return MFA_OK;
+}
+
+}  // namespace mfa
+
+using namespace mfa;
+
+extern "C" {
+
+int32_t mfa_abi_version(void) { return MFA_ABI_VERSION; }
+
+const char* mfa_status_string(mfa_status s) {
+  switch (s) {
+    case MFA_OK: return "ok";
+    case MFA_ERR_INVALID_ARG: return "invalid argument";
+    case MFA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MFA_ERR_WORKSPACE: return "workspace too small";
+    case MFA_ERR_CUDA: return "CUDA error";
+    case MFA_ERR_DEVICE_CHECK: return "device status word is nonzero";
+  }
+  return "unknown status";
+}
+
+mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, int32_t max_seq_len,
+                           int32_t num_sms, int32_t force_ctas, uint32_t flags, mfa_plan* plan) {
+  const mfa_status st = check_problem(pr);
+  if (st != MFA_OK) return st;
+  if (plan == nullptr || force_ctas < 0) return MFA_ERR_INVALID_ARG;
+  const long long cap = static_cast<long long>(pr->max_pages_per_seq) * kPage;
+  long long W = 0;
+  if (host_seq_lens != nullptr) {
+    for (int b = 0; b < pr->batch; ++b) {
+      if (host_seq_lens[b] < 0 || host_seq_lens[b] > cap) return MFA_ERR_INVALID_ARG;
+      W += (host_seq_lens[b] + kTile - 1) / kTile;
+    }
+  } else {
+    if (max_seq_len < 0 || max_seq_len > cap) return MFA_ERR_INVALID_ARG;
+    W = static_cast<long long>(pr->batch) * ((max_seq_len + kTile - 1) / kTile);
+  }
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MFA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MFA_ERR_CUDA;
+  }
+  long long G;
+  if (force_ctas > 0) {
+    G = force_ctas;
+  } else {
+    G = W < num_sms ? W : num_sms;
+    if (G < 1) G = 1;
+  }
+  const long long min_ctas = (W + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+  if (G < min_ctas) {
+    if (force_ctas > 0) return MFA_ERR_INVALID_ARG;
+    G = min_ctas;
+  }
+  if (G > INT_MAX / 2 || static_cast<long long>(pr->batch) + G - 1 > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
+  std::memset(plan, 0, sizeof(*plan));
+  plan->num_ctas = static_cast<int32_t>(G);
+  plan->tile_tokens = kTile;
+  plan->max_tiles_per_cta = static_cast<int32_t>((W + G - 1) / G);
+  plan->num_partials = static_cast<int32_t>(pr->batch + G - 1);
+  plan->batch = pr->batch;
+  plan->kv_dtype = pr->kv_dtype;
+  plan->flags = flags;
+  plan->num_sms = num_sms;
+  plan->total_tiles = static_cast<uint64_t>(W);
+  plan->workspace_bytes = workspace_bytes_for(plan->num_partials);
+  return MFA_OK;
+}
+
+mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
+                          const void* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
+                          void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
+  mfa_status st = check_problem(pr);
+  if (st != MFA_OK) return st;
+  st = check_plan(plan, pr);
+  if (st != MFA_OK) return st;
+  if (pr->batch == 0) return MFA_OK;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      seq_lens == nullptr || out == nullptr || workspace == nullptr)
+    return MFA_ERR_INVALID_ARG;
+  if (pr->kv_dtype == MFA_KV_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr)) return MFA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      (lse != nullptr && !aligned(lse, 4)))
+    return MFA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return MFA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+  DecodeParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  st = encode_maps(prm, pr, q, k_cache, v_cache);
+  if (st != MFA_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  prm.k_scale = k_scale;
+  prm.v_scale = v_scale;
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.lse = lse;
+  prm.part_o = reinterpret_cast<float*>(ws + partial_o_offset());
+  prm.part_lse = reinterpret_cast<float*>(ws + partial_lse_offset(plan->num_partials));
+  prm.status = reinterpret_cast<unsigned int*>(ws);
+  prm.batch = pr->batch;
+  prm.max_pages = pr->max_pages_per_seq;
+  prm.num_blocks = pr->num_blocks;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
+
+  const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
+  if (check && cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MFA_ERR_CUDA;
+  if (cudaFuncSetAttribute(mfa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return MFA_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  if (cudaLaunchKernelEx(&cfg, mfa_decode_kernel, prm) != cudaSuccess) return MFA_ERR_CUDA;
+  if (plan->num_ctas > 1 && (plan->flags & MFA_PLAN_NO_COMBINE) == 0) {
+    st = launch_combine(plan, pr, workspace, seq_lens, out, lse, stream, true);
+    if (st != MFA_OK) return st;
+  }
+  if (check) {
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MFA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MFA_ERR_CUDA;
+    if (word != 0) return MFA_ERR_DEVICE_CHECK;
+  }
+  return MFA_OK;
+}
+
+mfa_status mfa_combine(const mfa_plan* plan, const mfa_problem* pr, const void* workspace,
+                       uint64_t workspace_bytes, const int32_t* seq_lens, void* out, float* lse,
+                       void* stream_ptr) {
+  mfa_status st = check_problem(pr);
+  if (st != MFA_OK) return st;
+  st = check_plan(plan, pr);
+  if (st != MFA_OK) return st;
+  if (pr->batch == 0) return MFA_OK;
+  if (workspace == nullptr || seq_lens == nullptr || out == nullptr) return MFA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || !aligned(out, 16) || !aligned(seq_lens, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return MFA_ERR_INVALID_ARG;
+  if (workspace_bytes < plan->workspace_bytes) return MFA_ERR_WORKSPACE;
+  return launch_combine(plan, pr, workspace, seq_lens, out, lse, static_cast<cudaStream_t>(stream_ptr), false);
+}
+
+mfa_status mfa_read_device_status(void* workspace, uint32_t* status_bits, int32_t clear, void* stream_ptr) {
+  if (workspace == nullptr || status_bits == nullptr || !aligned(workspace, 256)) return MFA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MFA_ERR_CUDA;
+  if (clear && cudaMemsetAsync(workspace, 0, 4, stream) != cudaSuccess) return MFA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MFA_ERR_CUDA;
+  *status_bits = word;
+  return MFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+/*
+ * mfa.h -- C ABI of the MFA decode-attention library (libmfa.so), GB300 / sm_103a.
+ *
+ * The operation.  Step-3's Multi-Matrix Factorization Attention (MFA) keeps many
+ * query heads over a factorised QK circuit with one shared key head and one
+ * shared value head (Step-3, paperlayer.ai/abs/2507.19427v1, section 2 "Step-3
+ * Model Card").  Section 5 "Model-System Co-design" prints the arithmetic
+ * intensity (128 FLOP/B with 8-bit KV) and the effective rank (16,384), which
+ * fix H = 64 query heads of width d = 256.  One decode step computes, for every
+ * sequence b of a batch and every head h, over the L_b cached tokens t:
+ *
+ *     s_t        = softmax_scale * dot(q[b,h,:], k_t)
+ *     out[b,h,:] = sum_t exp(s_t) v_t / sum_t exp(s_t)
+ *     lse[b,h]   = ln sum_t exp(s_t)                      (natural log)
+ *
+ * with k_t = K[block_table[b][t / 64]][t % 64][:] (V likewise): a paged KV
+ * cache of 64-token pages.  Section 4 "Cost Analysis for LLM Decoding" states the
+ * cost model that the benchmark reports against: the larger of the compute
+ * time and the KV-memory-access time.
+ *
+ * The work is split along the tokens (split-KV, "flash decoding"): a persistent
+ * grid of CTAs divides all 128-token tiles of the batch evenly; each CTA writes
+ * either the finished output of a sequence it covers whole, or a partial
+ * result (normalised O and lse over its token range) that mfa_combine() merges
+ * with the log-sum-exp rule.  The pages give no interface; this one is the
+ * plainest carrier of the problem statement above.
+ *
+ * Conventions for every call:
+ *   - All device pointers are caller-owned (allocate them with any allocator);
+ *     the library allocates no device memory and keeps no state between calls.
+ *   - All tensors are dense, row-major, contiguous, with the strides implied by
+ *     their shapes below.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) on the current device; nothing synchronises
+ *     unless MFA_PLAN_CHECK is set.
+ *   - Host-detectable errors return a status before anything is enqueued.
+ *     Launch failures return MFA_ERR_CUDA.  Bad data that only the device sees
+ *     (a block id outside the pool, a length outside [0, max_pages*64]) never
+ *     faults: the affected loads read zeros, and a bit is set in the device
+ *     status word of the workspace (see mfa_read_device_status).
+ *   - A sequence with L = 0 yields out = 0 and lse = -inf.
+ */
+#ifndef MFA_H_
+#define MFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MFA_ABI_VERSION 1
+
+typedef enum mfa_status {
+    MFA_OK = 0,
+    MFA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, inconsistent plan */
+    MFA_ERR_UNSUPPORTED = 2,   /* a shape this build does not implement (H!=64, d!=256, page!=64) */
+    MFA_ERR_WORKSPACE = 3,     /* workspace smaller than plan->workspace_bytes */
+    MFA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
+    MFA_ERR_DEVICE_CHECK = 5   /* MFA_PLAN_CHECK found a nonzero device status word */
+} mfa_status;
+
+typedef enum mfa_kv_dtype {
+    MFA_KV_BF16 = 0,           /* K/V cache in bf16 */
+    MFA_KV_FP8_E4M3 = 1        /* K/V cache as OCP e4m3 codes, one fp32 scale per token row */
+} mfa_kv_dtype;
+
+/* Device status word bits (set by the kernels, never cleared by them). */
+#define MFA_DEV_TIMEOUT      0x1u  /* a pipeline wait exceeded its time limit; outputs invalid */
+#define MFA_DEV_BAD_BLOCK    0x2u  /* a block_table entry outside [0, num_blocks) was used */
+#define MFA_DEV_BAD_LENGTH   0x4u  /* a seq_lens entry outside [0, max_pages_per_seq*64] (clamped) */
+#define MFA_DEV_SCHEDULE     0x8u  /* device lengths need more tiles per CTA than the plan allows */
+
+/* Plan flags. */
+#define MFA_PLAN_CHECK       0x1u  /* run: clear the status word, then read it back (synchronises) */
+#define MFA_PLAN_NO_COMBINE  0x2u  /* run: launch only the decode kernel; call mfa_combine() yourself */
+
+typedef struct mfa_problem {
+    int32_t batch;             /* B >= 0 sequences, one new query token each */
+    int32_t num_q_heads;       /* H; this build supports 64 */
+    int32_t head_dim;          /* d; this build supports 256 */
+    int32_t page_size;         /* tokens per KV page; this build supports 64 */
+    int32_t max_pages_per_seq; /* columns of block_table (>= 1) */
+    int32_t num_blocks;        /* physical pages in each of the K and V pools (>= 1) */
+    int32_t kv_dtype;          /* mfa_kv_dtype */
+    float softmax_scale;       /* finite, > 0; 1/sqrt(256) = 0.0625 for MFA */
+} mfa_problem;
+
+typedef struct mfa_plan {
+    int32_t num_ctas;          /* decode grid size G (persistent CTAs) */
+    int32_t tile_tokens;       /* tokens per pipeline tile (128) */
+    int32_t max_tiles_per_cta; /* ceil(tiles / G) for the lengths planned with */
+    int32_t num_partials;      /* partial-result slots in the workspace: B + G - 1 */
+    int32_t batch;             /* copy of problem->batch (checked by run) */
+    int32_t kv_dtype;          /* copy of problem->kv_dtype (checked by run) */
+    uint32_t flags;            /* MFA_PLAN_* */
+    int32_t num_sms;           /* SM count the plan was made for */
+    uint64_t total_tiles;      /* 128-token tiles of the batch as planned */
+    uint64_t workspace_bytes;  /* device bytes the caller must pass to run/combine */
+} mfa_plan;
+
+/*
+ * Choose the split of the work (the "plan step": number of CTAs and therefore
+ * the number of KV splits per sequence) from the batch size and the context
+ * lengths.  Host only: no device memory is touched.
+ *   problem        : shapes and dtype (validated here).
+ *   host_seq_lens  : host int32 [B] lengths, or NULL to plan for B sequences of
+ *                    max_seq_len tokens (an upper bound: any lengths up to it run).
+ *   max_seq_len    : used when host_seq_lens is NULL; 0 <= max_seq_len <= max_pages*64.
+ *   num_sms        : SMs to plan for; 0 queries the current device.
+ *   force_ctas     : 0 = automatic (one CTA per SM, fewer when there are fewer
+ *                    tiles); > 0 forces the grid size (tests, tuning).
+ *   flags          : MFA_PLAN_* copied into the plan.
+ *   plan (out)     : filled on MFA_OK.
+ * The work is 128-token tiles; CTA g of G takes tiles [floor(g*W/G), floor((g+1)*W/G))
+ * of the batch's W tiles laid end to end, so every CTA gets the same share to
+ * within one tile whatever the length mix.  A sequence is split once per CTA
+ * boundary that falls inside it.
+ */
+mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_lens,
+                           int32_t max_seq_len, int32_t num_sms, int32_t force_ctas,
+                           uint32_t flags, mfa_plan* plan);
+
+/*
+ * Enqueue one decode step (decode kernel, then the combine kernel when the plan
+ * has more than one CTA and MFA_PLAN_NO_COMBINE is not set).
+ *   q            : device bf16 [B, 64, 256], 16-byte aligned.
+ *   k_cache      : device [num_blocks, 64, 256], bf16 or e4m3 codes (uint8), 16-byte aligned.
+ *   v_cache      : same layout as k_cache.
+ *   k_scale      : device fp32 [num_blocks, 64] (e4m3 only; NULL for bf16): value = code * scale.
+ *   v_scale      : same for V.
+ *   block_table  : device int32 [B, max_pages_per_seq]; entries past ceil(L_b/64) are never read.
+ *   seq_lens     : device int32 [B].
+ *   out          : device bf16 [B, 64, 256] (round to nearest even of the fp32 result).
+ *   lse          : device fp32 [B, 64] natural-log log-sum-exp of the scaled scores, or NULL.
+ *   workspace    : device buffer of >= plan->workspace_bytes bytes, 256-byte aligned.
+ *                  Layout: bytes [0,256) header (uint32 status word at offset 0);
+ *                  then partial O fp32 [num_partials, 64, 256]; then partial lse fp32
+ *                  [num_partials, 64].  The partial of sequence b from CTA g sits in
+ *                  slot b + g.  Contents between calls are scratch, except the status word.
+ *   stream       : cudaStream_t.
+ * Unused slots of a sequence's last page and unused pool pages may hold any bits
+ * (NaN included); they never reach the output.
+ */
+mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* problem,
+                          const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                          void* stream);
+
+/*
+ * Enqueue the log-sum-exp merge of the partial results in `workspace` (the split
+ * combine): for every sequence covered by more than one CTA,
+ *     lse* = M + ln sum_s exp(lse_s - M),  M = max_s lse_s,
+ *     out  = sum_s exp(lse_s - lse*) O_s          (O_s normalised partials)
+ * and writes out (bf16) and lse (fp32, if non-NULL).  Sequences covered by one
+ * CTA, and empty ones, were written by the decode kernel and are left alone.
+ * Arguments as for mfa_decode_run; seq_lens must equal the ones the decode used.
+ */
+mfa_status mfa_combine(const mfa_plan* plan, const mfa_problem* problem,
+                       const void* workspace, uint64_t workspace_bytes,
+                       const int32_t* seq_lens, void* out, float* lse, void* stream);
+
+/*
+ * Read the device status word of `workspace` into *status_bits (MFA_DEV_* bits),
+ * optionally clearing it; synchronises `stream`.
+ */
+mfa_status mfa_read_device_status(void* workspace, uint32_t* status_bits, int32_t clear,
+                                  void* stream);
+
+/* Static description of a status code. */
+const char* mfa_status_string(mfa_status status);
+
+/* MFA_ABI_VERSION of the loaded library. */
+int32_t mfa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MFA_H_ */

@@ -32,7 +32,8 @@
  *     O    = sum_s exp(lse_s - lse*) O_s
  * (all partials -inf -> O = 0, lse = -inf).
  *
- * Threads split the independent (b, h) pairs; no arithmetic is reordered.
+ * Threads split independent (sequence, group of heads) units; each head's
+ * arithmetic runs in the order written above.
  */
 #include <math.h>
 #include <pthread.h>
@@ -79,65 +80,110 @@ typedef struct {
     int tid;
 } worker_t;
 
-/* Element i of the key (or value) row of token t of sequence b, as a double. */
-static double kv_elem(const job_t *J, int which_v, int b, int t, int i) {
+/* Head groups: the heads of a sequence are split into groups of HEAD_GROUP so
+ * that the threads have independent work; a group decodes each key and value row
+ * once and uses it for its heads. */
+#define HEAD_GROUP 8
+
+/* Row (key or value) of token t of sequence b, decoded to doubles. */
+static void kv_row(const job_t *J, int which_v, int b, int t, double *dst) {
     int32_t blk = J->block_table[(size_t)b * J->max_pages + t / J->page];
     size_t row = (size_t)blk * J->page + (size_t)(t % J->page);
     if (J->kv_fp8) {
         const uint8_t *pool = (const uint8_t *)(which_v ? J->v_cache : J->k_cache);
         const float *sc = which_v ? J->v_scale : J->k_scale;
-        return mfa_oracle_e4m3_to_double(pool[row * J->d + i]) * (double)sc[row];
+        for (int i = 0; i < J->d; ++i)
+            dst[i] = mfa_oracle_e4m3_to_double(pool[row * J->d + i]) * (double)sc[row];
     } else {
         const uint16_t *pool = (const uint16_t *)(which_v ? J->v_cache : J->k_cache);
-        return bf16_to_double(pool[row * J->d + i]);
+        for (int i = 0; i < J->d; ++i) dst[i] = bf16_to_double(pool[row * J->d + i]);
     }
 }
 
-static void one_head(const job_t *J, int b, int h, double *s) {
+typedef struct {
+    double *s;    /* [HEAD_GROUP][maxlen] scores */
+    double *q;    /* [HEAD_GROUP][d] */
+    double *row;  /* [d] */
+} scratch_t;
+
+/* Heads [h0, h1) of sequence b over the token range of b. */
+static void head_group(const job_t *J, int b, int h0, int h1, size_t maxlen, scratch_t *W) {
     int L = J->seq_lens[b];
     int t0 = J->t_begin ? J->t_begin[b] : 0;
     int t1 = J->t_end ? J->t_end[b] : L;
-    double *o = J->out + ((size_t)b * J->H + h) * J->d;
-    const uint16_t *qh = J->q + ((size_t)b * J->H + h) * J->d;
-    for (int i = 0; i < J->d; ++i) o[i] = 0.0;
-    if (t1 <= t0) {
-        J->lse[(size_t)b * J->H + h] = -INFINITY;
-        return;
+    int d = J->d;
+    for (int h = h0; h < h1; ++h) {
+        double *o = J->out + ((size_t)b * J->H + h) * d;
+        const uint16_t *qh = J->q + ((size_t)b * J->H + h) * d;
+        for (int i = 0; i < d; ++i) {
+            o[i] = 0.0;
+            W->q[(size_t)(h - h0) * d + i] = bf16_to_double(qh[i]);
+        }
+        if (t1 <= t0) J->lse[(size_t)b * J->H + h] = -INFINITY;
     }
-    /* pass 1: scores and their maximum */
-    double m = -INFINITY;
+    if (t1 <= t0) return;
+    /* pass 1: scores s_t = scale * q.k_t and their maximum per head */
+    double m[HEAD_GROUP];
+    for (int h = h0; h < h1; ++h) m[h - h0] = -INFINITY;
     for (int t = t0; t < t1; ++t) {
-        double acc = 0.0;
-        for (int i = 0; i < J->d; ++i) acc += bf16_to_double(qh[i]) * kv_elem(J, 0, b, t, i);
-        s[t - t0] = J->scale * acc;
-        if (s[t - t0] > m) m = s[t - t0];
+        kv_row(J, 0, b, t, W->row);
+        for (int h = h0; h < h1; ++h) {
+            const double *qv = W->q + (size_t)(h - h0) * d;
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += qv[i] * W->row[i];
+            double st = J->scale * acc;
+            W->s[(size_t)(h - h0) * maxlen + (size_t)(t - t0)] = st;
+            if (st > m[h - h0]) m[h - h0] = st;
+        }
     }
-    /* pass 2: exponentials, their sum, and the weighted sum of values */
-    double l = 0.0;
+    /* pass 2: p_t = exp(s_t - m), l = sum p_t, O = sum p_t v_t / l, lse = m + ln l */
+    double l[HEAD_GROUP];
+    for (int h = h0; h < h1; ++h) l[h - h0] = 0.0;
     for (int t = t0; t < t1; ++t) {
-        double p = exp(s[t - t0] - m);
-        l += p;
-        for (int i = 0; i < J->d; ++i) o[i] += p * kv_elem(J, 1, b, t, i);
+        kv_row(J, 1, b, t, W->row);
+        for (int h = h0; h < h1; ++h) {
+            double p = exp(W->s[(size_t)(h - h0) * maxlen + (size_t)(t - t0)] - m[h - h0]);
+            l[h - h0] += p;
+            double *o = J->out + ((size_t)b * J->H + h) * d;
+            for (int i = 0; i < d; ++i) o[i] += p * W->row[i];
+        }
     }
-    for (int i = 0; i < J->d; ++i) o[i] /= l;
-    J->lse[(size_t)b * J->H + h] = m + log(l);
+    for (int h = h0; h < h1; ++h) {
+        double *o = J->out + ((size_t)b * J->H + h) * d;
+        for (int i = 0; i < d; ++i) o[i] /= l[h - h0];
+        J->lse[(size_t)b * J->H + h] = m[h - h0] + log(l[h - h0]);
+    }
 }
 
 static void *worker(void *arg) {
-    const worker_t *W = (const worker_t *)arg;
-    const job_t *J = W->job;
-    int maxlen = 1;
+    const worker_t *Wk = (const worker_t *)arg;
+    const job_t *J = Wk->job;
+    size_t maxlen = 1;
     for (int b = 0; b < J->B; ++b) {
         int t0 = J->t_begin ? J->t_begin[b] : 0;
         int t1 = J->t_end ? J->t_end[b] : J->seq_lens[b];
-        if (t1 - t0 > maxlen) maxlen = t1 - t0;
+        if (t1 - t0 > (int)maxlen) maxlen = (size_t)(t1 - t0);
     }
-    double *s = (double *)malloc(sizeof(double) * (size_t)maxlen);
-    if (!s) return (void *)1;
-    long npairs = (long)J->B * J->H;
-    for (long pidx = W->tid; pidx < npairs; pidx += J->nthreads)
-        one_head(J, (int)(pidx / J->H), (int)(pidx % J->H), s);
-    free(s);
+    scratch_t W;
+    W.s = (double *)malloc(sizeof(double) * maxlen * HEAD_GROUP);
+    W.q = (double *)malloc(sizeof(double) * (size_t)J->d * HEAD_GROUP);
+    W.row = (double *)malloc(sizeof(double) * (size_t)J->d);
+    if (!W.s || !W.q || !W.row) {
+        free(W.s);
+        free(W.q);
+        free(W.row);
+        return (void *)1;
+    }
+    int groups = (J->H + HEAD_GROUP - 1) / HEAD_GROUP;
+    long nunits = (long)J->B * groups;
+    for (long u = Wk->tid; u < nunits; u += J->nthreads) {
+        int b = (int)(u / groups), g = (int)(u % groups);
+        int h0 = g * HEAD_GROUP, h1 = h0 + HEAD_GROUP < J->H ? h0 + HEAD_GROUP : J->H;
+        head_group(J, b, h0, h1, maxlen, &W);
+    }
+    free(W.s);
+    free(W.q);
+    free(W.row);
     return NULL;
 }
 
@@ -171,9 +217,9 @@ int mfa_oracle_decode(int B, int H, int d, int page, int max_pages, int kv_fp8,
     job_t J = {B, H, d, page, max_pages, kv_fp8, q, k_cache, v_cache, k_scale, v_scale,
                block_table, seq_lens, t_begin, t_end, scale, out, lse, 0};
     if (nthreads <= 0) nthreads = mfa_oracle_num_cpus();
-    long npairs = (long)B * H;
-    if (npairs == 0) return 0;
-    if (nthreads > npairs) nthreads = (int)npairs;
+    long nunits = (long)B * ((H + HEAD_GROUP - 1) / HEAD_GROUP);
+    if (nunits == 0) return 0;
+    if (nthreads > nunits) nthreads = (int)nunits;
     J.nthreads = nthreads;
     worker_t *ws = (worker_t *)calloc((size_t)nthreads, sizeof(worker_t));
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));

@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI (no GPU needed): exports, validation, planning."""
+import ctypes
+import re
+import os
+
+import pytest
+
+import decode_attention_02_gb300 as mfa
+from decode_attention_02_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return mfa.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "mfa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mfa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(mfa.EXPORTED_SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    assert lib.mfa_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert mfa.status_string(s) not in ("", "unknown status")
+    assert mfa.status_string(99) == "unknown status"
+
+
+def problem(**kw):
+    args = dict(batch=4, max_pages_per_seq=8, num_blocks=32)
+    args.update(kw)
+    return mfa.make_problem(**args)
+
+
+def test_plan_one_cta_per_sm_when_enough_tiles(lib):
+    p = problem(batch=32, max_pages_per_seq=64, num_blocks=2048)
+    plan = mfa.mfa_decode_plan(p, [4096] * 32, num_sms=152)
+    assert plan.num_ctas == 152
+    assert plan.total_tiles == 32 * 32
+    assert plan.max_tiles_per_cta == 7          # ceil(1024 / 152)
+    assert plan.num_partials == 32 + 152 - 1
+    o_off, l_off = mfa.workspace_layout(plan)
+    assert plan.workspace_bytes >= l_off + plan.num_partials * 64 * 4
+    assert o_off == 256 and l_off % 256 == 0 and plan.workspace_bytes % 256 == 0
+
+
+def test_plan_fewer_ctas_than_sms_for_short_batches(lib):
+    plan = mfa.mfa_decode_plan(problem(batch=1), [512], num_sms=152)
+    assert plan.num_ctas == 4 and plan.max_tiles_per_cta == 1
+    plan = mfa.mfa_decode_plan(problem(batch=2), [0, 0], num_sms=152)
+    assert plan.num_ctas == 1
+
+
+def test_plan_without_host_lengths_uses_the_bound(lib):
+    plan = mfa.mfa_decode_plan(problem(batch=4, max_pages_per_seq=8), None, max_seq_len=300, num_sms=152)
+    assert plan.total_tiles == 4 * 3
+
+
+def test_plan_caps_tiles_per_cta(lib):
+    p = problem(batch=4, max_pages_per_seq=2048, num_blocks=8192)
+    plan = mfa.mfa_decode_plan(p, [131072] * 4, num_sms=2)
+    assert plan.max_tiles_per_cta <= 128 and plan.num_ctas == 32
+    with pytest.raises(mfa.MfaError):
+        mfa.mfa_decode_plan(p, [131072] * 4, num_sms=2, force_ctas=2)
+
+
+def test_plan_rejects_bad_input(lib):
+    with pytest.raises(mfa.MfaError) as e:
+        mfa.mfa_decode_plan(problem(), [1, 2, 3, 10 ** 6], num_sms=8)
+    assert e.value.status == mfa.MFA_ERR_INVALID_ARG
+    for bad, code in [(dict(num_q_heads=32), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(head_dim=128), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(page_size=16), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(softmax_scale=0.0), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(softmax_scale=float("nan")), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(kv_dtype=7), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(batch=-1), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(num_blocks=0), mfa.MFA_ERR_INVALID_ARG)]:
+        with pytest.raises(mfa.MfaError) as e:
+            mfa.mfa_decode_plan(problem(**bad), None, max_seq_len=64, num_sms=8)
+        assert e.value.status == code, bad
+
+
+def _run_raw(lib, plan, prob, ptrs, ws_bytes):
+    P = ctypes.c_void_p
+    return lib.mfa_decode_run(ctypes.byref(plan), ctypes.byref(prob), *[P(x) if x else None for x in ptrs],
+                              ctypes.c_uint64(ws_bytes), None)
+
+
+def test_run_validates_before_touching_the_device(lib):
+    prob = problem()
+    plan = mfa.mfa_decode_plan(prob, [10, 20, 30, 40], num_sms=8)
+    good = [0x1000, 0x2000, 0x3000, None, None, 0x4000, 0x5000, 0x6000, 0x7000, 0x10000]
+    # q, k, v, k_scale, v_scale, table, lens, out, lse, workspace
+    bad_null = list(good); bad_null[0] = None
+    assert _run_raw(lib, plan, prob, bad_null, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+    bad_align = list(good); bad_align[1] = 0x2008
+    assert _run_raw(lib, plan, prob, bad_align, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+    bad_ws = list(good); bad_ws[9] = 0x10010
+    assert _run_raw(lib, plan, prob, bad_ws, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+    assert _run_raw(lib, plan, prob, good, plan.workspace_bytes - 1) == mfa.MFA_ERR_WORKSPACE
+    other = problem(batch=5)
+    assert _run_raw(lib, plan, other, good, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG

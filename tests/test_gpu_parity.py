@@ -1,0 +1,220 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Limits (stated for the MFA decode step): bf16 KV max-abs <= 1e-2 and
+relative-L2 <= 5e-3 on the output; block-table and length indexing exact
+(NaN-poisoned unused slots and pages must not reach the output).  lse is
+compared to 2e-3 absolute.
+"""
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_02_gb300 as mfa
+import oracle
+from decode_attention_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX_ABS, BF16_REL_L2 = 1e-2, 5e-3
+LSE_ABS = 2e-3
+
+
+def to_dev(case, dev="cuda"):
+    return dict(q=case.q.to(dev), k_cache=case.k_cache.to(dev), v_cache=case.v_cache.to(dev),
+                block_table=case.block_table.to(dev), seq_lens=case.seq_lens.to(dev),
+                k_scale=None if case.k_scale is None else case.k_scale.to(dev),
+                v_scale=None if case.v_scale is None else case.v_scale.to(dev))
+
+
+def gpu_decode(case, force_ctas=0, flags=mfa.MFA_PLAN_CHECK, stream=None):
+    t = to_dev(case)
+    kv = mfa.MFA_KV_FP8_E4M3 if case.workload.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    dec = mfa.Decoder(case.q.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv,
+                      softmax_scale=case.workload.scale(), host_seq_lens=case.seq_lens.tolist(),
+                      force_ctas=force_ctas, flags=flags)
+    out, lse = dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                   k_scale=t["k_scale"], v_scale=t["v_scale"], stream=stream)
+    torch.cuda.synchronize()
+    return out, lse, dec
+
+
+def check_parity(case, out, lse, max_abs=BF16_MAX_ABS, rel_l2=BF16_REL_L2, ref=None):
+    ref_o, ref_lse = oracle.decode(case) if ref is None else ref
+    got = out.float().cpu().double().numpy()
+    assert np.all(np.isfinite(got)), "non-finite output"
+    err = np.abs(got - ref_o)
+    denom = np.linalg.norm(ref_o)
+    rel = np.linalg.norm(got - ref_o) / denom if denom > 0 else np.linalg.norm(got - ref_o)
+    assert err.max(initial=0.0) <= max_abs, f"max-abs {err.max():.3e}"
+    assert rel <= rel_l2, f"rel-L2 {rel:.3e}"
+    g_lse = lse.cpu().double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(g_lse), np.isneginf(ref_lse))
+    if fin.any():
+        assert np.abs(g_lse[fin] - ref_lse[fin]).max() <= LSE_ABS, "lse mismatch"
+    return err.max(initial=0.0), rel
+
+
+def test_tiny_workload_matches_oracle():
+    case = inputs.generate(inputs.WORKLOADS["tiny_b1_l512_bf16"])
+    out, lse, _ = gpu_decode(case)
+    check_parity(case, out, lse)
+
+
+RAGGED_LENS = [1, 63, 64, 65, 127, 128, 129, 200, 0, 517, 1000, 300]
+
+
+@pytest.mark.parametrize("force_ctas", [0, 1, 2, 3, 7, 16, 64])
+def test_ragged_lengths_any_split(force_ctas):
+    case = inputs.small("ragged", len(RAGGED_LENS), RAGGED_LENS, seed=7, extra_blocks=3)
+    out, lse, _ = gpu_decode(case, force_ctas=force_ctas)
+    check_parity(case, out, lse)
+
+
+def test_spiked_keys():
+    case = inputs.small("spike", 6, [1024, 2000, 1500, 777, 4096, 3000], seed=8, k_spike_frac=0.01)
+    out, lse, _ = gpu_decode(case)
+    check_parity(case, out, lse)
+
+
+def test_length_one_returns_v0_bit_exactly():
+    case = inputs.small("l1", 3, [1, 1, 1], seed=9)
+    out, lse, _ = gpu_decode(case)
+    for b in range(3):
+        blk = int(case.block_table[b, 0])
+        v0 = case.v_cache[blk, 0]
+        assert torch.equal(out[b].cpu().view(torch.int16), v0.expand(64, -1).view(torch.int16))
+
+
+def test_block_permutation_is_bitwise_invariant():
+    case = inputs.small("perm", 5, [100, 640, 1, 333, 2049], seed=10, extra_blocks=4)
+    out1, lse1, _ = gpu_decode(case, force_ctas=5)
+    nb = case.num_blocks
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(nb))
+    k2 = torch.empty_like(case.k_cache); k2[perm] = case.k_cache
+    v2 = torch.empty_like(case.v_cache); v2[perm] = case.v_cache
+    table = case.block_table.clone()
+    used = table >= 0
+    table[used] = perm[table[used].long()].to(torch.int32)
+    case2 = inputs.Case(case.workload, case.q, k2, v2, None, None, table, case.seq_lens)
+    out2, lse2, _ = gpu_decode(case2, force_ctas=5)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_constant_keys_give_mean_of_values():
+    case = inputs.small("constk", 2, [300, 1000], seed=11)
+    for b in range(2):
+        row = case.k_cache[int(case.block_table[b, 0]), 0].clone()
+        L = int(case.seq_lens[b])
+        for t in range(L):
+            case.k_cache[int(case.block_table[b, t // 64]), t % 64] = row
+    out, lse, _ = gpu_decode(case, force_ctas=3)
+    for b in range(2):
+        L = int(case.seq_lens[b])
+        t = np.arange(L)
+        V = case.v_cache[case.block_table[b, t // 64].long(), torch.from_numpy(t % 64)].double()
+        mean = V.mean(dim=0)
+        assert (out[b].cpu().double() - mean[None]).abs().max() <= BF16_MAX_ABS
+
+
+def test_empty_sequences_give_zero_and_minus_inf():
+    case = inputs.small("empty", 4, [0, 70, 0, 0], seed=12)
+    for fc in (0, 1, 3):
+        out, lse, _ = gpu_decode(case, force_ctas=fc)
+        assert torch.all(out[[0, 2, 3]] == 0)
+        assert torch.all(torch.isneginf(lse[[0, 2, 3]]))
+        check_parity(case, out, lse)
+
+
+def test_all_empty_batch():
+    case = inputs.small("allempty", 3, [0, 0, 0], seed=13)
+    out, lse, _ = gpu_decode(case)
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_separate_combine_matches_fused_run():
+    case = inputs.small("sep", 4, [900, 1, 2500, 64], seed=14)
+    out1, lse1, _ = gpu_decode(case, force_ctas=9)
+    t = to_dev(case)
+    dec = mfa.Decoder(4, case.max_pages, case.num_blocks, host_seq_lens=case.seq_lens.tolist(), force_ctas=9,
+                      flags=mfa.MFA_PLAN_NO_COMBINE)
+    out2 = torch.empty_like(out1)
+    lse2 = torch.empty_like(lse1)
+    dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"], out=out2, lse=lse2)
+    mfa.mfa_combine(dec.plan, dec.problem, dec.workspace, t["seq_lens"], out2, lse2)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse1, lse2)
+
+
+def test_combine_kernel_against_oracle_merge():
+    """mfa_combine alone on random partials laid out as include/mfa.h documents."""
+    lens = [129, 1000, 5, 640]
+    B, G = len(lens), 6
+    prob = mfa.make_problem(B, 16, 64)
+    plan = mfa.mfa_decode_plan(prob, lens, force_ctas=G, num_sms=152)
+    ws = torch.zeros(int(plan.workspace_bytes), dtype=torch.uint8, device="cuda")
+    o_off, l_off = mfa.workspace_layout(plan)
+    S = plan.num_partials
+    g = torch.Generator().manual_seed(0)
+    po = torch.randn(S, 64, 256, generator=g)
+    pl = torch.randn(S, 64, generator=g) * 3
+    ws[o_off:o_off + po.numel() * 4] = po.view(torch.uint8).reshape(-1).cuda()
+    ws[l_off:l_off + pl.numel() * 4] = pl.view(torch.uint8).reshape(-1).cuda()
+    out = torch.zeros(B, 64, 256, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(B, 64, device="cuda")
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    mfa.mfa_combine(plan, prob, ws, seq, out, lse)
+    torch.cuda.synchronize()
+    tiles = [(L + 127) // 128 for L in lens]
+    W = sum(tiles)
+    start = lambda gg: (gg * W) // G
+    before = 0
+    for b in range(B):
+        covering = [gg for gg in range(G) if start(gg) < before + tiles[b] and start(gg + 1) > before]
+        before += tiles[b]
+        if len(covering) < 2:
+            continue   # written by the decode kernel, not by combine
+        slots = [b + gg for gg in covering]
+        ro, rl = oracle.combine(po[slots].double().numpy(), pl[slots].double().numpy())
+        assert np.abs(out[b].cpu().double().numpy() - ro).max() <= 1e-2 + 1e-2 * np.abs(ro).max()
+        assert np.abs(lse[b].cpu().double().numpy() - rl).max() <= 1e-4
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    case = inputs.small("badblk", 2, [100, 200], seed=15)
+    case.block_table[1, 2] = case.num_blocks + 7
+    with pytest.raises(mfa.MfaError) as e:
+        gpu_decode(case)
+    assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
+
+
+def test_length_beyond_table_is_reported():
+    case = inputs.small("badlen", 2, [100, 200], seed=16)
+    t = to_dev(case)
+    dec = mfa.Decoder(2, case.max_pages, case.num_blocks, max_seq_len=case.max_pages * 64,
+                      flags=mfa.MFA_PLAN_CHECK)
+    t["seq_lens"][1] = case.max_pages * 64 + 1
+    with pytest.raises(mfa.MfaError) as e:
+        dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"])
+    assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
+    assert mfa.mfa_read_device_status(dec.workspace) & mfa.MFA_DEV_BAD_LENGTH
+
+
+def test_runs_on_a_side_stream():
+    case = inputs.small("stream", 3, [700, 50, 1300], seed=17)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out, lse, _ = gpu_decode(case, stream=s)
+    check_parity(case, out, lse)
+
+
+@pytest.mark.parametrize("name", ["b32_l4096_bf16", "ragged_b128_l1024_8192_bf16", "long_b4_l131072_bf16"])
+def test_full_size_workload(name):
+    """Full-size workloads in the launch configuration the benchmark times."""
+    case = inputs.generate(inputs.WORKLOADS[name])
+    out, lse, dec = gpu_decode(case)
+    assert dec.plan.num_ctas == min(torch.cuda.get_device_properties(0).multi_processor_count,
+                                    int(dec.plan.total_tiles))
+    check_parity(case, out, lse)

@@ -317,15 +317,16 @@ def test_thread_count_does_not_change_results():
 _MUTANTS = {
     "wrong_slot": ("(size_t)(t % J->page)", "(size_t)((t + 1) % J->page)"),
     "wrong_block": ("t / J->page]", "(t / J->page + 1) % J->max_pages]"),
-    "k_for_v": ("p * kv_elem(J, 1, b, t, i)", "p * kv_elem(J, 0, b, t, i)"),
-    "sign_flip": ("exp(s[t - t0] - m)", "exp(m - s[t - t0])"),
-    "no_scale": ("s[t - t0] = J->scale * acc;", "s[t - t0] = acc;"),
-    "lse_no_log": ("m + log(l)", "m + l"),
-    "no_normalise": ("o[i] /= l;", "o[i] /= 1.0;"),
+    "k_for_v": ("kv_row(J, 1, b, t, W->row);", "kv_row(J, 0, b, t, W->row);"),
+    "sign_flip": ("(t - t0)] - m[h - h0])", "(t - t0)] * -1.0 + m[h - h0])"),
+    "no_scale": ("double st = J->scale * acc;", "double st = acc;"),
+    "lse_no_log": ("m[h - h0] + log(l[h - h0])", "m[h - h0] + l[h - h0]"),
+    "no_normalise": ("o[i] /= l[h - h0];", "o[i] /= 1.0;"),
     "e4m3_bias": ("e - 7)", "e - 8)"),
     "e4m3_subnormal": ("(double)m / 8.0, -6)", "(double)m / 8.0, -7)"),
     "fp8_scale_dropped": ("* (double)sc[row]", "* 1.0"),
-    "head_index": ("((size_t)b * J->H + h) * J->d;\n    for", "((size_t)b * J->H + 0) * J->d;\n    for"),
+    "head_index": ("W->q[(size_t)(h - h0) * d + i] = bf16_to_double(qh[i]);",
+                   "W->q[(size_t)(h - h0) * d + i] = bf16_to_double(qh[i % 8]);"),
 }
 
 
