@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         int tot = 0, ftot = 0;
         const int incl = block_incl_scan(T, scratch, tot) + carry;
         const int excl = incl - T;
-        const int f = (T > 0 && excl < t1 && incl > t0) ? 1 : 0;
+        const int f = (max(t0, excl) < min(t1, incl)) ? 1 : 0;   // non-empty overlap
         const int fidx = nseg + block_incl_scan(f, scratch, ftot) - f;
         if (f) {
           const int lo = max(t0, excl), hi = min(t1, incl);
@@ -765,13 +765,19 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int g0 = cta_of_tile(before, total, p.num_ctas);
   const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
+  // CTAs between g0 and g1 with an empty tile range (grid larger than the work) hold no partial
+  auto empty_cta = [&](int g) {
+    return (static_cast<long long>(g) * total) / p.num_ctas == (static_cast<long long>(g + 1) * total) / p.num_ctas;
+  };
   const int d = threadIdx.x;
   for (int hh = 0; hh < kCombineHeadsPerCta; ++hh) {
     const int h = hg * kCombineHeadsPerCta + hh;
     float M = -INFINITY;
-    for (int g = g0; g <= g1; ++g) M = fmaxf(M, p.part_lse[static_cast<size_t>(b + g) * kH + h]);
+    for (int g = g0; g <= g1; ++g)
+      if (!empty_cta(g)) M = fmaxf(M, p.part_lse[static_cast<size_t>(b + g) * kH + h]);
     float sum = 0.f, acc = 0.f;
     for (int g = g0; g <= g1; ++g) {
+      if (empty_cta(g)) continue;
       const size_t slot = static_cast<size_t>(b + g);
       const float w = expf(p.part_lse[slot * kH + h] - M);
       sum += w;

@@ -172,7 +172,7 @@ def test_combine_kernel_against_oracle_merge():
     start = lambda gg: (gg * W) // G
     before = 0
     for b in range(B):
-        covering = [gg for gg in range(G) if start(gg) < before + tiles[b] and start(gg + 1) > before]
+        covering = [gg for gg in range(G) if max(start(gg), before) < min(start(gg + 1), before + tiles[b])]
         before += tiles[b]
         if len(covering) < 2:
             continue   # written by the decode kernel, not by combine
