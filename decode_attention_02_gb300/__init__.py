@@ -28,6 +28,9 @@ MFA_ERR_DEVICE_CHECK = 5
 MFA_KV_BF16 = 0
 MFA_KV_FP8_E4M3 = 1
 
+MFA_OUT_BF16 = 0
+MFA_OUT_FP32 = 1
+
 MFA_DEV_TIMEOUT = 0x1
 MFA_DEV_BAD_BLOCK = 0x2
 MFA_DEV_BAD_LENGTH = 0x4
@@ -49,7 +52,8 @@ class MfaProblem(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+                ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
+                ("out_dtype", ctypes.c_int32)]
 
 
 class MfaPlan(ctypes.Structure):
@@ -137,9 +141,9 @@ def _stream(stream) -> Optional[int]:
 
 def make_problem(batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
                  softmax_scale: float = HEAD_DIM ** -0.5, num_q_heads: int = NUM_Q_HEADS,
-                 head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE) -> MfaProblem:
+                 head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, out_dtype: int = MFA_OUT_BF16) -> MfaProblem:
     return MfaProblem(batch, num_q_heads, head_dim, page_size, max_pages_per_seq, num_blocks, kv_dtype,
-                      softmax_scale)
+                      softmax_scale, out_dtype)
 
 
 def mfa_decode_plan(problem: MfaProblem, host_seq_lens: Optional[Sequence[int]] = None, max_seq_len: int = 0,
@@ -201,9 +205,10 @@ class Decoder:
 
     def __init__(self, batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
                  softmax_scale: float = HEAD_DIM ** -0.5, host_seq_lens=None, max_seq_len: int = 0,
-                 force_ctas: int = 0, flags: int = 0, device=None):
+                 force_ctas: int = 0, flags: int = 0, device=None, out_dtype: int = MFA_OUT_BF16):
         import torch
-        self.problem = make_problem(batch, max_pages_per_seq, num_blocks, kv_dtype, softmax_scale)
+        self.problem = make_problem(batch, max_pages_per_seq, num_blocks, kv_dtype, softmax_scale,
+                                    out_dtype=out_dtype)
         if host_seq_lens is None and max_seq_len == 0:
             max_seq_len = max_pages_per_seq * PAGE_SIZE
         self.plan = mfa_decode_plan(self.problem, host_seq_lens, max_seq_len, 0, force_ctas, flags)
@@ -214,7 +219,8 @@ class Decoder:
                  lse=None, stream=None):
         import torch
         if out is None:
-            out = torch.empty((self.problem.batch, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=q.device)
+            dt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
+            out = torch.empty((self.problem.batch, NUM_Q_HEADS, HEAD_DIM), dtype=dt, device=q.device)
         if lse is None:
             lse = torch.empty((self.problem.batch, NUM_Q_HEADS), dtype=torch.float32, device=q.device)
         mfa_decode_run(self.plan, self.problem, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,

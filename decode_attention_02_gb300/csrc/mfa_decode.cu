@@ -102,7 +102,7 @@ struct DecodeParams {
   const float* v_scale;
   const int32_t* block_table;
   const int32_t* seq_lens;
-  __nv_bfloat16* out;
+  void* out;          // bf16 or fp32 [B, 64, 256]
   float* lse;
   float* part_o;
   float* part_lse;
@@ -110,6 +110,7 @@ struct DecodeParams {
   int batch;
   int max_pages;
   int num_blocks;
+  int out_f32;        // 1: fp32 output, 0: bf16 output
   float scale_log2;   // softmax_scale * log2(e)
 };
 
@@ -117,11 +118,12 @@ struct CombineParams {
   const float* part_o;
   const float* part_lse;
   const int32_t* seq_lens;
-  __nv_bfloat16* out;
+  void* out;
   float* lse;
   int batch;
   int max_pages;
   int num_ctas;
+  int out_f32;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -527,8 +529,9 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       bool dummy = false;
       if (clamp_len(p.seq_lens[b], cap, dummy) != 0) continue;
-      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(b) * kH * kD);
-      for (int i = t128; i < kH * kD * 2 / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
+      const int esz = p.out_f32 ? 4 : 2;
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * kH * kD * esz);
+      for (int i = t128; i < kH * kD * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
       if (p.lse != nullptr && t128 < kH) p.lse[b * kH + t128] = -INFINITY;
     }
 
@@ -636,9 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
               const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h);
               const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
               const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
-              lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + p0);
-              lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + p1);
               pk[e] = pack_bf16(p0, p1);
+              // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
+              // output is an exact convex combination of V rows under those weights
+              lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(pk[e] << 16));
+              lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(pk[e] & 0xFFFF0000u));
             }
             const int chunk = 4 * half + q;
             *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -688,15 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         uint32_t oa[32], ob[32];
         tmem_ld64(tmem + kTmemO + 128u * kb + 64u * hh + lane_base, oa, ob);
         const int d = 128 * hh + row;
-        if (whole) {
-          __nv_bfloat16* dst = p.out + static_cast<size_t>(b) * kH * kD + d;
+        if (whole && !p.out_f32) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b) * kH * kD + d;
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
             dst[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * linv[h]);
             dst[(h + 32) * kD] = __float2bfloat16_rn(__uint_as_float(ob[h]) * linv[h + 32]);
           }
         } else {
-          float* dst = p.part_o + static_cast<size_t>(slot_p) * kH * kD + d;
+          float* dst = whole ? static_cast<float*>(p.out) + static_cast<size_t>(b) * kH * kD + d
+                             : p.part_o + static_cast<size_t>(slot_p) * kH * kD + d;
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
             dst[h * kD] = __uint_as_float(oa[h]) * linv[h];
@@ -783,7 +789,11 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
       sum += w;
       acc = fmaf(w, p.part_o[(slot * kH + h) * kD + d], acc);
     }
-    p.out[(static_cast<size_t>(b) * kH + h) * kD + d] = __float2bfloat16_rn(acc / sum);
+    const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + d;
+    if (p.out_f32)
+      static_cast<float*>(p.out)[oi] = acc / sum;
+    else
+      static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(acc / sum);
     if (d == 0 && p.lse != nullptr) p.lse[b * kH + h] = M + logf(sum);
   }
 }
@@ -821,6 +831,7 @@ static mfa_status check_problem(const mfa_problem* pr) {
   if (pr == nullptr) return MFA_ERR_INVALID_ARG;
   if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
   if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;
+  if (pr->out_dtype != MFA_OUT_BF16 && pr->out_dtype != MFA_OUT_FP32) return MFA_ERR_INVALID_ARG;
   if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
   if (pr->num_q_heads != kH || pr->head_dim != kD || pr->page_size != kPage) return MFA_ERR_UNSUPPORTED;
   if (pr->kv_dtype != MFA_KV_BF16) return MFA_ERR_UNSUPPORTED;  // e4m3 path not in this build yet
@@ -875,7 +886,8 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.part_o = reinterpret_cast<const float*>(ws + partial_o_offset());
   cp.part_lse = reinterpret_cast<const float*>(ws + partial_lse_offset(pl->num_partials));
   cp.seq_lens = seq_lens;
-  cp.out = static_cast<__nv_bfloat16*>(out);
+  cp.out = out;
+  cp.out_f32 = pr->out_dtype == MFA_OUT_FP32 ? 1 : 0;
   cp.lse = lse;
   cp.batch = pr->batch;
   cp.max_pages = pr->max_pages_per_seq;
@@ -991,7 +1003,8 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.v_scale = v_scale;
   prm.block_table = block_table;
   prm.seq_lens = seq_lens;
-  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.out = out;
+  prm.out_f32 = pr->out_dtype == MFA_OUT_FP32 ? 1 : 0;
   prm.lse = lse;
   prm.part_o = reinterpret_cast<float*>(ws + partial_o_offset());
   prm.part_lse = reinterpret_cast<float*>(ws + partial_lse_offset(plan->num_partials));

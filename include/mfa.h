@@ -66,6 +66,11 @@ typedef enum mfa_kv_dtype {
     MFA_KV_FP8_E4M3 = 1        /* K/V cache as OCP e4m3 codes, one fp32 scale per token row */
 } mfa_kv_dtype;
 
+typedef enum mfa_out_dtype {
+    MFA_OUT_BF16 = 0,          /* out in bf16: round to nearest even of the fp32 result */
+    MFA_OUT_FP32 = 1           /* out in fp32 (the same fp32 result, unrounded) */
+} mfa_out_dtype;
+
 /* Device status word bits (set by the kernels, never cleared by them). */
 #define MFA_DEV_TIMEOUT      0x1u  /* a pipeline wait exceeded its time limit; outputs invalid */
 #define MFA_DEV_BAD_BLOCK    0x2u  /* a block_table entry outside [0, num_blocks) was used */
@@ -85,6 +90,7 @@ typedef struct mfa_problem {
     int32_t num_blocks;        /* physical pages in each of the K and V pools (>= 1) */
     int32_t kv_dtype;          /* mfa_kv_dtype */
     float softmax_scale;       /* finite, > 0; 1/sqrt(256) = 0.0625 for MFA */
+    int32_t out_dtype;         /* mfa_out_dtype */
 } mfa_problem;
 
 typedef struct mfa_plan {
@@ -132,7 +138,8 @@ mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_l
  *   v_scale      : same for V.
  *   block_table  : device int32 [B, max_pages_per_seq]; entries past ceil(L_b/64) are never read.
  *   seq_lens     : device int32 [B].
- *   out          : device bf16 [B, 64, 256] (round to nearest even of the fp32 result).
+ *   out          : device [B, 64, 256], 16-byte aligned: bf16 (round to nearest even of
+ *                  the fp32 result) or fp32, as problem->out_dtype says.
  *   lse          : device fp32 [B, 64] natural-log log-sum-exp of the scaled scores, or NULL.
  *   workspace    : device buffer of >= plan->workspace_bytes bytes, 256-byte aligned.
  *                  Layout: bytes [0,256) header (uint32 status word at offset 0);
@@ -155,7 +162,7 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* problem,
  * combine): for every sequence covered by more than one CTA,
  *     lse* = M + ln sum_s exp(lse_s - M),  M = max_s lse_s,
  *     out  = sum_s exp(lse_s - lse*) O_s          (O_s normalised partials)
- * and writes out (bf16) and lse (fp32, if non-NULL).  Sequences covered by one
+ * and writes out (in problem->out_dtype) and lse (fp32, if non-NULL).  Sequences covered by one
  * CTA, and empty ones, were written by the decode kernel and are left alone.
  * Arguments as for mfa_decode_run; seq_lens must equal the ones the decode used.
  */

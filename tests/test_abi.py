@@ -85,6 +85,7 @@ def test_plan_rejects_bad_input(lib):
                       (dict(softmax_scale=0.0), mfa.MFA_ERR_INVALID_ARG),
                       (dict(softmax_scale=float("nan")), mfa.MFA_ERR_INVALID_ARG),
                       (dict(kv_dtype=7), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(out_dtype=2), mfa.MFA_ERR_INVALID_ARG),
                       (dict(batch=-1), mfa.MFA_ERR_INVALID_ARG),
                       (dict(num_blocks=0), mfa.MFA_ERR_INVALID_ARG)]:
         with pytest.raises(mfa.MfaError) as e:
