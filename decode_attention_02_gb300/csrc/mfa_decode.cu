@@ -64,8 +64,8 @@ constexpr int kOffBar = kOffRing + kNumSlots * kSlotBytes;  // mbarriers
 constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..11] scan
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
-constexpr int kOffRed = kOffAlpha + 256;      // float[4][64] cross-warp reduction scratch
-constexpr int kOffLinv = kOffRed + 1024;      // float[64]  1 / row sum
+constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
+constexpr int kOffLinv = kOffRed + 2048;      // float[64]  1 / row sum
 constexpr int kOffSeg = kOffLinv + 256;       // int4[kMaxSeg] {b, first tile, end tile, L}
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileBlk = kOffSegN0 + 4 * kMaxSeg;    // int2[kMaxTilesPerCta] page ids
@@ -92,7 +92,8 @@ static_assert(kBarCount * 8 <= 512, "barrier area");
 // Tensor-memory columns.
 constexpr uint32_t kTmemS = 0;     // S^T buffers: [0,64) and [64,128)
 constexpr uint32_t kTmemO = 128;   // O^T buffer k, half hh: 128 + 128k + 64hh
-constexpr uint32_t kTmemL = 384;   // per-lane row-sum partials, 64 heads
+constexpr uint32_t kTmemL = 384;   // per-lane row sums of the bf16-rounded weights (normalise O)
+constexpr uint32_t kTmemLx = 448;  // per-lane row sums of the fp32 weights (lse)
 
 struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
@@ -537,7 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
 
     bool aborted = false;
     int n = 0;
-    const uint32_t l_tmem = tmem + kTmemL + lane_base;   // this thread's 64 row-sum partials
+    const uint32_t l_tmem = tmem + kTmemL + lane_base;    // this thread's 64 row-sum partials
+    const uint32_t lx_tmem = tmem + kTmemLx + lane_base;  // and their fp32-weight twins
     for (int s = 0; s < nseg; ++s) {
       const int4 sg = seg[s];
       const int b = sg.x, L = sg.w, kb = s & 1;
@@ -601,9 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           named_bar_sync(1, kSoftmaxThreads);
           if (!first) {
             // row-sum partials and O^T rows (d = row, 128 + row) times alpha per head column
-            for (int k3 = 0; k3 < 3; ++k3) {
+            #pragma unroll 1
+            for (int k3 = 0; k3 < 4; ++k3) {
               uint32_t oa[32], ob[32];
-              const uint32_t ta = (k3 == 2) ? l_tmem : tmem + kTmemO + 128u * kb + 64u * k3 + lane_base;
+              const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem
+                                : tmem + kTmemO + 128u * kb + 64u * k3 + lane_base;
               tmem_ld64(ta, oa, ob);
 #pragma unroll
               for (int h = 0; h < 32; ++h) {
@@ -618,17 +622,21 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         }
         // --- probabilities, row sums, P^T row (bf16, 128B-swizzled) for the PV MMA
         uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
-          uint32_t sv[32], lv[32];
+          uint32_t sv[32], lv[32], lx[32];
           tmem_ld32(s_tmem + 32 * half, sv);
-          if (!first) tmem_ld32(l_tmem + 32 * half, lv);
+          if (!first) {
+            tmem_ld32(l_tmem + 32 * half, lv);
+            tmem_ld32(lx_tmem + 32 * half, lx);
+          }
           tmem_ld_wait(sv);
           if (!first) {
             tmem_ld_wait(lv);
+            tmem_ld_wait(lx);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) lv[e] = 0u;
+            for (int e = 0; e < 32; ++e) lv[e] = lx[e] = 0u;
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -644,11 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
               // output is an exact convex combination of V rows under those weights
               lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(pk[e] << 16));
               lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(pk[e] & 0xFFFF0000u));
+              lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
+              lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
             }
             const int chunk = 4 * half + q;
             *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
           tmem_st32(l_tmem + 32 * half, lv);
+          tmem_st32(lx_tmem + 32 * half, lx);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -659,9 +670,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       if (stop) break;
 
       // ---------------- epilogue of sequence b's segment
-      {
+      #pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
         uint32_t la[32], lb[32];
-        tmem_ld64(l_tmem, la, lb);
+        tmem_ld64(which ? lx_tmem : l_tmem, la, lb);
         float lsum[64];
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
@@ -670,14 +682,15 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         }
         float r0, r1;
         warp_reduce_scatter64<false>(lsum, r0, r1);
-        red[sw * 64 + 2 * lane] = r0;
-        red[sw * 64 + 2 * lane + 1] = r1;
+        red[which * 256 + sw * 64 + 2 * lane] = r0;
+        red[which * 256 + sw * 64 + 2 * lane + 1] = r1;
       }
       named_bar_sync(1, kSoftmaxThreads);
       if (t128 < kH) {
         const float l = (red[t128] + red[64 + t128]) + (red[128 + t128] + red[192 + t128]);
         linv[t128] = 1.f / l;
-        const float lse_v = (m_ref[t128] + log2f(l)) * 0.69314718055994531f;
+        const float lx = (red[256 + t128] + red[320 + t128]) + (red[384 + t128] + red[448 + t128]);
+        const float lse_v = (m_ref[t128] + log2f(lx)) * 0.69314718055994531f;
         if (whole) {
           if (p.lse != nullptr) p.lse[b * kH + t128] = lse_v;
         } else {
@@ -689,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       aborted = aborted || !okO;
       if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) break;
       tc_fence_after();
+      #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t oa[32], ob[32];
         tmem_ld64(tmem + kTmemO + 128u * kb + 64u * hh + lane_base, oa, ob);
