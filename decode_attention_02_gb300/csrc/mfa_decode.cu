@@ -749,11 +749,19 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long W, long long G
 }
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineHeadsPerCta = 8;
+constexpr int kCombineHeadsPerCta = 4;       // 64 threads per head, 4 d per thread (float4)
+constexpr int kCombineMaxParts = 64;         // partials staged per pass
 
+// One CTA per (sequence, group of 4 heads).  The partial lse values of the
+// group are staged in shared memory once; every thread then owns 4 output
+// elements and streams its partials with independent float4 loads.
 __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
   grid_dep_wait();
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
+  __shared__ int slots[kCombineMaxParts];
+  __shared__ float wts[kCombineHeadsPerCta][kCombineMaxParts];
+  __shared__ float mx[kCombineHeadsPerCta], tot[kCombineHeadsPerCta];
+  __shared__ int nparts_s;
   const int b = blockIdx.x, hg = blockIdx.y;
   const int cap = p.max_pages * kPage;
   int before = 0, total = 0;
@@ -785,31 +793,87 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int g0 = cta_of_tile(before, total, p.num_ctas);
   const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
-  // CTAs between g0 and g1 with an empty tile range (grid larger than the work) hold no partial
-  auto empty_cta = [&](int g) {
-    return (static_cast<long long>(g) * total) / p.num_ctas == (static_cast<long long>(g + 1) * total) / p.num_ctas;
-  };
-  const int d = threadIdx.x;
-  for (int hh = 0; hh < kCombineHeadsPerCta; ++hh) {
-    const int h = hg * kCombineHeadsPerCta + hh;
-    float M = -INFINITY;
-    for (int g = g0; g <= g1; ++g)
-      if (!empty_cta(g)) M = fmaxf(M, p.part_lse[static_cast<size_t>(b + g) * kH + h]);
-    float sum = 0.f, acc = 0.f;
-    for (int g = g0; g <= g1; ++g) {
-      if (empty_cta(g)) continue;
-      const size_t slot = static_cast<size_t>(b + g);
-      const float w = expf(p.part_lse[slot * kH + h] - M);
-      sum += w;
-      acc = fmaf(w, p.part_o[(slot * kH + h) * kD + d], acc);
+
+  const int hl = threadIdx.x >> 6;                       // head within the group
+  const int h = hg * kCombineHeadsPerCta + hl;
+  const int d4 = threadIdx.x & 63;                        // float4 column
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float run_max = -INFINITY, run_sum = 0.f;               // merged over the passes
+  // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
+  for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
+    const int ge = min(g1 + 1, gs + kCombineMaxParts);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int n = 0;
+      for (int g = gs; g < ge; ++g) {
+        const bool empty = (static_cast<long long>(g) * total) / p.num_ctas ==
+                           (static_cast<long long>(g + 1) * total) / p.num_ctas;
+        if (!empty) slots[n++] = b + g;
+      }
+      nparts_s = n;
     }
-    const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + d;
-    if (p.out_f32)
-      static_cast<float*>(p.out)[oi] = acc / sum;
-    else
-      static_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(acc / sum);
-    if (d == 0 && p.lse != nullptr) p.lse[b * kH + h] = M + logf(sum);
+    __syncthreads();
+    const int n = nparts_s;
+    // lse of every (partial, head) of the group -> pass max and weights
+    for (int i = threadIdx.x; i < n * kCombineHeadsPerCta; i += kCombineThreads) {
+      const int k = i / kCombineHeadsPerCta, hh = i % kCombineHeadsPerCta;
+      wts[hh][k] = p.part_lse[static_cast<size_t>(slots[k]) * kH + hg * kCombineHeadsPerCta + hh];
+    }
+    __syncthreads();
+    if (threadIdx.x < kCombineHeadsPerCta) {
+      float m = -INFINITY;
+      for (int k = 0; k < n; ++k) m = fmaxf(m, wts[threadIdx.x][k]);
+      float sum = 0.f;
+      for (int k = 0; k < n; ++k) {
+        const float w = expf(wts[threadIdx.x][k] - m);
+        wts[threadIdx.x][k] = w;
+        sum += w;
+      }
+      mx[threadIdx.x] = m;
+      tot[threadIdx.x] = sum;
+    }
+    __syncthreads();
+    // rescale what earlier passes accumulated to this pass's reference
+    const float m_new = fmaxf(run_max, mx[hl]);
+    const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
+    const float a_new = expf(mx[hl] - m_new);
+    acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
+    run_sum = run_sum * a_old + tot[hl] * a_new;
+    run_max = m_new;
+    int k = 0;
+    for (; k + 4 <= n; k += 4) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k + u]) * kH + h) * kD)[d4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = wts[hl][k + u] * a_new;
+        acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+      }
+    }
+    for (; k < n; ++k) {
+      const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
+      const float w = wts[hl][k] * a_new;
+      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    }
   }
+  const float inv = 1.f / run_sum;
+  const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
+  if (p.out_f32) {
+    reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
+  }
+  if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h] = run_max + logf(run_sum);
 }
 
 // ------------------------------------------------------------------ host side
