@@ -53,6 +53,7 @@ constexpr int kMaxTilesPerCta = 128;
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
+constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the producer, in tiles
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
 
@@ -99,6 +100,8 @@ struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
   CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256], box {64, 64, 1}, 128B swizzle
   CUtensorMap tm_v;
+  CUtensorMap tm_pk;  // 3-D, box {256, 64, 1} (one whole page), no swizzle: L2 prefetch only
+  CUtensorMap tm_pv;
   const float* k_scale;
   const float* v_scale;
   const int32_t* block_table;
@@ -360,9 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       const int4 sg = seg[s];
       const int32_t* row = p.block_table + static_cast<size_t>(sg.x) * p.max_pages;
       for (int j = sg.y + lane; j < sg.z; j += 32) {
-        const int b0 = row[2 * j];
-        const int b1 = (kPage * (2 * j + 1) < sg.w) ? row[2 * j + 1] : 0;
-        if (b0 < 0 || b0 >= p.num_blocks || b1 < 0 || b1 >= p.num_blocks) bad_blk = true;
+        int b0 = row[2 * j];
+        const bool has1 = kPage * (2 * j + 1) < sg.w;
+        int b1 = has1 ? row[2 * j + 1] : -1;
+        // an id outside the pool is reported and replaced by page 0, so every TMA
+        // coordinate stays inside the pool (the output of that sequence is then wrong)
+        if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = 0; }
+        if (has1 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = 0; }
         tile_blk[seg_n0[s] + j - sg.y] = make_int2(b0, b1);
       }
     }
@@ -374,7 +381,20 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       int nq = 0;           // Q loads issued
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
+      // pull the pages of upcoming tiles into L2 so that ring loads see L2 latency
+      auto prefetch_tile = [&](int t) {
+        if (t >= ntiles) return;
+        const int2 bk = tile_blk[t];
+        tma_prefetch_3d(&p.tm_pk, 0, 0, bk.x);
+        tma_prefetch_3d(&p.tm_pv, 0, 0, bk.x);
+        if (bk.y >= 0) {
+          tma_prefetch_3d(&p.tm_pk, 0, 0, bk.y);
+          tma_prefetch_3d(&p.tm_pv, 0, 0, bk.y);
+        }
+      };
+      for (int t = 1; t < kPrefetchTiles; ++t) prefetch_tile(t);
       for (int n = 0; n <= ntiles && ok; ++n) {
+        prefetch_tile(n + kPrefetchTiles);
         if (n < ntiles) {
           const int4 sg = seg[sk];
           if (jk == sg.y) {
@@ -552,9 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         const bool first = (j == sg.y);
         const uint32_t s_tmem = tmem + kTmemS + 64u * (n & 1) + lane_base;
         const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
-        // --- PV of the previous tile must be done before P or O are touched
-        const bool okPV = (n == 0) ? true : wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
-        aborted = aborted || !okS || !okPV;
+        aborted = aborted || !okS;
+        bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
         // --- validity of this thread's row (the last page's rows sit at the end of the box)
         const int pg = row >> 6, i = row & 63;
         const int rp = min(kPage, L - kTile * j - kPage * pg);
@@ -601,6 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             alpha_s[t128] = a;
           }
           named_bar_sync(1, kSoftmaxThreads);
+          if (!pv_waited) {
+            const bool okPV = wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
+            pv_waited = true;
+            if (named_bar_or(1, kSoftmaxThreads, !okPV || *abort_flag)) { aborted = true; stop = true; break; }
+          }
           if (!first) {
             // row-sum partials and O^T rows (d = row, 128 + row) times alpha per head column
             #pragma unroll 1
@@ -620,9 +644,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             tmem_st_wait();
           }
         }
-        // --- probabilities, row sums, P^T row (bf16, 128B-swizzled) for the PV MMA
-        uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll 1
+        // --- probabilities and row sums; the P^T row (bf16) is kept in registers until the
+        //     previous tile's PV has released the P buffer
+        uint32_t pk[32];
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t sv[32], lv[32], lx[32];
           tmem_ld32(s_tmem + 32 * half, sv);
@@ -639,24 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             for (int e = 0; e < 32; ++e) lv[e] = lx[e] = 0u;
           }
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int hl = 8 * q + 2 * e, h = 32 * half + hl;
-              const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h);
-              const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
-              const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
-              pk[e] = pack_bf16(p0, p1);
-              // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
-              // output is an exact convex combination of V rows under those weights
-              lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(pk[e] << 16));
-              lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(pk[e] & 0xFFFF0000u));
-              lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
-              lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
-            }
-            const int chunk = 4 * half + q;
-            *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int e = 0; e < 16; ++e) {
+            const int hl = 2 * e, h = 32 * half + hl;
+            const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h);
+            const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
+            const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
+            const uint32_t w = pack_bf16(p0, p1);
+            pk[16 * half + e] = w;
+            // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
+            // output is an exact convex combination of V rows under those weights
+            lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(w << 16));
+            lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(w & 0xFFFF0000u));
+            lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
+            lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
           }
           tmem_st32(l_tmem + 32 * half, lv);
           tmem_st32(lx_tmem + 32 * half, lx);
@@ -664,6 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarSEmpty + (n & 1)));
+        if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
+        uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarPFull));
       }
@@ -942,6 +968,18 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   }
   const void* pools[2] = {k, v};
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
+  CUtensorMap* pf_maps[2] = {&prm.tm_pk, &prm.tm_pv};
+  for (int i = 0; i < 2; ++i) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
+                          static_cast<cuuint64_t>(pr->num_blocks)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(kD) * 2 * kPage};
+    cuuint32_t box[3] = {kD, kPage, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(pf_maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return MFA_ERR_CUDA;
+  }
   for (int i = 0; i < 2; ++i) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
                           static_cast<cuuint64_t>(pr->num_blocks)};

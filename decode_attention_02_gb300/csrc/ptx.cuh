@@ -105,6 +105,14 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, 
       : "memory");
 }
 
+// Prefetch one tensor-map box into L2 (no shared memory, no barrier); boxes outside the
+// tensor are skipped by the hardware.
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Tensor-memory allocation (whole warp). The allocated base address is written to smem.
 __device__ __forceinline__ void tmem_alloc(uint32_t smem_dst, uint32_t ncols) {
