@@ -53,7 +53,6 @@ constexpr int kMaxTilesPerCta = 128;
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
-constexpr int kPrefetchTiles = 2;          // L2 prefetch distance of the producer, in tiles
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
 
@@ -100,8 +99,6 @@ struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
   CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256], box {64, 64, 1}, 128B swizzle
   CUtensorMap tm_v;
-  CUtensorMap tm_pk;  // 3-D, box {256, 64, 1} (one whole page), no swizzle: L2 prefetch only
-  CUtensorMap tm_pv;
   const float* k_scale;
   const float* v_scale;
   const int32_t* block_table;
@@ -314,7 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     int* scratch = misc + 4;
     bool bad = false;
     int loc = 0;
-    for (int b = tid; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
+    const int L_first = (tid < p.batch) ? p.seq_lens[tid] : 0;   // reused by the segment scan below
+    loc += tiles_of(clamp_len(L_first, cap, bad));
+    for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     int W = 0;
     block_incl_scan(loc, scratch, W);
@@ -329,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       for (int c0 = 0; c0 < p.batch && carry < t1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
-        const int L = (b < p.batch) ? clamp_len(p.seq_lens[b], cap, dummy) : 0;
+        const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
         const int T = tiles_of(L);
         int tot = 0, ftot = 0;
         const int incl = block_incl_scan(T, scratch, tot) + carry;
@@ -359,10 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   if (warp == 0) {
     // ---------------- producer: page ids, then TMA loads of Q, K, V
     bool bad_blk = false;
-    for (int s = 0; s < nseg; ++s) {
+    // all of this CTA's page ids in one round of independent loads (lane = tile)
+    for (int n = lane; n < ntiles; n += 32) {
+      int s = 0;
+      while (s + 1 < nseg && seg_n0[s + 1] <= n) ++s;
       const int4 sg = seg[s];
       const int32_t* row = p.block_table + static_cast<size_t>(sg.x) * p.max_pages;
-      for (int j = sg.y + lane; j < sg.z; j += 32) {
+      {
+        const int j = sg.y + (n - seg_n0[s]);
         int b0 = row[2 * j];
         const bool has1 = kPage * (2 * j + 1) < sg.w;
         int b1 = has1 ? row[2 * j + 1] : -1;
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         // coordinate stays inside the pool (the output of that sequence is then wrong)
         if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = 0; }
         if (has1 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = 0; }
-        tile_blk[seg_n0[s] + j - sg.y] = make_int2(b0, b1);
+        tile_blk[n] = make_int2(b0, b1);
       }
     }
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
@@ -381,20 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       int nq = 0;           // Q loads issued
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
-      // pull the pages of upcoming tiles into L2 so that ring loads see L2 latency
-      auto prefetch_tile = [&](int t) {
-        if (t >= ntiles) return;
-        const int2 bk = tile_blk[t];
-        tma_prefetch_3d(&p.tm_pk, 0, 0, bk.x);
-        tma_prefetch_3d(&p.tm_pv, 0, 0, bk.x);
-        if (bk.y >= 0) {
-          tma_prefetch_3d(&p.tm_pk, 0, 0, bk.y);
-          tma_prefetch_3d(&p.tm_pv, 0, 0, bk.y);
-        }
-      };
-      for (int t = 1; t < kPrefetchTiles; ++t) prefetch_tile(t);
       for (int n = 0; n <= ntiles && ok; ++n) {
-        prefetch_tile(n + kPrefetchTiles);
         if (n < ntiles) {
           const int4 sg = seg[sk];
           if (jk == sg.y) {
@@ -775,20 +765,21 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long W, long long G
 }
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineHeadsPerCta = 4;       // 64 threads per head, 4 d per thread (float4)
-constexpr int kCombineMaxParts = 64;         // partials staged per pass
+constexpr int kCombineGroups = 4;            // groups of 64 threads; each takes every 4th partial
+constexpr int kCombineMaxParts = 256;        // partials staged per pass
 
-// One CTA per (sequence, group of 4 heads).  The partial lse values of the
-// group are staged in shared memory once; every thread then owns 4 output
-// elements and streams its partials with independent float4 loads.
+// One CTA per (sequence, head).  The head's partial lse values are staged in
+// shared memory; thread group k of 4 accumulates partials k, k+4, ... with
+// float4 loads (64 threads x 4 = 256 d), and the groups are summed at the end.
 __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
   grid_dep_wait();
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
-  __shared__ float wts[kCombineHeadsPerCta][kCombineMaxParts];
-  __shared__ float mx[kCombineHeadsPerCta], tot[kCombineHeadsPerCta];
+  __shared__ float wts[kCombineMaxParts];
+  __shared__ float4 part_acc[kCombineGroups - 1][64];
+  __shared__ float pass_max, pass_sum;
   __shared__ int nparts_s;
-  const int b = blockIdx.x, hg = blockIdx.y;
+  const int b = blockIdx.x, h = blockIdx.y;
   const int cap = p.max_pages * kPage;
   int before = 0, total = 0;
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
@@ -820,71 +811,85 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
 
-  const int hl = threadIdx.x >> 6;                       // head within the group
-  const int h = hg * kCombineHeadsPerCta + hl;
-  const int d4 = threadIdx.x & 63;                        // float4 column
+  const int grp = threadIdx.x >> 6;
+  const int d4 = threadIdx.x & 63;   // float4 column: d = 4*d4 .. 4*d4+3
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float run_max = -INFINITY, run_sum = 0.f;               // merged over the passes
+  float run_max = -INFINITY, run_sum = 0.f;   // merged over the passes (same in every thread)
   // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
   for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
     const int ge = min(g1 + 1, gs + kCombineMaxParts);
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 32) {
+      // compact the non-empty CTAs of [gs, ge) into slots[] (ballot over the warp)
       int n = 0;
-      for (int g = gs; g < ge; ++g) {
-        const bool empty = (static_cast<long long>(g) * total) / p.num_ctas ==
-                           (static_cast<long long>(g + 1) * total) / p.num_ctas;
-        if (!empty) slots[n++] = b + g;
+      for (int g = gs + threadIdx.x; g - threadIdx.x < ge; g += 32) {
+        const bool live = g < ge && (static_cast<long long>(g) * total) / p.num_ctas !=
+                                        (static_cast<long long>(g + 1) * total) / p.num_ctas;
+        const unsigned m = __ballot_sync(0xffffffffu, live);
+        if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
+        n += __popc(m);
       }
-      nparts_s = n;
+      if (threadIdx.x == 0) nparts_s = n;
     }
     __syncthreads();
     const int n = nparts_s;
-    // lse of every (partial, head) of the group -> pass max and weights
-    for (int i = threadIdx.x; i < n * kCombineHeadsPerCta; i += kCombineThreads) {
-      const int k = i / kCombineHeadsPerCta, hh = i % kCombineHeadsPerCta;
-      wts[hh][k] = p.part_lse[static_cast<size_t>(slots[k]) * kH + hg * kCombineHeadsPerCta + hh];
-    }
+    for (int k = threadIdx.x; k < n; k += kCombineThreads)
+      wts[k] = p.part_lse[static_cast<size_t>(slots[k]) * kH + h];
     __syncthreads();
-    if (threadIdx.x < kCombineHeadsPerCta) {
+    if (threadIdx.x < 32) {
       float m = -INFINITY;
-      for (int k = 0; k < n; ++k) m = fmaxf(m, wts[threadIdx.x][k]);
+      for (int k = threadIdx.x; k < n; k += 32) m = fmaxf(m, wts[k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
       float sum = 0.f;
-      for (int k = 0; k < n; ++k) {
-        const float w = expf(wts[threadIdx.x][k] - m);
-        wts[threadIdx.x][k] = w;
+      for (int k = threadIdx.x; k < n; k += 32) {
+        const float w = expf(wts[k] - m);
+        wts[k] = w;
         sum += w;
       }
-      mx[threadIdx.x] = m;
-      tot[threadIdx.x] = sum;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (threadIdx.x == 0) {
+        pass_max = m;
+        pass_sum = sum;
+      }
     }
     __syncthreads();
     // rescale what earlier passes accumulated to this pass's reference
-    const float m_new = fmaxf(run_max, mx[hl]);
+    const float m_new = fmaxf(run_max, pass_max);
     const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
-    const float a_new = expf(mx[hl] - m_new);
+    const float a_new = expf(pass_max - m_new);
     acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
-    run_sum = run_sum * a_old + tot[hl] * a_new;
+    run_sum = run_sum * a_old + pass_sum * a_new;
     run_max = m_new;
-    int k = 0;
-    for (; k + 4 <= n; k += 4) {
+    int k = grp;
+    for (; k + 3 * kCombineGroups < n; k += 4 * kCombineGroups) {
       float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        v[u] = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k + u]) * kH + h) * kD)[d4];
+        v[u] = reinterpret_cast<const float4*>(
+            p.part_o + (static_cast<size_t>(slots[k + u * kCombineGroups]) * kH + h) * kD)[d4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const float w = wts[hl][k + u] * a_new;
+        const float w = wts[k + u * kCombineGroups] * a_new;
         acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
         acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
       }
     }
-    for (; k < n; ++k) {
+    for (; k < n; k += kCombineGroups) {
       const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
-      const float w = wts[hl][k] * a_new;
+      const float w = wts[k] * a_new;
       acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
     }
+  }
+  if (grp > 0) part_acc[grp - 1][d4] = acc;
+  __syncthreads();
+  if (grp != 0) return;
+#pragma unroll
+  for (int k = 0; k < kCombineGroups - 1; ++k) {
+    const float4 o = part_acc[k][d4];
+    acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
   }
   const float inv = 1.f / run_sum;
   const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
@@ -968,18 +973,6 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   }
   const void* pools[2] = {k, v};
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
-  CUtensorMap* pf_maps[2] = {&prm.tm_pk, &prm.tm_pv};
-  for (int i = 0; i < 2; ++i) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
-                          static_cast<cuuint64_t>(pr->num_blocks)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(kD) * 2 * kPage};
-    cuuint32_t box[3] = {kD, kPage, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (enc(pf_maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MFA_ERR_CUDA;
-  }
   for (int i = 0; i < 2; ++i) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
                           static_cast<cuuint64_t>(pr->num_blocks)};
@@ -1009,7 +1002,7 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH / kCombineHeadsPerCta, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
