@@ -45,7 +45,7 @@ PAGE_SIZE = 64
 
 # Every symbol include/mfa.h declares.
 EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
-                    "mfa_status_string", "mfa_abi_version")
+                    "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error")
 
 
 class MfaProblem(ctypes.Structure):
@@ -66,7 +66,10 @@ class MfaPlan(ctypes.Structure):
 
 class MfaError(RuntimeError):
     def __init__(self, status: int, where: str):
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        msg = f"{where}: {status_string(status)} (status {status})"
+        if status == MFA_ERR_CUDA and _lib is not None:
+            msg += ": " + _lib.mfa_last_cuda_error().decode()
+        super().__init__(msg)
         self.status = status
 
 
@@ -97,6 +100,8 @@ def load_library(path: str = LIB_PATH):
     lib.mfa_status_string.restype = ctypes.c_char_p
     lib.mfa_abi_version.argtypes = []
     lib.mfa_abi_version.restype = ctypes.c_int32
+    lib.mfa_last_cuda_error.argtypes = []
+    lib.mfa_last_cuda_error.restype = ctypes.c_char_p
     _lib = lib
     return lib
 

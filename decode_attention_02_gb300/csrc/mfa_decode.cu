@@ -35,6 +35,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "mfa.h"
 #include "ptx.cuh"
@@ -45,8 +46,8 @@ constexpr int kH = 64;             // query heads
 constexpr int kD = 256;            // head width
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
-constexpr int kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
-constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
+constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
 constexpr int kNumSlots = 10;
 constexpr int kSlotBytes = 16384;
 constexpr int kMaxTilesPerCta = 128;
@@ -65,8 +66,8 @@ constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nse
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
-constexpr int kOffLinv = kOffRed + 2048;      // float[64]  1 / row sum
-constexpr int kOffSeg = kOffLinv + 256;       // int4[kMaxSeg] {b, first tile, end tile, L}
+constexpr int kOffLinv = kOffRed + 2048;      // float[2][64]  1 / row sum per O buffer
+constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, end tile, L}
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileBlk = kOffSegN0 + 4 * kMaxSeg;    // int2[kMaxTilesPerCta] page ids
 constexpr int kSmemUsed = kOffTileBlk + 8 * kMaxTilesPerCta;
@@ -125,6 +126,7 @@ struct CombineParams {
   int max_pages;
   int num_ctas;
   int out_f32;
+  int heads_per_cta;  // 1, 4 or 16
 };
 
 // ------------------------------------------------------------------ helpers
@@ -155,7 +157,7 @@ __device__ __forceinline__ int tiles_of(int L) { return (L + kTile - 1) / kTile;
 
 // Bounded wait on an mbarrier phase.  Returns false after kWaitLimitNs, or at
 // once when another role has raised the CTA's abort flag.
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -233,6 +235,44 @@ __device__ __forceinline__ void warp_reduce_scatter64(float (&v)[64], float& r0,
   }
   r0 = v[0];
   r1 = v[1];
+}
+
+// Reduce 32 per-thread values across the 32 lanes of a warp by halving exchanges;
+// lane l ends with the result for value index l.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const bool hi = lane & 16;
+    const float keep = hi ? v[i + 16] : v[i], send = hi ? v[i] : v[i + 16];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hi = lane & 8;
+    const float keep = hi ? v[i + 8] : v[i], send = hi ? v[i] : v[i + 8];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool hi = lane & 4;
+    const float keep = hi ? v[i + 4] : v[i], send = hi ? v[i] : v[i + 4];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool hi = lane & 2;
+    const float keep = hi ? v[i + 2] : v[i], send = hi ? v[i] : v[i + 2];
+    v[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+  {
+    const bool hi = lane & 1;
+    const float keep = hi ? v[1] : v[0], send = hi ? v[0] : v[1];
+    v[0] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+  }
+  return v[0];
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -524,17 +564,20 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
     }
   } else {
-    // ---------------- softmax + epilogue (128 threads, one per TMEM lane)
-    const int t128 = tid - 64;
+    // ---------------- softmax + epilogue (256 threads: two warps per TMEM lane quarter)
+    const int ts = tid - 64;                       // 0..255
+    const int sw = warp - 2;                       // 0..7
+    const int grp = sw >> 2;                       // head half: heads [32*grp, 32*grp + 32)
+    const int h0 = 32 * grp;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;                // token row of a tile / d within an O half
-    const int sw = warp - 2;                       // 0..3
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     float* m_ref = reinterpret_cast<float*>(smem + kOffMref);
     float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     float* linv = reinterpret_cast<float*>(smem + kOffLinv);
     const float c = p.scale_log2;
+    const bool issuer = (lane == 0) && ((sw & 3) == 0);   // one bulk-store thread per head half
 
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
@@ -542,25 +585,115 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       if (clamp_len(p.seq_lens[b], cap, dummy) != 0) continue;
       const int esz = p.out_f32 ? 4 : 2;
       uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * kH * kD * esz);
-      for (int i = t128; i < kH * kD * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
-      if (p.lse != nullptr && t128 < kH) p.lse[b * kH + t128] = -INFINITY;
+      for (int i = ts; i < kH * kD * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr && ts < kH) p.lse[b * kH + ts] = -INFINITY;
     }
 
     bool aborted = false;
     int n = 0;
-    const uint32_t l_tmem = tmem + kTmemL + lane_base;    // this thread's 64 row-sum partials
-    const uint32_t lx_tmem = tmem + kTmemLx + lane_base;  // and their fp32-weight twins
+    const uint32_t l_tmem = tmem + kTmemL + h0 + lane_base;    // this thread's 32 row-sum partials
+    const uint32_t lx_tmem = tmem + kTmemLx + h0 + lane_base;  // and their fp32-weight twins
+    int defer_b[2] = {0, 0}, defer_slot[2] = {0, 0};
+    bool defer_whole[2] = {false, false};
+
+    // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx & 1),
+    // normalised by 1/l from linv: [head][d] rows are staged in shared memory and sent
+    // with bulk async copies.  With `from_ring` the rows go through the idle ring at
+    // 64 KB offset `ring_k`; otherwise through this half's 8 KB of the P buffer in
+    // double-buffered 4 KB rounds.  Returns false if the CTA is aborting.
+    auto write_segment = [&](int sidx, int b, int slot_p, bool whole, bool from_ring, int ring_k) -> bool {
+      const int kb = sidx & 1;
+      const bool okO = wait_warp(bar(kBarOFull + kb), (sidx >> 1) & 1, abort_flag);
+      aborted = aborted || !okO;
+      if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) return false;
+      tc_fence_after();
+      const uint32_t o_tmem = tmem + kTmemO + 128u * kb + h0 + lane_base;
+      uint32_t oa[32], ob[32];
+      tmem_ld32(o_tmem, oa);
+      tmem_ld32(o_tmem + 64, ob);
+      tmem_ld_wait(oa);
+      tmem_ld_wait(ob);
+      tc_fence_before();
+      mbar_arrive(bar(kBarOEmpty + kb));   // the accumulator is free; the stores below use registers
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const float li = linv[kb * kH + h0 + h];
+        oa[h] = __float_as_uint(__uint_as_float(oa[h]) * li);
+        ob[h] = __float_as_uint(__uint_as_float(ob[h]) * li);
+      }
+      const bool bf16_out = whole && !p.out_f32;
+      const int esz = bf16_out ? 2 : 4;
+      uint8_t* gdst = whole ? static_cast<uint8_t*>(p.out) + (static_cast<size_t>(b) * kH + h0) * kD * esz
+                            : reinterpret_cast<uint8_t*>(p.part_o) + (static_cast<size_t>(slot_p) * kH + h0) * kD * 4;
+      auto put = [&](uint8_t* stg, int hl, float v0, float v1) {
+        if (bf16_out) {
+          reinterpret_cast<__nv_bfloat16*>(stg)[hl * kD + row] = __float2bfloat16_rn(v0);
+          reinterpret_cast<__nv_bfloat16*>(stg)[hl * kD + 128 + row] = __float2bfloat16_rn(v1);
+        } else {
+          reinterpret_cast<float*>(stg)[hl * kD + row] = v0;
+          reinterpret_cast<float*>(stg)[hl * kD + 128 + row] = v1;
+        }
+      };
+      if (from_ring) {
+        const uint32_t off = kOffRing + ring_k * 65536 + grp * 32768;
+        uint8_t* stg = smem + off;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) put(stg, h, __uint_as_float(oa[h]), __uint_as_float(ob[h]));
+        fence_proxy_async_smem();
+        named_bar_sync(2 + grp, kSoftmaxThreads / 2);
+        if (issuer) {
+          bulk_store_s2g(gdst, sbase + off, 32 * kD * esz);
+          bulk_commit();
+        }
+        return true;
+      }
+      // 4 KB per round: 4 heads (fp32) or 8 heads (bf16); round sizes are compile-time so
+      // the register arrays are indexed by constants
+      constexpr int kRoundBytes = 4096;
+      auto rounds = [&](auto hpr_tag) {
+        constexpr int hpr = decltype(hpr_tag)::value;
+#pragma unroll
+        for (int r = 0; r < 32 / hpr; ++r) {
+          const int buf = r & 1;
+          if (r >= 2) {
+            if (issuer) bulk_wait_read1();
+            named_bar_sync(2 + grp, kSoftmaxThreads / 2);
+          }
+          uint8_t* stg = smem + kOffP + grp * 8192 + buf * kRoundBytes;
+#pragma unroll
+          for (int hl = 0; hl < hpr; ++hl)
+            put(stg, hl, __uint_as_float(oa[r * hpr + hl]), __uint_as_float(ob[r * hpr + hl]));
+          fence_proxy_async_smem();
+          named_bar_sync(2 + grp, kSoftmaxThreads / 2);
+          if (issuer) {
+            bulk_store_s2g(gdst + static_cast<size_t>(r * hpr) * kD * esz,
+                           sbase + kOffP + grp * 8192 + buf * kRoundBytes, kRoundBytes);
+            bulk_commit();
+          }
+        }
+      };
+      if (bf16_out)
+        rounds(std::integral_constant<int, 8>());
+      else
+        rounds(std::integral_constant<int, 4>());
+      // the P buffer must be read out before the next segment's first tile writes it
+      if (issuer) bulk_wait_read0();
+      named_bar_sync(2 + grp, kSoftmaxThreads / 2);
+      return true;
+    };
+
     for (int s = 0; s < nseg; ++s) {
       const int4 sg = seg[s];
       const int b = sg.x, L = sg.w, kb = s & 1;
       const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
       const int slot_p = b + static_cast<int>(blockIdx.x);
-      if (t128 < kH) m_ref[t128] = -INFINITY;
+      const uint32_t o_tmem = tmem + kTmemO + 128u * kb + h0 + lane_base;   // + 64 for d in [128, 256)
+      if (ts < kH) m_ref[ts] = -INFINITY;
       named_bar_sync(1, kSoftmaxThreads);
       bool stop = false;
       for (int j = sg.y; j < sg.z; ++j, ++n) {
         const bool first = (j == sg.y);
-        const uint32_t s_tmem = tmem + kTmemS + 64u * (n & 1) + lane_base;
+        const uint32_t s_tmem = tmem + kTmemS + 64u * (n & 1) + h0 + lane_base;
         const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
         aborted = aborted || !okS;
         bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
@@ -572,15 +705,16 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         bool need = false;
         if (okS) {
           tc_fence_after();
-          uint32_t sa[32], sb[32];
-          tmem_ld64(s_tmem, sa, sb);
+          uint32_t sv[32];
+          tmem_ld32(s_tmem, sv);
+          tmem_ld_wait(sv);
 #pragma unroll
-          for (int h = 0; h < 64; h += 4) {
-            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h);
-            need |= (fmaf(__uint_as_float(SV(h + 0)), c, -m4.x) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(SV(h + 1)), c, -m4.y) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(SV(h + 2)), c, -m4.z) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(SV(h + 3)), c, -m4.w) > kRescaleThreshold);
+          for (int h = 0; h < 32; h += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h0 + h);
+            need |= (fmaf(__uint_as_float(sv[h + 0]), c, -m4.x) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 1]), c, -m4.y) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 2]), c, -m4.z) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 3]), c, -m4.w) > kRescaleThreshold);
           }
           need = need && valid;
         }
@@ -588,26 +722,24 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) { stop = true; break; }
           // --- rare path: new reference max for heads whose scores jumped by > 2^8
           {
-            uint32_t sa[32], sb[32];
-            tmem_ld64(s_tmem, sa, sb);
-            float mv[64];
+            uint32_t sv[32];
+            tmem_ld32(s_tmem, sv);
+            tmem_ld_wait(sv);
+            float mv[32];
 #pragma unroll
-            for (int h = 0; h < 64; ++h) mv[h] = valid ? __uint_as_float(SV(h)) * c : -INFINITY;
-            float r0, r1;
-            warp_reduce_scatter64<true>(mv, r0, r1);
-            red[sw * 64 + 2 * lane] = r0;
-            red[sw * 64 + 2 * lane + 1] = r1;
+            for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sv[h]) * c : -INFINITY;
+            red[wq * 64 + h0 + lane] = warp_reduce_scatter32<true>(mv);
           }
           named_bar_sync(1, kSoftmaxThreads);
-          if (t128 < kH) {
-            const float mt = fmaxf(fmaxf(red[t128], red[64 + t128]), fmaxf(red[128 + t128], red[192 + t128]));
-            const float mo = m_ref[t128];
+          if (ts < kH) {
+            const float mt = fmaxf(fmaxf(red[ts], red[64 + ts]), fmaxf(red[128 + ts], red[192 + ts]));
+            const float mo = m_ref[ts];
             float a = 1.f;
             if (mt > mo + kRescaleThreshold) {
               a = exp2f(mo - mt);
-              m_ref[t128] = mt;
+              m_ref[ts] = mt;
             }
-            alpha_s[t128] = a;
+            alpha_s[ts] = a;
           }
           named_bar_sync(1, kSoftmaxThreads);
           if (!pv_waited) {
@@ -616,34 +748,30 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             if (named_bar_or(1, kSoftmaxThreads, !okPV || *abort_flag)) { aborted = true; stop = true; break; }
           }
           if (!first) {
-            // row-sum partials and O^T rows (d = row, 128 + row) times alpha per head column
-            #pragma unroll 1
+            // row sums and O^T rows (d = row, 128 + row) times alpha per head column
+#pragma unroll 1
             for (int k3 = 0; k3 < 4; ++k3) {
-              uint32_t oa[32], ob[32];
-              const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem
-                                : tmem + kTmemO + 128u * kb + 64u * k3 + lane_base;
-              tmem_ld64(ta, oa, ob);
+              uint32_t ov[32];
+              const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem : o_tmem + 64u * k3;
+              tmem_ld32(ta, ov);
+              tmem_ld_wait(ov);
 #pragma unroll
-              for (int h = 0; h < 32; ++h) {
-                oa[h] = __float_as_uint(__uint_as_float(oa[h]) * alpha_s[h]);
-                ob[h] = __float_as_uint(__uint_as_float(ob[h]) * alpha_s[h + 32]);
-              }
-              tmem_st32(ta, oa);
-              tmem_st32(ta + 32, ob);
+              for (int h = 0; h < 32; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha_s[h0 + h]);
+              tmem_st32(ta, ov);
             }
             tmem_st_wait();
           }
         }
-        // --- probabilities and row sums; the P^T row (bf16) is kept in registers until the
-        //     previous tile's PV has released the P buffer
-        uint32_t pk[32];
+        // --- probabilities and row sums; the P^T row piece (bf16) stays in registers until
+        //     the previous tile's PV has released the P buffer
+        uint32_t pk[16];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t sv[32], lv[32], lx[32];
-          tmem_ld32(s_tmem + 32 * half, sv);
+          uint32_t sv[16], lv[16], lx[16];
+          tmem_ld16(s_tmem + 16 * half, sv);
           if (!first) {
-            tmem_ld32(l_tmem + 32 * half, lv);
-            tmem_ld32(lx_tmem + 32 * half, lx);
+            tmem_ld16(l_tmem + 16 * half, lv);
+            tmem_ld16(lx_tmem + 16 * half, lx);
           }
           tmem_ld_wait(sv);
           if (!first) {
@@ -651,16 +779,16 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             tmem_ld_wait(lx);
           } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) lv[e] = lx[e] = 0u;
+            for (int e = 0; e < 16; ++e) lv[e] = lx[e] = 0u;
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int hl = 2 * e, h = 32 * half + hl;
-            const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h);
+          for (int e = 0; e < 8; ++e) {
+            const int hl = 2 * e, h = 16 * half + hl;
+            const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h0 + h);
             const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
             const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
             const uint32_t w = pack_bf16(p0, p1);
-            pk[16 * half + e] = w;
+            pk[8 * half + e] = w;
             // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
             // output is an exact convex combination of V rows under those weights
             lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(w << 16));
@@ -668,17 +796,18 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
             lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
           }
-          tmem_st32(l_tmem + 32 * half, lv);
-          tmem_st32(lx_tmem + 32 * half, lx);
+          tmem_st16(l_tmem + 16 * half, lv);
+          tmem_st16(lx_tmem + 16 * half, lx);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarSEmpty + (n & 1)));
         if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
+        // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
         uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(prow + ((q ^ (row & 7)) << 4)) =
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(prow + (((4 * grp + q) ^ (row & 7)) << 4)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarPFull));
@@ -686,65 +815,52 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       if (stop) break;
 
       // ---------------- epilogue of sequence b's segment
-      #pragma unroll 1
+#pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        uint32_t la[32], lb[32];
-        tmem_ld64(which ? lx_tmem : l_tmem, la, lb);
-        float lsum[64];
+        uint32_t lv[32];
+        tmem_ld32(which ? lx_tmem : l_tmem, lv);
+        tmem_ld_wait(lv);
+        float lsum[32];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          lsum[h] = __uint_as_float(la[h]);
-          lsum[h + 32] = __uint_as_float(lb[h]);
-        }
-        float r0, r1;
-        warp_reduce_scatter64<false>(lsum, r0, r1);
-        red[which * 256 + sw * 64 + 2 * lane] = r0;
-        red[which * 256 + sw * 64 + 2 * lane + 1] = r1;
+        for (int h = 0; h < 32; ++h) lsum[h] = __uint_as_float(lv[h]);
+        red[which * 256 + wq * 64 + h0 + lane] = warp_reduce_scatter32<false>(lsum);
       }
       named_bar_sync(1, kSoftmaxThreads);
-      if (t128 < kH) {
-        const float l = (red[t128] + red[64 + t128]) + (red[128 + t128] + red[192 + t128]);
-        linv[t128] = 1.f / l;
-        const float lx = (red[256 + t128] + red[320 + t128]) + (red[384 + t128] + red[448 + t128]);
-        const float lse_v = (m_ref[t128] + log2f(lx)) * 0.69314718055994531f;
+      if (ts < kH) {
+        const float l = (red[ts] + red[64 + ts]) + (red[128 + ts] + red[192 + ts]);
+        linv[kb * kH + ts] = 1.f / l;
+        const float lx = (red[256 + ts] + red[320 + ts]) + (red[384 + ts] + red[448 + ts]);
+        const float lse_v = (m_ref[ts] + log2f(lx)) * 0.69314718055994531f;
         if (whole) {
-          if (p.lse != nullptr) p.lse[b * kH + t128] = lse_v;
+          if (p.lse != nullptr) p.lse[b * kH + ts] = lse_v;
         } else {
-          p.part_lse[static_cast<size_t>(slot_p) * kH + t128] = lse_v;
+          p.part_lse[static_cast<size_t>(slot_p) * kH + ts] = lse_v;
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
-      const bool okO = wait_warp(bar(kBarOFull + kb), (s >> 1) & 1, abort_flag);
-      aborted = aborted || !okO;
-      if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) break;
-      tc_fence_after();
-      #pragma unroll 1
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t oa[32], ob[32];
-        tmem_ld64(tmem + kTmemO + 128u * kb + 64u * hh + lane_base, oa, ob);
-        const int d = 128 * hh + row;
-        if (whole && !p.out_f32) {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(b) * kH * kD + d;
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            dst[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * linv[h]);
-            dst[(h + 32) * kD] = __float2bfloat16_rn(__uint_as_float(ob[h]) * linv[h + 32]);
-          }
-        } else {
-          float* dst = whole ? static_cast<float*>(p.out) + static_cast<size_t>(b) * kH * kD + d
-                             : p.part_o + static_cast<size_t>(slot_p) * kH * kD + d;
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            dst[h * kD] = __uint_as_float(oa[h]) * linv[h];
-            dst[(h + 32) * kD] = __uint_as_float(ob[h]) * linv[h + 32];
-          }
-        }
+      if (s + 2 < nseg) {
+        // the accumulator is needed again by segment s + 2: write it out now
+        if (!write_segment(s, b, slot_p, whole, false, 0)) break;
+      } else {
+        // one of the CTA's last two segments: its accumulator stays in tensor memory
+        // and is written after the last tile, when the ring is idle
+        defer_b[kb] = b;
+        defer_slot[kb] = slot_p;
+        defer_whole[kb] = whole;
       }
-      tc_fence_before();
-      mbar_arrive(bar(kBarOEmpty + kb));
-      named_bar_sync(1, kSoftmaxThreads);
     }
-    if (aborted && t128 == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
+    if (!aborted && !*abort_flag) {
+      // deferred accumulators, newest first: the wait for the last segment's accumulator
+      // also means every MMA has finished reading the ring, which then stages the rows
+      // (uniform: every thread reads the same values)
+      const int first_def = nseg >= 2 ? nseg - 2 : 0;
+      for (int s = nseg - 1; s >= first_def; --s) {
+        const int kb = s & 1;
+        if (!write_segment(s, defer_b[kb], defer_slot[kb], defer_whole[kb], true, s - first_def)) break;
+      }
+    }
+    if (issuer) bulk_wait_read0();
+    if (aborted && ts == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
   }
 
   // ---------------- teardown
@@ -765,21 +881,27 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long W, long long G
 }
 
 constexpr int kCombineThreads = 256;
-constexpr int kCombineGroups = 4;            // groups of 64 threads; each takes every 4th partial
 constexpr int kCombineMaxParts = 256;        // partials staged per pass
 
-// One CTA per (sequence, head).  The head's partial lse values are staged in
-// shared memory; thread group k of 4 accumulates partials k, k+4, ... with
-// float4 loads (64 threads x 4 = 256 d), and the groups are summed at the end.
+// One CTA per (sequence, group of `heads_per_cta` heads).  The 256 threads form
+// four quads of 64 (each thread owns 4 consecutive d, a float4).  With one head
+// per CTA the quads split the partials four ways; with four or more heads each
+// quad owns a head and the CTA walks its heads in rounds of four.  Partial lse
+// values are staged in shared memory; partial O rows stream in with batched
+// independent float4 loads.
 __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
   grid_dep_wait();
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
-  __shared__ float wts[kCombineMaxParts];
-  __shared__ float4 part_acc[kCombineGroups - 1][64];
-  __shared__ float pass_max, pass_sum;
+  __shared__ float wts[4][kCombineMaxParts];
+  __shared__ float4 part_acc[3][64];
+  __shared__ float pass_max[4], pass_sum[4];
   __shared__ int nparts_s;
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.x;
+  const int hpc = p.heads_per_cta;
+  const int hpr = hpc < 4 ? hpc : 4;          // heads per round
+  const int groups = 4 / hpr;                 // quads sharing one head
+  const int rounds = hpc / hpr;
   const int cap = p.max_pages * kPage;
   int before = 0, total = 0;
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
@@ -811,105 +933,131 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
 
-  const int grp = threadIdx.x >> 6;
-  const int d4 = threadIdx.x & 63;   // float4 column: d = 4*d4 .. 4*d4+3
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float run_max = -INFINITY, run_sum = 0.f;   // merged over the passes (same in every thread)
-  // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
-  for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
-    const int ge = min(g1 + 1, gs + kCombineMaxParts);
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      // compact the non-empty CTAs of [gs, ge) into slots[] (ballot over the warp)
-      int n = 0;
-      for (int g = gs + threadIdx.x; g - threadIdx.x < ge; g += 32) {
-        const bool live = g < ge && (static_cast<long long>(g) * total) / p.num_ctas !=
-                                        (static_cast<long long>(g + 1) * total) / p.num_ctas;
-        const unsigned m = __ballot_sync(0xffffffffu, live);
-        if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
-        n += __popc(m);
+  const int quad = threadIdx.x >> 6;
+  const int hr = quad / groups;               // head of the round owned by this quad
+  const int grp = quad % groups;              // partial group within that head
+  const int d4 = threadIdx.x & 63;            // float4 column: d = 4*d4 .. 4*d4+3
+  for (int r = 0; r < rounds; ++r) {
+    const int h = blockIdx.y * hpc + r * hpr + hr;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float run_max = -INFINITY, run_sum = 0.f;
+    // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
+    for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
+      const int ge = min(g1 + 1, gs + kCombineMaxParts);
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        int n = 0;
+        for (int g = gs + threadIdx.x; g - static_cast<int>(threadIdx.x) < ge; g += 32) {
+          const bool live = g < ge && (static_cast<long long>(g) * total) / p.num_ctas !=
+                                          (static_cast<long long>(g + 1) * total) / p.num_ctas;
+          const unsigned m = __ballot_sync(0xffffffffu, live);
+          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
+          n += __popc(m);
+        }
+        if (threadIdx.x == 0) nparts_s = n;
       }
-      if (threadIdx.x == 0) nparts_s = n;
-    }
-    __syncthreads();
-    const int n = nparts_s;
-    for (int k = threadIdx.x; k < n; k += kCombineThreads)
-      wts[k] = p.part_lse[static_cast<size_t>(slots[k]) * kH + h];
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      float m = -INFINITY;
-      for (int k = threadIdx.x; k < n; k += 32) m = fmaxf(m, wts[k]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-      for (int k = threadIdx.x; k < n; k += 32) {
-        const float w = expf(wts[k] - m);
-        wts[k] = w;
-        sum += w;
+      __syncthreads();
+      const int n = nparts_s;
+      for (int k = threadIdx.x; k < n * hpr; k += kCombineThreads) {
+        const int kk = k / hpr, hh = k % hpr;
+        wts[hh][kk] = p.part_lse[static_cast<size_t>(slots[kk]) * kH + blockIdx.y * hpc + r * hpr + hh];
       }
+      __syncthreads();
+      {
+        // warp w < hpr turns head w's lse values into weights relative to their max
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        if (w < hpr) {
+          float m = -INFINITY;
+          for (int k = l; k < n; k += 32) m = fmaxf(m, wts[w][k]);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (threadIdx.x == 0) {
-        pass_max = m;
-        pass_sum = sum;
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          float sum = 0.f;
+          for (int k = l; k < n; k += 32) {
+            const float e = expf(wts[w][k] - m);
+            wts[w][k] = e;
+            sum += e;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (l == 0) {
+            pass_max[w] = m;
+            pass_sum[w] = sum;
+          }
+        }
+      }
+      __syncthreads();
+      // rescale what earlier passes accumulated to this pass's reference
+      const float m_new = fmaxf(run_max, pass_max[hr]);
+      const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
+      const float a_new = expf(pass_max[hr] - m_new);
+      acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
+      run_sum = run_sum * a_old + pass_sum[hr] * a_new;
+      run_max = m_new;
+      const float* wrow = wts[hr];
+      int k = grp;
+      for (; k + 3 * groups < n; k += 4 * groups) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v[u] = reinterpret_cast<const float4*>(
+              p.part_o + (static_cast<size_t>(slots[k + u * groups]) * kH + h) * kD)[d4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = wrow[k + u * groups] * a_new;
+          acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
+          acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+        }
+      }
+      for (; k < n; k += groups) {
+        const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
+        const float w = wrow[k] * a_new;
+        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
       }
     }
-    __syncthreads();
-    // rescale what earlier passes accumulated to this pass's reference
-    const float m_new = fmaxf(run_max, pass_max);
-    const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
-    const float a_new = expf(pass_max - m_new);
-    acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
-    run_sum = run_sum * a_old + pass_sum * a_new;
-    run_max = m_new;
-    int k = grp;
-    for (; k + 3 * kCombineGroups < n; k += 4 * kCombineGroups) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        v[u] = reinterpret_cast<const float4*>(
-            p.part_o + (static_cast<size_t>(slots[k + u * kCombineGroups]) * kH + h) * kD)[d4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = wts[k + u * kCombineGroups] * a_new;
-        acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
-        acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+    if (groups > 1) {
+      __syncthreads();
+      if (grp > 0) part_acc[grp - 1][d4] = acc;
+      __syncthreads();
+      if (grp != 0) continue;
+      for (int k = 0; k < groups - 1; ++k) {
+        const float4 o = part_acc[k][d4];
+        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
       }
     }
-    for (; k < n; k += kCombineGroups) {
-      const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
-      const float w = wts[k] * a_new;
-      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    const float inv = 1.f / run_sum;
+    const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
+    if (p.out_f32) {
+      reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
     }
+    if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h] = run_max + logf(run_sum);
   }
-  if (grp > 0) part_acc[grp - 1][d4] = acc;
-  __syncthreads();
-  if (grp != 0) return;
-#pragma unroll
-  for (int k = 0; k < kCombineGroups - 1; ++k) {
-    const float4 o = part_acc[k][d4];
-    acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
-  }
-  const float inv = 1.f / run_sum;
-  const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
-  if (p.out_f32) {
-    reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  } else {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 pk;
-    pk.x = *reinterpret_cast<uint32_t*>(&lo);
-    pk.y = *reinterpret_cast<uint32_t*>(&hi);
-    reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
-  }
-  if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h] = run_max + logf(run_sum);
 }
 
 // ------------------------------------------------------------------ host side
 
 constexpr uint64_t kWsHeader = 256;
+
+// Text of the last CUDA failure seen by this host thread (static strings only).
+static thread_local const char* g_last_error = "no error";
+
+static mfa_status cuda_fail(cudaError_t e, const char* where) {
+  (void)where;
+  g_last_error = cudaGetErrorString(e);
+  return MFA_ERR_CUDA;
+}
+static mfa_status cuda_fail_msg(const char* msg) {
+  g_last_error = msg;
+  return MFA_ERR_CUDA;
+}
 
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
@@ -960,7 +1108,7 @@ static mfa_status check_plan(const mfa_plan* pl, const mfa_problem* pr) {
 static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const void* q, const void* k,
                               const void* v) {
   auto enc = encode_fn();
-  if (enc == nullptr) return MFA_ERR_CUDA;
+  if (enc == nullptr) return cuda_fail_msg("cuTensorMapEncodeTiled is not available from the driver");
   {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr->batch) * kH};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
@@ -969,7 +1117,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
     if (enc(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MFA_ERR_CUDA;
+      return cuda_fail_msg("cuTensorMapEncodeTiled rejected a tensor map");
   }
   const void* pools[2] = {k, v};
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
@@ -982,7 +1130,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
     if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return MFA_ERR_CUDA;
+      return cuda_fail_msg("cuTensorMapEncodeTiled rejected a tensor map");
   }
   return MFA_OK;
 }
@@ -1002,7 +1150,11 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH, 1);
+  // about two CTAs per SM: many sequences -> more heads per CTA
+  const long long want = 2LL * (pl->num_sms > 0 ? pl->num_sms : 148);
+  cp.heads_per_cta = (static_cast<long long>(pr->batch) * kH >= 16 * want) ? 16
+                     : (static_cast<long long>(pr->batch) * kH >= 4 * want) ? 4 : 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH / cp.heads_per_cta, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -1011,7 +1163,8 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, mfa_combine_kernel, cp) != cudaSuccess) return MFA_ERR_CUDA;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, mfa_combine_kernel, cp);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return MFA_OK;
 }
 
@@ -1022,6 +1175,8 @@ using namespace mfa;
 extern "C" {
 
 int32_t mfa_abi_version(void) { return MFA_ABI_VERSION; }
+
+const char* mfa_last_cuda_error(void) { return g_last_error; }
 
 const char* mfa_status_string(mfa_status s) {
   switch (s) {
@@ -1053,8 +1208,10 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   }
   if (num_sms <= 0) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MFA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MFA_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   }
   long long G;
   if (force_ctas > 0) {
@@ -1124,10 +1281,10 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
 
   const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
-  if (check && cudaMemsetAsync(ws, 0, 4, stream) != cudaSuccess) return MFA_ERR_CUDA;
-  if (cudaFuncSetAttribute(mfa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
-    return MFA_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (check && (e = cudaMemsetAsync(ws, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
+  e = cudaFuncSetAttribute(mfa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1135,15 +1292,16 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (cudaLaunchKernelEx(&cfg, mfa_decode_kernel, prm) != cudaSuccess) return MFA_ERR_CUDA;
+  e = cudaLaunchKernelEx(&cfg, mfa_decode_kernel, prm);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (plan->num_ctas > 1 && (plan->flags & MFA_PLAN_NO_COMBINE) == 0) {
     st = launch_combine(plan, pr, workspace, seq_lens, out, lse, stream, true);
     if (st != MFA_OK) return st;
   }
   if (check) {
     uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MFA_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return MFA_ERR_CUDA;
+    if ((e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, stream)) != cudaSuccess) return cuda_fail(e, "copy");
+    if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "sync");
     if (word != 0) return MFA_ERR_DEVICE_CHECK;
   }
   return MFA_OK;
@@ -1168,9 +1326,10 @@ mfa_status mfa_read_device_status(void* workspace, uint32_t* status_bits, int32_
   if (workspace == nullptr || status_bits == nullptr || !aligned(workspace, 256)) return MFA_ERR_INVALID_ARG;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint32_t word = 0;
-  if (cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MFA_ERR_CUDA;
-  if (clear && cudaMemsetAsync(workspace, 0, 4, stream) != cudaSuccess) return MFA_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return MFA_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy");
+  if (clear && (e = cudaMemsetAsync(workspace, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "sync");
   *status_bits = word;
   return MFA_OK;
 }

@@ -183,6 +183,10 @@ const char* mfa_status_string(mfa_status status);
 /* MFA_ABI_VERSION of the loaded library. */
 int32_t mfa_abi_version(void);
 
+/* Text of the last CUDA failure behind an MFA_ERR_CUDA on the calling host thread
+ * ("no error" if none); a static string, valid until the next call on this thread. */
+const char* mfa_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif
