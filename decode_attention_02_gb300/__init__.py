@@ -38,6 +38,7 @@ MFA_DEV_SCHEDULE = 0x8
 
 MFA_PLAN_CHECK = 0x1
 MFA_PLAN_NO_COMBINE = 0x2
+MFA_PLAN_EARLY_METADATA = 0x4
 
 NUM_Q_HEADS = 64
 HEAD_DIM = 256

@@ -113,6 +113,7 @@ struct DecodeParams {
   int max_pages;
   int num_blocks;
   int out_f32;        // 1: fp32 output, 0: bf16 output
+  int early_metadata; // 1: seq_lens/block_table may be read before the preceding grid completes
   float scale_log2;   // softmax_scale * log2(e)
 };
 
@@ -345,6 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     tma_prefetch_desc(&p.tm_v);
   }
 
+  // Launched as a programmatic dependent of the preceding kernel on the stream: nothing
+  // that kernel may write is touched before griddepcontrol.wait.  With early metadata
+  // the lengths and the block table are read first (the caller guarantees the preceding
+  // kernel does not write them); q, K, V and every output wait.
+  if (!p.early_metadata) grid_dep_wait();
+
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
   const int cap = p.max_pages * kPage;
   {
@@ -419,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
     __syncwarp();
     if (lane == 0 && ntiles > 0) {
+      if (p.early_metadata) grid_dep_wait();
       const uint64_t pol = l2_policy_evict_first();
       uint32_t u = 0;       // ring uses issued
       int nq = 0;           // Q loads issued
@@ -579,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     const float c = p.scale_log2;
     const bool issuer = (lane == 0) && ((sw & 3) == 0);   // one bulk-store thread per head half
 
+    if (p.early_metadata) grid_dep_wait();
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       bool dummy = false;
@@ -891,6 +900,7 @@ constexpr int kCombineMaxParts = 256;        // partials staged per pass
 // independent float4 loads.
 __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
   grid_dep_wait();
+  grid_dep_launch();   // the next kernel may start its own set-up
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
   __shared__ float wts[4][kCombineMaxParts];
@@ -1279,6 +1289,7 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.max_pages = pr->max_pages_per_seq;
   prm.num_blocks = pr->num_blocks;
   prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
+  prm.early_metadata = (plan->flags & MFA_PLAN_EARLY_METADATA) ? 1 : 0;
 
   const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
   cudaError_t e = cudaSuccess;
@@ -1290,8 +1301,11 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, mfa_decode_kernel, prm);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (plan->num_ctas > 1 && (plan->flags & MFA_PLAN_NO_COMBINE) == 0) {

@@ -208,6 +208,25 @@ def test_length_beyond_table_is_reported():
     assert mfa.mfa_read_device_status(dec.workspace) & mfa.MFA_DEV_BAD_LENGTH
 
 
+def test_early_metadata_chain_matches():
+    """Back-to-back steps with MFA_PLAN_EARLY_METADATA (decode launched as a programmatic
+    dependent of the previous step's combine) give the same bits as plain steps."""
+    case = inputs.small("pdl", 6, [4096, 1000, 64, 2500, 1, 3000], seed=19)
+    ref16, refl, _ = gpu_decode(case, out_dtype=mfa.MFA_OUT_BF16)
+    t = to_dev(case)
+    dec = mfa.Decoder(6, case.max_pages, case.num_blocks, host_seq_lens=case.seq_lens.tolist(),
+                      flags=mfa.MFA_PLAN_EARLY_METADATA)
+    outs = []
+    for _ in range(4):
+        o, l = dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"])
+        outs.append((o, l))
+    torch.cuda.synchronize()
+    assert mfa.mfa_read_device_status(dec.workspace) == 0
+    for o, l in outs:
+        assert torch.equal(o.view(torch.int16), ref16.view(torch.int16))
+        assert torch.equal(l, refl)
+
+
 def test_runs_on_a_side_stream():
     case = inputs.small("stream", 3, [700, 50, 1300], seed=17)
     s = torch.cuda.Stream()
