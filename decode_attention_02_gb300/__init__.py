@@ -46,7 +46,11 @@ PAGE_SIZE = 64
 
 # Every symbol include/mfa.h declares.
 EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
-                    "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error")
+                    "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error",
+                    "mfa_decode_run_static_workspace")
+
+# Size of the library's own scratch array used by mfa_decode_run_static_workspace.
+MFA_STATIC_WORKSPACE_BYTES = 24 * 1024 * 1024
 
 
 class MfaProblem(ctypes.Structure):
@@ -103,6 +107,9 @@ def load_library(path: str = LIB_PATH):
     lib.mfa_abi_version.restype = ctypes.c_int32
     lib.mfa_last_cuda_error.argtypes = []
     lib.mfa_last_cuda_error.restype = ctypes.c_char_p
+    lib.mfa_decode_run_static_workspace.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P,
+                                                    P, P, P, P, P, P, P]
+    lib.mfa_decode_run_static_workspace.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -175,6 +182,20 @@ def mfa_decode_run(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_sc
                             _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out),
                             _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "mfa_decode_run")
+
+
+def mfa_decode_run_static_workspace(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_scale, v_scale,
+                                    block_table, seq_lens, out, lse, stream=None) -> None:
+    """mfa_decode_run with the library's own fixed scratch array instead of a workspace.
+
+    For callers that must not allocate device memory; see include/mfa.h for the
+    size limit and the rule that calls sharing a device must not overlap.
+    """
+    lib = load_library()
+    st = lib.mfa_decode_run_static_workspace(ctypes.byref(plan), ctypes.byref(problem), _ptr(q), _ptr(k_cache),
+                                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                                             _ptr(seq_lens), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "mfa_decode_run_static_workspace")
 
 
 def mfa_combine(plan: MfaPlan, problem: MfaProblem, workspace, seq_lens, out, lse, stream=None,

@@ -35,6 +35,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "mfa.h"
@@ -1349,3 +1350,49 @@ mfa_status mfa_read_device_status(void* workspace, uint32_t* status_bits, int32_
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ workspace-free entry point
+//
+// Scratch for mfa_decode_run_static_workspace(): one fixed array per device that
+// loads this library, held until the process exits.  In host code the symbol is
+// only a stand-in; its device address comes from cudaGetSymbolAddress, looked up
+// once per device with that device current.
+static __device__ __align__(256) unsigned char g_static_workspace[MFA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" mfa_status mfa_decode_run_static_workspace(
+    const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache, const void* v_cache,
+    const float* k_scale, const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out,
+    float* lse, void* stream_ptr) {
+  mfa_status st = check_problem(pr);
+  if (st != MFA_OK) return st;
+  st = check_plan(plan, pr);
+  if (st != MFA_OK) return st;
+  if (plan->workspace_bytes > MFA_STATIC_WORKSPACE_BYTES) return MFA_ERR_WORKSPACE;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return MFA_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (g_static_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_static_workspace);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+      g_static_ptr[dev] = ptr;
+    }
+    ws = g_static_ptr[dev];
+  }
+  // the status word is the only part that must start at zero; partial results are
+  // always written before they are read
+  e = cudaMemsetAsync(ws, 0, 4, static_cast<cudaStream_t>(stream_ptr));
+  if (e != cudaSuccess) return cuda_fail(e, "memset");
+  return mfa_decode_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse, ws,
+                        MFA_STATIC_WORKSPACE_BYTES, stream_ptr);
+}

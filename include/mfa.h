@@ -186,6 +186,35 @@ mfa_status mfa_read_device_status(void* workspace, uint32_t* status_bits, int32_
 /* Static description of a status code. */
 const char* mfa_status_string(mfa_status status);
 
+/*
+ * mfa_decode_run without a caller-supplied workspace.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory: for example a plugin inside a host application whose own
+ * allocator owns the GPU's memory (a cudaMalloc from the plugin would bypass the
+ * application's accounting), or a latency-critical path where cudaMalloc's
+ * implicit device synchronisation is not acceptable.
+ *
+ * The scratch is a fixed array of MFA_STATIC_WORKSPACE_BYTES inside the library,
+ * created on every device that loads it and kept until the process exits.  This
+ * call allocates nothing.  Its first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  Each call clears the array's status word,
+ * then enqueues exactly what mfa_decode_run enqueues (MFA_PLAN_CHECK included).
+ * All calls on a device share the one array and it keeps the last call's
+ * contents, so two calls whose kernels may overlap on the GPU (different
+ * streams, no ordering between them) race on it: order them on one stream.
+ * Plans whose workspace_bytes exceed MFA_STATIC_WORKSPACE_BYTES are rejected
+ * with MFA_ERR_WORKSPACE; at the default 24 MiB that covers
+ * batch + num_ctas - 1 <= 382 partial slots (for example B <= 231 on 152 SMs).
+ * Arguments are those of mfa_decode_run without the workspace.
+ */
+#define MFA_STATIC_WORKSPACE_BYTES (24u * 1024u * 1024u)
+mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_problem* problem,
+                                           const void* q, const void* k_cache, const void* v_cache,
+                                           const float* k_scale, const float* v_scale,
+                                           const int32_t* block_table, const int32_t* seq_lens,
+                                           void* out, float* lse, void* stream);
+
 /* MFA_ABI_VERSION of the loaded library. */
 int32_t mfa_abi_version(void);
 
