@@ -35,6 +35,7 @@ MFA_DEV_TIMEOUT = 0x1
 MFA_DEV_BAD_BLOCK = 0x2
 MFA_DEV_BAD_LENGTH = 0x4
 MFA_DEV_SCHEDULE = 0x8
+MFA_DEV_RANGE = 0x10
 
 MFA_PLAN_CHECK = 0x1
 MFA_PLAN_NO_COMBINE = 0x2

@@ -49,8 +49,6 @@ constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
-constexpr int kNumSlots = 10;
-constexpr int kSlotBytes = 16384;
 constexpr int kMaxTilesPerCta = 128;
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
@@ -58,12 +56,40 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between resc
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
+// Shared-memory map (offsets from a 1024-byte aligned base).  Both KV formats put the
+// barriers at the same offset; they differ below it:
+//   bf16 : Q 32 KB | P 16 KB | ring 10 x 16 KB (K/V operand tiles as TMA writes them)
+//   e4m3 : Q 32 KB | P 16 KB | V f16 64 KB (dequantised PV operand) | ring 12 x 8 KB (raw
+//          e4m3 boxes) and, after the common area, a 4-tile ring of per-token scales
 constexpr int kOffQ = 0;                                     // 4 x [64 heads x 128 B]
 constexpr int kOffP = 32768;                                 // [128 tokens x 128 B]
-constexpr int kOffRing = 49152;                              // kNumSlots x 16 KB
-constexpr int kOffBar = kOffRing + kNumSlots * kSlotBytes;  // mbarriers
-constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..11] scan
+constexpr int kOffBar = 212992;                              // mbarriers
+template <bool kFp8>
+struct KvLayout;
+template <>
+struct KvLayout<false> {
+  static constexpr int kOffRing = 49152;
+  static constexpr int kNumSlots = 10;
+  static constexpr int kSlotBytes = 16384;
+  static constexpr int kOffStageFinal = kOffRing;   // 128 KB free after the last MMA
+  static constexpr int kExtraSmem = 0;
+};
+template <>
+struct KvLayout<true> {
+  static constexpr int kOffVh = 49152;              // 4 x 16 KB: (page, d-half) f16 tiles
+  static constexpr int kOffRing = 114688;
+  static constexpr int kNumSlots = 12;
+  static constexpr int kSlotBytes = 8192;
+  static constexpr int kOffStageFinal = kOffVh;     // V f16 + ring: 160 KB free after the last MMA
+  // scale ring, per tile: K scales of the 2 pages, then V scales of the 2 pages once per
+  // d-half (each half's box brings its own copy, so its consumers wait on their own box)
+  static constexpr int kScaleTiles = 4;
+  static constexpr int kScaleTileBytes = 6 * 256;
+  static constexpr int kExtraSmem = kScaleTiles * kScaleTileBytes;
+};
+static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
+static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
+constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..15] scan
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -72,13 +98,15 @@ constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, e
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileBlk = kOffSegN0 + 4 * kMaxSeg;    // int2[kMaxTilesPerCta] page ids
 constexpr int kSmemUsed = kOffTileBlk + 8 * kMaxTilesPerCta;
-constexpr int kSmemBytes = kSmemUsed + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr int kOffScale = kSmemUsed;                    // e4m3 only
+template <bool kFp8>
+constexpr int smem_bytes() { return kSmemUsed + KvLayout<kFp8>::kExtraSmem + 1024; }
+static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
 
 enum Bar : int {
   kBarFull = 0,
-  kBarEmpty = kBarFull + kNumSlots,
-  kBarQFull = kBarEmpty + kNumSlots,
+  kBarEmpty = kBarFull + 12,   // room for the larger ring
+  kBarQFull = kBarEmpty + 12,
   kBarQEmpty,
   kBarSFull,   // 2
   kBarSEmpty = kBarSFull + 2,
@@ -87,6 +115,9 @@ enum Bar : int {
   kBarOFull,   // 2
   kBarOEmpty = kBarOFull + 2,
   kBarDrain = kBarOEmpty + 2,
+  kBarQReady,   // e4m3: q converted to f16 in place
+  kBarKReady,   // e4m3: K tile dequantised into tensor memory
+  kBarKFree,    // e4m3: the QK MMAs have read that K tile
   kBarCount
 };
 static_assert(kBarCount * 8 <= 512, "barrier area");
@@ -94,12 +125,13 @@ static_assert(kBarCount * 8 <= 512, "barrier area");
 // Tensor-memory columns.
 constexpr uint32_t kTmemS = 0;     // S^T buffers: [0,64) and [64,128)
 constexpr uint32_t kTmemO = 128;   // O^T buffer k, half hh: 128 + 128k + 64hh
-constexpr uint32_t kTmemL = 384;   // per-lane row sums of the bf16-rounded weights (normalise O)
-constexpr uint32_t kTmemLx = 448;  // per-lane row sums of the fp32 weights (lse)
+constexpr uint32_t kTmemL = 384;   // bf16: per-lane row sums of the bf16-rounded weights (normalise O)
+constexpr uint32_t kTmemLx = 448;  // bf16: per-lane row sums of the fp32 weights (lse)
+constexpr uint32_t kTmemK = 384;   // e4m3: K tile in f16, lane = token, 2 d per column (A operand)
 
 struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
-  CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256], box {64, 64, 1}, 128B swizzle
+  CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256]: bf16 box {64, 64, 1}, e4m3 box {128, 64, 1}; 128B swizzle
   CUtensorMap tm_v;
   const float* k_scale;
   const float* v_scale;
@@ -305,7 +337,38 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 
 // ------------------------------------------------------------------ decode kernel
 
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  const uint16_t v = static_cast<uint16_t>(two_codes);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Ring use index of the K (is_v = false) or V part (page pg, d-half dh) of tile t of a
+// CTA with `ntiles` tiles.  The producer issues K(0), then K(t) and V(t-1) for t = 1..N-1,
+// then V(N-1), four uses each: K(0) = 0..3, K(t) = 8t-4.., V(t) = 8t+8.. except the last
+// tile's V, which directly follows its K: V(N-1) = 8N-4...
+__device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v, int pg, int dh) {
+  const uint32_t base = is_v ? (t + 1 < ntiles ? 8u * t + 8u : 8u * t + 4u) : (t == 0 ? 0u : 8u * t - 4u);
+  return base + 2u * pg + dh;
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
+  using Lay = KvLayout<kFp8>;
+  constexpr int kNumSlots = Lay::kNumSlots;
+  constexpr int kSlotBytes = Lay::kSlotBytes;
+  constexpr int kOffRing = Lay::kOffRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -321,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   if (tid == 0) {
     for (int i = 0; i < kNumSlots; ++i) {
       mbar_init(bar(kBarFull + i), 1);
-      mbar_init(bar(kBarEmpty + i), 1);
+      // bf16: released by the MMA commit; e4m3: by the 64 threads that dequantise the box
+      mbar_init(bar(kBarEmpty + i), kFp8 ? 64 : 1);
     }
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
@@ -334,6 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     mbar_init(bar(kBarPFull), kSoftmaxThreads);
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarQReady), kSoftmaxThreads);
+    mbar_init(bar(kBarKReady), kSoftmaxThreads);
+    mbar_init(bar(kBarKFree), 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -404,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   const int ntiles = misc[3];
 
   if (warp == 0) {
-    // ---------------- producer: page ids, then TMA loads of Q, K, V
+    // ---------------- producer: page ids, then TMA loads of Q, K, V (and e4m3 scales)
     bool bad_blk = false;
     // all of this CTA's page ids in one round of independent loads (lane = tile)
     for (int n = lane; n < ntiles; n += 32) {
@@ -433,6 +500,53 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       int nq = 0;           // Q loads issued
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
+      // one ring use: wait for the slot, then load a K or V part (bf16: chunk of 64 d over
+      // both pages, or page x d-half; e4m3: page x d-half box, plus the page's scales)
+      auto issue = [&](bool is_v, int t, int a, int b2, int r0, int r1, const int2 bk) -> bool {
+        const uint32_t slot = u % kNumSlots;
+        if (!wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag)) return false;
+        const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
+        const uint32_t fb = bar(kBarFull + slot);
+        const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+        if constexpr (!kFp8) {
+          if (!is_v) {   // a = 64-d chunk, both pages
+            mbar_arrive_expect_tx(fb, r1 > 0 ? 16384 : 8192);
+            tma_load_3d_hint(dst, map, fb, 64 * a, r0 - kPage, bk.x, pol);
+            if (r1 > 0) tma_load_3d_hint(dst + 8192, map, fb, 64 * a, r1 - kPage, bk.y, pol);
+          } else {       // a = page, b2 = d-half
+            const int r = a ? r1 : r0;
+            const int blk = a ? bk.y : bk.x;
+            if (r > 0) {
+              mbar_arrive_expect_tx(fb, 16384);
+              tma_load_3d_hint(dst, map, fb, 128 * b2, r - kPage, blk, pol);
+              tma_load_3d_hint(dst + 8192, map, fb, 128 * b2 + 64, r - kPage, blk, pol);
+            } else {
+              mbar_arrive(fb);
+            }
+          }
+        } else {         // a = page, b2 = d-half
+          const int r = a ? r1 : r0;
+          const int blk = a ? bk.y : bk.x;
+          if (r > 0) {
+            // K: the page's scales with its d-half-0 box (read only once QK has run, which
+            // needs both halves); V: a copy with each half's box, read by that half's threads
+            const bool with_scale = is_v || (b2 == 0);
+            mbar_arrive_expect_tx(fb, 8192 + (with_scale ? 256 : 0));
+            tma_load_3d_hint(dst, map, fb, 128 * b2, r - kPage, blk, pol);
+            if (with_scale) {
+              const float* src = (is_v ? p.v_scale : p.k_scale) + static_cast<size_t>(blk) * kPage;
+              const int idx = is_v ? 2 + 2 * a + b2 : a;
+              const uint32_t sdst = sbase + kOffScale + (t % KvLayout<true>::kScaleTiles) * KvLayout<true>::kScaleTileBytes +
+                                    idx * 256;
+              bulk_load_g2s(sdst, src, 256, fb);
+            }
+          } else {
+            mbar_arrive(fb);
+          }
+        }
+        ++u;
+        return true;
+      };
       for (int n = 0; n <= ntiles && ok; ++n) {
         if (n < ntiles) {
           const int4 sg = seg[sk];
@@ -447,16 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           const int2 bk = tile_blk[n];
           const int r0 = min(kPage, sg.w - kTile * jk);
           const int r1 = min(kPage, sg.w - kTile * jk - kPage);
-          for (int c = 0; c < 4; ++c, ++u) {
-            const uint32_t slot = u % kNumSlots;
-            ok = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
-            if (!ok) break;
-            const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
-            mbar_arrive_expect_tx(bar(kBarFull + slot), r1 > 0 ? 16384 : 8192);
-            tma_load_3d_hint(dst, &p.tm_k, bar(kBarFull + slot), 64 * c, r0 - kPage, bk.x, pol);
-            if (r1 > 0)
-              tma_load_3d_hint(dst + 8192, &p.tm_k, bar(kBarFull + slot), 64 * c, r1 - kPage, bk.y, pol);
-          }
+          for (int c = 0; c < 4 && ok; ++c) ok = issue(false, n, kFp8 ? (c >> 1) : c, c & 1, r0, r1, bk);
           if (!ok) break;
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
         }
@@ -465,23 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           const int2 bk = tile_blk[n - 1];
           const int rr0 = min(kPage, sg.w - kTile * jv);
           const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
-          for (int pg = 0; pg < 2 && ok; ++pg) {
-            const int r = pg ? rr1 : rr0;
-            const int blk = pg ? bk.y : bk.x;
-            for (int hh = 0; hh < 2; ++hh, ++u) {
-              const uint32_t slot = u % kNumSlots;
-              ok = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
-              if (!ok) break;
-              const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
-              if (r > 0) {
-                mbar_arrive_expect_tx(bar(kBarFull + slot), 16384);
-                tma_load_3d_hint(dst, &p.tm_v, bar(kBarFull + slot), 128 * hh, r - kPage, blk, pol);
-                tma_load_3d_hint(dst + 8192, &p.tm_v, bar(kBarFull + slot), 128 * hh + 64, r - kPage, blk, pol);
-              } else {
-                mbar_arrive(bar(kBarFull + slot));
-              }
-            }
-          }
+          for (int c = 0; c < 4 && ok; ++c) ok = issue(true, n - 1, c >> 1, c & 1, rr0, rr1, bk);
           if (!ok) break;
           if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
         }
@@ -489,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       if (!ok) {
         atomicOr(p.status, MFA_DEV_TIMEOUT);
         // let every copy already issued land before the CTA can exit
-        const uint32_t first = (u > kNumSlots) ? u - kNumSlots : 0;
+        const uint32_t first = (u > static_cast<uint32_t>(kNumSlots)) ? u - kNumSlots : 0;
         for (uint32_t v = first; v < u; ++v)
           wait_slow(bar(kBarFull + v % kNumSlots), (v / kNumSlots) & 1, nullptr, kDrainLimitNs);
         if (nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
@@ -498,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdescQK = idesc_f16(true, false, false, 128, 64);
-      constexpr uint32_t kIdescPV = idesc_f16(true, true, true, 128, 64);
+      constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
+      constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, 64);
       uint32_t u = 0;
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
@@ -507,25 +596,37 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         if (n < ntiles) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
-          if (first) ok = wait_bar(bar(kBarQFull), sk & 1, abort_flag);
+          if (first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + 64u * (n & 1);
-          for (int c = 0; c < 4; ++c, ++u) {
-            const uint32_t slot = u % kNumSlots;
-            ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+          if constexpr (!kFp8) {
+            for (int c = 0; c < 4; ++c, ++u) {
+              const uint32_t slot = u % kNumSlots;
+              ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
+              const uint32_t b0 = sbase + kOffQ + c * 8192;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f16_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
+                            kIdescQK, (c | kk) != 0);
+              umma_commit(bar(kBarEmpty + slot));
+            }
+            if (!ok) break;
+          } else {
+            // K(n) in tensor memory: lane = token, column kTmemK + d/2
+            ok = wait_bar(bar(kBarKReady), n & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
-            const uint32_t b0 = sbase + kOffQ + c * 8192;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_f16_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
-                          kIdescQK, (c | kk) != 0);
-            umma_commit(bar(kBarEmpty + slot));
+            for (int kk = 0; kk < 16; ++kk)
+              umma_f16_ts(d_tmem, tmem + kTmemK + 8u * kk,
+                          smem_desc(sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3), 16, 1024), kIdescQK, kk != 0);
+            umma_commit(bar(kBarKFree));
           }
-          if (!ok) break;
           umma_commit(bar(kBarSFull + (n & 1)));
           if (last) umma_commit(bar(kBarQEmpty));
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
@@ -543,13 +644,18 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
           for (int pg = 0; pg < 2 && ok; ++pg) {
             const int r = pg ? rr1 : rr0;
-            for (int hh = 0; hh < 2; ++hh, ++u) {
-              const uint32_t slot = u % kNumSlots;
-              ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
-              if (!ok) break;
-              tc_fence_after();
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t a0;
+              if constexpr (!kFp8) {
+                const uint32_t slot = u % kNumSlots;
+                ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                a0 = sbase + kOffRing + slot * kSlotBytes;
+              } else {
+                a0 = sbase + KvLayout<true>::kOffVh + (2 * pg + hh) * 16384;   // filled by the softmax warps
+              }
               if (r > 0) {
-                const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
                 const uint32_t b0 = sbase + kOffP + pg * 8192;
                 const uint32_t d_tmem = tmem + kTmemO + 128u * kb + 64u * hh;
 #pragma unroll
@@ -558,7 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
                               smem_desc(b0 + 2048 * kk, 1024, 1024), kIdescPV,
                               !(first && pg == 0 && kk == 0));
               }
-              umma_commit(bar(kBarEmpty + slot));
+              if constexpr (!kFp8) {
+                umma_commit(bar(kBarEmpty + u % kNumSlots));
+                ++u;
+              }
             }
           }
           if (!ok) break;
@@ -576,10 +685,11 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     // ---------------- softmax + epilogue (256 threads: two warps per TMEM lane quarter)
     const int ts = tid - 64;                       // 0..255
     const int sw = warp - 2;                       // 0..7
-    const int grp = sw >> 2;                       // head half: heads [32*grp, 32*grp + 32)
+    const int grp = sw >> 2;                       // head half [32*grp, +32); e4m3 dequant: d-half
     const int h0 = 32 * grp;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;                // token row of a tile / d within an O half
+    const int rpg = row >> 6, ri = row & 63;       // page of the tile and row within the page
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     float* m_ref = reinterpret_cast<float*>(smem + kOffMref);
     float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
@@ -587,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     float* linv = reinterpret_cast<float*>(smem + kOffLinv);
     const float c = p.scale_log2;
     const bool issuer = (lane == 0) && ((sw & 3) == 0);   // one bulk-store thread per head half
+    bool range_bad = false;                        // e4m3: a value left the f16 range
 
     if (p.early_metadata) grid_dep_wait();
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
@@ -601,16 +712,105 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
 
     bool aborted = false;
     int n = 0;
-    const uint32_t l_tmem = tmem + kTmemL + h0 + lane_base;    // this thread's 32 row-sum partials
-    const uint32_t lx_tmem = tmem + kTmemLx + h0 + lane_base;  // and their fp32-weight twins
+    const uint32_t l_tmem = tmem + kTmemL + h0 + lane_base;    // bf16: this thread's 32 row-sum partials
+    const uint32_t lx_tmem = tmem + kTmemLx + h0 + lane_base;  // bf16: and their fp32-weight twins
+    float lreg[32];                                            // e4m3: row-sum partials in registers
     int defer_b[2] = {0, 0}, defer_slot[2] = {0, 0};
     bool defer_whole[2] = {false, false};
 
+    // valid rows of a tile's page pg: the last page's rows sit at the end of the box
+    auto page_rows = [&](int L, int j, int pg) { return min(kPage, L - kTile * j - kPage * pg); };
+
+    // e4m3: per-token scale of this thread's row in tile t (0 for rows past the length)
+    auto row_scale = [&](int t, bool is_v, int rp) -> float {
+      if (rp <= 0 || ri < kPage - rp) return 0.f;
+      const int idx = is_v ? 2 + 2 * rpg + grp : rpg;
+      const float* sc = reinterpret_cast<const float*>(
+          smem + kOffScale + (t % KvLayout<true>::kScaleTiles) * KvLayout<true>::kScaleTileBytes + idx * 256);
+      return sc[ri - (kPage - rp)];
+    };
+
+    // e4m3: wait until ring use `use` is filled (every consumer waits, even when its page
+    // is past the sequence end and nothing is read, so that the slot's full and empty
+    // phases advance in step with the producer's)
+    auto wait_filled = [&](uint32_t use) -> bool {
+      return wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
+    };
+    // e4m3: this thread's 128 raw codes (its token row, its d-half) of a filled ring box
+    auto read_raw = [&](uint32_t use, uint4 (&rw)[8]) {
+      const uint8_t* box = smem + kOffRing + (use % kNumSlots) * kSlotBytes + ri * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) rw[q] = *reinterpret_cast<const uint4*>(box + ((q ^ (ri & 7)) << 4));
+    };
+    // e4m3: dequantise tile t's K part of this thread into tensor memory (lane = token)
+    auto dequant_k = [&](int t, int L, int j) -> bool {
+      if (t >= 1 && !wait_warp(bar(kBarKFree), (t - 1) & 1, abort_flag)) return false;
+      const uint32_t use = ring_use(t, ntiles, false, rpg, grp);
+      if (!wait_filled(use)) return false;
+      if (page_rows(L, j, rpg) > 0) {
+        uint4 rw[8];
+        read_raw(use, rw);
+        tc_fence_after();
+#pragma unroll
+        for (int hq = 0; hq < 2; ++hq) {
+          uint32_t kv[32];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 w = rw[4 * hq + q];
+            kv[8 * q + 0] = e4m3x2_to_f16x2(w.x);
+            kv[8 * q + 1] = e4m3x2_to_f16x2(w.x >> 16);
+            kv[8 * q + 2] = e4m3x2_to_f16x2(w.y);
+            kv[8 * q + 3] = e4m3x2_to_f16x2(w.y >> 16);
+            kv[8 * q + 4] = e4m3x2_to_f16x2(w.z);
+            kv[8 * q + 5] = e4m3x2_to_f16x2(w.z >> 16);
+            kv[8 * q + 6] = e4m3x2_to_f16x2(w.w);
+            kv[8 * q + 7] = e4m3x2_to_f16x2(w.w >> 16);
+          }
+          tmem_st32(tmem + kTmemK + 64u * grp + 32u * hq + lane_base, kv);
+        }
+        tmem_st_wait();
+      }
+      mbar_arrive(bar(kBarEmpty + use % kNumSlots));
+      tc_fence_before();
+      mbar_arrive(bar(kBarKReady));
+      return true;
+    };
+    // e4m3: dequantise tile t's V part of this thread into the f16 PV operand tile; the
+    // token's V scale (it arrives with the box) multiplies the row here, so that P keeps
+    // plain weights.  Scales above 146 would let 448 * scale leave the f16 range: they
+    // are clamped and reported.
+    auto dequant_v = [&](int t, int L, int j) -> bool {
+      const uint32_t use = ring_use(t, ntiles, true, rpg, grp);
+      if (!wait_filled(use)) return false;
+      const int rp = page_rows(L, j, rpg);
+      if (rp > 0) {
+        uint4 rw[8];
+        read_raw(use, rw);
+        float sv = row_scale(t, true, rp);             // 0 for rows past the length
+        range_bad |= !(sv <= 146.f);
+        sv = fminf(sv, 146.f);
+        const uint32_t sv2 = pack_f16_sat(sv, sv);
+        auto cv = [&](uint32_t two) { return hmul2(e4m3x2_to_f16x2(two), sv2); };
+        // [64 tokens x 64 d] f16 boxes, 128 B rows, 128B swizzle (as TMA would lay them out)
+        uint8_t* vh = smem + KvLayout<true>::kOffVh + (2 * rpg + grp) * 16384 + ri * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 w = rw[q];
+          const uint4 lo = make_uint4(cv(w.x), cv(w.x >> 16), cv(w.y), cv(w.y >> 16));
+          const uint4 hi = make_uint4(cv(w.z), cv(w.z >> 16), cv(w.w), cv(w.w >> 16));
+          const int j0 = 2 * q, j1 = 2 * q + 1;   // 16-byte f16 chunks 0..15 of the 128-d row
+          *reinterpret_cast<uint4*>(vh + (j0 >> 3) * 8192 + (((j0 & 7) ^ (ri & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(vh + (j1 >> 3) * 8192 + (((j1 & 7) ^ (ri & 7)) << 4)) = hi;
+        }
+      }
+      mbar_arrive(bar(kBarEmpty + use % kNumSlots));
+      return true;
+    };
     // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx & 1),
     // normalised by 1/l from linv: [head][d] rows are staged in shared memory and sent
-    // with bulk async copies.  With `from_ring` the rows go through the idle ring at
-    // 64 KB offset `ring_k`; otherwise through this half's 8 KB of the P buffer in
-    // double-buffered 4 KB rounds.  Returns false if the CTA is aborting.
+    // with bulk async copies.  With `from_ring` the rows go through the idle operand
+    // buffers at 64 KB offset `ring_k`; otherwise through this half's 8 KB of the P
+    // buffer in double-buffered 4 KB rounds.  Returns false if the CTA is aborting.
     auto write_segment = [&](int sidx, int b, int slot_p, bool whole, bool from_ring, int ring_k) -> bool {
       const int kb = sidx & 1;
       const bool okO = wait_warp(bar(kBarOFull + kb), (sidx >> 1) & 1, abort_flag);
@@ -645,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         }
       };
       if (from_ring) {
-        const uint32_t off = kOffRing + ring_k * 65536 + grp * 32768;
+        const uint32_t off = Lay::kOffStageFinal + ring_k * 65536 + grp * 32768;
         uint8_t* stg = smem + off;
 #pragma unroll
         for (int h = 0; h < 32; ++h) put(stg, h, __uint_as_float(oa[h]), __uint_as_float(ob[h]));
@@ -692,13 +892,52 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       return true;
     };
 
-    for (int s = 0; s < nseg; ++s) {
+    // e4m3: q of segment sidx arrives in bf16; the e4m3 path multiplies in f16, so convert
+    // it in place.  Done as soon as the segment's first K tile is in tensor memory (for a
+    // later segment: before the previous segment's epilogue, whose wait for its last PV
+    // must not depend on this segment's first QK).
+    auto convert_q = [&](int sidx) {
+      if (wait_warp(bar(kBarQFull), sidx & 1, abort_flag)) {
+        uint4* qv = reinterpret_cast<uint4*>(smem + kOffQ) + ts * 8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint4 w = qv[q];
+          uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x0 = __uint_as_float(e[k] << 16), x1 = __uint_as_float(e[k] & 0xFFFF0000u);
+            range_bad |= !(fabsf(x0) <= 65504.f) | !(fabsf(x1) <= 65504.f);
+            e[k] = pack_f16_sat(x0, x1);
+          }
+          qv[q] = w;
+        }
+        fence_proxy_async_smem();
+      } else {
+        aborted = true;
+      }
+      mbar_arrive(bar(kBarQReady));
+    };
+
+    if constexpr (kFp8) {
+      // the first tile's K goes into tensor memory before the loop; each iteration then
+      // dequantises the next tile's K after its own softmax
+      if (ntiles > 0) {
+        if (!dequant_k(0, seg[0].w, seg[0].y)) aborted = true;
+        convert_q(0);
+      }
+    }
+
+    for (int s = 0; s < nseg && !aborted; ++s) {
       const int4 sg = seg[s];
       const int b = sg.x, L = sg.w, kb = s & 1;
       const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
       const int slot_p = b + static_cast<int>(blockIdx.x);
       const uint32_t o_tmem = tmem + kTmemO + 128u * kb + h0 + lane_base;   // + 64 for d in [128, 256)
       if (ts < kH) m_ref[ts] = -INFINITY;
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int h = 0; h < 32; ++h) lreg[h] = 0.f;
+      }
       named_bar_sync(1, kSoftmaxThreads);
       bool stop = false;
       for (int j = sg.y; j < sg.z; ++j, ++n) {
@@ -707,10 +946,12 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
         aborted = aborted || !okS;
         bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
-        // --- validity of this thread's row (the last page's rows sit at the end of the box)
-        const int pg = row >> 6, i = row & 63;
-        const int rp = min(kPage, L - kTile * j - kPage * pg);
-        const bool valid = okS && rp > 0 && i >= kPage - rp;
+        const int rp = page_rows(L, j, rpg);
+        const bool valid = okS && rp > 0 && ri >= kPage - rp;
+        // score multiplier of this row: scale*log2(e), times the token's K scale for e4m3
+        // (the K box and its scales were waited for when K was dequantised)
+        float ck = c;
+        if constexpr (kFp8) ck = c * row_scale(n, false, rp);
         // --- does any score of this row exceed its head's reference max by > 2^8?
         bool need = false;
         if (okS) {
@@ -721,10 +962,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h0 + h);
-            need |= (fmaf(__uint_as_float(sv[h + 0]), c, -m4.x) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 1]), c, -m4.y) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 2]), c, -m4.z) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 3]), c, -m4.w) > kRescaleThreshold);
+            need |= (fmaf(__uint_as_float(sv[h + 0]), ck, -m4.x) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 1]), ck, -m4.y) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 2]), ck, -m4.z) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sv[h + 3]), ck, -m4.w) > kRescaleThreshold);
           }
           need = need && valid;
         }
@@ -737,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             tmem_ld_wait(sv);
             float mv[32];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sv[h]) * c : -INFINITY;
+            for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sv[h]) * ck : -INFINITY;
             red[wq * 64 + h0 + lane] = warp_reduce_scatter32<true>(mv);
           }
           named_bar_sync(1, kSoftmaxThreads);
@@ -759,8 +1000,12 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           }
           if (!first) {
             // row sums and O^T rows (d = row, 128 + row) times alpha per head column
+            if constexpr (kFp8) {
+#pragma unroll
+              for (int h = 0; h < 32; ++h) lreg[h] *= alpha_s[h0 + h];
+            }
 #pragma unroll 1
-            for (int k3 = 0; k3 < 4; ++k3) {
+            for (int k3 = 0; k3 < (kFp8 ? 2 : 4); ++k3) {
               uint32_t ov[32];
               const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem : o_tmem + 64u * k3;
               tmem_ld32(ta, ov);
@@ -772,19 +1017,19 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             tmem_st_wait();
           }
         }
-        // --- probabilities and row sums; the P^T row piece (bf16) stays in registers until
-        //     the previous tile's PV has released the P buffer
+        // --- probabilities and row sums; the P^T row piece stays in registers until the
+        //     previous tile's PV has released the P buffer
         uint32_t pk[16];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t sv[16], lv[16], lx[16];
           tmem_ld16(s_tmem + 16 * half, sv);
-          if (!first) {
+          if (!kFp8 && !first) {
             tmem_ld16(l_tmem + 16 * half, lv);
             tmem_ld16(lx_tmem + 16 * half, lx);
           }
           tmem_ld_wait(sv);
-          if (!first) {
+          if (!kFp8 && !first) {
             tmem_ld_wait(lv);
             tmem_ld_wait(lx);
           } else {
@@ -795,24 +1040,45 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           for (int e = 0; e < 8; ++e) {
             const int hl = 2 * e, h = 16 * half + hl;
             const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h0 + h);
-            const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), c, -m2.x)) : 0.f;
-            const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), c, -m2.y)) : 0.f;
-            const uint32_t w = pack_bf16(p0, p1);
-            pk[8 * half + e] = w;
-            // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
-            // output is an exact convex combination of V rows under those weights
-            lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(w << 16));
-            lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(w & 0xFFFF0000u));
-            lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
-            lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
+            const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), ck, -m2.x)) : 0.f;
+            const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), ck, -m2.y)) : 0.f;
+            if constexpr (kFp8) {
+              pk[8 * half + e] = pack_f16_sat(p0, p1);   // p <= 2^8: inside the f16 range
+              lreg[h] += p0;
+              lreg[h + 1] += p1;
+            } else {
+              const uint32_t w = pack_bf16(p0, p1);
+              pk[8 * half + e] = w;
+              // the row sum adds the same bf16-rounded weights the PV MMA uses, so the
+              // output is an exact convex combination of V rows under those weights
+              lv[hl] = __float_as_uint(__uint_as_float(lv[hl]) + __uint_as_float(w << 16));
+              lv[hl + 1] = __float_as_uint(__uint_as_float(lv[hl + 1]) + __uint_as_float(w & 0xFFFF0000u));
+              lx[hl] = __float_as_uint(__uint_as_float(lx[hl]) + p0);
+              lx[hl + 1] = __float_as_uint(__uint_as_float(lx[hl + 1]) + p1);
+            }
           }
-          tmem_st16(l_tmem + 16 * half, lv);
-          tmem_st16(lx_tmem + 16 * half, lx);
+          if constexpr (!kFp8) {
+            tmem_st16(l_tmem + 16 * half, lv);
+            tmem_st16(lx_tmem + 16 * half, lx);
+          }
         }
-        tmem_st_wait();
+        if constexpr (!kFp8) tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bar(kBarSEmpty + (n & 1)));
+        if constexpr (kFp8) {
+          // next tile's K into tensor memory (the MMA warp can start its QK right away)
+          if (n + 1 < ntiles) {
+            const int s1 = (j + 1 < sg.z) ? s : s + 1;
+            const int j1 = (j + 1 < sg.z) ? j + 1 : seg[s1].y;
+            if (!dequant_k(n + 1, seg[s1].w, j1)) aborted = true;
+            if (s1 != s) convert_q(s1);
+          }
+        }
         if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
+        if constexpr (kFp8) {
+          // this tile's V into the f16 operand tile (free: the previous PV is done)
+          if (!dequant_v(n, L, j)) aborted = true;
+        }
         // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
         uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -826,20 +1092,25 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
 
       // ---------------- epilogue of sequence b's segment
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        uint32_t lv[32];
-        tmem_ld32(which ? lx_tmem : l_tmem, lv);
-        tmem_ld_wait(lv);
+      for (int which = 0; which < (kFp8 ? 1 : 2); ++which) {
         float lsum[32];
+        if constexpr (kFp8) {
 #pragma unroll
-        for (int h = 0; h < 32; ++h) lsum[h] = __uint_as_float(lv[h]);
+          for (int h = 0; h < 32; ++h) lsum[h] = lreg[h];
+        } else {
+          uint32_t lv[32];
+          tmem_ld32(which ? lx_tmem : l_tmem, lv);
+          tmem_ld_wait(lv);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) lsum[h] = __uint_as_float(lv[h]);
+        }
         red[which * 256 + wq * 64 + h0 + lane] = warp_reduce_scatter32<false>(lsum);
       }
       named_bar_sync(1, kSoftmaxThreads);
       if (ts < kH) {
         const float l = (red[ts] + red[64 + ts]) + (red[128 + ts] + red[192 + ts]);
         linv[kb * kH + ts] = 1.f / l;
-        const float lx = (red[256 + ts] + red[320 + ts]) + (red[384 + ts] + red[448 + ts]);
+        const float lx = kFp8 ? l : (red[256 + ts] + red[320 + ts]) + (red[384 + ts] + red[448 + ts]);
         const float lse_v = (m_ref[ts] + log2f(lx)) * 0.69314718055994531f;
         if (whole) {
           if (p.lse != nullptr) p.lse[b * kH + ts] = lse_v;
@@ -853,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         if (!write_segment(s, b, slot_p, whole, false, 0)) break;
       } else {
         // one of the CTA's last two segments: its accumulator stays in tensor memory
-        // and is written after the last tile, when the ring is idle
+        // and is written after the last tile, when the operand buffers are idle
         defer_b[kb] = b;
         defer_slot[kb] = slot_p;
         defer_whole[kb] = whole;
@@ -861,8 +1132,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     }
     if (!aborted && !*abort_flag) {
       // deferred accumulators, newest first: the wait for the last segment's accumulator
-      // also means every MMA has finished reading the ring, which then stages the rows
-      // (uniform: every thread reads the same values)
+      // also means every MMA has finished reading the operand buffers, which then stage
+      // the rows (uniform: every thread reads the same values)
       const int first_def = nseg >= 2 ? nseg - 2 : 0;
       for (int s = nseg - 1; s >= first_def; --s) {
         const int kb = s & 1;
@@ -870,6 +1141,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       }
     }
     if (issuer) bulk_wait_read0();
+    if (range_bad) atomicOr(p.status, MFA_DEV_RANGE);
     if (aborted && ts == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
   }
 
@@ -1102,7 +1374,6 @@ static mfa_status check_problem(const mfa_problem* pr) {
   if (pr->out_dtype != MFA_OUT_BF16 && pr->out_dtype != MFA_OUT_FP32) return MFA_ERR_INVALID_ARG;
   if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
   if (pr->num_q_heads != kH || pr->head_dim != kD || pr->page_size != kPage) return MFA_ERR_UNSUPPORTED;
-  if (pr->kv_dtype != MFA_KV_BF16) return MFA_ERR_UNSUPPORTED;  // e4m3 path not in this build yet
   if (static_cast<long long>(pr->max_pages_per_seq) * kPage > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   if (static_cast<long long>(pr->batch) * kH > INT_MAX) return MFA_ERR_INVALID_ARG;
   return MFA_OK;
@@ -1132,13 +1403,17 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   }
   const void* pools[2] = {k, v};
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
+  const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
+  const cuuint64_t esz = fp8 ? 1 : 2;
   for (int i = 0; i < 2; ++i) {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
                           static_cast<cuuint64_t>(pr->num_blocks)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(kD) * 2 * kPage};
-    cuuint32_t box[3] = {64, 64, 1};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esz, static_cast<cuuint64_t>(kD) * esz * kPage};
+    // one 128-byte swizzle row per box row: 64 bf16 or 128 e4m3 codes
+    cuuint32_t box[3] = {fp8 ? 128u : 64u, 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pools[i]), dims, strides, box, es,
+    if (enc(maps[i], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(pools[i]), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cuda_fail_msg("cuTensorMapEncodeTiled rejected a tensor map");
@@ -1263,7 +1538,9 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       seq_lens == nullptr || out == nullptr || workspace == nullptr)
     return MFA_ERR_INVALID_ARG;
-  if (pr->kv_dtype == MFA_KV_FP8_E4M3 && (k_scale == nullptr || v_scale == nullptr)) return MFA_ERR_INVALID_ARG;
+  if (pr->kv_dtype == MFA_KV_FP8_E4M3 &&
+      (k_scale == nullptr || v_scale == nullptr || !aligned(k_scale, 16) || !aligned(v_scale, 16)))
+    return MFA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
       !aligned(workspace, 256) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
       (lse != nullptr && !aligned(lse, 4)))
@@ -1295,19 +1572,22 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
   cudaError_t e = cudaSuccess;
   if (check && (e = cudaMemsetAsync(ws, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
-  e = cudaFuncSetAttribute(mfa_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
+  auto kernel = fp8 ? mfa_decode_kernel<true> : mfa_decode_kernel<false>;
+  const int smem = fp8 ? smem_bytes<true>() : smem_bytes<false>();
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mfa_decode_kernel, prm);
+  e = cudaLaunchKernelEx(&cfg, kernel, prm);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (plan->num_ctas > 1 && (plan->flags & MFA_PLAN_NO_COMBINE) == 0) {
     st = launch_combine(plan, pr, workspace, seq_lens, out, lse, stream, true);

@@ -113,6 +113,13 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* map, int x, int y, i
                : "memory");
 }
 
+// Bulk copy global -> shared completing on an mbarrier (tx bytes); 16-byte aligned, size % 16 == 0.
+__device__ __forceinline__ void bulk_load_g2s(uint32_t sdst, const void* gsrc, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(sdst), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Bulk copy shared -> global (async proxy, bulk-group completion); 16-byte aligned, size % 16 == 0.
 __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"

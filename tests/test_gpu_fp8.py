@@ -1,0 +1,67 @@
+"""Parity of the e4m3-KV path with the fp64 oracle fed the same dequantised values.
+
+Limits for FP8 KV: max-abs <= 3e-2 and relative-L2 <= 1.5e-2 (on the fp32 result;
+the bf16 output may add half a bf16 ulp).  The oracle decodes every e4m3 code
+exactly and multiplies by its per-token scale in double precision.
+"""
+import numpy as np
+import pytest
+import torch
+
+import decode_attention_02_gb300 as mfa
+import oracle
+from decode_attention_02_gb300 import inputs
+from test_gpu_parity import check_parity, gpu_decode, to_dev
+
+pytestmark = pytest.mark.gpu
+
+FP8 = dict(max_abs=3e-2, rel_l2=1.5e-2)
+
+
+def test_fp8_length_one_returns_the_dequantised_value():
+    # one token: the output is v_0 (code * scale); exercises the V dequantisation alone
+    case = inputs.small("f1", 3, [1, 1, 1], kv_dtype="fp8_e4m3", seed=40)
+    out, lse, _ = gpu_decode(case)
+    check_parity(case, out, lse, **FP8)
+
+
+def test_fp8_two_tokens():
+    case = inputs.small("f2", 3, [2, 2, 2], kv_dtype="fp8_e4m3", seed=41)
+    out, lse, _ = gpu_decode(case)
+    check_parity(case, out, lse, **FP8)
+
+
+@pytest.mark.parametrize("force_ctas", [0, 1, 3, 16, 64])
+def test_fp8_ragged_lengths_any_split(force_ctas):
+    lens = [1, 63, 64, 65, 127, 128, 129, 200, 0, 517, 1000, 300]
+    case = inputs.small("fr", len(lens), lens, kv_dtype="fp8_e4m3", seed=42, extra_blocks=3)
+    out, lse, _ = gpu_decode(case, force_ctas=force_ctas)
+    check_parity(case, out, lse, **FP8)
+
+
+def test_fp8_bf16_output_is_rne_of_fp32_output():
+    case = inputs.small("fo", 4, [3000, 1, 700, 1500], kv_dtype="fp8_e4m3", seed=43)
+    o32, l32, _ = gpu_decode(case, force_ctas=5)
+    o16, l16, _ = gpu_decode(case, force_ctas=5, out_dtype=mfa.MFA_OUT_BF16)
+    assert torch.equal(o16.view(torch.int16), o32.to(torch.bfloat16).view(torch.int16))
+    ref = oracle.decode(case)
+    check_parity(case, o32, l32, ref=ref, **FP8)
+    check_parity(case, o16, l16, ref=ref, **FP8)
+
+
+def test_fp8_v_scale_out_of_range_is_reported():
+    case = inputs.small("fs", 2, [100, 200], kv_dtype="fp8_e4m3", seed=44)
+    blk = int(case.block_table[1, 0])
+    case.v_scale[blk, 3] = 1000.0          # 448 * 1000 is beyond the f16 range of dequantised V
+    with pytest.raises(mfa.MfaError) as e:
+        gpu_decode(case)
+    assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
+
+
+@pytest.mark.parametrize("name", ["b128_l4096_fp8", "b32_l4096_fp8", "long_b4_l131072_fp8"])
+def test_fp8_full_size_workload(name):
+    case = inputs.generate(inputs.WORKLOADS[name])
+    out, lse, dec = gpu_decode(case)
+    assert dec.plan.num_ctas == min(torch.cuda.get_device_properties(0).multi_processor_count,
+                                    int(dec.plan.total_tiles))
+    check_parity(case, out, lse, **FP8)
