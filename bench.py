@@ -245,6 +245,31 @@ def workload_config(case, extra=None):
     return cfg
 
 
+def rank_workload(w, rank: int):
+    """The shard of a multi-GPU run that rank ``rank`` decodes: the same workload
+    shape with its own sequences (the seed moves with the rank).  Ranks share no
+    data, so the timed steps have no collective; whole-job throughput is
+    world x one rank's bytes over the slowest rank's time (weak scaling)."""
+    if rank == 0:
+        return w
+    import dataclasses
+    return dataclasses.replace(w, seed=w.seed + 7919 * rank)
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest of one float over all ranks (the value itself on one rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def run_native(args, case, rank: int, world: int):
     import torch
     import decode_attention_02_gb300 as mfa
@@ -326,10 +351,7 @@ def run_native(args, case, rank: int, world: int):
     barrier()
     windows.append((t_start, time.time()))
     ms_total = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
 
     # the same K steps without the early-metadata overlap (every read after the previous step)
@@ -343,7 +365,7 @@ def run_native(args, case, rank: int, world: int):
     graph2.replay()
     e1.record(stream)
     barrier()
-    ms_step_strict = e0.elapsed_time(e1) / args.steps
+    ms_step_strict = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
 
     # --- decode kernel alone: per-launch CUDA events, queued behind a GPU sleep so
     #     the launches run back to back whatever the host-side cost of enqueueing them
@@ -361,7 +383,7 @@ def run_native(args, case, rank: int, world: int):
     barrier()
     windows.append((t_start, time.time()))
     kern_ms = [a.elapsed_time(b) for a, b in evs]
-    kern_mean_ms = sum(kern_ms) / len(kern_ms)
+    kern_mean_ms = max_over_ranks(sum(kern_ms) / len(kern_ms), dist, dev)
 
     # --- end to end through the public API: host inputs in, host outputs out
     q_h = case.q.pin_memory()
@@ -394,7 +416,7 @@ def run_native(args, case, rank: int, world: int):
     e1.record(stream)
     barrier()
     windows.append((t_start, time.time()))
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
 
     # keep sampling clocks until the windows hold enough samples
     clocks = sampler.summary(windows)
@@ -411,7 +433,7 @@ def run_native(args, case, rank: int, world: int):
     sampler.stop()
 
     hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
-    kv_gbs = acct["kv"] * world / (ms_step * 1e-3) / 1e9
+    kv_gbs = whole_job_gbs(acct["kv"], world, ms_step)
     achieved = acct["total"] / (kern_mean_ms * 1e-3) / 1e9
     tflops = flops * world / (ms_step * 1e-3) / 1e12
     t_hbm = acct["total"] / (hbm_peak * 1e9)
@@ -433,7 +455,7 @@ def run_native(args, case, rank: int, world: int):
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic(w.name),
                      "kernel": "mfa_decode_kernel", "mean_launch_ms": kern_mean_ms,
                      "algorithmic_bytes_per_launch": acct["total"], "peak_source": f"{peak_src} hbm_gbs"},
-        "e2e": {"value": acct["kv"] * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": whole_job_gbs(acct["kv"], world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
@@ -456,7 +478,7 @@ def main():
     from decode_attention_02_gb300 import inputs
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    case = inputs.generate(inputs.WORKLOADS[args.workload])
+    case = inputs.generate(rank_workload(inputs.WORKLOADS[args.workload], rank))
 
     if args.impl == "reference":
         res = run_reference(args, case, rank, world)
