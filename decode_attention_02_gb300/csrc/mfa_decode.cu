@@ -14,20 +14,27 @@
 //    combine kernel merges (split-KV with a log-sum-exp merge).
 //  * Each CTA holds all 64 heads of its sequence, so K and V are read once.
 //  * Warp 0 streams K/V pages with TMA (3-D tensor maps over the page pool; the
-//    block table supplies the page coordinate) into a 10-slot, 16 KB/slot ring.
+//    block table supplies the page coordinate) into a ring of shared-memory slots,
+//    four ring uses at a time from four lanes.
 //  * Warp 1 issues tcgen05 MMAs in the transposed form, which fills the M=128
 //    datapath: S^T[128 tokens x 64 heads] = K_tile . Q^T and
 //    O^T[256 d x 64 heads] += V^T . P^T (two M=128 halves), fp32 accumulators in
 //    tensor memory (S double-buffered, O double-buffered across sequences).
-//  * Warps 2-5 (one thread per tensor-memory lane = token) run the online softmax
-//    in fp32.  The running max is lazy: a head's reference max moves only when a
-//    score exceeds it by 2^8, so the common tile needs no cross-thread reduction;
-//    row sums accumulate per thread and are reduced once per sequence.
+//  * Eight softmax warps (two per tensor-memory lane quarter, 32 heads each) run the
+//    online softmax in fp32.  The running max is lazy: a head's reference max moves
+//    only when a score exceeds it by 2^8, so the common tile needs no cross-thread
+//    reduction; row sums accumulate per thread and are reduced once per sequence.
+//  * e4m3 KV: q.K^T runs as a kind::f8f6f4 MMA on the e4m3 K boxes exactly as TMA
+//    wrote them, against q split into e4m3 hi + lo parts (N = 128); four more warps
+//    turn each V box into the f16 PV operand, with the token's V scale; K scales
+//    multiply the fp32 scores.  A warpgroup register split gives the softmax warps
+//    their registers.
 //  * The ragged last page is loaded with its valid rows shifted to the end of the
 //    box (negative row start; TMA fills the rest with zeros), so NaN or stale data
 //    in unused page slots never enters an MMA.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -47,20 +54,34 @@ constexpr int kH = 64;             // query heads
 constexpr int kD = 256;            // head width
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
-constexpr int kThreads = 320;      // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
+constexpr int kDequantThreads = 128;  // e4m3: one thread per token row of a tile
+// bf16 : warp 0 TMA, warp 1 MMA, warps 2..9 softmax (320 threads, 168 registers each).
+// e4m3 : warpgroup 0 = warp 0 TMA, warp 1 MMA (warps 2, 3 idle), warpgroups 1-2 = warps
+//        4..11 softmax, warpgroup 3 = warps 12..15 V dequantisation; launched with 128
+//        registers per thread and rebalanced to 80 / 168 / 168 / 96 (sum 4 x 128).
+template <bool kFp8>
+__host__ __device__ constexpr int threads_of() { return kFp8 ? 512 : 320; }
+template <bool kFp8>
+__host__ __device__ constexpr int softmax_warp0() { return kFp8 ? 4 : 2; }
+constexpr int kDequantWarp0 = 12;
+constexpr uint32_t kRegsCtl = 80, kRegsSoftmax = 168, kRegsDequant = 96;
+static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsDequant == 4 * (65536 / 512),
+              "e4m3 register split must add up to the launch budget (4 warpgroups x 128)");
 constexpr int kMaxTilesPerCta = 128;
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
 
 // Shared-memory map (offsets from a 1024-byte aligned base).  Both KV formats put the
 // barriers at the same offset; they differ below it:
 //   bf16 : Q 32 KB | P 16 KB | ring 10 x 16 KB (K/V operand tiles as TMA writes them)
-//   e4m3 : Q 32 KB | P 16 KB | V f16 64 KB (dequantised PV operand) | ring 12 x 8 KB (raw
-//          e4m3 boxes) and, after the common area, a 4-tile ring of per-token scales
+//   e4m3 : Q 32 KB (e4m3 hi and lo parts) | P 16 KB | V f16 64 KB (dequantised PV operand) |
+//          ring 12 x 8 KB (raw e4m3 boxes, K read by the MMA as they are); the per-token
+//          scales are read from global memory by the threads that apply them
 constexpr int kOffQ = 0;                                     // 4 x [64 heads x 128 B]
 constexpr int kOffP = 32768;                                 // [128 tokens x 128 B]
 constexpr int kOffBar = 212992;                              // mbarriers
@@ -81,24 +102,19 @@ struct KvLayout<true> {
   static constexpr int kNumSlots = 12;
   static constexpr int kSlotBytes = 8192;
   static constexpr int kOffStageFinal = kOffVh;     // V f16 + ring: 160 KB free after the last MMA
-  // scale ring, per tile: K scales of the 2 pages, then V scales of the 2 pages once per
-  // d-half (each half's box brings its own copy, so its consumers wait on their own box)
-  static constexpr int kScaleTiles = 4;
-  static constexpr int kScaleTileBytes = 6 * 256;
-  static constexpr int kExtraSmem = kScaleTiles * kScaleTileBytes;
+  static constexpr int kExtraSmem = 0;
 };
 static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
 static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
-constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..15] scan
+constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan [24..31] q maxima
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
 constexpr int kOffLinv = kOffRed + 2048;      // float[2][64]  1 / row sum per O buffer
 constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, end tile, L}
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
-constexpr int kOffTileBlk = kOffSegN0 + 4 * kMaxSeg;    // int2[kMaxTilesPerCta] page ids
-constexpr int kSmemUsed = kOffTileBlk + 8 * kMaxTilesPerCta;
-constexpr int kOffScale = kSmemUsed;                    // e4m3 only
+constexpr int kOffTileInfo = kOffSegN0 + 4 * kMaxSeg;   // int4[kMaxTilesPerCta] {page 0, page 1, rows 0, rows 1}
+constexpr int kSmemUsed = kOffTileInfo + 16 * kMaxTilesPerCta;
 template <bool kFp8>
 constexpr int smem_bytes() { return kSmemUsed + KvLayout<kFp8>::kExtraSmem + 1024; }
 static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
@@ -115,19 +131,21 @@ enum Bar : int {
   kBarOFull,   // 2
   kBarOEmpty = kBarOFull + 2,
   kBarDrain = kBarOEmpty + 2,
-  kBarQReady,   // e4m3: q converted to f16 in place
-  kBarKReady,   // e4m3: K tile dequantised into tensor memory
-  kBarKFree,    // e4m3: the QK MMAs have read that K tile
+  kBarQReady,   // e4m3: q split in place into e4m3 hi and lo parts
+  kBarVhFull,   // e4m3: a tile's V is in the f16 operand tile
   kBarCount
 };
 static_assert(kBarCount * 8 <= 512, "barrier area");
 
 // Tensor-memory columns.
-constexpr uint32_t kTmemS = 0;     // S^T buffers: [0,64) and [64,128)
-constexpr uint32_t kTmemO = 128;   // O^T buffer k, half hh: 128 + 128k + 64hh
+constexpr uint32_t kTmemS = 0;     // S^T buffers: bf16 [0,64) and [64,128); e4m3 [0,128) and
+                                   // [128,256) (64 columns of hi-part scores, then 64 of lo)
+template <bool kFp8>
+__host__ __device__ constexpr uint32_t s_cols() { return kFp8 ? 128u : 64u; }
+template <bool kFp8>
+__host__ __device__ constexpr uint32_t tmem_o() { return kFp8 ? 256u : 128u; }   // O^T buffer k, half hh: + 128k + 64hh
 constexpr uint32_t kTmemL = 384;   // bf16: per-lane row sums of the bf16-rounded weights (normalise O)
 constexpr uint32_t kTmemLx = 448;  // bf16: per-lane row sums of the fp32 weights (lse)
-constexpr uint32_t kTmemK = 384;   // e4m3: K tile in f16, lane = token, 2 d per column (A operand)
 
 struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
@@ -181,6 +199,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn, bool b_mn
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// tcgen05 instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0),
+// fp32 D, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
 __device__ __forceinline__ int clamp_len(int L, int cap, bool& bad) {
   if (L < 0) { bad = true; return 0; }
   if (L > cap) { bad = true; return cap; }
@@ -209,7 +234,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return ok;
 }
 
-// Block-wide (kThreads) inclusive scan of one int per thread; also returns the total.
+// Block-wide (kThreads threads) inclusive scan of one int per thread; also returns the total.
+template <int kThreads>
 __device__ __forceinline__ int block_incl_scan(int v, int* scratch, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -353,19 +379,51 @@ __device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
   asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Two floats to two e4m3 codes (round to nearest even, saturating); lo in the low byte.
+__device__ __forceinline__ uint32_t pack_e4m3_sat(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2))); }
+__device__ __forceinline__ float f16_hi(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))); }
 
-// Ring use index of the K (is_v = false) or V part (page pg, d-half dh) of tile t of a
+// Split two scaled q values x into e4m3 pairs hi + lo with hi = e4m3(x) and lo = e4m3(x - hi).
+// x is a bf16 value times a power of two (8 significant bits) and the largest |x| of the
+// sequence lies in [64, 128).  x - hi is exact in fp32 and is k * ulp(x) with |k| <= 8, so
+// it fits e4m3's 4 significant bits: hi + lo = x exactly when ulp(x) >= 2^-9 (the e4m3
+// subnormal step), i.e. for |x| >= 2^-2, which covers every element at least 2^-9 of the
+// largest.  Smaller elements err by at most 2^-10, under 2^-16 of the largest.
+__device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_e4m3_sat(x0, x1);
+  const uint32_t back = e4m3x2_to_f16x2(hi);
+  lo = pack_e4m3_sat(x0 - f16_lo(back), x1 - f16_hi(back));
+}
+
+// e4m3: per-token scale of box row ri of page pg of tile `ti` ({page 0, page 1, rows 0,
+// rows 1}); 0 for rows past the sequence end (the last page's valid rows sit at the end of
+// the box, so box row ri holds page row ri - (64 - rows)).
+__device__ __forceinline__ float token_scale(const float* __restrict__ sc, const int4 ti, int pg, int ri) {
+  const int r = pg ? ti.w : ti.z;
+  if (r <= 0 || ri < kPage - r) return 0.f;
+  return __ldg(sc + static_cast<size_t>(pg ? ti.y : ti.x) * kPage + ri - (kPage - r));
+}
+
+// e4m3 ring use index of the K (is_v = false) or V part (page pg, d-half dh) of tile t of a
 // CTA with `ntiles` tiles.  The producer issues K(0), then K(t) and V(t-1) for t = 1..N-1,
 // then V(N-1), four uses each: K(0) = 0..3, K(t) = 8t-4.., V(t) = 8t+8.. except the last
-// tile's V, which directly follows its K: V(N-1) = 8N-4...
+// tile's V, which directly follows its K: V(N-1) = 8N-4...  Every group of four starts at
+// a multiple of 4 and the ring has 12 slots, so a group never wraps: K's two pages of one
+// d-half sit in adjacent slots and form one 128-row MMA operand.
 __device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v, int pg, int dh) {
   const uint32_t base = is_v ? (t + 1 < ntiles ? 8u * t + 8u : 8u * t + 4u) : (t == 0 ? 0u : 8u * t - 4u);
-  return base + 2u * pg + dh;
+  return base + (is_v ? 2u * pg + dh : 2u * dh + pg);
 }
 
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
   using Lay = KvLayout<kFp8>;
+  constexpr int kThreads = threads_of<kFp8>();
   constexpr int kNumSlots = Lay::kNumSlots;
   constexpr int kSlotBytes = Lay::kSlotBytes;
   constexpr int kOffRing = Lay::kOffRing;
@@ -376,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   volatile int* abort_flag = misc + 1;
   int4* seg = reinterpret_cast<int4*>(smem + kOffSeg);
   int* seg_n0 = reinterpret_cast<int*>(smem + kOffSegN0);
-  int2* tile_blk = reinterpret_cast<int2*>(smem + kOffTileBlk);
+  int4* tile_info = reinterpret_cast<int4*>(smem + kOffTileInfo);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
@@ -384,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   if (tid == 0) {
     for (int i = 0; i < kNumSlots; ++i) {
       mbar_init(bar(kBarFull + i), 1);
-      // bf16: released by the MMA commit; e4m3: by the 64 threads that dequantise the box
-      mbar_init(bar(kBarEmpty + i), kFp8 ? 64 : 1);
+      // released by the MMA commit, or (e4m3 V boxes) by the leader of the dequant warps
+      mbar_init(bar(kBarEmpty + i), 1);
     }
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
@@ -399,8 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarQReady), kSoftmaxThreads);
-    mbar_init(bar(kBarKReady), kSoftmaxThreads);
-    mbar_init(bar(kBarKFree), 1);
+    mbar_init(bar(kBarVhFull), kDequantThreads);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -431,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     int W = 0;
-    block_incl_scan(loc, scratch, W);
+    block_incl_scan<kThreads>(loc, scratch, W);
     const int G = gridDim.x, g = blockIdx.x;
     const int t0 = static_cast<int>((static_cast<long long>(g) * W) / G);
     const int t1 = static_cast<int>((static_cast<long long>(g + 1) * W) / G);
@@ -446,10 +503,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
         const int T = tiles_of(L);
         int tot = 0, ftot = 0;
-        const int incl = block_incl_scan(T, scratch, tot) + carry;
+        const int incl = block_incl_scan<kThreads>(T, scratch, tot) + carry;
         const int excl = incl - T;
         const int f = (max(t0, excl) < min(t1, incl)) ? 1 : 0;   // non-empty overlap
-        const int fidx = nseg + block_incl_scan(f, scratch, ftot) - f;
+        const int fidx = nseg + block_incl_scan<kThreads>(f, scratch, ftot) - f;
         if (f) {
           const int lo = max(t0, excl), hi = min(t1, incl);
           seg[fidx] = make_int4(b, lo - excl, hi - excl, L);
@@ -469,127 +526,127 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int nseg = misc[2];
   const int ntiles = misc[3];
-
-  if (warp == 0) {
-    // ---------------- producer: page ids, then TMA loads of Q, K, V (and e4m3 scales)
+  // ---------------- page ids and valid rows of each of this CTA's tiles (one round of
+  // independent loads, one tile per thread).  Rows r of a page: the last page of a sequence
+  // has r < 64 (its valid rows land at the end of the box), an absent second page r <= 0.
+  {
     bool bad_blk = false;
-    // all of this CTA's page ids in one round of independent loads (lane = tile)
-    for (int n = lane; n < ntiles; n += 32) {
+    for (int n = tid; n < ntiles; n += kThreads) {
       int s = 0;
       while (s + 1 < nseg && seg_n0[s + 1] <= n) ++s;
       const int4 sg = seg[s];
+      const int j = sg.y + (n - seg_n0[s]);
+      const int r0 = min(kPage, sg.w - kTile * j), r1 = min(kPage, sg.w - kTile * j - kPage);
       const int32_t* row = p.block_table + static_cast<size_t>(sg.x) * p.max_pages;
-      {
-        const int j = sg.y + (n - seg_n0[s]);
-        int b0 = row[2 * j];
-        const bool has1 = kPage * (2 * j + 1) < sg.w;
-        int b1 = has1 ? row[2 * j + 1] : -1;
-        // an id outside the pool is reported and replaced by page 0, so every TMA
-        // coordinate stays inside the pool (the output of that sequence is then wrong)
-        if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = 0; }
-        if (has1 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = 0; }
-        tile_blk[n] = make_int2(b0, b1);
-      }
+      int b0 = row[2 * j];
+      int b1 = (r1 > 0) ? row[2 * j + 1] : 0;
+      // an id outside the pool is reported and replaced by page 0, so every TMA coordinate
+      // stays inside the pool (the output of that sequence is then wrong)
+      if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = 0; }
+      if (r1 > 0 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = 0; }
+      tile_info[n] = make_int4(b0, b1, r0, r1);
     }
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
-    __syncwarp();
-    if (lane == 0 && ntiles > 0) {
+  }
+  __syncthreads();
+
+  // e4m3 warpgroup register split (see threads_of), at the top of each role so that the
+  // role's budget covers all of its code: control warps give registers up, the softmax
+  // warpgroups take them; the four budgets add up to the launch's 4 x 128
+  if (warp == 0) {
+    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
+    // ---------------- producer: TMA loads of Q, K and V in ring order.  Each group of four
+    // ring uses (a tile's K, or a tile's V) is issued by lanes 0..3 together, one use per
+    // lane; groups go out strictly in ring order, so every slot's phases stay in step.
+    if (ntiles > 0) {
       if (p.early_metadata) grid_dep_wait();
       const uint64_t pol = l2_policy_evict_first();
-      uint32_t u = 0;       // ring uses issued
-      int nq = 0;           // Q loads issued
-      int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
+      const bool act = lane < 4;
+      const int c = lane & 3;
       bool ok = true;
-      // one ring use: wait for the slot, then load a K or V part (bf16: chunk of 64 d over
-      // both pages, or page x d-half; e4m3: page x d-half box, plus the page's scales)
-      auto issue = [&](bool is_v, int t, int a, int b2, int r0, int r1, const int2 bk) -> bool {
-        const uint32_t slot = u % kNumSlots;
-        if (!wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag)) return false;
-        const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
-        const uint32_t fb = bar(kBarFull + slot);
-        const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-        if constexpr (!kFp8) {
-          if (!is_v) {   // a = 64-d chunk, both pages
-            mbar_arrive_expect_tx(fb, r1 > 0 ? 16384 : 8192);
-            tma_load_3d_hint(dst, map, fb, 64 * a, r0 - kPage, bk.x, pol);
-            if (r1 > 0) tma_load_3d_hint(dst + 8192, map, fb, 64 * a, r1 - kPage, bk.y, pol);
-          } else {       // a = page, b2 = d-half
-            const int r = a ? r1 : r0;
-            const int blk = a ? bk.y : bk.x;
-            if (r > 0) {
-              mbar_arrive_expect_tx(fb, 16384);
-              tma_load_3d_hint(dst, map, fb, 128 * b2, r - kPage, blk, pol);
-              tma_load_3d_hint(dst + 8192, map, fb, 128 * b2 + 64, r - kPage, blk, pol);
+      int sq = 0, nq = 0;                 // next segment whose q is loaded; q loads issued
+      uint32_t mine[3] = {0u, 0u, 0u};    // this lane's last three uses (drain after an abort)
+      int nmine = 0;
+      // lane c: use c of the group (bf16 K: 64-d chunk c of both pages; e4m3 K: page c & 1,
+      // d-half c >> 1; V: page c >> 1, d-half c & 1)
+      auto group = [&](bool is_v, int t) -> bool {
+        bool okl = true;
+        if (act) {
+          const int4 ti = tile_info[t];
+          const uint32_t u = ring_use(t, ntiles, is_v, 0, 0) + c;
+          const uint32_t slot = u % kNumSlots;
+          okl = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
+          if (okl) {
+            const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
+            const uint32_t fb = bar(kBarFull + slot);
+            const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+            if (!kFp8 && !is_v) {
+              mbar_arrive_expect_tx(fb, ti.w > 0 ? 16384 : 8192);
+              tma_load_3d_hint(dst, map, fb, 64 * c, ti.z - kPage, ti.x, pol);
+              if (ti.w > 0) tma_load_3d_hint(dst + 8192, map, fb, 64 * c, ti.w - kPage, ti.y, pol);
             } else {
-              mbar_arrive(fb);
+              const int pg = (kFp8 && !is_v) ? (c & 1) : (c >> 1);
+              const int dh = (kFp8 && !is_v) ? (c >> 1) : (c & 1);
+              const int r = pg ? ti.w : ti.z;
+              const int blk = pg ? ti.y : ti.x;
+              if (r <= 0) {
+                mbar_arrive(fb);
+              } else if constexpr (kFp8) {
+                mbar_arrive_expect_tx(fb, 8192);
+                tma_load_3d_hint(dst, map, fb, 128 * dh, r - kPage, blk, pol);
+              } else {
+                mbar_arrive_expect_tx(fb, 16384);
+                tma_load_3d_hint(dst, map, fb, 128 * dh, r - kPage, blk, pol);
+                tma_load_3d_hint(dst + 8192, map, fb, 128 * dh + 64, r - kPage, blk, pol);
+              }
             }
-          }
-        } else {         // a = page, b2 = d-half
-          const int r = a ? r1 : r0;
-          const int blk = a ? bk.y : bk.x;
-          if (r > 0) {
-            // K: the page's scales with its d-half-0 box (read only once QK has run, which
-            // needs both halves); V: a copy with each half's box, read by that half's threads
-            const bool with_scale = is_v || (b2 == 0);
-            mbar_arrive_expect_tx(fb, 8192 + (with_scale ? 256 : 0));
-            tma_load_3d_hint(dst, map, fb, 128 * b2, r - kPage, blk, pol);
-            if (with_scale) {
-              const float* src = (is_v ? p.v_scale : p.k_scale) + static_cast<size_t>(blk) * kPage;
-              const int idx = is_v ? 2 + 2 * a + b2 : a;
-              const uint32_t sdst = sbase + kOffScale + (t % KvLayout<true>::kScaleTiles) * KvLayout<true>::kScaleTileBytes +
-                                    idx * 256;
-              bulk_load_g2s(sdst, src, 256, fb);
-            }
-          } else {
-            mbar_arrive(fb);
+            mine[nmine % 3] = u;
+            ++nmine;
           }
         }
-        ++u;
-        return true;
+        return __all_sync(0xffffffffu, okl);
       };
       for (int n = 0; n <= ntiles && ok; ++n) {
         if (n < ntiles) {
-          const int4 sg = seg[sk];
-          if (jk == sg.y) {
-            if (sk > 0) ok = wait_bar(bar(kBarQEmpty), (sk - 1) & 1, abort_flag);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar(kBarQFull), kH * kD * 2);
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(sbase + kOffQ + c * 8192, &p.tm_q, bar(kBarQFull), 64 * c, kH * sg.x);
-            ++nq;
+          if (sq < nseg && n == seg_n0[sq]) {
+            bool okq = true;
+            if (lane == 0) {
+              if (sq > 0) okq = wait_bar(bar(kBarQEmpty), (sq - 1) & 1, abort_flag);
+              if (okq) {
+                mbar_arrive_expect_tx(bar(kBarQFull), kH * kD * 2);
+                for (int q = 0; q < 4; ++q)
+                  tma_load_2d(sbase + kOffQ + q * 8192, &p.tm_q, bar(kBarQFull), 64 * q, kH * seg[sq].x);
+                ++nq;
+                // the next segment's q waits for this segment's last QK^T; bring it into L2
+                // now so that its load then comes from L2
+                if (sq + 1 < nseg)
+                  for (int q = 0; q < 4; ++q) tma_prefetch_2d(&p.tm_q, 64 * q, kH * seg[sq + 1].x);
+              }
+            }
+            ok = __all_sync(0xffffffffu, okq);
+            ++sq;
           }
-          const int2 bk = tile_blk[n];
-          const int r0 = min(kPage, sg.w - kTile * jk);
-          const int r1 = min(kPage, sg.w - kTile * jk - kPage);
-          for (int c = 0; c < 4 && ok; ++c) ok = issue(false, n, kFp8 ? (c >> 1) : c, c & 1, r0, r1, bk);
-          if (!ok) break;
-          if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
+          if (ok) ok = group(false, n);
         }
-        if (n >= 1) {
-          const int4 sg = seg[sv];
-          const int2 bk = tile_blk[n - 1];
-          const int rr0 = min(kPage, sg.w - kTile * jv);
-          const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
-          for (int c = 0; c < 4 && ok; ++c) ok = issue(true, n - 1, c >> 1, c & 1, rr0, rr1, bk);
-          if (!ok) break;
-          if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
-        }
+        if (ok && n >= 1) ok = group(true, n - 1);
       }
       if (!ok) {
-        atomicOr(p.status, MFA_DEV_TIMEOUT);
+        if (lane == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
         // let every copy already issued land before the CTA can exit
-        const uint32_t first = (u > static_cast<uint32_t>(kNumSlots)) ? u - kNumSlots : 0;
-        for (uint32_t v = first; v < u; ++v)
-          wait_slow(bar(kBarFull + v % kNumSlots), (v / kNumSlots) & 1, nullptr, kDrainLimitNs);
-        if (nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
+        if (act)
+          for (int i = 0; i < (nmine < 3 ? nmine : 3); ++i)
+            wait_slow(bar(kBarFull + mine[i] % kNumSlots), (mine[i] / kNumSlots) & 1, nullptr, kDrainLimitNs);
+        if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
+    // ---------------- MMA issuer: QK^T of tile n, then PV of tile n - 1, so the next tile's
+    // scores are computed while the softmax works on the current one
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
+      constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
       constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, 64);
-      uint32_t u = 0;
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
       for (int n = 0; n <= ntiles && ok; ++n) {
@@ -600,11 +657,12 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t d_tmem = tmem + kTmemS + 64u * (n & 1);
+          const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
+          const uint32_t u0 = ring_use(n, ntiles, false, 0, 0);
           if constexpr (!kFp8) {
-            for (int c = 0; c < 4; ++c, ++u) {
-              const uint32_t slot = u % kNumSlots;
-              ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+            for (int c = 0; c < 4; ++c) {
+              const uint32_t slot = (u0 + c) % kNumSlots;
+              ok = wait_bar(bar(kBarFull + slot), ((u0 + c) / kNumSlots) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
               const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
@@ -617,15 +675,23 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             }
             if (!ok) break;
           } else {
-            // K(n) in tensor memory: lane = token, column kTmemK + d/2
-            ok = wait_bar(bar(kBarKReady), n & 1, abort_flag);
+            // e4m3 K boxes as TMA wrote them: the two pages of d-half dh are adjacent slots,
+            // one 128-row A operand; B stacks q's e4m3 hi part (rows 0..63) over its lo part
+            // (rows 64..127), so each K step (32) reads K once for both
+            for (int c = 0; c < 4 && ok; ++c)
+              ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk)
-              umma_f16_ts(d_tmem, tmem + kTmemK + 8u * kk,
-                          smem_desc(sbase + kOffQ + (kk >> 2) * 8192 + 32 * (kk & 3), 16, 1024), kIdescQK, kk != 0);
-            umma_commit(bar(kBarKFree));
+            for (int dh = 0; dh < 2; ++dh) {
+              const uint32_t a0 = sbase + kOffRing + ((u0 + 2 * dh) % kNumSlots) * kSlotBytes;
+              const uint32_t b0 = sbase + kOffQ + dh * 16384;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_f8_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
+                           kIdescQK8, (dh | kk) != 0);
+            }
+            for (int c = 0; c < 4; ++c) umma_commit(bar(kBarEmpty + (u0 + c) % kNumSlots));
           }
           umma_commit(bar(kBarSFull + (n & 1)));
           if (last) umma_commit(bar(kBarQEmpty));
@@ -636,38 +702,36 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           const int4 sg = seg[sv];
           const bool first = (jv == sg.y), last = (jv == sg.z - 1);
           const int kb = sv & 1;
+          const int4 ti = tile_info[m];
+          const uint32_t uv = ring_use(m, ntiles, true, 0, 0);
           ok = wait_bar(bar(kBarPFull), m & 1, abort_flag);
+          if (kFp8 && ok) ok = wait_bar(bar(kBarVhFull), m & 1, abort_flag);
           if (ok && first && sv >= 2) ok = wait_bar(bar(kBarOEmpty + kb), ((sv >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const int rr0 = min(kPage, sg.w - kTile * jv);
-          const int rr1 = min(kPage, sg.w - kTile * jv - kPage);
           for (int pg = 0; pg < 2 && ok; ++pg) {
-            const int r = pg ? rr1 : rr0;
+            const int r = pg ? ti.w : ti.z;
             for (int hh = 0; hh < 2; ++hh) {
               uint32_t a0;
               if constexpr (!kFp8) {
-                const uint32_t slot = u % kNumSlots;
-                ok = wait_bar(bar(kBarFull + slot), (u / kNumSlots) & 1, abort_flag);
+                const uint32_t u = uv + 2 * pg + hh;
+                ok = wait_bar(bar(kBarFull + u % kNumSlots), (u / kNumSlots) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                a0 = sbase + kOffRing + slot * kSlotBytes;
+                a0 = sbase + kOffRing + (u % kNumSlots) * kSlotBytes;
               } else {
-                a0 = sbase + KvLayout<true>::kOffVh + (2 * pg + hh) * 16384;   // filled by the softmax warps
+                a0 = sbase + KvLayout<true>::kOffVh + (2 * pg + hh) * 16384;   // filled by the dequant warps
               }
               if (r > 0) {
                 const uint32_t b0 = sbase + kOffP + pg * 8192;
-                const uint32_t d_tmem = tmem + kTmemO + 128u * kb + 64u * hh;
+                const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 128u * kb + 64u * hh;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   umma_f16_ss(d_tmem, smem_desc(a0 + 2048 * kk, 8192, 1024),
                               smem_desc(b0 + 2048 * kk, 1024, 1024), kIdescPV,
                               !(first && pg == 0 && kk == 0));
               }
-              if constexpr (!kFp8) {
-                umma_commit(bar(kBarEmpty + u % kNumSlots));
-                ++u;
-              }
+              if constexpr (!kFp8) umma_commit(bar(kBarEmpty + (uv + 2 * pg + hh) % kNumSlots));
             }
           }
           if (!ok) break;
@@ -681,10 +745,67 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       umma_commit(bar(kBarDrain));
       wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
     }
+  } else if (kFp8 && warp < softmax_warp0<kFp8>()) {
+    // e4m3: warps 2 and 3 complete warpgroup 0 and have no role
+    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
+  } else if (kFp8 && warp >= kDequantWarp0) {
+    if constexpr (kFp8) {
+      reg_dealloc<kRegsDequant>();
+      // ---------------- e4m3 V -> f16 PV operand (warps 12..15; thread = token row of a tile)
+      // The token's V scale multiplies its row here (P keeps plain weights).  Scales above
+      // 146 would let 448 * scale leave the f16 range: they are clamped and reported.
+      using L8 = KvLayout<true>;
+      const int dt = tid - 32 * kDequantWarp0;   // 0..127
+      const int pg = dt >> 6, ri = dt & 63;       // page of the tile (warp-uniform), row
+      bool aborted = false, range_bad = false;
+      if (p.early_metadata) grid_dep_wait();      // v_scale may be written by the preceding kernel
+      float sv_next = (ntiles > 0) ? token_scale(p.v_scale, tile_info[0], pg, ri) : 0.f;
+      for (int n = 0; n < ntiles; ++n) {
+        const int4 ti = tile_info[n];
+        const int rp = pg ? ti.w : ti.z;
+        float sv = sv_next;                      // loaded one tile ahead
+        if (n + 1 < ntiles) sv_next = token_scale(p.v_scale, tile_info[n + 1], pg, ri);
+        range_bad |= !(sv <= 146.f);
+        sv = fminf(sv, 146.f);
+        const uint32_t sv2 = pack_f16_sat(sv, sv);
+        auto cv = [&](uint32_t two) { return hmul2(e4m3x2_to_f16x2(two), sv2); };
+        // the f16 tile is free once the previous tile's PV has read it
+        bool ok = (n == 0) || wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
+        for (int dh = 0; dh < 2 && ok; ++dh) {
+          const uint32_t use = ring_use(n, ntiles, true, pg, dh);
+          ok = wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
+          if (!ok || rp <= 0) continue;
+          const uint8_t* box = smem + kOffRing + (use % kNumSlots) * kSlotBytes + ri * 128;
+          uint4 rw[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) rw[q] = *reinterpret_cast<const uint4*>(box + ((q ^ (ri & 7)) << 4));
+          // [64 tokens x 64 d] f16 boxes, 128 B rows, 128B swizzle (as TMA would lay them out)
+          uint8_t* vh = smem + L8::kOffVh + (2 * pg + dh) * 16384 + ri * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint4 w = rw[q];
+            const uint4 lo = make_uint4(cv(w.x), cv(w.x >> 16), cv(w.y), cv(w.y >> 16));
+            const uint4 hi = make_uint4(cv(w.z), cv(w.z >> 16), cv(w.w), cv(w.w >> 16));
+            const int j0 = 2 * q, j1 = 2 * q + 1;   // 16-byte f16 chunks 0..15 of the 128-d row
+            *reinterpret_cast<uint4*>(vh + (j0 >> 3) * 8192 + (((j0 & 7) ^ (ri & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(vh + (j1 >> 3) * 8192 + (((j1 & 7) ^ (ri & 7)) << 4)) = hi;
+          }
+        }
+        // the four warps agree; past this point every ring read of the tile is done
+        if (named_bar_or(4, kDequantThreads, !ok || *abort_flag)) { aborted = true; break; }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarVhFull));
+        if (dt == 0)
+          for (int c = 0; c < 4; ++c) mbar_arrive(bar(kBarEmpty + ring_use(n, ntiles, true, c >> 1, c & 1) % kNumSlots));
+      }
+      if (range_bad) atomicOr(p.status, MFA_DEV_RANGE);
+      if (aborted && dt == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
+    }
   } else {
+    if constexpr (kFp8) reg_alloc<kRegsSoftmax>();
     // ---------------- softmax + epilogue (256 threads: two warps per TMEM lane quarter)
-    const int ts = tid - 64;                       // 0..255
-    const int sw = warp - 2;                       // 0..7
+    const int ts = tid - 32 * softmax_warp0<kFp8>();   // 0..255
+    const int sw = warp - softmax_warp0<kFp8>();       // 0..7
     const int grp = sw >> 2;                       // head half [32*grp, +32); e4m3 dequant: d-half
     const int h0 = 32 * grp;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
@@ -697,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     float* linv = reinterpret_cast<float*>(smem + kOffLinv);
     const float c = p.scale_log2;
     const bool issuer = (lane == 0) && ((sw & 3) == 0);   // one bulk-store thread per head half
-    bool range_bad = false;                        // e4m3: a value left the f16 range
+    float qinv = 1.f, qinv_next = 1.f;              // e4m3: 2^-sigma of the segment's q split
 
     if (p.early_metadata) grid_dep_wait();
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
@@ -721,91 +842,6 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
     // valid rows of a tile's page pg: the last page's rows sit at the end of the box
     auto page_rows = [&](int L, int j, int pg) { return min(kPage, L - kTile * j - kPage * pg); };
 
-    // e4m3: per-token scale of this thread's row in tile t (0 for rows past the length)
-    auto row_scale = [&](int t, bool is_v, int rp) -> float {
-      if (rp <= 0 || ri < kPage - rp) return 0.f;
-      const int idx = is_v ? 2 + 2 * rpg + grp : rpg;
-      const float* sc = reinterpret_cast<const float*>(
-          smem + kOffScale + (t % KvLayout<true>::kScaleTiles) * KvLayout<true>::kScaleTileBytes + idx * 256);
-      return sc[ri - (kPage - rp)];
-    };
-
-    // e4m3: wait until ring use `use` is filled (every consumer waits, even when its page
-    // is past the sequence end and nothing is read, so that the slot's full and empty
-    // phases advance in step with the producer's)
-    auto wait_filled = [&](uint32_t use) -> bool {
-      return wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
-    };
-    // e4m3: this thread's 128 raw codes (its token row, its d-half) of a filled ring box
-    auto read_raw = [&](uint32_t use, uint4 (&rw)[8]) {
-      const uint8_t* box = smem + kOffRing + (use % kNumSlots) * kSlotBytes + ri * 128;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) rw[q] = *reinterpret_cast<const uint4*>(box + ((q ^ (ri & 7)) << 4));
-    };
-    // e4m3: dequantise tile t's K part of this thread into tensor memory (lane = token)
-    auto dequant_k = [&](int t, int L, int j) -> bool {
-      if (t >= 1 && !wait_warp(bar(kBarKFree), (t - 1) & 1, abort_flag)) return false;
-      const uint32_t use = ring_use(t, ntiles, false, rpg, grp);
-      if (!wait_filled(use)) return false;
-      if (page_rows(L, j, rpg) > 0) {
-        uint4 rw[8];
-        read_raw(use, rw);
-        tc_fence_after();
-#pragma unroll
-        for (int hq = 0; hq < 2; ++hq) {
-          uint32_t kv[32];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 w = rw[4 * hq + q];
-            kv[8 * q + 0] = e4m3x2_to_f16x2(w.x);
-            kv[8 * q + 1] = e4m3x2_to_f16x2(w.x >> 16);
-            kv[8 * q + 2] = e4m3x2_to_f16x2(w.y);
-            kv[8 * q + 3] = e4m3x2_to_f16x2(w.y >> 16);
-            kv[8 * q + 4] = e4m3x2_to_f16x2(w.z);
-            kv[8 * q + 5] = e4m3x2_to_f16x2(w.z >> 16);
-            kv[8 * q + 6] = e4m3x2_to_f16x2(w.w);
-            kv[8 * q + 7] = e4m3x2_to_f16x2(w.w >> 16);
-          }
-          tmem_st32(tmem + kTmemK + 64u * grp + 32u * hq + lane_base, kv);
-        }
-        tmem_st_wait();
-      }
-      mbar_arrive(bar(kBarEmpty + use % kNumSlots));
-      tc_fence_before();
-      mbar_arrive(bar(kBarKReady));
-      return true;
-    };
-    // e4m3: dequantise tile t's V part of this thread into the f16 PV operand tile; the
-    // token's V scale (it arrives with the box) multiplies the row here, so that P keeps
-    // plain weights.  Scales above 146 would let 448 * scale leave the f16 range: they
-    // are clamped and reported.
-    auto dequant_v = [&](int t, int L, int j) -> bool {
-      const uint32_t use = ring_use(t, ntiles, true, rpg, grp);
-      if (!wait_filled(use)) return false;
-      const int rp = page_rows(L, j, rpg);
-      if (rp > 0) {
-        uint4 rw[8];
-        read_raw(use, rw);
-        float sv = row_scale(t, true, rp);             // 0 for rows past the length
-        range_bad |= !(sv <= 146.f);
-        sv = fminf(sv, 146.f);
-        const uint32_t sv2 = pack_f16_sat(sv, sv);
-        auto cv = [&](uint32_t two) { return hmul2(e4m3x2_to_f16x2(two), sv2); };
-        // [64 tokens x 64 d] f16 boxes, 128 B rows, 128B swizzle (as TMA would lay them out)
-        uint8_t* vh = smem + KvLayout<true>::kOffVh + (2 * rpg + grp) * 16384 + ri * 128;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 w = rw[q];
-          const uint4 lo = make_uint4(cv(w.x), cv(w.x >> 16), cv(w.y), cv(w.y >> 16));
-          const uint4 hi = make_uint4(cv(w.z), cv(w.z >> 16), cv(w.w), cv(w.w >> 16));
-          const int j0 = 2 * q, j1 = 2 * q + 1;   // 16-byte f16 chunks 0..15 of the 128-d row
-          *reinterpret_cast<uint4*>(vh + (j0 >> 3) * 8192 + (((j0 & 7) ^ (ri & 7)) << 4)) = lo;
-          *reinterpret_cast<uint4*>(vh + (j1 >> 3) * 8192 + (((j1 & 7) ^ (ri & 7)) << 4)) = hi;
-        }
-      }
-      mbar_arrive(bar(kBarEmpty + use % kNumSlots));
-      return true;
-    };
     // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx & 1),
     // normalised by 1/l from linv: [head][d] rows are staged in shared memory and sent
     // with bulk async copies.  With `from_ring` the rows go through the idle operand
@@ -817,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       aborted = aborted || !okO;
       if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) return false;
       tc_fence_after();
-      const uint32_t o_tmem = tmem + kTmemO + 128u * kb + h0 + lane_base;
+      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 128u * kb + h0 + lane_base;
       uint32_t oa[32], ob[32];
       tmem_ld32(o_tmem, oa);
       tmem_ld32(o_tmem + 64, ob);
@@ -892,24 +928,72 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       return true;
     };
 
-    // e4m3: q of segment sidx arrives in bf16; the e4m3 path multiplies in f16, so convert
-    // it in place.  Done as soon as the segment's first K tile is in tensor memory (for a
-    // later segment: before the previous segment's epilogue, whose wait for its last PV
-    // must not depend on this segment's first QK).
+    // 32 scores of this thread's row (token) for its heads: e4m3 adds the hi-part and the
+    // lo-part columns of S^T (the two halves of the N = 128 QK^T result)
+    auto ld_s32 = [&](uint32_t taddr, uint32_t (&sv)[32]) {
+      tmem_ld32(taddr, sv);
+      if constexpr (kFp8) {
+        uint32_t sl[32];
+        tmem_ld32(taddr + 64, sl);
+        tmem_ld_wait(sv);
+        tmem_ld_wait(sl);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) sv[h] = __float_as_uint(__uint_as_float(sv[h]) + __uint_as_float(sl[h]));
+      } else {
+        tmem_ld_wait(sv);
+      }
+    };
+
+    // e4m3: q of segment sidx arrives in bf16 and is split in place into two e4m3 parts,
+    // hi = e4m3(2^sigma q) and lo = e4m3(2^sigma q - hi), with one power of two 2^sigma per
+    // sequence putting its largest |q| in [64, 128): hi + lo reproduces 2^sigma q (see
+    // split_e4m3) and the QK^T MMA runs on e4m3 K as stored.  Thread ts converts row
+    // ts & 63 (a head) of bf16 box ts >> 6 (64 d); all reads precede all writes.  Done for
+    // a later segment right after the previous segment's last scores are read, so its
+    // first QK^T can overlap that segment's last PV and epilogue.
     auto convert_q = [&](int sidx) {
-      if (wait_warp(bar(kBarQFull), sidx & 1, abort_flag)) {
-        uint4* qv = reinterpret_cast<uint4*>(smem + kOffQ) + ts * 8;
+      const bool okQ = wait_warp(bar(kBarQFull), sidx & 1, abort_flag);
+      const int hq = ts & 63, cq = ts >> 6;
+      uint4 w[8];
+      float mx = 0.f;
+      if (okQ) {
+        const uint8_t* src = smem + kOffQ + cq * 8192 + hq * 128;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          uint4 w = qv[q];
-          uint32_t* e = reinterpret_cast<uint32_t*>(&w);
+          w[q] = *reinterpret_cast<const uint4*>(src + 16 * q);
+          const uint32_t* e = reinterpret_cast<const uint32_t*>(&w[q]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x0 = __uint_as_float(e[k] << 16), x1 = __uint_as_float(e[k] & 0xFFFF0000u);
-            range_bad |= !(fabsf(x0) <= 65504.f) | !(fabsf(x1) <= 65504.f);
-            e[k] = pack_f16_sat(x0, x1);
-          }
-          qv[q] = w;
+          for (int k = 0; k < 4; ++k)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(e[k] << 16)), fabsf(__uint_as_float(e[k] & 0xFFFF0000u))));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float* qmax = reinterpret_cast<float*>(misc + 24);   // [8] per softmax warp
+      if (lane == 0) qmax[sw] = mx;
+      named_bar_sync(1, kSoftmaxThreads);
+      float M = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) M = fmaxf(M, qmax[i]);
+      int sig = 0;
+      if (M > 0.f && M <= 3.0e38f) sig = min(126, max(-126, 6 - static_cast<int>((__float_as_uint(M) >> 23) & 0xFFu) + 127));
+      const float qs = __uint_as_float(static_cast<uint32_t>(127 + sig) << 23);
+      qinv_next = __uint_as_float(static_cast<uint32_t>(127 - sig) << 23);
+      if (okQ) {
+        uint8_t* dst = smem + kOffQ + (cq >> 1) * 16384 + hq * 128;   // hi part (rows 0..63); lo rows at +8 KB
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int k = q ^ (hq & 7);                       // logical 16-byte chunk of the bf16 row
+          const uint32_t* e = reinterpret_cast<const uint32_t*>(&w[q]);
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            split_e4m3(__uint_as_float(e[i] << 16) * qs, __uint_as_float(e[i] & 0xFFFF0000u) * qs, hi[i], lo[i]);
+          // d = 64 cq + 8 k .. +7: bytes 8 (k & 1) of logical e4m3 chunk 4 (cq & 1) + (k >> 1)
+          const int ci = 4 * (cq & 1) + (k >> 1);
+          const int off = ((ci ^ (hq & 7)) << 4) + 8 * (k & 1);
+          *reinterpret_cast<uint2*>(dst + off) = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+          *reinterpret_cast<uint2*>(dst + 8192 + off) = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
         }
         fence_proxy_async_smem();
       } else {
@@ -918,11 +1002,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       mbar_arrive(bar(kBarQReady));
     };
 
+    float sk_next = 0.f;                            // e4m3: K scale of this row in the next tile
     if constexpr (kFp8) {
-      // the first tile's K goes into tensor memory before the loop; each iteration then
-      // dequantises the next tile's K after its own softmax
       if (ntiles > 0) {
-        if (!dequant_k(0, seg[0].w, seg[0].y)) aborted = true;
+        sk_next = token_scale(p.k_scale, tile_info[0], rpg, ri);
         convert_q(0);
       }
     }
@@ -932,9 +1015,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       const int b = sg.x, L = sg.w, kb = s & 1;
       const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
       const int slot_p = b + static_cast<int>(blockIdx.x);
-      const uint32_t o_tmem = tmem + kTmemO + 128u * kb + h0 + lane_base;   // + 64 for d in [128, 256)
+      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 128u * kb + h0 + lane_base;   // + 64 for d in [128, 256)
       if (ts < kH) m_ref[ts] = -INFINITY;
       if constexpr (kFp8) {
+        qinv = qinv_next;
 #pragma unroll
         for (int h = 0; h < 32; ++h) lreg[h] = 0.f;
       }
@@ -942,23 +1026,25 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       bool stop = false;
       for (int j = sg.y; j < sg.z; ++j, ++n) {
         const bool first = (j == sg.y);
-        const uint32_t s_tmem = tmem + kTmemS + 64u * (n & 1) + h0 + lane_base;
+        const uint32_t s_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1) + h0 + lane_base;
         const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
         aborted = aborted || !okS;
         bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
         const int rp = page_rows(L, j, rpg);
         const bool valid = okS && rp > 0 && ri >= kPage - rp;
-        // score multiplier of this row: scale*log2(e), times the token's K scale for e4m3
-        // (the K box and its scales were waited for when K was dequantised)
+        // score multiplier of this row: scale*log2(e), times (e4m3) the token's K scale and
+        // the 2^-sigma that undoes q's split scaling
         float ck = c;
-        if constexpr (kFp8) ck = c * row_scale(n, false, rp);
+        if constexpr (kFp8) {
+          ck = c * qinv * sk_next;                 // loaded one tile ahead
+          if (n + 1 < ntiles) sk_next = token_scale(p.k_scale, tile_info[n + 1], rpg, ri);
+        }
         // --- does any score of this row exceed its head's reference max by > 2^8?
         bool need = false;
         if (okS) {
           tc_fence_after();
           uint32_t sv[32];
-          tmem_ld32(s_tmem, sv);
-          tmem_ld_wait(sv);
+          ld_s32(s_tmem, sv);
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h0 + h);
@@ -969,13 +1055,13 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
           }
           need = need && valid;
         }
-        if (named_bar_or(1, kSoftmaxThreads, need || aborted || *abort_flag)) {
+        const bool any_need = named_bar_or(1, kSoftmaxThreads, need || aborted || *abort_flag);
+        if (any_need) {
           if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) { stop = true; break; }
           // --- rare path: new reference max for heads whose scores jumped by > 2^8
           {
             uint32_t sv[32];
-            tmem_ld32(s_tmem, sv);
-            tmem_ld_wait(sv);
+            ld_s32(s_tmem, sv);
             float mv[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sv[h]) * ck : -INFINITY;
@@ -1028,7 +1114,13 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
             tmem_ld16(l_tmem + 16 * half, lv);
             tmem_ld16(lx_tmem + 16 * half, lx);
           }
+          if constexpr (kFp8) tmem_ld16(s_tmem + 64 + 16 * half, lv);   // lo-part scores
           tmem_ld_wait(sv);
+          if constexpr (kFp8) {
+            tmem_ld_wait(lv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) + __uint_as_float(lv[e]));
+          }
           if (!kFp8 && !first) {
             tmem_ld_wait(lv);
             tmem_ld_wait(lx);
@@ -1066,19 +1158,10 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
         tc_fence_before();
         mbar_arrive(bar(kBarSEmpty + (n & 1)));
         if constexpr (kFp8) {
-          // next tile's K into tensor memory (the MMA warp can start its QK right away)
-          if (n + 1 < ntiles) {
-            const int s1 = (j + 1 < sg.z) ? s : s + 1;
-            const int j1 = (j + 1 < sg.z) ? j + 1 : seg[s1].y;
-            if (!dequant_k(n + 1, seg[s1].w, j1)) aborted = true;
-            if (s1 != s) convert_q(s1);
-          }
+          // the next segment's q, as soon as this segment's last scores are read
+          if (j + 1 == sg.z && s + 1 < nseg) convert_q(s + 1);
         }
         if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
-        if constexpr (kFp8) {
-          // this tile's V into the f16 operand tile (free: the previous PV is done)
-          if (!dequant_v(n, L, j)) aborted = true;
-        }
         // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
         uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
@@ -1141,7 +1224,6 @@ __global__ void __launch_bounds__(kThreads, 1) mfa_decode_kernel(const __grid_co
       }
     }
     if (issuer) bulk_wait_read0();
-    if (range_bad) atomicOr(p.status, MFA_DEV_RANGE);
     if (aborted && ts == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
   }
 
@@ -1579,7 +1661,7 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(fp8 ? threads_of<true>() : threads_of<false>(), 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

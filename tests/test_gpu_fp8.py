@@ -58,6 +58,31 @@ def test_fp8_v_scale_out_of_range_is_reported():
     assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
 
 
+def test_fp8_q_beyond_the_f16_range():
+    # q.K^T runs on e4m3 codes with q split into hi + lo under a per-sequence power of two,
+    # so a q far outside the f16 range is still exact (here: one-hot attention)
+    case = inputs.small("fq", 3, [300, 129, 64], kv_dtype="fp8_e4m3", seed=45)
+    case.q[0] *= 2.0 ** 20
+    case.q[2] *= 2.0 ** -20
+    out, lse, _ = gpu_decode(case)
+    ref_o, ref_lse = oracle.decode(case)
+    got = out.double().cpu().numpy()
+    assert np.abs(got - ref_o).max() <= FP8["max_abs"]
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= FP8["rel_l2"]
+    # lse of sequence 0 is ~3e6: the fp32 scores that make it carry the accumulator's
+    # relative rounding (about 1e-6 over 256 products), so the bound is relative there
+    g = lse.double().cpu().numpy()
+    assert np.all(np.abs(g - ref_lse) <= 2e-3 + 1e-5 * np.abs(ref_lse))
+
+
+def test_fp8_heads_of_mixed_magnitude_share_one_split_scale():
+    case = inputs.small("fm", 2, [700, 1500], kv_dtype="fp8_e4m3", seed=46)
+    mult = torch.tensor([2.0 ** ((h % 9) - 4) for h in range(64)], dtype=torch.float32)
+    case.q.copy_((case.q.float() * mult[None, :, None]).to(torch.bfloat16))
+    out, lse, _ = gpu_decode(case, force_ctas=3)
+    check_parity(case, out, lse, **FP8)
+
+
 @pytest.mark.parametrize("name", ["b128_l4096_fp8", "b32_l4096_fp8", "long_b4_l131072_fp8"])
 def test_fp8_full_size_workload(name):
     case = inputs.generate(inputs.WORKLOADS[name])
