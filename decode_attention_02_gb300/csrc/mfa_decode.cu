@@ -92,7 +92,6 @@ struct KvLayout<false> {
   static constexpr int kOffRing = 49152;
   static constexpr int kNumSlots = 10;
   static constexpr int kSlotBytes = 16384;
-  static constexpr int kOffStageFinal = kOffRing;   // 128 KB free after the last MMA
   static constexpr int kExtraSmem = 0;
 };
 template <>
@@ -101,7 +100,6 @@ struct KvLayout<true> {
   static constexpr int kOffRing = 114688;
   static constexpr int kNumSlots = 12;
   static constexpr int kSlotBytes = 8192;
-  static constexpr int kOffStageFinal = kOffVh;     // V f16 + ring: 160 KB free after the last MMA
   static constexpr int kExtraSmem = 0;
 };
 static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
@@ -488,13 +486,37 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     int W = 0;
-    block_incl_scan<kThreads>(loc, scratch, W);
+    const int incl0 = block_incl_scan<kThreads>(loc, scratch, W);
     const int G = gridDim.x, g = blockIdx.x;
     const int t0 = static_cast<int>((static_cast<long long>(g) * W) / G);
     const int t1 = static_cast<int>((static_cast<long long>(g + 1) * W) / G);
     int nseg = 0;
     if (t1 - t0 > kMaxTilesPerCta) {
       if (tid == 0) atomicOr(p.status, MFA_DEV_SCHEDULE);
+    } else if (p.batch <= kThreads) {
+      // one sequence per thread: its tiles are [incl0 - T, incl0) of the first scan; the
+      // overlapping sequences are numbered by a ballot count
+      bool dummy = false;
+      const int L = (tid < p.batch) ? clamp_len(L_first, cap, dummy) : 0;
+      const int T = tiles_of(L);
+      const int excl = incl0 - T;
+      const bool f = (tid < p.batch) && (max(t0, excl) < min(t1, incl0));
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      if (lane == 0) scratch[warp] = __popc(m);
+      __syncthreads();
+      int before = 0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) {
+        const int x = scratch[w];
+        before += (w < warp) ? x : 0;
+        nseg += x;
+      }
+      if (f) {
+        const int fidx = before + __popc(m & ((1u << lane) - 1u));
+        const int lo = max(t0, excl), hi = min(t1, incl0);
+        seg[fidx] = make_int4(tid, lo - excl, hi - excl, L);
+        seg_n0[fidx] = lo - t0;
+      }
     } else {
       int carry = 0;
       for (int c0 = 0; c0 < p.batch && carry < t1; c0 += kThreads) {
@@ -608,7 +630,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       };
       for (int n = 0; n <= ntiles && ok; ++n) {
         if (n < ntiles) {
-          if (sq < nseg && n == seg_n0[sq]) {
+          if (ok) ok = group(false, n);
+          if (ok && sq < nseg && n == seg_n0[sq]) {
             bool okq = true;
             if (lane == 0) {
               if (sq > 0) okq = wait_bar(bar(kBarQEmpty), (sq - 1) & 1, abort_flag);
@@ -626,7 +649,6 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             ok = __all_sync(0xffffffffu, okq);
             ++sq;
           }
-          if (ok) ok = group(false, n);
         }
         if (ok && n >= 1) ok = group(true, n - 1);
       }
@@ -843,11 +865,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     auto page_rows = [&](int L, int j, int pg) { return min(kPage, L - kTile * j - kPage * pg); };
 
     // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx & 1),
-    // normalised by 1/l from linv: [head][d] rows are staged in shared memory and sent
-    // with bulk async copies.  With `from_ring` the rows go through the idle operand
-    // buffers at 64 KB offset `ring_k`; otherwise through this half's 8 KB of the P
-    // buffer in double-buffered 4 KB rounds.  Returns false if the CTA is aborting.
-    auto write_segment = [&](int sidx, int b, int slot_p, bool whole, bool from_ring, int ring_k) -> bool {
+    // normalised by 1/l from linv, as [head][d] rows.  `direct`: plain stores from
+    // registers (the CTA's last two segments, after its last MMA); otherwise the rows are
+    // staged in this half's 8 KB of the P buffer and sent by bulk async copies in
+    // double-buffered 4 KB rounds, off the threads' critical path.  Returns false if the
+    // CTA is aborting.
+    auto write_segment = [&](int sidx, int b, int slot_p, bool whole, bool direct) -> bool {
       const int kb = sidx & 1;
       const bool okO = wait_warp(bar(kBarOFull + kb), (sidx >> 1) & 1, abort_flag);
       aborted = aborted || !okO;
@@ -880,17 +903,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           reinterpret_cast<float*>(stg)[hl * kD + 128 + row] = v1;
         }
       };
-      if (from_ring) {
-        const uint32_t off = Lay::kOffStageFinal + ring_k * 65536 + grp * 32768;
-        uint8_t* stg = smem + off;
+      if (direct) {
+        // straight from registers: for each head a warp writes 32 consecutive d values
 #pragma unroll
-        for (int h = 0; h < 32; ++h) put(stg, h, __uint_as_float(oa[h]), __uint_as_float(ob[h]));
-        fence_proxy_async_smem();
-        named_bar_sync(2 + grp, kSoftmaxThreads / 2);
-        if (issuer) {
-          bulk_store_s2g(gdst, sbase + off, 32 * kD * esz);
-          bulk_commit();
-        }
+        for (int h = 0; h < 32; ++h) put(gdst, h, __uint_as_float(oa[h]), __uint_as_float(ob[h]));
         return true;
       }
       // 4 KB per round: 4 heads (fp32) or 8 heads (bf16); round sizes are compile-time so
@@ -1039,32 +1055,37 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           ck = c * qinv * sk_next;                 // loaded one tile ahead
           if (n + 1 < ntiles) sk_next = token_scale(p.k_scale, tile_info[n + 1], rpg, ri);
         }
-        // --- does any score of this row exceed its head's reference max by > 2^8?
+        // --- this row's 32 scores, read from tensor memory once per tile; does any exceed
+        //     its head's reference max by > 2^8?
+        // (bf16 keeps the scores in registers for the exponentials; e4m3, whose row sums
+        // already live in registers, reads them again there)
         bool need = false;
+        uint32_t sc[32];
         if (okS) {
           tc_fence_after();
-          uint32_t sv[32];
-          ld_s32(s_tmem, sv);
+          ld_s32(s_tmem, sc);
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h0 + h);
-            need |= (fmaf(__uint_as_float(sv[h + 0]), ck, -m4.x) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 1]), ck, -m4.y) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 2]), ck, -m4.z) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sv[h + 3]), ck, -m4.w) > kRescaleThreshold);
+            need |= (fmaf(__uint_as_float(sc[h + 0]), ck, -m4.x) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sc[h + 1]), ck, -m4.y) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sc[h + 2]), ck, -m4.z) > kRescaleThreshold) |
+                    (fmaf(__uint_as_float(sc[h + 3]), ck, -m4.w) > kRescaleThreshold);
           }
           need = need && valid;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sc[h] = 0u;
         }
         const bool any_need = named_bar_or(1, kSoftmaxThreads, need || aborted || *abort_flag);
         if (any_need) {
           if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) { stop = true; break; }
           // --- rare path: new reference max for heads whose scores jumped by > 2^8
           {
-            uint32_t sv[32];
-            ld_s32(s_tmem, sv);
+            if constexpr (kFp8) ld_s32(s_tmem, sc);
             float mv[32];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sv[h]) * ck : -INFINITY;
+            for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sc[h]) * ck : -INFINITY;
             red[wq * 64 + h0 + lane] = warp_reduce_scatter32<true>(mv);
           }
           named_bar_sync(1, kSoftmaxThreads);
@@ -1108,18 +1129,21 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         uint32_t pk[16];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t sv[16], lv[16], lx[16];
-          tmem_ld16(s_tmem + 16 * half, sv);
+          uint32_t lv[16], lx[16], sf[16];
+          const uint32_t* sv = sc + 16 * half;
+          if constexpr (kFp8) {
+            // hi-part and lo-part scores, summed
+            tmem_ld16(s_tmem + 16 * half, sf);
+            tmem_ld16(s_tmem + 64 + 16 * half, lv);
+            tmem_ld_wait(sf);
+            tmem_ld_wait(lv);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) sf[e] = __float_as_uint(__uint_as_float(sf[e]) + __uint_as_float(lv[e]));
+            sv = sf;
+          }
           if (!kFp8 && !first) {
             tmem_ld16(l_tmem + 16 * half, lv);
             tmem_ld16(lx_tmem + 16 * half, lx);
-          }
-          if constexpr (kFp8) tmem_ld16(s_tmem + 64 + 16 * half, lv);   // lo-part scores
-          tmem_ld_wait(sv);
-          if constexpr (kFp8) {
-            tmem_ld_wait(lv);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sv[e] = __float_as_uint(__uint_as_float(sv[e]) + __uint_as_float(lv[e]));
           }
           if (!kFp8 && !first) {
             tmem_ld_wait(lv);
@@ -1204,7 +1228,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       named_bar_sync(1, kSoftmaxThreads);
       if (s + 2 < nseg) {
         // the accumulator is needed again by segment s + 2: write it out now
-        if (!write_segment(s, b, slot_p, whole, false, 0)) break;
+        if (!write_segment(s, b, slot_p, whole, false)) break;
       } else {
         // one of the CTA's last two segments: its accumulator stays in tensor memory
         // and is written after the last tile, when the operand buffers are idle
@@ -1214,13 +1238,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       }
     }
     if (!aborted && !*abort_flag) {
-      // deferred accumulators, newest first: the wait for the last segment's accumulator
-      // also means every MMA has finished reading the operand buffers, which then stage
-      // the rows (uniform: every thread reads the same values)
+      // deferred accumulators, newest first, stored straight from registers (uniform:
+      // every thread reads the same values)
       const int first_def = nseg >= 2 ? nseg - 2 : 0;
       for (int s = nseg - 1; s >= first_def; --s) {
         const int kb = s & 1;
-        if (!write_segment(s, defer_b[kb], defer_slot[kb], defer_whole[kb], true, s - first_def)) break;
+        if (!write_segment(s, defer_b[kb], defer_slot[kb], defer_whole[kb], true)) break;
       }
     }
     if (issuer) bulk_wait_read0();

@@ -235,6 +235,19 @@ def test_runs_on_a_side_stream():
     check_parity(case, out, lse)
 
 
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_batch_larger_than_one_thread_per_sequence(kv_dtype):
+    # more sequences than the decode kernel has threads: the schedule takes its chunked path
+    rng = np.random.default_rng(77)
+    lens = [int(x) for x in rng.integers(0, 300, size=600)]
+    lens[5] = 0
+    lens[599] = 257
+    case = inputs.small("bigb", len(lens), lens, kv_dtype=kv_dtype, seed=78)
+    out, lse, dec = gpu_decode(case)
+    limits = dict(max_abs=3e-2, rel_l2=1.5e-2) if kv_dtype != "bf16" else {}
+    check_parity(case, out, lse, **limits)
+
+
 @pytest.mark.parametrize("name", ["b32_l4096_bf16", "ragged_b128_l1024_8192_bf16", "long_b4_l131072_bf16"])
 def test_full_size_workload(name):
     """Full-size workloads in the launch configuration the benchmark times."""
