@@ -44,6 +44,8 @@
 #include <cstring>
 #include <mutex>
 #include <type_traits>
+#include <vector>
+#include <algorithm>
 
 #include "mfa.h"
 #include "ptx.cuh"
@@ -232,21 +234,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return ok;
 }
 
-// Block-wide (kThreads threads) inclusive scan of one int per thread; also returns the total.
-template <int kThreads>
-__device__ __forceinline__ int block_incl_scan(int v, int* scratch, int& total) {
+// Block-wide (kThreads threads) inclusive scan of one value per thread; also returns the total.
+template <int kThreads, typename V = int>
+__device__ __forceinline__ V block_incl_scan(V v, V* scratch, V& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    const V t = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += t;
   }
   if (lane == 31) scratch[warp] = v;
   __syncthreads();
-  int before = 0, tot = 0;
+  V before = 0, tot = 0;
 #pragma unroll
   for (int w = 0; w < kThreads / 32; ++w) {
-    const int x = scratch[w];
+    const V x = scratch[w];
     before += (w < warp) ? x : 0;
     tot += x;
   }
@@ -476,66 +478,117 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   if (!p.early_metadata) grid_dep_wait();
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
+  // Cost-balanced split: tile k of sequence b sits at cost 4 (S_b + k) + 3 N_b, S_b being the
+  // tiles and N_b the non-empty sequences before b, so a sequence boundary inside a CTA's
+  // range weighs 3/4 of a tile (the next sequence's q load and one more epilogue).  CTA g owns
+  // the tiles whose cost lies in [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1):
+  // a contiguous run of tiles, in sequence order across CTAs.  Tile counts and non-empty
+  // counts are scanned together (low and high 32 bits).
   const int cap = p.max_pages * kPage;
   {
-    int* scratch = misc + 4;
+    long long* scratch = reinterpret_cast<long long*>(smem + kOffRed);   // idle until the softmax
+    int* tb = misc + 20;   // [0] first tile, [1] end tile of this CTA (written by their owners)
     bool bad = false;
-    int loc = 0;
+    auto packed = [](int T) { return static_cast<long long>(T) | (static_cast<long long>(T > 0) << 32); };
+    long long loc = 0;
     const int L_first = (tid < p.batch) ? p.seq_lens[tid] : 0;   // reused by the segment scan below
-    loc += tiles_of(clamp_len(L_first, cap, bad));
-    for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += tiles_of(clamp_len(p.seq_lens[b], cap, bad));
+    loc += packed(tiles_of(clamp_len(L_first, cap, bad)));
+    for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += packed(tiles_of(clamp_len(p.seq_lens[b], cap, bad)));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
-    int W = 0;
-    const int incl0 = block_incl_scan<kThreads>(loc, scratch, W);
+    long long tot0 = 0;
+    const long long incl0 = block_incl_scan<kThreads, long long>(loc, scratch, tot0);
+    const int W = static_cast<int>(tot0 & 0xFFFFFFFFll), N = static_cast<int>(tot0 >> 32);
     const int G = gridDim.x, g = blockIdx.x;
-    const int t0 = static_cast<int>((static_cast<long long>(g) * W) / G);
-    const int t1 = static_cast<int>((static_cast<long long>(g + 1) * W) / G);
-    int nseg = 0;
-    if (t1 - t0 > kMaxTilesPerCta) {
-      if (tid == 0) atomicOr(p.status, MFA_DEV_SCHEDULE);
-    } else if (p.batch <= kThreads) {
-      // one sequence per thread: its tiles are [incl0 - T, incl0) of the first scan; the
-      // overlapping sequences are numbered by a ballot count
+    const long long C = 4LL * W + 3LL * max(N - 1, 0);
+    const long long X0 = (static_cast<long long>(g) * C) / G, X1 = (static_cast<long long>(g + 1) * C) / G;
+    // sequence with first-tile cost `base` and T tiles: first of its tiles at cost >= X
+    auto first_at = [](long long X, long long base, int T) -> int {
+      return X <= base ? 0 : static_cast<int>(min(static_cast<long long>(T), (X - base + 3) / 4));
+    };
+    // this sequence's contribution to the CTA's [first, end) tiles: the non-empty sequence
+    // whose cost span [base, next base) holds X0 (X1) fixes the first (end) tile.  Those spans
+    // tile [0, C) exactly, so only X = C (X1 of the last CTA) has no owner: it stands for W.
+    auto mark_bounds = [&](long long base, int S, int T) {
+      if (T == 0) return;
+      const long long nxt = base + 4LL * T + 3;
+      if (base <= X0 && X0 < nxt) tb[0] = S + first_at(X0, base, T);
+      if (base <= X1 && X1 < nxt) tb[1] = S + first_at(X1, base, T);
+    };
+    int nseg = 0, t0 = 0, t1 = 0;
+    if (p.batch <= kThreads) {
+      // one sequence per thread: its tiles are [S, S + T) of the first scan; the sequences
+      // overlapping the CTA are numbered by a ballot count
       bool dummy = false;
       const int L = (tid < p.batch) ? clamp_len(L_first, cap, dummy) : 0;
       const int T = tiles_of(L);
-      const int excl = incl0 - T;
-      const bool f = (tid < p.batch) && (max(t0, excl) < min(t1, incl0));
+      const long long ex = incl0 - packed(T);
+      const int S = static_cast<int>(ex & 0xFFFFFFFFll), Nb = static_cast<int>(ex >> 32);
+      const long long base = 4LL * S + 3LL * Nb;
+      if (tid < p.batch) mark_bounds(base, S, T);
+      const int k_lo = first_at(X0, base, T), k_hi = first_at(X1, base, T);
+      const bool f = (tid < p.batch) && (k_lo < k_hi);
       const unsigned m = __ballot_sync(0xffffffffu, f);
-      if (lane == 0) scratch[warp] = __popc(m);
+      if (lane == 0) misc[4 + warp] = __popc(m);
       __syncthreads();
+      t0 = (X0 < C) ? tb[0] : W;
+      t1 = (X1 < C) ? tb[1] : W;
       int before = 0;
 #pragma unroll
       for (int w = 0; w < kThreads / 32; ++w) {
-        const int x = scratch[w];
+        const int x = misc[4 + w];
         before += (w < warp) ? x : 0;
         nseg += x;
       }
-      if (f) {
+      if (t1 - t0 > kMaxTilesPerCta) {
+        if (tid == 0) atomicOr(p.status, MFA_DEV_SCHEDULE);
+        nseg = 0;
+      } else if (f) {
         const int fidx = before + __popc(m & ((1u << lane) - 1u));
-        const int lo = max(t0, excl), hi = min(t1, incl0);
-        seg[fidx] = make_int4(tid, lo - excl, hi - excl, L);
-        seg_n0[fidx] = lo - t0;
+        seg[fidx] = make_int4(tid, k_lo, k_hi, L);
+        seg_n0[fidx] = S + k_lo - t0;
       }
     } else {
-      int carry = 0;
-      for (int c0 = 0; c0 < p.batch && carry < t1; c0 += kThreads) {
+      // pass 1: the CTA's first and end tiles (sequences beyond cost X1 cannot matter)
+      long long carry = 0;
+      auto cost_of = [](long long pk) { return 4LL * (pk & 0xFFFFFFFFll) + 3LL * (pk >> 32); };
+      for (int c0 = 0; c0 < p.batch && cost_of(carry) <= X1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
         const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
         const int T = tiles_of(L);
-        int tot = 0, ftot = 0;
-        const int incl = block_incl_scan<kThreads>(T, scratch, tot) + carry;
-        const int excl = incl - T;
-        const int f = (max(t0, excl) < min(t1, incl)) ? 1 : 0;   // non-empty overlap
-        const int fidx = nseg + block_incl_scan<kThreads>(f, scratch, ftot) - f;
-        if (f) {
-          const int lo = max(t0, excl), hi = min(t1, incl);
-          seg[fidx] = make_int4(b, lo - excl, hi - excl, L);
-          seg_n0[fidx] = lo - t0;
-        }
+        long long tot = 0;
+        const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
+        if (b < p.batch) mark_bounds(cost_of(ex), static_cast<int>(ex & 0xFFFFFFFFll), T);
         carry += tot;
-        nseg += ftot;
+      }
+      __syncthreads();
+      t0 = (X0 < C) ? tb[0] : W;
+      t1 = (X1 < C) ? tb[1] : W;
+      if (t1 - t0 > kMaxTilesPerCta) {
+        if (tid == 0) atomicOr(p.status, MFA_DEV_SCHEDULE);
+      } else {
+        // pass 2: the segments
+        carry = 0;
+        for (int c0 = 0; c0 < p.batch && (carry & 0xFFFFFFFFll) < t1; c0 += kThreads) {
+          const int b = c0 + tid;
+          bool dummy = false;
+          const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
+          const int T = tiles_of(L);
+          long long tot = 0;
+          const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
+          const int S = static_cast<int>(ex & 0xFFFFFFFFll);
+          const long long base = cost_of(ex);
+          const int k_lo = first_at(X0, base, T), k_hi = first_at(X1, base, T);
+          const int f = (b < p.batch && k_lo < k_hi) ? 1 : 0;
+          int ftot = 0;
+          const int fidx = nseg + block_incl_scan<kThreads>(f, misc + 4, ftot) - f;
+          if (f) {
+            seg[fidx] = make_int4(b, k_lo, k_hi, L);
+            seg_n0[fidx] = S + k_lo - t0;
+          }
+          carry += tot;
+          nseg += ftot;
+        }
       }
     }
     if (tid == 0) {
@@ -1262,9 +1315,11 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
 
 // ------------------------------------------------------------------ combine kernel
 
-__device__ __forceinline__ int cta_of_tile(long long t, long long W, long long G) {
-  // largest g with floor(g*W/G) <= t
-  return static_cast<int>(((t + 1) * G + W - 1) / W - 1);
+// Largest g with floor(g C / G) <= c: the CTA owning cost position c (see the decode
+// kernel's cost-balanced split: tile k of sequence b at cost 4 (S_b + k) + 3 N_b, N_b the
+// non-empty sequences before b, C = 4 W + 3 (N - 1)).
+__device__ __forceinline__ int cta_of_cost(long long c, long long C, long long G) {
+  return static_cast<int>(((c + 1) * G + C - 1) / C - 1);
 }
 
 constexpr int kCombineThreads = 256;
@@ -1280,6 +1335,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   grid_dep_wait();
   grid_dep_launch();   // the next kernel may start its own set-up
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
+  __shared__ int red_nb[kCombineThreads / 32], red_nt[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
   __shared__ float wts[4][kCombineMaxParts];
   __shared__ float4 part_acc[3][64];
@@ -1291,34 +1347,44 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int groups = 4 / hpr;                 // quads sharing one head
   const int rounds = hpc / hpr;
   const int cap = p.max_pages * kPage;
-  int before = 0, total = 0;
+  // tiles (and non-empty sequences) before b and in all: the decode kernel's cost positions
+  int before = 0, total = 0, nb = 0, nt = 0;
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
     bool dummy = false;
     const int T = tiles_of(clamp_len(p.seq_lens[i], cap, dummy));
     total += T;
+    nt += (T > 0);
     before += (i < b) ? T : 0;
+    nb += (i < b && T > 0);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     before += __shfl_xor_sync(0xffffffffu, before, o);
     total += __shfl_xor_sync(0xffffffffu, total, o);
+    nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    nt += __shfl_xor_sync(0xffffffffu, nt, o);
   }
   if ((threadIdx.x & 31) == 0) {
     red_b[threadIdx.x >> 5] = before;
     red_t[threadIdx.x >> 5] = total;
+    red_nb[threadIdx.x >> 5] = nb;
+    red_nt[threadIdx.x >> 5] = nt;
   }
   __syncthreads();
-  before = 0;
-  total = 0;
+  before = total = nb = nt = 0;
   for (int w = 0; w < kCombineThreads / 32; ++w) {
     before += red_b[w];
     total += red_t[w];
+    nb += red_nb[w];
+    nt += red_nt[w];
   }
   bool dummy = false;
   const int Tb = tiles_of(clamp_len(p.seq_lens[b], cap, dummy));
   if (Tb == 0) return;
-  const int g0 = cta_of_tile(before, total, p.num_ctas);
-  const int g1 = cta_of_tile(before + Tb - 1, total, p.num_ctas);
+  const long long C = 4LL * total + 3LL * max(nt - 1, 0);
+  const long long base = 4LL * before + 3LL * nb;   // cost of sequence b's first tile
+  const int g0 = cta_of_cost(base, C, p.num_ctas);
+  const int g1 = cta_of_cost(base + 4LL * (Tb - 1), C, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
 
   const int quad = threadIdx.x >> 6;
@@ -1336,8 +1402,15 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
       if (threadIdx.x < 32) {
         int n = 0;
         for (int g = gs + threadIdx.x; g - static_cast<int>(threadIdx.x) < ge; g += 32) {
-          const bool live = g < ge && (static_cast<long long>(g) * total) / p.num_ctas !=
-                                          (static_cast<long long>(g + 1) * total) / p.num_ctas;
+          // CTA g holds a tile of b if a tile cost of b lies in its cost range
+          bool live = false;
+          if (g < ge) {
+            const long long x0 = (static_cast<long long>(g) * C) / p.num_ctas;
+            const long long x1 = (static_cast<long long>(g + 1) * C) / p.num_ctas;
+            const long long k_lo = x0 <= base ? 0 : (x0 - base + 3) / 4;
+            const long long k_hi = x1 <= base ? 0 : (x1 - base + 3) / 4;
+            live = k_lo < min(k_hi, static_cast<long long>(Tb));
+          }
           const unsigned m = __ballot_sync(0xffffffffu, live);
           if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
           n += __popc(m);
@@ -1472,6 +1545,36 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Most tiles any CTA gets under the decode kernel's cost-balanced split (tile k of sequence b
+// at cost 4 (S_b + k) + 3 N_b, N_b the non-empty sequences before b; CTA g owns costs
+// [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1)) for sequences of T[b] tiles:
+// the CTA boundaries walked in order over the non-empty sequences.
+static long long max_cta_tiles(const std::vector<long long>& Tall, long long G) {
+  std::vector<long long> T;
+  for (long long t : Tall)
+    if (t > 0) T.push_back(t);
+  const long long B = static_cast<long long>(T.size());
+  long long W = 0;
+  for (long long t : T) W += t;
+  const long long C = 4 * W + 3 * std::max(B - 1, 0ll);
+  if (C == 0 || G <= 0) return 0;
+  long long b = 0, S = 0;
+  // first tile with cost >= X, for non-decreasing X
+  auto tile_at = [&](long long X) -> long long {
+    if (X >= C) return W;
+    while (b + 1 < B && 4 * (S + T[b]) + 3 * (b + 1) <= X) { S += T[b]; ++b; }
+    const long long base = 4 * S + 3 * b;
+    return S + (X <= base ? 0 : std::min(T[b], (X - base + 3) / 4));
+  };
+  long long prev = tile_at(0), most = 0;
+  for (long long g = 0; g < G; ++g) {
+    const long long t1 = tile_at(((g + 1) * C) / G);
+    most = std::max(most, t1 - prev);
+    prev = t1;
+  }
+  return most;
+}
+
 static mfa_status check_problem(const mfa_problem* pr) {
   if (pr == nullptr) return MFA_ERR_INVALID_ARG;
   if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
@@ -1587,14 +1690,17 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   if (st != MFA_OK) return st;
   if (plan == nullptr || force_ctas < 0) return MFA_ERR_INVALID_ARG;
   const long long cap = static_cast<long long>(pr->max_pages_per_seq) * kPage;
+  std::vector<long long> T(static_cast<size_t>(pr->batch));
   long long W = 0;
   if (host_seq_lens != nullptr) {
     for (int b = 0; b < pr->batch; ++b) {
       if (host_seq_lens[b] < 0 || host_seq_lens[b] > cap) return MFA_ERR_INVALID_ARG;
-      W += (host_seq_lens[b] + kTile - 1) / kTile;
+      T[b] = (host_seq_lens[b] + kTile - 1) / kTile;
+      W += T[b];
     }
   } else {
     if (max_seq_len < 0 || max_seq_len > cap) return MFA_ERR_INVALID_ARG;
+    for (int b = 0; b < pr->batch; ++b) T[b] = (max_seq_len + kTile - 1) / kTile;
     W = static_cast<long long>(pr->batch) * ((max_seq_len + kTile - 1) / kTile);
   }
   if (num_sms <= 0) {
@@ -1610,17 +1716,26 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   } else {
     G = W < num_sms ? W : num_sms;
     if (G < 1) G = 1;
+    G = std::max(G, (W + kMaxTilesPerCta - 1) / kMaxTilesPerCta);   // then the smallest G that fits
   }
-  const long long min_ctas = (W + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
-  if (G < min_ctas) {
+  // planned from a bound, any shorter mix must fit too: a CTA's cost range of at most
+  // ceil(C / G) units holds at most ceil(ceil(C / G) / 4) tiles
+  const long long Cb = 4 * W + 3 * std::max(static_cast<long long>(pr->batch) - 1, 0ll);
+  auto worst = [&](long long g) {
+    const long long exact = max_cta_tiles(T, g);
+    return host_seq_lens != nullptr ? exact : std::max(exact, ((Cb + g - 1) / g + 3) / 4);
+  };
+  long long most = worst(G);
+  while (most > kMaxTilesPerCta) {
     if (force_ctas > 0) return MFA_ERR_INVALID_ARG;
-    G = min_ctas;
+    ++G;
+    most = worst(G);
   }
   if (G > INT_MAX / 2 || static_cast<long long>(pr->batch) + G - 1 > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_ctas = static_cast<int32_t>(G);
   plan->tile_tokens = kTile;
-  plan->max_tiles_per_cta = static_cast<int32_t>((W + G - 1) / G);
+  plan->max_tiles_per_cta = static_cast<int32_t>(most);
   plan->num_partials = static_cast<int32_t>(pr->batch + G - 1);
   plan->batch = pr->batch;
   plan->kv_dtype = pr->kv_dtype;

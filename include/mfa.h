@@ -103,7 +103,7 @@ typedef struct mfa_problem {
 typedef struct mfa_plan {
     int32_t num_ctas;          /* decode grid size G (persistent CTAs) */
     int32_t tile_tokens;       /* tokens per pipeline tile (128) */
-    int32_t max_tiles_per_cta; /* ceil(tiles / G) for the lengths planned with */
+    int32_t max_tiles_per_cta; /* most tiles one CTA gets for the lengths planned with (<= 128) */
     int32_t num_partials;      /* partial-result slots in the workspace: B + G - 1 */
     int32_t batch;             /* copy of problem->batch (checked by run) */
     int32_t kv_dtype;          /* copy of problem->kv_dtype (checked by run) */
@@ -126,10 +126,15 @@ typedef struct mfa_plan {
  *                    tiles); > 0 forces the grid size (tests, tuning).
  *   flags          : MFA_PLAN_* copied into the plan.
  *   plan (out)     : filled on MFA_OK.
- * The work is 128-token tiles; CTA g of G takes tiles [floor(g*W/G), floor((g+1)*W/G))
- * of the batch's W tiles laid end to end, so every CTA gets the same share to
- * within one tile whatever the length mix.  A sequence is split once per CTA
- * boundary that falls inside it.
+ * The work is 128-token tiles laid end to end in sequence order.  Tile k of sequence b
+ * sits at cost 4 (S_b + k) + 3 N_b, with S_b the tiles and N_b the non-empty sequences
+ * before b, and CTA g of G takes the tiles whose cost lies in
+ * [floor(g*C/G), floor((g+1)*C/G)), C = 4 W + 3 (N - 1) for W tiles in N non-empty
+ * sequences: every CTA gets the same share whatever the length mix, a sequence boundary
+ * inside a CTA's range counting as 3/4 of a tile (the next sequence's q and one more
+ * epilogue).  A sequence is split once per CTA boundary that falls inside it.  Planned
+ * from a length bound (host_seq_lens NULL), the grid keeps every CTA within 128 tiles
+ * for any lengths up to the bound.
  */
 mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_lens,
                            int32_t max_seq_len, int32_t num_sms, int32_t force_ctas,

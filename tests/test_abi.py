@@ -48,7 +48,7 @@ def test_plan_one_cta_per_sm_when_enough_tiles(lib):
     plan = mfa.mfa_decode_plan(p, [4096] * 32, num_sms=152)
     assert plan.num_ctas == 152
     assert plan.total_tiles == 32 * 32
-    assert plan.max_tiles_per_cta == 7          # ceil(1024 / 152)
+    assert plan.max_tiles_per_cta == 7          # 1024 tiles and 31 boundaries over 152 CTAs
     assert plan.num_partials == 32 + 152 - 1
     o_off, l_off = mfa.workspace_layout(plan)
     assert plan.workspace_bytes >= l_off + plan.num_partials * 64 * 4
@@ -70,9 +70,22 @@ def test_plan_without_host_lengths_uses_the_bound(lib):
 def test_plan_caps_tiles_per_cta(lib):
     p = problem(batch=4, max_pages_per_seq=2048, num_blocks=8192)
     plan = mfa.mfa_decode_plan(p, [131072] * 4, num_sms=2)
-    assert plan.max_tiles_per_cta <= 128 and plan.num_ctas == 32
+    # 4096 tiles: 32 CTAs would be the floor, but the sequence boundaries' cost leaves one of
+    # them 129 tiles, so the plan takes the smallest count that fits
+    assert plan.max_tiles_per_cta <= 128 and plan.num_ctas == 33
     with pytest.raises(mfa.MfaError):
         mfa.mfa_decode_plan(p, [131072] * 4, num_sms=2, force_ctas=2)
+
+
+def test_plan_from_a_bound_fits_any_shorter_lengths(lib):
+    # planned for B sequences of at most max_seq_len tokens, the grid must keep every CTA
+    # within 128 tiles whatever the actual mix: its cost range of ceil(C / G) units holds
+    # at most ceil(ceil(C / G) / 4) tiles, C = 4 W + 3 (B - 1)
+    p = problem(batch=4, max_pages_per_seq=2048, num_blocks=8192)
+    plan = mfa.mfa_decode_plan(p, None, max_seq_len=131072, num_sms=2)
+    C = 4 * 4096 + 3 * 3
+    G = plan.num_ctas
+    assert (-(-C // G) + 3) // 4 <= 128 and (-(-C // (G - 1)) + 3) // 4 > 128
 
 
 def test_plan_rejects_bad_input(lib):

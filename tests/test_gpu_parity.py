@@ -173,13 +173,18 @@ def test_combine_kernel_against_oracle_merge():
     assert prob.out_dtype == mfa.MFA_OUT_BF16
     mfa.mfa_combine(plan, prob, ws, seq, out, lse)
     torch.cuda.synchronize()
+    # the documented split: tile k of sequence b at cost 4 (S_b + k) + 3 N_b; CTA g owns
+    # costs [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1)
     tiles = [(L + 127) // 128 for L in lens]
-    W = sum(tiles)
-    start = lambda gg: (gg * W) // G
-    before = 0
+    W, N = sum(tiles), sum(1 for t in tiles if t > 0)
+    C = 4 * W + 3 * max(N - 1, 0)
+    before = nonempty = 0
     for b in range(B):
-        covering = [gg for gg in range(G) if max(start(gg), before) < min(start(gg + 1), before + tiles[b])]
+        base = 4 * before + 3 * nonempty
+        costs = [base + 4 * k for k in range(tiles[b])]
+        covering = sorted({max(gg for gg in range(G) if (gg * C) // G <= c) for c in costs})
         before += tiles[b]
+        nonempty += tiles[b] > 0
         if len(covering) < 2:
             continue   # written by the decode kernel, not by combine
         slots = [b + gg for gg in covering]
@@ -233,6 +238,19 @@ def test_runs_on_a_side_stream():
     with torch.cuda.stream(s):
         out, lse, _ = gpu_decode(case, stream=s)
     check_parity(case, out, lse)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("force_ctas", [1, 2, 5, 9, 13, 14, 15, 17])
+def test_cost_balanced_split_with_empty_runs(kv_dtype, force_ctas):
+    # 13 tiles over sequences with runs of empties: CTA ranges fall on sequence boundaries,
+    # inside boundary costs and (beyond 13 CTAs) on nothing at all; decode and combine must
+    # agree on which CTA holds which tiles
+    lens = [0, 0, 129, 0, 1, 256, 0, 0, 700, 64, 0, 65, 0]
+    case = inputs.small("cost", len(lens), lens, kv_dtype=kv_dtype, seed=79)
+    out, lse, dec = gpu_decode(case, force_ctas=force_ctas)
+    limits = dict(max_abs=3e-2, rel_l2=1.5e-2) if kv_dtype != "bf16" else {}
+    check_parity(case, out, lse, **limits)
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
