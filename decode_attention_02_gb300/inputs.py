@@ -23,6 +23,10 @@ Storage: bf16 by round-to-nearest-even, or FP8 e4m3 with one fp32 scale per
 token row (absmax/448, 1 for an all-zero row), codes = e4m3(RNE(x/scale))
 after clamping to +-448.  Unused page slots and unused physical pages are
 filled with NaN when ``poison`` is set, so any read of them shows up.
+
+KV append inputs (``append_step``): the case is drawn for the lengths after the step, and
+each sequence's new bf16 key and value rows (``new_token_rows``, eight row kinds from N(0,1)
+to all-zero, signed-zero, wide-range, huge and tiny rows) go to its last position.
 """
 from __future__ import annotations
 
@@ -231,3 +235,72 @@ def small(name: str, batch: int, lens: Sequence[int], kv_dtype: str = "bf16", se
                  k_spike_frac=k_spike_frac, softmax_scale=softmax_scale,
                  num_q_heads=num_q_heads, head_dim=head_dim, page_size=page_size)
     return generate(w)
+
+
+# ------------------------------------------------------------------ new-token rows (KV append)
+
+# Row kinds of new_token_rows, by row index modulo len(ROW_KINDS) (row 0 is "normal").
+ROW_KINDS = ("normal", "zero", "signed_zero", "wide_range", "one_spike", "huge", "tiny", "spiky")
+
+
+@dataclasses.dataclass
+class AppendStep:
+    """One decode step's new key/value rows and where they go."""
+    k_new: torch.Tensor        # bf16 [B, d]
+    v_new: torch.Tensor        # bf16 [B, d]
+    positions: torch.Tensor    # int32 [B]: token index of the new row, -1 = no new token
+
+
+def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0) -> torch.Tensor:
+    """Seeded bf16 [batch, d] rows covering the structures an FP8 row quantiser meets.
+
+    Row r has kind ROW_KINDS[r % 8]: N(0,1) ("normal"); all +0 ("zero"); a mix of +0
+    and -0 ("signed_zero"); N(0,1) times 2^U[-20, 20] per element ("wide_range", many
+    codes in the e4m3 subnormal range); N(0,1) * 1e-3 with one element 1e3 ("one_spike");
+    N(0,1) * 1e30 ("huge"); N(0,1) * 1e-30 ("tiny"); N(0,1) with 1% of elements * 20
+    ("spiky").  Values are drawn in fp32 and rounded to bf16 (nearest even).
+    """
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((batch, d), dtype=np.float32)
+    e = rng.integers(-20, 21, size=(batch, d))
+    spike = rng.random((batch, d), dtype=np.float32) < np.float32(0.01)
+    sign = rng.random((batch, d)) < 0.5
+    where = rng.integers(0, d, size=batch)
+    for r in range(batch):
+        kind = ROW_KINDS[r % len(ROW_KINDS)]
+        if kind == "zero":
+            x[r] = 0.0
+        elif kind == "signed_zero":
+            x[r] = np.where(sign[r], np.float32(-0.0), np.float32(0.0))
+        elif kind == "wide_range":
+            x[r] = x[r] * np.exp2(e[r]).astype(np.float32)
+        elif kind == "one_spike":
+            x[r] *= np.float32(1e-3)
+            x[r, where[r]] = np.float32(1e3)
+        elif kind == "huge":
+            x[r] *= np.float32(1e30)
+        elif kind == "tiny":
+            x[r] *= np.float32(1e-30)
+        elif kind == "spiky":
+            x[r, spike[r]] *= np.float32(20.0)
+    return _to_bf16(x).contiguous()
+
+
+def append_step(case: Case, seed: int = 0, inactive_every: int = 0) -> AppendStep:
+    """New rows for every sequence of ``case``, written at position seq_lens[b] - 1.
+
+    Build ``case`` for the lengths after the append (each sequence one token longer), so
+    its block table already holds the page of the new token, as a serving system
+    allocates it before the step; the slot's old contents are then overwritten.  With
+    inactive_every = n > 0, every n-th sequence (b % n == n - 1) has no new token
+    (position -1).  k rows use ``seed``, v rows ``seed + 1``.
+    """
+    B = case.q.shape[0]
+    d = case.q.shape[2]
+    pos = case.seq_lens.to(torch.int64) - 1
+    if inactive_every > 0:
+        idx = torch.arange(B)
+        pos[idx % inactive_every == inactive_every - 1] = -1
+    pos[case.seq_lens <= 0] = -1
+    return AppendStep(k_new=new_token_rows(B, d, seed), v_new=new_token_rows(B, d, seed + 1),
+                      positions=pos.to(torch.int32).contiguous())

@@ -12,7 +12,11 @@ Pins (tests/test_oracle.py): torch SDPA in float64 on a dense gather done by
 numpy indexing, scipy logsumexp for lse, the two-token logistic closed form,
 L=1 -> v_0, constant K -> mean of V, key-shift and block-permutation
 invariance, convex hull, split/merge identity, and every e4m3 code against
-torch.float8_e4m3fn.
+torch.float8_e4m3fn.  The KV append (tests/test_oracle_append.py): the e4m3
+encoder against torch.float8_e4m3fn on every fp32 value it can decide
+differently (codes, midpoints, their neighbours), round trips of every code,
+saturation, signed zeros; the append against the dequantisation error bound,
+the row maximum landing on code 448, and untouched slots left unchanged.
 """
 from __future__ import annotations
 
@@ -53,6 +57,12 @@ def load_library(path: str):
     lib.mfa_oracle_e4m3_to_double.restype = ctypes.c_double
     lib.mfa_oracle_num_cpus.argtypes = []
     lib.mfa_oracle_num_cpus.restype = I
+    lib.mfa_oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+    lib.mfa_oracle_e4m3_from_float.restype = ctypes.c_uint8
+    lib.mfa_oracle_e4m3_from_float_array.argtypes = [P, ctypes.c_long, P]
+    lib.mfa_oracle_e4m3_from_float_array.restype = None
+    lib.mfa_oracle_kv_append.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+    lib.mfa_oracle_kv_append.restype = I
     return lib
 
 
@@ -70,6 +80,52 @@ def num_cpus() -> int:
 
 def e4m3_to_double(code: int, lib=None) -> float:
     return float((lib or _load()).mfa_oracle_e4m3_to_double(int(code) & 0xFF))
+
+
+def e4m3_from_float(y: float, lib=None) -> int:
+    """Nearest e4m3 code to the fp32 value y (ties to the even code, |y| >= 448 -> 448)."""
+    return int((lib or _load()).mfa_oracle_e4m3_from_float(float(y)))
+
+
+def e4m3_from_float_array(y, lib=None) -> np.ndarray:
+    """e4m3_from_float over an fp32 array; returns uint8 codes of the same shape."""
+    a = np.ascontiguousarray(np.asarray(y, dtype=np.float32))
+    out = np.zeros(a.shape, dtype=np.uint8)
+    (lib or _load()).mfa_oracle_e4m3_from_float_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+APPEND_BAD_BLOCK = 1      # return-mask bits of kv_append
+APPEND_BAD_POSITION = 2
+
+
+def kv_append(k_new, v_new, positions, block_table, k_cache, v_cache, k_scale=None, v_scale=None,
+              page_size: int = 64, lib=None):
+    """Oracle KV append: returns (k_cache, v_cache, k_scale, v_scale, mask), updated copies.
+
+    k_new/v_new: bf16 [B, d] (torch) or uint16 bit arrays; positions: int [B], the token
+    index each sequence's new row goes to (< 0: none); block_table int32 [B, max_pages];
+    caches as produced by the input generator (bf16 [nb, page, d], or uint8 e4m3 codes with
+    fp32 scales [nb, page]).  The inputs are not modified.
+    """
+    kn = np.ascontiguousarray(_np(k_new)).view(np.uint16)
+    vn = np.ascontiguousarray(_np(v_new)).view(np.uint16)
+    B, d = kn.shape
+    pos = np.ascontiguousarray(np.asarray(_np(positions), dtype=np.int32))
+    table = np.ascontiguousarray(_np(block_table).astype(np.int32))
+    kc = np.array(_np(k_cache), copy=True)
+    vc = np.array(_np(v_cache), copy=True)
+    fp8 = kc.dtype == np.uint8
+    ks = vs = None
+    if fp8:
+        ks = np.array(_np(k_scale), dtype=np.float32, copy=True)
+        vs = np.array(_np(v_scale), dtype=np.float32, copy=True)
+    mask = (lib or _load()).mfa_oracle_kv_append(
+        B, d, page_size, table.shape[1], kc.shape[0], 1 if fp8 else 0, _ptr(kn), _ptr(vn), _ptr(pos),
+        _ptr(table), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs))
+    if mask < 0:
+        raise ValueError("mfa_oracle_kv_append: bad argument")
+    return kc, vc, ks, vs, int(mask)
 
 
 def _np(t):

@@ -34,6 +34,9 @@
  *
  * Threads split independent (sequence, group of heads) units; each head's
  * arithmetic runs in the order written above.
+ *
+ * mfa_oracle_kv_append() (end of file) writes a decode step's new key and value rows into
+ * the paged cache, quantising them to e4m3 with per-row scales for an FP8 cache.
  */
 #include <math.h>
 #include <pthread.h>
@@ -275,4 +278,105 @@ int mfa_oracle_combine(int S, long R, int d, const double *part_o, const double 
         lse[r] = L;
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------------------------
+ * KV-cache append with FP8 quantisation (the step before attention in a decode step: the
+ * attention instances own and fill their KV caches, Step-3 page section 7 "Implementation
+ * and Results"; the cache holds 8-bit KV, section 5 "Model-System Co-design").
+ *
+ * For every sequence b with positions[b] = t >= 0, the new token's key row k_new[b][:] and
+ * value row v_new[b][:] (bf16) go to slot t % page of page block_table[b][t / page]:
+ *   - bf16 cache: the bf16 bits unchanged;
+ *   - e4m3 cache: one fp32 scale per row, s = absmax / 448 (s = 1 for an all-zero row), and
+ *     codes e4m3(x_i / s), x_i the row's bf16 values; both divisions are fp32 divisions
+ *     rounded to nearest, and the e4m3 rounding is to the nearest value, ties to the even
+ *     code, with magnitudes above 448 saturating to 448.
+ * positions[b] < 0: no token for b (nothing written).  t >= max_pages * page, or a page id
+ * outside [0, num_blocks): nothing written for b, and bit 1 (position) or bit 0 (page id)
+ * of the return mask is set.
+ */
+
+static float bf16_to_float(uint16_t bits) {
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return f;
+}
+
+/* Nearest e4m3 value to y, found by trying every non-negative finite code (0x00..0x7E,
+ * whose values increase with the code); of two equally near codes the even one wins.
+ * |y| >= 448 gives 448.  The sign bit of y is kept, so a negative y that rounds to zero
+ * gives 0x80.  y must not be NaN. */
+uint8_t mfa_oracle_e4m3_from_float(float y) {
+    const int neg = signbit(y) != 0;
+    const double a = fabs((double)y);
+    int best = 0x7E;
+    if (a < 448.0) {
+        double bd = a;   /* distance to code 0 (value 0) */
+        best = 0;
+        for (int c = 1; c <= 0x7E; ++c) {
+            const double dist = fabs(mfa_oracle_e4m3_to_double((uint8_t)c) - a);
+            if (dist < bd || (dist == bd && (c & 1) == 0)) {
+                best = c;
+                bd = dist;
+            }
+        }
+    }
+    return (uint8_t)(neg ? (0x80 | best) : best);
+}
+
+/* mfa_oracle_e4m3_from_float over an array (for the encoder's pins). */
+void mfa_oracle_e4m3_from_float_array(const float *y, long n, uint8_t *codes) {
+    for (long i = 0; i < n; ++i) codes[i] = mfa_oracle_e4m3_from_float(y[i]);
+}
+
+static void quantise_row(const uint16_t *x, int d, uint8_t *codes, float *scale) {
+    float absmax = 0.0f;
+    for (int i = 0; i < d; ++i) {
+        const float a = fabsf(bf16_to_float(x[i]));
+        if (a > absmax) absmax = a;
+    }
+    const float s = (absmax > 0.0f) ? absmax / 448.0f : 1.0f;
+    for (int i = 0; i < d; ++i) codes[i] = mfa_oracle_e4m3_from_float(bf16_to_float(x[i]) / s);
+    *scale = s;
+}
+
+/*
+ * k_new/v_new: bf16 bits [B,d]; positions: int32 [B]; block_table: int32 [B,max_pages];
+ * k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,d], updated in place;
+ * k_scale/v_scale: fp32 [num_blocks,page] (FP8 only), updated in place.
+ * Returns the error mask described above (0 = every row written or skipped by choice),
+ * or -1 on a bad argument.
+ */
+int mfa_oracle_kv_append(int B, int d, int page, int max_pages, int num_blocks, int kv_fp8,
+                         const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
+                         const int32_t *block_table, void *k_cache, void *v_cache,
+                         float *k_scale, float *v_scale) {
+    if (B < 0 || d <= 0 || page <= 0 || max_pages <= 0 || num_blocks <= 0) return -1;
+    if (!k_new || !v_new || !positions || !block_table || !k_cache || !v_cache) return -1;
+    if (kv_fp8 && (!k_scale || !v_scale)) return -1;
+    int mask = 0;
+    for (int b = 0; b < B; ++b) {
+        const int t = positions[b];
+        if (t < 0) continue;
+        if (t >= max_pages * page) {
+            mask |= 2;
+            continue;
+        }
+        const int blk = block_table[(size_t)b * max_pages + t / page];
+        if (blk < 0 || blk >= num_blocks) {
+            mask |= 1;
+            continue;
+        }
+        const size_t row = (size_t)blk * page + (size_t)(t % page);
+        if (kv_fp8) {
+            quantise_row(k_new + (size_t)b * d, d, (uint8_t *)k_cache + row * d, k_scale + row);
+            quantise_row(v_new + (size_t)b * d, d, (uint8_t *)v_cache + row * d, v_scale + row);
+        } else {
+            memcpy((uint16_t *)k_cache + row * d, k_new + (size_t)b * d, (size_t)d * sizeof(uint16_t));
+            memcpy((uint16_t *)v_cache + row * d, v_new + (size_t)b * d, (size_t)d * sizeof(uint16_t));
+        }
+    }
+    return mask;
 }
