@@ -48,7 +48,7 @@ PAGE_SIZE = 64
 # Every symbol include/mfa.h declares.
 EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
                     "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error",
-                    "mfa_decode_run_static_workspace")
+                    "mfa_decode_run_static_workspace", "mfa_kv_append")
 
 # Size of the library's own scratch array used by mfa_decode_run_static_workspace.
 MFA_STATIC_WORKSPACE_BYTES = 24 * 1024 * 1024
@@ -111,6 +111,8 @@ def load_library(path: str = LIB_PATH):
     lib.mfa_decode_run_static_workspace.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P,
                                                     P, P, P, P, P, P, P]
     lib.mfa_decode_run_static_workspace.restype = ctypes.c_int
+    lib.mfa_kv_append.argtypes = [ctypes.POINTER(MfaProblem), P, P, P, P, P, P, P, P, P, P]
+    lib.mfa_kv_append.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -207,6 +209,21 @@ def mfa_combine(plan: MfaPlan, problem: MfaProblem, workspace, seq_lens, out, ls
     st = lib.mfa_combine(ctypes.byref(plan), ctypes.byref(problem), _ptr(workspace), int(workspace_bytes),
                          _ptr(seq_lens), _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "mfa_combine")
+
+
+def mfa_kv_append(problem: MfaProblem, k_new, v_new, positions, block_table, k_cache, v_cache, k_scale=None,
+                  v_scale=None, device_status=None, stream=None) -> None:
+    """Write each sequence's new key/value row into the paged cache (FP8: quantised).
+
+    k_new/v_new: bf16 [B, 256]; positions: int32 [B] (token index, < 0 = none);
+    device_status: a uint32 device tensor (or a decode workspace, whose first word is
+    the status word) that collects bad-position / bad-page bits, or None.
+    """
+    lib = load_library()
+    st = lib.mfa_kv_append(ctypes.byref(problem), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(block_table),
+                           _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(device_status),
+                           _stream(stream))
+    _check(st, "mfa_kv_append")
 
 
 def mfa_read_device_status(workspace, clear: bool = True, stream=None) -> int:

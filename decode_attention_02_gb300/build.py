@@ -9,7 +9,7 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 LIB = os.path.join(PKG, "libmfa.so")
-SOURCES = [os.path.join(PKG, "csrc", "mfa_decode.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "mfa_decode.cu"), os.path.join(PKG, "csrc", "mfa_kv_append.cu")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -21,7 +21,8 @@ def _nvcc() -> str:
 
 
 def _inputs():
-    return SOURCES + glob.glob(os.path.join(PKG, "csrc", "*.cuh")) + [os.path.join(ROOT, "include", "mfa.h")]
+    return (SOURCES + glob.glob(os.path.join(PKG, "csrc", "*.cuh")) + glob.glob(os.path.join(PKG, "csrc", "*.h")) +
+            [os.path.join(ROOT, "include", "mfa.h")])
 
 
 def needs_build() -> bool:

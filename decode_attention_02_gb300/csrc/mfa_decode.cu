@@ -8,10 +8,11 @@
 // KV-memory access.  At 64 FLOP/B (bf16 KV) the step is HBM-bound on GB300, so the
 // design streams each KV byte exactly once per step:
 //
-//  * One CTA per SM (persistent).  CTA g owns tiles [floor(gW/G), floor((g+1)W/G))
-//    of the batch's W 128-token tiles laid end to end, so the load is even for any
-//    length mix; a sequence cut by a CTA boundary yields partial results that the
-//    combine kernel merges (split-KV with a log-sum-exp merge).
+//  * One CTA per SM (persistent).  The batch's 128-token tiles are laid end to end
+//    and CTA g owns an equal share of their cost, a sequence boundary counting as 3/4
+//    of a tile, so the load is even for any length mix; a sequence cut by a CTA
+//    boundary yields partial results that the combine kernel merges (split-KV with a
+//    log-sum-exp merge).
 //  * Each CTA holds all 64 heads of its sequence, so K and V are read once.
 //  * Warp 0 streams K/V pages with TMA (3-D tensor maps over the page pool; the
 //    block table supplies the page coordinate) into a ring of shared-memory slots,
@@ -48,6 +49,7 @@
 #include <algorithm>
 
 #include "mfa.h"
+#include "mfa_host.h"
 #include "ptx.cuh"
 
 namespace mfa {
@@ -1510,7 +1512,7 @@ constexpr uint64_t kWsHeader = 256;
 // Text of the last CUDA failure seen by this host thread (static strings only).
 static thread_local const char* g_last_error = "no error";
 
-static mfa_status cuda_fail(cudaError_t e, const char* where) {
+mfa_status cuda_fail(cudaError_t e, const char* where) {
   (void)where;
   g_last_error = cudaGetErrorString(e);
   return MFA_ERR_CUDA;
@@ -1543,7 +1545,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Most tiles any CTA gets under the decode kernel's cost-balanced split (tile k of sequence b
 // at cost 4 (S_b + k) + 3 N_b, N_b the non-empty sequences before b; CTA g owns costs
@@ -1575,7 +1577,7 @@ static long long max_cta_tiles(const std::vector<long long>& Tall, long long G) 
   return most;
 }
 
-static mfa_status check_problem(const mfa_problem* pr) {
+mfa_status check_problem(const mfa_problem* pr) {
   if (pr == nullptr) return MFA_ERR_INVALID_ARG;
   if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
   if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;

@@ -251,10 +251,10 @@ class AppendStep:
     positions: torch.Tensor    # int32 [B]: token index of the new row, -1 = no new token
 
 
-def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0) -> torch.Tensor:
+def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0, kinds: Sequence[str] = ROW_KINDS) -> torch.Tensor:
     """Seeded bf16 [batch, d] rows covering the structures an FP8 row quantiser meets.
 
-    Row r has kind ROW_KINDS[r % 8]: N(0,1) ("normal"); all +0 ("zero"); a mix of +0
+    Row r has kind kinds[r % len(kinds)], by default ROW_KINDS[r % 8]: N(0,1) ("normal"); all +0 ("zero"); a mix of +0
     and -0 ("signed_zero"); N(0,1) times 2^U[-20, 20] per element ("wide_range", many
     codes in the e4m3 subnormal range); N(0,1) * 1e-3 with one element 1e3 ("one_spike");
     N(0,1) * 1e30 ("huge"); N(0,1) * 1e-30 ("tiny"); N(0,1) with 1% of elements * 20
@@ -267,7 +267,7 @@ def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0) -> torch.Tensor
     sign = rng.random((batch, d)) < 0.5
     where = rng.integers(0, d, size=batch)
     for r in range(batch):
-        kind = ROW_KINDS[r % len(ROW_KINDS)]
+        kind = kinds[r % len(kinds)]
         if kind == "zero":
             x[r] = 0.0
         elif kind == "signed_zero":
@@ -286,14 +286,16 @@ def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0) -> torch.Tensor
     return _to_bf16(x).contiguous()
 
 
-def append_step(case: Case, seed: int = 0, inactive_every: int = 0) -> AppendStep:
+def append_step(case: Case, seed: int = 0, inactive_every: int = 0,
+                kinds: Sequence[str] = ROW_KINDS) -> AppendStep:
     """New rows for every sequence of ``case``, written at position seq_lens[b] - 1.
 
     Build ``case`` for the lengths after the append (each sequence one token longer), so
     its block table already holds the page of the new token, as a serving system
     allocates it before the step; the slot's old contents are then overwritten.  With
     inactive_every = n > 0, every n-th sequence (b % n == n - 1) has no new token
-    (position -1).  k rows use ``seed``, v rows ``seed + 1``.
+    (position -1).  k rows use ``seed``, v rows ``seed + 1``; ``kinds`` as for
+    new_token_rows (("normal",) for rows inside the FP8 decode's V-scale range).
     """
     B = case.q.shape[0]
     d = case.q.shape[2]
@@ -302,5 +304,5 @@ def append_step(case: Case, seed: int = 0, inactive_every: int = 0) -> AppendSte
         idx = torch.arange(B)
         pos[idx % inactive_every == inactive_every - 1] = -1
     pos[case.seq_lens <= 0] = -1
-    return AppendStep(k_new=new_token_rows(B, d, seed), v_new=new_token_rows(B, d, seed + 1),
+    return AppendStep(k_new=new_token_rows(B, d, seed, kinds), v_new=new_token_rows(B, d, seed + 1, kinds),
                       positions=pos.to(torch.int32).contiguous())

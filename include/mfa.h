@@ -227,6 +227,46 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
                                            const int32_t* block_table, const int32_t* seq_lens,
                                            void* out, float* lse, void* stream);
 
+/*
+ * Enqueue the KV-cache append of one decode step: each sequence's new key row and
+ * value row go into the paged cache (the attention instances own and fill their KV
+ * caches, Step-3 page section 7 "Implementation and Results"; the cache holds 8-bit
+ * KV, section 5 "Model-System Co-design").  For every b with t = positions[b] >= 0,
+ * row k_new[b] goes to K slot t % 64 of page block_table[b][t / 64], v_new[b] to the
+ * same V slot:
+ *   - bf16 cache: the bf16 bits, unchanged;
+ *   - e4m3 cache (quantisation fused in the same pass): the row's scale
+ *     s = absmax / 448 in fp32 (s = 1 for an all-zero row) goes to
+ *     k_scale/v_scale[page][slot], and each value x to the e4m3 code of x / s
+ *     (both divisions fp32, rounded to nearest; the code rounded to nearest even,
+ *     magnitudes above 448 saturated to 448; a negative x that rounds to zero gives
+ *     the code 0x80).  The row maximum always lands on code +-448.
+ *   problem      : the decode's problem description (kv_dtype, batch, table width and
+ *                  pool size are used); validated as for mfa_decode_plan.
+ *   k_new, v_new : device bf16 [B, 256], 16-byte aligned, finite values (non-finite
+ *                  values give unspecified codes and scales).
+ *   positions    : device int32 [B]: the token index each sequence's new row takes
+ *                  (usually its length before the step); a negative entry means no
+ *                  new token for that sequence (nothing is written).
+ *   block_table  : device int32 [B, max_pages_per_seq]: must already hold the page of
+ *                  position t (allocate it before the step).
+ *   k_cache, v_cache, k_scale, v_scale : the pools of mfa_decode_run, written in place;
+ *                  only the target slots change.  Scales NULL for a bf16 cache.
+ *   device_status: device uint32, or NULL.  A position >= max_pages_per_seq * 64 sets
+ *                  MFA_DEV_BAD_LENGTH, a page id outside [0, num_blocks) sets
+ *                  MFA_DEV_BAD_BLOCK; that sequence's rows are then not written.  The
+ *                  status word of a decode workspace (offset 0) may be passed, so that
+ *                  mfa_read_device_status() reports both steps.
+ *   stream       : cudaStream_t.  The kernel is launched as a programmatic dependent
+ *                  of the preceding kernel and lets the next kernel start early; a
+ *                  decode kernel launched next reads the cache only after the append
+ *                  has completed.
+ */
+mfa_status mfa_kv_append(const mfa_problem* problem, const void* k_new, const void* v_new,
+                         const int32_t* positions, const int32_t* block_table,
+                         void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                         uint32_t* device_status, void* stream);
+
 /* MFA_ABI_VERSION of the loaded library. */
 int32_t mfa_abi_version(void);
 

@@ -126,3 +126,30 @@ def test_run_validates_before_touching_the_device(lib):
     assert _run_raw(lib, plan, prob, good, plan.workspace_bytes - 1) == mfa.MFA_ERR_WORKSPACE
     other = problem(batch=5)
     assert _run_raw(lib, plan, other, good, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+
+
+def _append_raw(lib, prob, ptrs):
+    # k_new, v_new, positions, table, k_cache, v_cache, k_scale, v_scale, status
+    return lib.mfa_kv_append(ctypes.byref(prob), *ptrs, None)
+
+
+def test_kv_append_validates_before_touching_the_device(lib):
+    bf = problem()
+    f8 = problem(kv_dtype=mfa.MFA_KV_FP8_E4M3)
+    good = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000, 0x7000, 0x8000, 0x9000]
+    for i in range(6):                       # every array but the scales and the status word
+        bad = list(good); bad[i] = None
+        assert _append_raw(lib, bf, bad) == mfa.MFA_ERR_INVALID_ARG
+    for i, off in ((0, 8), (1, 8), (2, 2), (3, 2), (4, 8), (5, 8)):
+        bad = list(good); bad[i] += off
+        assert _append_raw(lib, bf, bad) == mfa.MFA_ERR_INVALID_ARG
+    no_scale = list(good); no_scale[6] = None
+    assert _append_raw(lib, f8, no_scale) == mfa.MFA_ERR_INVALID_ARG
+    odd_status = list(good); odd_status[8] = 0x9002
+    assert _append_raw(lib, f8, odd_status) == mfa.MFA_ERR_INVALID_ARG
+    assert _append_raw(lib, problem(head_dim=128), good) == mfa.MFA_ERR_UNSUPPORTED
+    assert _append_raw(lib, problem(batch=-1), good) == mfa.MFA_ERR_INVALID_ARG
+
+
+def test_kv_append_of_an_empty_batch_enqueues_nothing(lib):
+    assert _append_raw(lib, problem(batch=0), [None] * 9) == mfa.MFA_OK
