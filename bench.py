@@ -15,6 +15,9 @@ e2e        : the same metric through the public Python API with the per-step
 roofline   : the decode kernel alone, algorithmic bytes per launch / its mean
              CUDA-event duration, against the measured HBM copy bandwidth.
 cpu_baseline: the fp64 CPU oracle on a bounded sample of the same workload.
+kv_append  : the KV-cache append kernel for the same batch (each sequence's new key
+             and value row, FP8-quantised for an e4m3 cache), alone, and the decode
+             step with the append chained in front of it.
 
 --impl reference times the oracle itself (the reference arm) on the same
 workload, each step a bounded sample.
@@ -57,6 +60,13 @@ def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int 
     kv = tokens * kv_bytes_per_token(kv_dtype)
     other = B * (H * d * 2) * 2 + pages * 4 + B * 4 + B * H * 4
     return {"kv": kv, "total": kv + other}
+
+
+def append_bytes(batch: int, kv_dtype: str, d: int = 256) -> int:
+    """Algorithmic bytes of one KV append: per sequence the new bf16 K and V rows, its
+    position and page id in, and the stored rows out (bf16, or e4m3 codes + fp32 scale)."""
+    out_row = 2 * d if kv_dtype == "bf16" else d + 4
+    return batch * (2 * 2 * d + 4 + 4 + 2 * out_row)
 
 
 def algorithmic_flops(lens, H: int = 64, d: int = 256) -> int:
@@ -273,7 +283,7 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
 def run_native(args, case, rank: int, world: int):
     import torch
     import decode_attention_02_gb300 as mfa
-    from decode_attention_02_gb300 import build
+    from decode_attention_02_gb300 import build, inputs
 
     build.build_library()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
@@ -418,6 +428,46 @@ def run_native(args, case, rank: int, world: int):
     windows.append((t_start, time.time()))
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
 
+    # --- the KV append of the same batch (each sequence's new row at its last position),
+    #     alone (per-launch events behind a GPU sleep) and chained in front of the decode
+    #     step (append -> decode -> combine, K steps from one CUDA graph)
+    k_new = inputs.new_token_rows(B, seed=w.seed + 101, kinds=("normal",)).to(dev)
+    v_new = inputs.new_token_rows(B, seed=w.seed + 102, kinds=("normal",)).to(dev)
+    positions = (case.seq_lens.to(torch.int32) - 1).to(dev)
+
+    def append(i):
+        s = sets[i % nsets]
+        mfa.mfa_kv_append(dec.problem, k_new, v_new, positions, s["table"], s["k"], s["v"], s["ks"], s["vs"],
+                          device_status=dec.workspace)
+
+    for i in range(3):
+        append(i)
+    barrier()
+    aevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+    t_start = time.time()
+    torch.cuda._sleep(int(2e7))
+    for i in range(nk):
+        aevs[i][0].record(stream)
+        append(i)
+        aevs[i][1].record(stream)
+    barrier()
+    windows.append((t_start, time.time()))
+    app_mean_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in aevs) / nk, dist, dev)
+    graph3 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph3):
+        for i in range(args.steps):
+            append(i)
+            step(i)
+    graph3.replay()
+    barrier()
+    e0.record(stream)
+    graph3.replay()
+    e1.record(stream)
+    barrier()
+    ms_step_append = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    app_status = mfa.mfa_read_device_status(dec.workspace)
+    app_bytes = append_bytes(B, w.kv_dtype)
+
     # keep sampling clocks until the windows hold enough samples
     clocks = sampler.summary(windows)
     if clocks["samples"] < 5:
@@ -460,6 +510,15 @@ def run_native(args, case, rank: int, world: int):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "device_status": status,
+        "kv_append": {"kernel": "mfa_kv_append_kernel", "mean_launch_ms": app_mean_ms,
+                      "algorithmic_bytes_per_launch": app_bytes,
+                      "achieved_gbs": app_bytes / (app_mean_ms * 1e-3) / 1e9,
+                      "frac_of_hbm": app_bytes / (app_mean_ms * 1e-3) / 1e9 / hbm_peak,
+                      "bound": "latency: one dependent load chain (position, page id, row) per row",
+                      "ms_per_step_with_append": ms_step_append,
+                      "timing": "append alone: per-launch events behind a GPU sleep; with append: "
+                                "K steps of append + decode + combine from one CUDA graph",
+                      "device_status": app_status},
     }
     return result
 

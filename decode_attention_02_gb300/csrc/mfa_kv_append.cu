@@ -8,7 +8,8 @@
 //
 // The work is 2B independent rows of 256 values (512 bytes of bf16 in; 512 bytes of bf16
 // or 260 bytes of codes and scale out), so it is a latency-bound scatter: one warp per
-// row, one 16-byte load and one 16- or 8-byte store per lane, a warp max for the scale.
+// row, one 16-byte load and one 16- or 8-byte store per lane, a warp max for the scale;
+// the row's load is issued before the dependent position and page-id loads.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -62,6 +63,9 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mfa_kv_append_kernel(const 
   if (r >= 2 * p.batch) return;
   const int b = r >> 1;
   const bool is_v = (r & 1) != 0;
+  // lane l holds elements 8l .. 8l+7 of the row; the load is issued first, so that it
+  // overlaps the position -> page id chain
+  const uint4 x = __ldg((is_v ? p.v_new : p.k_new) + static_cast<size_t>(b) * (kAppendRowLen / 8) + lane);
   const int t = p.positions[b];
   if (t < 0) return;                                    // no new token for this sequence
   if (t >= p.max_pages * kAppendPage) {
@@ -74,8 +78,6 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mfa_kv_append_kernel(const 
     return;
   }
   const size_t row = static_cast<size_t>(blk) * kAppendPage + (t % kAppendPage);
-  // lane l holds elements 8l .. 8l+7 of the row
-  const uint4 x = __ldg((is_v ? p.v_new : p.k_new) + static_cast<size_t>(b) * (kAppendRowLen / 8) + lane);
   if (!p.fp8) {
     uint4* dst = static_cast<uint4*>(is_v ? p.v_cache : p.k_cache) + row * (kAppendRowLen / 8) + lane;
     *dst = x;
