@@ -20,7 +20,9 @@
 //  * Warp 1 issues tcgen05 MMAs in the transposed form, which fills the M=128
 //    datapath: S^T[128 tokens x 64 heads] = K_tile . Q^T and
 //    O^T[256 d x 64 heads] += V^T . P^T (two M=128 halves), fp32 accumulators in
-//    tensor memory (S double-buffered, O double-buffered across sequences).
+//    tensor memory (S double-buffered, O double-buffered across sequences).  For
+//    e4m3 KV warp 2 issues the PV MMAs and warp 1 only QK^T, so that a PV whose
+//    operands are ready never waits behind the issue of the next tile's QK^T.
 //  * Eight softmax warps (two per tensor-memory lane quarter, 32 heads each) run the
 //    online softmax in fp32.  The running max is lazy: a head's reference max moves
 //    only when a score exceeds it by 2^8, so the common tile needs no cross-thread
@@ -61,7 +63,7 @@ constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
 constexpr int kDequantThreads = 128;  // e4m3: one thread per token row of a tile
 // bf16 : warp 0 TMA, warp 1 MMA, warps 2..9 softmax (320 threads, 168 registers each).
-// e4m3 : warpgroup 0 = warp 0 TMA, warp 1 MMA (warps 2, 3 idle), warpgroups 1-2 = warps
+// e4m3 : warpgroup 0 = warp 0 TMA, warp 1 QK^T MMAs, warp 2 PV MMAs (warp 3 idle), warpgroups 1-2 = warps
 //        4..11 softmax, warpgroup 3 = warps 12..15 V dequantisation; launched with 128
 //        registers per thread and rebalanced to 80 / 168 / 168 / 96 (sum 4 x 128).
 template <bool kFp8>
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     }
     mbar_init(bar(kBarPFull), kSoftmaxThreads);
     mbar_init(bar(kBarPvDone), 1);
-    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarDrain), kFp8 ? 2 : 1);
     mbar_init(bar(kBarQReady), kSoftmaxThreads);
     mbar_init(bar(kBarVhFull), kDequantThreads);
     misc[1] = 0;
@@ -716,10 +718,13 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (kFp8 && warp == 2)) {
     if constexpr (kFp8) reg_dealloc<kRegsCtl>();
-    // ---------------- MMA issuer: QK^T of tile n, then PV of tile n - 1, so the next tile's
-    // scores are computed while the softmax works on the current one
+    // ---------------- MMA issuers: QK^T of tile n, then PV of tile n - 1, so the next tile's
+    // scores are computed while the softmax works on the current one.  bf16: one thread
+    // issues both streams.  e4m3: warp 1 issues the QK^T stream and warp 2 the PV stream
+    // (they share no operand, accumulator or barrier), each with its own commits; both
+    // commit to the drain barrier before tensor memory is released.
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
       constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
@@ -727,7 +732,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
       for (int n = 0; n <= ntiles && ok; ++n) {
-        if (n < ntiles) {
+        if (n < ntiles && (!kFp8 || warp == 1)) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
           if (first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           if (last) umma_commit(bar(kBarQEmpty));
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
         }
-        if (n >= 1) {
+        if (n >= 1 && (!kFp8 || warp == 2)) {
           const int m = n - 1;
           const int4 sg = seg[sv];
           const bool first = (jv == sg.y), last = (jv == sg.z - 1);
@@ -823,7 +828,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
     }
   } else if (kFp8 && warp < softmax_warp0<kFp8>()) {
-    // e4m3: warps 2 and 3 complete warpgroup 0 and have no role
+    // e4m3: warp 3 completes warpgroup 0 and has no role
     if constexpr (kFp8) reg_dealloc<kRegsCtl>();
   } else if (kFp8 && warp >= kDequantWarp0) {
     if constexpr (kFp8) {
