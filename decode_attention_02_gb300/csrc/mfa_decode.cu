@@ -17,12 +17,12 @@
 //  * Warp 0 streams K/V pages with TMA (3-D tensor maps over the page pool; the
 //    block table supplies the page coordinate) into a ring of shared-memory slots,
 //    four ring uses at a time from four lanes.
-//  * Warp 1 issues tcgen05 MMAs in the transposed form, which fills the M=128
-//    datapath: S^T[128 tokens x 64 heads] = K_tile . Q^T and
-//    O^T[256 d x 64 heads] += V^T . P^T (two M=128 halves), fp32 accumulators in
-//    tensor memory (S double-buffered, O double-buffered across sequences).  For
-//    e4m3 KV warp 2 issues the PV MMAs and warp 1 only QK^T, so that a PV whose
-//    operands are ready never waits behind the issue of the next tile's QK^T.
+//  * tcgen05 MMAs in the transposed form fill the M=128 datapath:
+//    S^T[128 tokens x 64 heads] = K_tile . Q^T, issued by warp 1, and
+//    O^T[256 d x 64 heads] += V^T . P^T (two M=128 halves), issued by another warp so
+//    that a PV whose operands are ready never waits behind the issue of the next
+//    tile's QK^T; fp32 accumulators in tensor memory (S double-buffered, O
+//    double-buffered across sequences).
 //  * Eight softmax warps (two per tensor-memory lane quarter, 32 heads each) run the
 //    online softmax in fp32.  The running max is lazy: a head's reference max moves
 //    only when a score exceeds it by 2^8, so the common tile needs no cross-thread
@@ -62,12 +62,15 @@ constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
 constexpr int kDequantThreads = 128;  // e4m3: one thread per token row of a tile
-// bf16 : warp 0 TMA, warp 1 MMA, warps 2..9 softmax (320 threads, 168 registers each).
+// bf16 : warp 0 TMA, warp 1 QK^T MMAs, warps 2..9 softmax, warp 10 PV MMAs (352 threads,
+//        168 registers each).
 // e4m3 : warpgroup 0 = warp 0 TMA, warp 1 QK^T MMAs, warp 2 PV MMAs (warp 3 idle), warpgroups 1-2 = warps
 //        4..11 softmax, warpgroup 3 = warps 12..15 V dequantisation; launched with 128
 //        registers per thread and rebalanced to 80 / 168 / 168 / 96 (sum 4 x 128).
 template <bool kFp8>
-__host__ __device__ constexpr int threads_of() { return kFp8 ? 512 : 320; }
+__host__ __device__ constexpr int threads_of() { return kFp8 ? 512 : 352; }
+template <bool kFp8>
+__host__ __device__ constexpr int pv_warp() { return kFp8 ? 2 : 10; }   // issues the PV MMAs
 template <bool kFp8>
 __host__ __device__ constexpr int softmax_warp0() { return kFp8 ? 4 : 2; }
 constexpr int kDequantWarp0 = 12;
@@ -110,7 +113,21 @@ struct KvLayout<true> {
 };
 static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
 static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
-constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan [24..31] q maxima
+constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan
+                                         //      [20..21] CTA tile range [22..23] ring-order counts [24..31] q maxima
+// Ring-order counts.  K and V uses share one ring, and a consumer may only wait on a slot's
+// Full barrier once the slot's previous use has landed: a waiter two phases behind would see
+// the parity it wants and read a slot still being written.  With the QK^T and PV streams in
+// different threads, a tile's K uses follow the V uses of three tiles earlier in some slots
+// (and, for e4m3, its V uses follow its own K uses), with no barrier between the two streams
+// that orders them.  So each stream publishes how many tiles of its uses have landed:
+//   misc[kCntK]: K tiles whose four uses the QK^T issuer has seen land;
+//   misc[kCntV]: V tiles whose four uses the V consumer (bf16: the PV issuer; e4m3: the
+//                dequant warps) has seen land.
+// The QK^T issuer waits for misc[kCntV] >= n - 2 before tile n's K uses; the e4m3 dequant
+// warps wait for misc[kCntK] >= n + 1 before tile n's V uses.  (A bf16 PV of tile n already
+// follows tile n's K through the softmax's P.)
+constexpr int kCntK = 22, kCntV = 23;
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -236,6 +253,26 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   const bool ok = wait_slow(bar, parity, abort_flag, kWaitLimitNs);
   if (!ok && abort_flag != nullptr) *abort_flag = 1;
   return ok;
+}
+
+// Bounded wait until a monotonic shared-memory count reaches target (see the ring-order
+// counts in the kernel); sets the abort flag when it gives up.
+__device__ __forceinline__ bool wait_count(const int* count, int target, volatile int* abort_flag) {
+  if (ld_acquire_cta(count) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(32);
+    if (ld_acquire_cta(count) >= target) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_count_warp(const int* count, int target, volatile int* abort_flag) {
+  const bool ok = wait_count(count, target, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Block-wide (kThreads threads) inclusive scan of one value per thread; also returns the total.
@@ -459,10 +496,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     }
     mbar_init(bar(kBarPFull), kSoftmaxThreads);
     mbar_init(bar(kBarPvDone), 1);
-    mbar_init(bar(kBarDrain), kFp8 ? 2 : 1);
+    mbar_init(bar(kBarDrain), 2);   // one commit from each MMA issuer
     mbar_init(bar(kBarQReady), kSoftmaxThreads);
     mbar_init(bar(kBarVhFull), kDequantThreads);
     misc[1] = 0;
+    misc[kCntK] = 0;
+    misc[kCntV] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -718,13 +757,14 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
       }
     }
-  } else if (warp == 1 || (kFp8 && warp == 2)) {
+  } else if (warp == 1 || warp == pv_warp<kFp8>()) {
     if constexpr (kFp8) reg_dealloc<kRegsCtl>();
     // ---------------- MMA issuers: QK^T of tile n, then PV of tile n - 1, so the next tile's
-    // scores are computed while the softmax works on the current one.  bf16: one thread
-    // issues both streams.  e4m3: warp 1 issues the QK^T stream and warp 2 the PV stream
-    // (they share no operand, accumulator or barrier), each with its own commits; both
-    // commit to the drain barrier before tensor memory is released.
+    // scores are computed while the softmax works on the current one.  Warp 1 issues the
+    // QK^T stream and warp pv_warp the PV stream (they share no operand, accumulator or
+    // barrier), each with its own commits, so that a PV whose operands are ready never
+    // waits behind the issue of the next QK^T; both commit to the drain barrier before
+    // tensor memory is released.
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
       constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
@@ -732,11 +772,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
       for (int n = 0; n <= ntiles && ok; ++n) {
-        if (n < ntiles && (!kFp8 || warp == 1)) {
+        if (n < ntiles && warp == 1) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
           if (first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
+          if (ok && n >= 3) ok = wait_count(misc + kCntV, n - 2, abort_flag);   // V(n - 3) has landed
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
@@ -756,6 +797,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               umma_commit(bar(kBarEmpty + slot));
             }
             if (!ok) break;
+            st_release_cta(misc + kCntK, n + 1);
           } else {
             // e4m3 K boxes as TMA wrote them: the two pages of d-half dh are adjacent slots,
             // one 128-row A operand; B stacks q's e4m3 hi part (rows 0..63) over its lo part
@@ -763,6 +805,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             for (int c = 0; c < 4 && ok; ++c)
               ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
             if (!ok) break;
+            st_release_cta(misc + kCntK, n + 1);
             tc_fence_after();
 #pragma unroll
             for (int dh = 0; dh < 2; ++dh) {
@@ -779,7 +822,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           if (last) umma_commit(bar(kBarQEmpty));
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
         }
-        if (n >= 1 && (!kFp8 || warp == 2)) {
+        if (n >= 1 && warp == pv_warp<kFp8>()) {
           const int m = n - 1;
           const int4 sg = seg[sv];
           const bool first = (jv == sg.y), last = (jv == sg.z - 1);
@@ -817,6 +860,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             }
           }
           if (!ok) break;
+          if constexpr (!kFp8) st_release_cta(misc + kCntV, m + 1);   // V(m) has landed
           umma_commit(bar(kBarPvDone));
           if (last) umma_commit(bar(kBarOFull + kb));
           if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
@@ -853,6 +897,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         auto cv = [&](uint32_t two) { return hmul2(e4m3x2_to_f16x2(two), sv2); };
         // the f16 tile is free once the previous tile's PV has read it
         bool ok = (n == 0) || wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
+        // tile n's V uses follow its K uses in the ring: K(n) must have landed first
+        if (ok) ok = wait_count_warp(misc + kCntK, n + 1, abort_flag);
         for (int dh = 0; dh < 2 && ok; ++dh) {
           const uint32_t use = ring_use(n, ntiles, true, pg, dh);
           ok = wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
@@ -877,8 +923,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         if (named_bar_or(4, kDequantThreads, !ok || *abort_flag)) { aborted = true; break; }
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarVhFull));
-        if (dt == 0)
+        if (dt == 0) {
+          st_release_cta(misc + kCntV, n + 1);   // V(n) has landed (and is read)
           for (int c = 0; c < 4; ++c) mbar_arrive(bar(kBarEmpty + ring_use(n, ntiles, true, c >> 1, c & 1) % kNumSlots));
+        }
       }
       if (range_bad) atomicOr(p.status, MFA_DEV_RANGE);
       if (aborted && dt == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
