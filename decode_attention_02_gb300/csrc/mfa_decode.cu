@@ -114,20 +114,23 @@ struct KvLayout<true> {
 static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
 static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
 constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan
-                                         //      [20..21] CTA tile range [22..23] ring-order counts [24..31] q maxima
+                                         //      [20..21] CTA tile range [24..31] q maxima
 // Ring-order counts.  K and V uses share one ring, and a consumer may only wait on a slot's
 // Full barrier once the slot's previous use has landed: a waiter two phases behind would see
 // the parity it wants and read a slot still being written.  With the QK^T and PV streams in
 // different threads, a tile's K uses follow the V uses of three tiles earlier in some slots
 // (and, for e4m3, its V uses follow its own K uses), with no barrier between the two streams
 // that orders them.  So each stream publishes how many tiles of its uses have landed:
-//   misc[kCntK]: K tiles whose four uses the QK^T issuer has seen land;
-//   misc[kCntV]: V tiles whose four uses the V consumer (bf16: the PV issuer; e4m3: the
-//                dequant warps) has seen land.
-// The QK^T issuer waits for misc[kCntV] >= n - 2 before tile n's K uses; the e4m3 dequant
-// warps wait for misc[kCntK] >= n + 1 before tile n's V uses.  (A bf16 PV of tile n already
-// follows tile n's K through the softmax's P.)
-constexpr int kCntK = 22, kCntV = 23;
+//   cnt[0]: K tiles whose four uses the QK^T issuer has seen land (the e4m3 issuer waits
+//           for a tile's K before it waits for the softmax, so that the count does not
+//           lag behind the softmax);
+//   cnt[1], cnt[2]: V tiles whose uses the V consumer (bf16: the PV issuer after its waits;
+//           e4m3: the dequant warps after the tile) has seen land, for page 0 and page 1
+//           (both written together).
+// The QK^T issuer waits for both V counts >= n - 2 before tile n's K uses; the e4m3
+// dequant warps wait for the K count >= n + 1 before tile n's V uses.  (A bf16 PV of tile n
+// already follows tile n's K through the softmax's P.)
+constexpr int kOffCnt = kOffBar + 448;   // int[3]: K tiles, V tiles of page 0, V tiles of page 1
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -156,7 +159,7 @@ enum Bar : int {
   kBarVhFull,   // e4m3: a tile's V is in the f16 operand tile
   kBarCount
 };
-static_assert(kBarCount * 8 <= 512, "barrier area");
+static_assert(kBarCount * 8 <= kOffCnt - kOffBar, "barrier area (the ring-order counts follow it)");
 
 // Tensor-memory columns.
 constexpr uint32_t kTmemS = 0;     // S^T buffers: bf16 [0,64) and [64,128); e4m3 [0,128) and
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   int* misc = reinterpret_cast<int*>(smem + kOffMisc);
+  int* cnt = reinterpret_cast<int*>(smem + kOffCnt);   // ring-order counts
   volatile int* abort_flag = misc + 1;
   int4* seg = reinterpret_cast<int4*>(smem + kOffSeg);
   int* seg_n0 = reinterpret_cast<int*>(smem + kOffSegN0);
@@ -500,8 +504,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     mbar_init(bar(kBarQReady), kSoftmaxThreads);
     mbar_init(bar(kBarVhFull), kDequantThreads);
     misc[1] = 0;
-    misc[kCntK] = 0;
-    misc[kCntV] = 0;
+    for (int i = 0; i < 3; ++i) cnt[i] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -775,13 +778,21 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         if (n < ntiles && warp == 1) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
-          if (first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
+          const uint32_t u0 = ring_use(n, ntiles, false, 0, 0);
+          // the slots of tile n's K last held V(n - 3): it must have landed (ring-order counts)
+          if (n >= 3) ok = wait_count(cnt + 1, n - 2, abort_flag) && wait_count(cnt + 2, n - 2, abort_flag);
+          if constexpr (kFp8) {
+            // e4m3: the tile's K first, so that its count reaches the dequant warps without
+            // waiting for the softmax
+            for (int c = 0; c < 4 && ok; ++c)
+              ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
+            if (ok) st_release_cta(cnt, n + 1);
+          }
+          if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
-          if (ok && n >= 3) ok = wait_count(misc + kCntV, n - 2, abort_flag);   // V(n - 3) has landed
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
-          const uint32_t u0 = ring_use(n, ntiles, false, 0, 0);
           if constexpr (!kFp8) {
             for (int c = 0; c < 4; ++c) {
               const uint32_t slot = (u0 + c) % kNumSlots;
@@ -797,16 +808,11 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               umma_commit(bar(kBarEmpty + slot));
             }
             if (!ok) break;
-            st_release_cta(misc + kCntK, n + 1);
+            st_release_cta(cnt, n + 1);
           } else {
             // e4m3 K boxes as TMA wrote them: the two pages of d-half dh are adjacent slots,
             // one 128-row A operand; B stacks q's e4m3 hi part (rows 0..63) over its lo part
-            // (rows 64..127), so each K step (32) reads K once for both
-            for (int c = 0; c < 4 && ok; ++c)
-              ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
-            if (!ok) break;
-            st_release_cta(misc + kCntK, n + 1);
-            tc_fence_after();
+            // (rows 64..127), so each K step (32) reads K once for both (its Full waits are above)
 #pragma unroll
             for (int dh = 0; dh < 2; ++dh) {
               const uint32_t a0 = sbase + kOffRing + ((u0 + 2 * dh) % kNumSlots) * kSlotBytes;
@@ -860,7 +866,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             }
           }
           if (!ok) break;
-          if constexpr (!kFp8) st_release_cta(misc + kCntV, m + 1);   // V(m) has landed
+          if constexpr (!kFp8) {   // V(m) has landed
+            st_release_cta(cnt + 1, m + 1);
+            st_release_cta(cnt + 2, m + 1);
+          }
           umma_commit(bar(kBarPvDone));
           if (last) umma_commit(bar(kBarOFull + kb));
           if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
@@ -898,7 +907,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         // the f16 tile is free once the previous tile's PV has read it
         bool ok = (n == 0) || wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
         // tile n's V uses follow its K uses in the ring: K(n) must have landed first
-        if (ok) ok = wait_count_warp(misc + kCntK, n + 1, abort_flag);
+        if (ok) ok = wait_count_warp(cnt, n + 1, abort_flag);
         for (int dh = 0; dh < 2 && ok; ++dh) {
           const uint32_t use = ring_use(n, ntiles, true, pg, dh);
           ok = wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
@@ -924,7 +933,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarVhFull));
         if (dt == 0) {
-          st_release_cta(misc + kCntV, n + 1);   // V(n) has landed (and is read)
+          st_release_cta(cnt + 1, n + 1);   // V(n) landed (and is read)
+          st_release_cta(cnt + 2, n + 1);
           for (int c = 0; c < 4; ++c) mbar_arrive(bar(kBarEmpty + ring_use(n, ntiles, true, c >> 1, c & 1) % kNumSlots));
         }
       }
