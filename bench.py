@@ -314,8 +314,10 @@ def run_native(args, case, rank: int, world: int):
                       host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev)
     dec_strict = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
                              host_seq_lens=lens, device=dev)
+    # the decode kernel alone, in the configuration the timed steps launch it with
     dec_only = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                           host_seq_lens=lens, flags=mfa.MFA_PLAN_NO_COMBINE, device=dev)
+                           host_seq_lens=lens, flags=mfa.MFA_PLAN_NO_COMBINE | mfa.MFA_PLAN_EARLY_METADATA,
+                           device=dev)
     stream = torch.cuda.current_stream(dev)
     G = dec.plan.num_ctas
     launches_per_step = 1 + (1 if G > 1 else 0)

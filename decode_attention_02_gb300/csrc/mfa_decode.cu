@@ -483,35 +483,38 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
-  // ---------------- set-up: barriers, tensor memory
-  if (tid == 0) {
-    for (int i = 0; i < kNumSlots; ++i) {
-      mbar_init(bar(kBarFull + i), 1);
-      // released by the MMA commit, or (e4m3 V boxes) by the leader of the dequant warps
-      mbar_init(bar(kBarEmpty + i), 1);
+  // With early metadata the lengths are read before anything else: the schedule below
+  // waits on them and on nothing the set-up does.
+  int L_first = 0;
+  if (p.early_metadata && tid < p.batch) L_first = p.seq_lens[tid];
+
+  // ---------------- set-up: barriers (one per lane of warp 0), tensor memory
+  if (warp == 0) {
+    for (int i = lane; i < kBarCount; i += 32) {
+      // arrivals per phase: the softmax threads for the barriers they release, the dequant
+      // threads for the f16 V tile, one commit from each MMA issuer for the drain, and one
+      // (a commit, an expect_tx arrive, or the dequant warps' leader) for the others
+      uint32_t count = 1;
+      if (i == kBarSEmpty || i == kBarSEmpty + 1 || i == kBarOEmpty || i == kBarOEmpty + 1 ||
+          i == kBarPFull || i == kBarQReady)
+        count = kSoftmaxThreads;
+      else if (i == kBarVhFull)
+        count = kDequantThreads;
+      else if (i == kBarDrain)
+        count = 2;
+      mbar_init(bar(i), count);
     }
-    mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSEmpty + i), kSoftmaxThreads);
-      mbar_init(bar(kBarOFull + i), 1);
-      mbar_init(bar(kBarOEmpty + i), kSoftmaxThreads);
+    if (lane == 0) {
+      misc[1] = 0;
+      for (int i = 0; i < 3; ++i) cnt[i] = 0;
     }
-    mbar_init(bar(kBarPFull), kSoftmaxThreads);
-    mbar_init(bar(kBarPvDone), 1);
-    mbar_init(bar(kBarDrain), 2);   // one commit from each MMA issuer
-    mbar_init(bar(kBarQReady), kSoftmaxThreads);
-    mbar_init(bar(kBarVhFull), kDequantThreads);
-    misc[1] = 0;
-    for (int i = 0; i < 3; ++i) cnt[i] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     tmem_alloc(sbase + kOffMisc, kTmemCols);
     tmem_relinquish();
   }
-  if (tid == 32 * 0) {
+  if (tid == 32 * 2) {
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
@@ -521,7 +524,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // that kernel may write is touched before griddepcontrol.wait.  With early metadata
   // the lengths and the block table are read first (the caller guarantees the preceding
   // kernel does not write them); q, K, V and every output wait.
-  if (!p.early_metadata) grid_dep_wait();
+  if (!p.early_metadata) {
+    grid_dep_wait();
+    if (tid < p.batch) L_first = p.seq_lens[tid];
+  }
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
   // Cost-balanced split: tile k of sequence b sits at cost 4 (S_b + k) + 3 N_b, S_b being the
@@ -537,7 +543,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     bool bad = false;
     auto packed = [](int T) { return static_cast<long long>(T) | (static_cast<long long>(T > 0) << 32); };
     long long loc = 0;
-    const int L_first = (tid < p.batch) ? p.seq_lens[tid] : 0;   // reused by the segment scan below
+    // L_first (read above) is reused by the segment scan below
     loc += packed(tiles_of(clamp_len(L_first, cap, bad)));
     for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += packed(tiles_of(clamp_len(p.seq_lens[b], cap, bad)));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
@@ -546,7 +552,15 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     const int W = static_cast<int>(tot0 & 0xFFFFFFFFll), N = static_cast<int>(tot0 >> 32);
     const int G = gridDim.x, g = blockIdx.x;
     const long long C = 4LL * W + 3LL * max(N - 1, 0);
-    const long long X0 = (static_cast<long long>(g) * C) / G, X1 = (static_cast<long long>(g + 1) * C) / G;
+    long long X0, X1;
+    if (C <= 0x7FFFFFFFll / G) {   // (g + 1) C fits in 32 bits: the short division
+      const uint32_t Cu = static_cast<uint32_t>(C), Gu = static_cast<uint32_t>(G), gu = static_cast<uint32_t>(g);
+      X0 = (gu * Cu) / Gu;
+      X1 = ((gu + 1u) * Cu) / Gu;
+    } else {
+      X0 = (static_cast<long long>(g) * C) / G;
+      X1 = (static_cast<long long>(g + 1) * C) / G;
+    }
     // sequence with first-tile cost `base` and T tiles: first of its tiles at cost >= X
     auto first_at = [](long long X, long long base, int T) -> int {
       return X <= base ? 0 : static_cast<int>(min(static_cast<long long>(T), (X - base + 3) / 4));
