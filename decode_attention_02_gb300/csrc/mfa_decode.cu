@@ -992,6 +992,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     float lreg[32];                                            // e4m3: row-sum partials in registers
     int defer_b[2] = {0, 0}, defer_slot[2] = {0, 0};
     bool defer_whole[2] = {false, false};
+    bool prev_written = false;   // the second-to-last segment was written during the last one
 
     // valid rows of a tile's page pg: the last page's rows sit at the end of the box
     auto page_rows = [&](int L, int j, int pg) { return min(kPage, L - kTile * j - kPage * pg); };
@@ -1326,6 +1327,15 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarPFull));
+        // bf16: the second-to-last segment's output, once the last segment's first P is out:
+        // its last PV completed before that P could be written, so the stores overlap the
+        // remaining tiles instead of adding to the CTA's tail (the e4m3 softmax, which bounds
+        // its tile period, keeps both writes for the end)
+        if (!kFp8 && first && s >= 1 && s == nseg - 1) {
+          const int ps = s - 1, pkb = ps & 1;
+          if (!write_segment(ps, defer_b[pkb], defer_slot[pkb], defer_whole[pkb], true)) { stop = true; break; }
+          prev_written = true;
+        }
       }
       if (stop) break;
 
@@ -1362,8 +1372,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         // the accumulator is needed again by segment s + 2: write it out now
         if (!write_segment(s, b, slot_p, whole, false)) break;
       } else {
-        // one of the CTA's last two segments: its accumulator stays in tensor memory
-        // and is written after the last tile, when the operand buffers are idle
+        // one of the CTA's last two segments: its accumulator stays in tensor memory and is
+        // written from registers after the last tile (bf16: the one before the last during the
+        // last segment's first tile)
         defer_b[kb] = b;
         defer_slot[kb] = slot_p;
         defer_whole[kb] = whole;
@@ -1372,7 +1383,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     if (!aborted && !*abort_flag) {
       // deferred accumulators, newest first, stored straight from registers (uniform:
       // every thread reads the same values)
-      const int first_def = nseg >= 2 ? nseg - 2 : 0;
+      const int first_def = (nseg >= 2 && !prev_written) ? nseg - 2 : nseg - 1;
       for (int s = nseg - 1; s >= first_def; --s) {
         const int kb = s & 1;
         if (!write_segment(s, defer_b[kb], defer_slot[kb], defer_whole[kb], true)) break;
