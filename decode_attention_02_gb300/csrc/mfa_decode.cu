@@ -130,7 +130,10 @@ constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nse
 // The QK^T issuer waits for both V counts >= n - 2 before tile n's K uses; the e4m3
 // dequant warps wait for the K count >= n + 1 before tile n's V uses.  (A bf16 PV of tile n
 // already follows tile n's K through the softmax's P.)
-constexpr int kOffCnt = kOffBar + 448;   // int[3]: K tiles, V tiles of page 0, V tiles of page 1
+//   cnt[3]: e4m3 PV tiles issued.  The e4m3 QK^T issuer issues tile n only after PV(n - 2),
+//           so that a ready PV is not queued behind the next QK^T in the tensor pipe (the
+//           softmax cannot start tile n before PV(n - 2) completes anyway).
+constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1, PV tiles
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -506,7 +509,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     }
     if (lane == 0) {
       misc[1] = 0;
-      for (int i = 0; i < 3; ++i) cnt[i] = 0;
+      for (int i = 0; i < 4; ++i) cnt[i] = 0;
     }
     fence_mbar_init();
   }
@@ -804,6 +807,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           }
           if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
+          if (kFp8 && ok && n >= 2) ok = wait_count(cnt + 3, n - 1, abort_flag);   // PV(n - 2) issued first
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
@@ -886,6 +890,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           }
           umma_commit(bar(kBarPvDone));
           if (last) umma_commit(bar(kBarOFull + kb));
+          if constexpr (kFp8) st_release_cta(cnt + 3, m + 1);   // PV(m) issued
           if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
         }
       }
