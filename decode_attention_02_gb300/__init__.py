@@ -48,7 +48,7 @@ PAGE_SIZE = 64
 # Every symbol include/mfa.h declares.
 EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
                     "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error",
-                    "mfa_decode_run_static_workspace", "mfa_kv_append")
+                    "mfa_decode_run_static_workspace", "mfa_kv_append", "mfa_decode_run_host")
 
 # Size of the library's own scratch array used by mfa_decode_run_static_workspace.
 MFA_STATIC_WORKSPACE_BYTES = 24 * 1024 * 1024
@@ -113,6 +113,9 @@ def load_library(path: str = LIB_PATH):
     lib.mfa_decode_run_static_workspace.restype = ctypes.c_int
     lib.mfa_kv_append.argtypes = [ctypes.POINTER(MfaProblem), P, P, P, P, P, P, P, P, P, P]
     lib.mfa_kv_append.restype = ctypes.c_int
+    lib.mfa_decode_run_host.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P, P, P,
+                                        P, P, P, P, P, P, P, P, P, P, ctypes.c_uint64, P]
+    lib.mfa_decode_run_host.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -201,6 +204,34 @@ def mfa_decode_run_static_workspace(plan: MfaPlan, problem: MfaProblem, q, k_cac
     _check(st, "mfa_decode_run_static_workspace")
 
 
+def _host_ptr(x) -> Optional[int]:
+    """Address of a CPU torch tensor (contiguous), an int, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if x.is_cuda:
+        raise ValueError("expected a CPU (pinned) tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def mfa_decode_run_host(plan: MfaPlan, problem: MfaProblem, q_host, block_table_host, seq_lens_host, out_host,
+                        lse_host, q_dev, block_table_dev, seq_lens_dev, out_dev, lse_dev, k_cache, v_cache, k_scale,
+                        v_scale, workspace, stream=None, workspace_bytes: Optional[int] = None) -> None:
+    """One decode step from host buffers (copies in, decode, copies out on one stream)."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    st = lib.mfa_decode_run_host(ctypes.byref(plan), ctypes.byref(problem), _host_ptr(q_host),
+                                 _host_ptr(block_table_host), _host_ptr(seq_lens_host), _host_ptr(out_host),
+                                 _host_ptr(lse_host), _ptr(q_dev), _ptr(block_table_dev), _ptr(seq_lens_dev),
+                                 _ptr(out_dev), _ptr(lse_dev), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(st, "mfa_decode_run_host")
+
+
 def mfa_combine(plan: MfaPlan, problem: MfaProblem, workspace, seq_lens, out, lse, stream=None,
                 workspace_bytes: Optional[int] = None) -> None:
     lib = load_library()
@@ -271,3 +302,23 @@ class Decoder:
         mfa_decode_run(self.plan, self.problem, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                        out, lse, self.workspace, stream)
         return out, lse
+
+    def run_host(self, q_host, block_table_host, seq_lens_host, out_host, lse_host, k_cache, v_cache, k_scale=None,
+                 v_scale=None, stream=None):
+        """One step from pinned host buffers into pinned host outputs (mfa_decode_run_host),
+        on device staging buffers this decoder owns.  Asynchronous on ``stream``."""
+        import torch
+        if not hasattr(self, "_staging"):
+            dev = self.device
+            B = self.problem.batch
+            odt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
+            self._staging = dict(
+                q=torch.empty((B, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev),
+                table=torch.empty((B, self.problem.max_pages_per_seq), dtype=torch.int32, device=dev),
+                lens=torch.empty((B,), dtype=torch.int32, device=dev),
+                out=torch.empty((B, NUM_Q_HEADS, HEAD_DIM), dtype=odt, device=dev),
+                lse=torch.empty((B, NUM_Q_HEADS), dtype=torch.float32, device=dev))
+        st = self._staging
+        mfa_decode_run_host(self.plan, self.problem, q_host, block_table_host, seq_lens_host, out_host, lse_host,
+                            st["q"], st["table"], st["lens"], st["out"], None if lse_host is None else st["lse"],
+                            k_cache, v_cache, k_scale, v_scale, self.workspace, stream)

@@ -1841,10 +1841,11 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   return MFA_OK;
 }
 
-mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
-                          const void* v_cache, const float* k_scale, const float* v_scale,
-                          const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
-                          void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
+// Host-side checks of one decode step's arguments (everything mfa_decode_run validates).
+static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
+                            const void* v_cache, const float* k_scale, const float* v_scale,
+                            const int32_t* block_table, const int32_t* seq_lens, const void* out,
+                            const float* lse, const void* workspace, uint64_t workspace_bytes) {
   mfa_status st = check_problem(pr);
   if (st != MFA_OK) return st;
   st = check_plan(plan, pr);
@@ -1861,6 +1862,16 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
       (lse != nullptr && !aligned(lse, 4)))
     return MFA_ERR_INVALID_ARG;
   if (workspace_bytes < plan->workspace_bytes) return MFA_ERR_WORKSPACE;
+  return MFA_OK;
+}
+
+mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
+                          const void* v_cache, const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
+                          void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
+  mfa_status st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse,
+                            workspace, workspace_bytes);
+  if (st != MFA_OK || pr->batch == 0) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
   DecodeParams prm;
@@ -1914,6 +1925,38 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
     if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return cuda_fail(e, "sync");
     if (word != 0) return MFA_ERR_DEVICE_CHECK;
   }
+  return MFA_OK;
+}
+
+mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* pr, const void* q_host,
+                               const int32_t* block_table_host, const int32_t* seq_lens_host, void* out_host,
+                               float* lse_host, void* q_dev, int32_t* block_table_dev, int32_t* seq_lens_dev,
+                               void* out_dev, float* lse_dev, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, void* workspace,
+                               uint64_t workspace_bytes, void* stream_ptr) {
+  // the whole step is validated before anything is enqueued
+  mfa_status st = check_run(plan, pr, q_dev, k_cache, v_cache, k_scale, v_scale, block_table_dev, seq_lens_dev,
+                            out_dev, lse_dev, workspace, workspace_bytes);
+  if (st != MFA_OK || pr->batch == 0) return st;
+  if (!q_host || !block_table_host || !seq_lens_host || !out_host) return MFA_ERR_INVALID_ARG;
+  if ((lse_host == nullptr) != (lse_dev == nullptr)) return MFA_ERR_INVALID_ARG;
+  const size_t B = static_cast<size_t>(pr->batch);
+  const size_t q_bytes = B * kH * kD * 2, table_bytes = B * pr->max_pages_per_seq * 4, lens_bytes = B * 4;
+  const size_t out_bytes = B * kH * kD * (pr->out_dtype == MFA_OUT_FP32 ? 4 : 2), lse_bytes = B * kH * 4;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(block_table_dev, block_table_host, table_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(seq_lens_dev, seq_lens_host, lens_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e, "host to device copy");
+  st = mfa_decode_run(plan, pr, q_dev, k_cache, v_cache, k_scale, v_scale, block_table_dev, seq_lens_dev, out_dev,
+                      lse_dev, workspace, workspace_bytes, stream_ptr);
+  if (st != MFA_OK) return st;
+  if ((e = cudaMemcpyAsync(out_host, out_dev, out_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "device to host copy");
+  if (lse_host != nullptr &&
+      (e = cudaMemcpyAsync(lse_host, lse_dev, lse_bytes, cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    return cuda_fail(e, "device to host copy");
   return MFA_OK;
 }
 

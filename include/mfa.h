@@ -176,6 +176,33 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* problem,
                           void* stream);
 
 /*
+ * One decode step from host buffers: enqueue on `stream` the copies of q, the block table and
+ * the lengths from host memory into the caller's device buffers, the decode step exactly as
+ * mfa_decode_run enqueues it (on the device buffers), and the copies of out and lse back to
+ * host memory.  Nothing synchronises (MFA_PLAN_CHECK excepted, as for mfa_decode_run); the
+ * host outputs are valid once the stream has reached this point.  Host buffers should be
+ * page-locked (cudaHostAlloc / pinned), or the copies are not asynchronous.
+ *   q_host, block_table_host, seq_lens_host : host, same layouts as mfa_decode_run's q,
+ *                  block_table and seq_lens.
+ *   out_host, lse_host : host, same layouts as out and lse; lse_host NULL iff lse_dev NULL.
+ *   q_dev, block_table_dev, seq_lens_dev, out_dev, lse_dev : the device buffers the step
+ *                  runs on (the requirements of mfa_decode_run's arguments); the caller owns
+ *                  them and must not reuse them until the stream has passed this step.
+ *   k_cache .. workspace_bytes, stream : as for mfa_decode_run.
+ * Every argument is validated before anything is enqueued.  Two such steps on two streams,
+ * each with its own device buffers and workspace, overlap one step's copies with the other's
+ * kernels.
+ */
+mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* problem,
+                               const void* q_host, const int32_t* block_table_host,
+                               const int32_t* seq_lens_host, void* out_host, float* lse_host,
+                               void* q_dev, int32_t* block_table_dev, int32_t* seq_lens_dev,
+                               void* out_dev, float* lse_dev,
+                               const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               void* workspace, uint64_t workspace_bytes, void* stream);
+
+/*
  * Enqueue the log-sum-exp merge of the partial results in `workspace` (the split
  * combine): for every sequence covered by more than one CTA,
  *     lse* = M + ln sum_s exp(lse_s - M),  M = max_s lse_s,

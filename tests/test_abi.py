@@ -153,3 +153,25 @@ def test_kv_append_validates_before_touching_the_device(lib):
 
 def test_kv_append_of_an_empty_batch_enqueues_nothing(lib):
     assert _append_raw(lib, problem(batch=0), [None] * 9) == mfa.MFA_OK
+
+
+def test_run_host_validates_before_enqueuing_anything(lib):
+    prob = problem()
+    plan = mfa.mfa_decode_plan(prob, [10, 20, 30, 40], num_sms=8)
+    P = ctypes.c_void_p
+    # q_h, table_h, lens_h, out_h, lse_h, q_d, table_d, lens_d, out_d, lse_d, k, v, ks, vs, ws
+    good = [0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 0x10000, 0x20000, 0x30000, 0x40000, 0x50000,
+            0x60000, 0x70000, None, None, 0x100000]
+
+    def call(ptrs, ws_bytes=plan.workspace_bytes, pr=prob):
+        return lib.mfa_decode_run_host(ctypes.byref(plan), ctypes.byref(pr), *[P(x) if x else None for x in ptrs],
+                                       ctypes.c_uint64(ws_bytes), None)
+    for i in (0, 1, 2, 3, 5, 6, 7, 8, 10, 11, 14):   # every required host or device buffer
+        bad = list(good); bad[i] = None
+        assert call(bad) == mfa.MFA_ERR_INVALID_ARG, i
+    no_lse_host = list(good); no_lse_host[4] = None     # lse on one side only
+    assert call(no_lse_host) == mfa.MFA_ERR_INVALID_ARG
+    odd = list(good); odd[5] = 0x10008                  # q on the device must be 16-byte aligned
+    assert call(odd) == mfa.MFA_ERR_INVALID_ARG
+    assert call(good, plan.workspace_bytes - 1) == mfa.MFA_ERR_WORKSPACE
+    assert call(good, pr=problem(batch=5)) == mfa.MFA_ERR_INVALID_ARG

@@ -323,3 +323,32 @@ def test_repeated_steps_are_bitwise_identical(name):
     got = o0[sample].cpu().double().numpy()
     tol = 1e-2 if kv == mfa.MFA_KV_BF16 else 3e-2
     assert np.abs(got - ref_o).max() <= tol
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_host_buffer_steps_on_two_streams_match_the_device_path(kv_dtype):
+    """mfa_decode_run_host: pinned host q, table and lengths in, pinned host out and lse back,
+    with two streams alternating (each with its own staging buffers and workspace, so one
+    step's copies overlap the other's kernels).  Every step must give the device path's bits."""
+    case = inputs.small("host", 9, [1, 64, 65, 300, 2000, 0, 129, 700, 4096], kv_dtype=kv_dtype, seed=72)
+    ref_out, ref_lse, _ = gpu_decode(case, flags=0, out_dtype=mfa.MFA_OUT_BF16)
+    t = to_dev(case)
+    kv = mfa.MFA_KV_FP8_E4M3 if kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    lanes = []
+    for _ in range(2):
+        dec = mfa.Decoder(case.q.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv,
+                          softmax_scale=case.workload.scale(), host_seq_lens=case.seq_lens.tolist(),
+                          flags=mfa.MFA_PLAN_EARLY_METADATA)
+        lanes.append((dec, torch.cuda.Stream()))
+    q_h, table_h, lens_h = case.q.pin_memory(), case.block_table.pin_memory(), case.seq_lens.pin_memory()
+    outs = [(torch.empty(ref_out.shape, dtype=torch.bfloat16).pin_memory(),
+             torch.empty(ref_lse.shape, dtype=torch.float32).pin_memory()) for _ in range(6)]
+    torch.cuda.synchronize()
+    for i, (o_h, l_h) in enumerate(outs):
+        dec, st = lanes[i % 2]
+        dec.run_host(q_h, table_h, lens_h, o_h, l_h, t["k_cache"], t["v_cache"], t["k_scale"], t["v_scale"],
+                     stream=st)
+    torch.cuda.synchronize()
+    for o_h, l_h in outs:
+        assert torch.equal(o_h.view(torch.int16), ref_out.cpu().view(torch.int16))
+        assert torch.equal(l_h, ref_lse.cpu())
