@@ -55,7 +55,7 @@ extern "C" {
 typedef enum mfa_status {
     MFA_OK = 0,
     MFA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, inconsistent plan */
-    MFA_ERR_UNSUPPORTED = 2,   /* a shape this build does not implement (H!=64, d!=256, page!=64) */
+    MFA_ERR_UNSUPPORTED = 2,   /* a shape this library does not implement (H!=64, d!=256, page!=64) */
     MFA_ERR_WORKSPACE = 3,     /* workspace smaller than plan->workspace_bytes */
     MFA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed */
     MFA_ERR_DEVICE_CHECK = 5   /* MFA_PLAN_CHECK found a nonzero device status word */
@@ -90,9 +90,9 @@ typedef enum mfa_out_dtype {
 
 typedef struct mfa_problem {
     int32_t batch;             /* B >= 0 sequences, one new query token each */
-    int32_t num_q_heads;       /* H; this build supports 64 */
-    int32_t head_dim;          /* d; this build supports 256 */
-    int32_t page_size;         /* tokens per KV page; this build supports 64 */
+    int32_t num_q_heads;       /* H; this library supports 64 */
+    int32_t head_dim;          /* d; this library supports 256 */
+    int32_t page_size;         /* tokens per KV page; this library supports 64 */
     int32_t max_pages_per_seq; /* columns of block_table (>= 1) */
     int32_t num_blocks;        /* physical pages in each of the K and V pools (>= 1) */
     int32_t kv_dtype;          /* mfa_kv_dtype */
