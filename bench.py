@@ -52,14 +52,15 @@ def kv_bytes_per_token(kv_dtype: str) -> int:
     return 2 * 256 * 2 if kv_dtype == "bf16" else 2 * 256 * 1 + 2 * 4
 
 
-def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64) -> dict:
-    """HBM bytes one decode step must move: every cached K/V row once, q and out once,
-    the used block-table entries, the lengths and the lse."""
+def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64, T: int = 1) -> dict:
+    """HBM bytes one decode step must move: every cached K/V row once (shared by a sequence's
+    T new query tokens), q, out and lse once per query token, the used block-table entries
+    and the lengths."""
     tokens = int(sum(lens))
     pages = int(sum((L + page - 1) // page for L in lens))
     B = len(lens)
     kv = tokens * kv_bytes_per_token(kv_dtype)
-    other = B * (H * d * 2) * 2 + pages * 4 + B * 4 + B * H * 4
+    other = B * T * (H * d * 2) * 2 + pages * 4 + B * 4 + B * T * H * 4
     return {"kv": kv, "total": kv + other}
 
 
@@ -70,9 +71,11 @@ def append_bytes(batch: int, kv_dtype: str, d: int = 256) -> int:
     return batch * (2 * 2 * d + 4 + 4 + 2 * out_row)
 
 
-def algorithmic_flops(lens, H: int = 64, d: int = 256) -> int:
-    """2*H*d for q.K^T plus 2*H*d for P.V per cached token (softmax not counted)."""
-    return int(sum(lens)) * 4 * H * d
+def algorithmic_flops(lens, H: int = 64, d: int = 256, T: int = 1) -> int:
+    """2*H*d for q.K^T plus 2*H*d for P.V per (query token, visible cached token) pair
+    (softmax not counted); query token i of T sees L - T + 1 + i tokens."""
+    pairs = sum(max(0, int(L) - (T - 1 - i)) for L in lens for i in range(T))
+    return int(pairs) * 4 * H * d
 
 
 def intensity_per_token(kv_dtype: str, H: int = 64, d: int = 256, kv_heads_bytes: float = None) -> float:
@@ -191,18 +194,19 @@ def cpu_oracle_sample(case, target_s: float = 10.0, nthreads: int = 0):
     """
     import oracle
     lens = case.seq_lens.tolist()
+    T = case.workload.tokens_per_seq   # the oracle's rows are (sequence, query token) pairs
     order = [b for b in range(len(lens)) if lens[b] > 0]
     t0 = time.perf_counter()
-    oracle.decode(case, batch_slice=slice(order[0], order[0] + 1), nthreads=nthreads)
+    oracle.decode(case, batch_slice=slice(order[0] * T, (order[0] + 1) * T), nthreads=nthreads)
     t1 = time.perf_counter() - t0
     k = max(1, min(len(lens), int(target_s / max(t1, 1e-3))))
     t0 = time.perf_counter()
-    oracle.decode(case, batch_slice=slice(0, k), nthreads=nthreads)
+    oracle.decode(case, batch_slice=slice(0, k * T), nthreads=nthreads)
     once = time.perf_counter() - t0
     reps = max(1, int(target_s / max(once, 1e-3)))
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.decode(case, batch_slice=slice(0, k), nthreads=nthreads)
+        oracle.decode(case, batch_slice=slice(0, k * T), nthreads=nthreads)
     dt = time.perf_counter() - t0
     kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"] * reps
     return kv / dt / 1e9, dt, k, reps
@@ -215,17 +219,18 @@ def run_reference(args, case, rank: int, world: int):
     oracle.build()
     cores = oracle.num_cpus()
     lens = case.seq_lens.tolist()
+    T = case.workload.tokens_per_seq   # the oracle's rows are (sequence, query token) pairs
     # bounded sample per step: enough sequences for ~1-3 s of oracle work on all cores
     t0 = time.perf_counter()
-    oracle.decode(case, batch_slice=slice(0, 1))
+    oracle.decode(case, batch_slice=slice(0, T))
     t1 = time.perf_counter() - t0
     k = max(1, min(len(lens), int(2.0 / max(t1, 1e-3))))
     for _ in range(args.warmup):
-        oracle.decode(case, batch_slice=slice(0, 1))
+        oracle.decode(case, batch_slice=slice(0, T))
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.decode(case, batch_slice=slice(0, k))
+        oracle.decode(case, batch_slice=slice(0, k * T))
         times.append(time.perf_counter() - t0)
     kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"]
     total = sum(times)
@@ -250,7 +255,8 @@ def workload_config(case, extra=None):
     cfg = {"workload": w.name, "batch": len(lens), "total_tokens": int(sum(lens)),
            "min_len": int(min(lens)), "max_len": int(max(lens)), "num_q_heads": w.num_q_heads,
            "head_dim": w.head_dim, "kv_heads": 1, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
-           "softmax_scale": w.scale(), "parallelism": "replica per GPU"}
+           "softmax_scale": w.scale(), "parallelism": "replica per GPU",
+           "new_tokens_per_seq": w.tokens_per_seq}
     if extra:
         cfg.update(extra)
     return cfg
@@ -293,8 +299,9 @@ def run_native(args, case, rank: int, world: int):
     lens = case.seq_lens.tolist()
     kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
     B = len(lens)
-    acct = algorithmic_bytes(lens, w.kv_dtype)
-    flops = algorithmic_flops(lens)
+    T = w.tokens_per_seq
+    acct = algorithmic_bytes(lens, w.kv_dtype, T=T)
+    flops = algorithmic_flops(lens, T=T)
 
     # rotating input copies: consecutive steps never find their KV in L2
     set_bytes = case.k_cache.numel() * case.k_cache.element_size() * 2
@@ -306,19 +313,20 @@ def run_native(args, case, rank: int, world: int):
             ks=None if case.k_scale is None else case.k_scale.to(dev),
             vs=None if case.v_scale is None else case.v_scale.to(dev),
             table=case.block_table.to(dev), lens=case.seq_lens.to(dev)))
-    out = torch.empty(B, 64, 256, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B, 64, dtype=torch.float32, device=dev)
+    out = torch.empty(B * T, 64, 256, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B * T, 64, dtype=torch.float32, device=dev)
     # the timed steps are back-to-back decode steps whose lengths and block table are
     # filled once, before the loop: each step's decode may therefore read them while the
     # previous step's combine is still running (q, K, V and all outputs stay ordered)
     dec = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                      host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev)
+                      host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev,
+                      tokens_per_seq=T)
     dec_strict = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                             host_seq_lens=lens, device=dev)
+                             host_seq_lens=lens, device=dev, tokens_per_seq=T)
     # the decode kernel alone, in the configuration the timed steps launch it with
     dec_only = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
                            host_seq_lens=lens, flags=mfa.MFA_PLAN_NO_COMBINE | mfa.MFA_PLAN_EARLY_METADATA,
-                           device=dev)
+                           device=dev, tokens_per_seq=T)
     stream = torch.cuda.current_stream(dev)
     G = dec.plan.num_ctas
     launches_per_step = 1 + (1 if G > 1 else 0)
@@ -408,9 +416,9 @@ def run_native(args, case, rank: int, world: int):
     lanes = []
     for _ in range(2):
         d_k = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                          host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev)
-        lanes.append((d_k, torch.cuda.Stream(dev), torch.empty(B, 64, 256, dtype=torch.bfloat16).pin_memory(),
-                      torch.empty(B, 64, dtype=torch.float32).pin_memory()))
+                          host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev, tokens_per_seq=T)
+        lanes.append((d_k, torch.cuda.Stream(dev), torch.empty(B * T, 64, 256, dtype=torch.bfloat16).pin_memory(),
+                      torch.empty(B * T, 64, dtype=torch.float32).pin_memory()))
     h2d = sum(t.numel() * t.element_size() for t in (q_h, table_h, lens_h))
     d2h = sum(t.numel() * t.element_size() for t in lanes[0][2:])
 

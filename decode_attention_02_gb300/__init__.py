@@ -59,7 +59,7 @@ class MfaProblem(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
-                ("out_dtype", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("tokens_per_seq", ctypes.c_int32)]
 
 
 class MfaPlan(ctypes.Structure):
@@ -67,7 +67,8 @@ class MfaPlan(ctypes.Structure):
                 ("max_tiles_per_cta", ctypes.c_int32), ("num_partials", ctypes.c_int32),
                 ("batch", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("flags", ctypes.c_uint32), ("num_sms", ctypes.c_int32),
-                ("total_tiles", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64)]
+                ("total_tiles", ctypes.c_uint64), ("workspace_bytes", ctypes.c_uint64),
+                ("tokens_per_seq", ctypes.c_int32)]
 
 
 class MfaError(RuntimeError):
@@ -160,9 +161,10 @@ def _stream(stream) -> Optional[int]:
 
 def make_problem(batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
                  softmax_scale: float = HEAD_DIM ** -0.5, num_q_heads: int = NUM_Q_HEADS,
-                 head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, out_dtype: int = MFA_OUT_BF16) -> MfaProblem:
+                 head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, out_dtype: int = MFA_OUT_BF16,
+                 tokens_per_seq: int = 1) -> MfaProblem:
     return MfaProblem(batch, num_q_heads, head_dim, page_size, max_pages_per_seq, num_blocks, kv_dtype,
-                      softmax_scale, out_dtype)
+                      softmax_scale, out_dtype, tokens_per_seq)
 
 
 def mfa_decode_plan(problem: MfaProblem, host_seq_lens: Optional[Sequence[int]] = None, max_seq_len: int = 0,
@@ -281,10 +283,11 @@ class Decoder:
 
     def __init__(self, batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
                  softmax_scale: float = HEAD_DIM ** -0.5, host_seq_lens=None, max_seq_len: int = 0,
-                 force_ctas: int = 0, flags: int = 0, device=None, out_dtype: int = MFA_OUT_BF16):
+                 force_ctas: int = 0, flags: int = 0, device=None, out_dtype: int = MFA_OUT_BF16,
+                 tokens_per_seq: int = 1):
         import torch
         self.problem = make_problem(batch, max_pages_per_seq, num_blocks, kv_dtype, softmax_scale,
-                                    out_dtype=out_dtype)
+                                    out_dtype=out_dtype, tokens_per_seq=tokens_per_seq)
         if host_seq_lens is None and max_seq_len == 0:
             max_seq_len = max_pages_per_seq * PAGE_SIZE
         self.plan = mfa_decode_plan(self.problem, host_seq_lens, max_seq_len, 0, force_ctas, flags)
@@ -294,11 +297,12 @@ class Decoder:
     def __call__(self, q, k_cache, v_cache, block_table, seq_lens, k_scale=None, v_scale=None, out=None,
                  lse=None, stream=None):
         import torch
+        rows = self.problem.batch * self.problem.tokens_per_seq   # (sequence, new token) pairs
         if out is None:
             dt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
-            out = torch.empty((self.problem.batch, NUM_Q_HEADS, HEAD_DIM), dtype=dt, device=q.device)
+            out = torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=dt, device=q.device)
         if lse is None:
-            lse = torch.empty((self.problem.batch, NUM_Q_HEADS), dtype=torch.float32, device=q.device)
+            lse = torch.empty((rows, NUM_Q_HEADS), dtype=torch.float32, device=q.device)
         mfa_decode_run(self.plan, self.problem, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                        out, lse, self.workspace, stream)
         return out, lse
@@ -311,13 +315,14 @@ class Decoder:
         if not hasattr(self, "_staging"):
             dev = self.device
             B = self.problem.batch
+            rows = B * self.problem.tokens_per_seq
             odt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
             self._staging = dict(
-                q=torch.empty((B, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev),
+                q=torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev),
                 table=torch.empty((B, self.problem.max_pages_per_seq), dtype=torch.int32, device=dev),
                 lens=torch.empty((B,), dtype=torch.int32, device=dev),
-                out=torch.empty((B, NUM_Q_HEADS, HEAD_DIM), dtype=odt, device=dev),
-                lse=torch.empty((B, NUM_Q_HEADS), dtype=torch.float32, device=dev))
+                out=torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=odt, device=dev),
+                lse=torch.empty((rows, NUM_Q_HEADS), dtype=torch.float32, device=dev))
         st = self._staging
         mfa_decode_run_host(self.plan, self.problem, q_host, block_table_host, seq_lens_host, out_host, lse_host,
                             st["q"], st["table"], st["lens"], st["out"], None if lse_host is None else st["lse"],

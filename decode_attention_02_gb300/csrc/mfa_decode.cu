@@ -78,6 +78,7 @@ constexpr uint32_t kRegsCtl = 80, kRegsSoftmax = 168, kRegsDequant = 96;
 static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsDequant == 4 * (65536 / 512),
               "e4m3 register split must add up to the launch budget (4 warpgroups x 128)");
 constexpr int kMaxTilesPerCta = 128;
+constexpr int kMaxTokensPerSeq = 4;   // new query tokens per sequence (multi-token decode)
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
@@ -193,6 +194,7 @@ struct DecodeParams {
   int out_f32;        // 1: fp32 output, 0: bf16 output
   int early_metadata; // 1: seq_lens/block_table may be read before the preceding grid completes
   float scale_log2;   // softmax_scale * log2(e)
+  int tokens;         // new query tokens per sequence T: batch counts the B * T (sequence, token) pairs
 };
 
 struct CombineParams {
@@ -206,6 +208,7 @@ struct CombineParams {
   int num_ctas;
   int out_f32;
   int heads_per_cta;  // 1, 4 or 16
+  int tokens;         // as DecodeParams::tokens
 };
 
 // ------------------------------------------------------------------ helpers
@@ -240,6 +243,16 @@ __device__ __forceinline__ int clamp_len(int L, int cap, bool& bad) {
 }
 
 __device__ __forceinline__ int tiles_of(int L) { return (L + kTile - 1) / kTile; }
+
+// Multi-token decode: with T new query tokens per sequence (the last T of its L cached tokens),
+// query token i of sequence b is the "sequence" x = b T + i of length L - T + 1 + i: it
+// attends to the cached tokens up to its own position, which is the causal mask among the new
+// tokens.  T = 1 is the ordinary decode step (x = b, length L).
+__device__ __forceinline__ int raw_len(const int32_t* lens, int T, int x) { return lens[T == 1 ? x : x / T]; }
+__device__ __forceinline__ int vlen_from(int L_raw, int T, int x, int cap, bool& bad) {
+  const int L = clamp_len(L_raw, cap, bad);
+  return T == 1 ? L : max(0, L - (T - 1 - x % T));
+}
 
 // Bounded wait on an mbarrier phase.  Returns false after kWaitLimitNs, or at
 // once when another role has raised the CTA's abort flag.
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // With early metadata the lengths are read before anything else: the schedule below
   // waits on them and on nothing the set-up does.
   int L_first = 0;
-  if (p.early_metadata && tid < p.batch) L_first = p.seq_lens[tid];
+  if (p.early_metadata && tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, tid);
 
   // ---------------- set-up: barriers (one per lane of warp 0), tensor memory
   if (warp == 0) {
@@ -529,7 +542,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // kernel does not write them); q, K, V and every output wait.
   if (!p.early_metadata) {
     grid_dep_wait();
-    if (tid < p.batch) L_first = p.seq_lens[tid];
+    if (tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, tid);
   }
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
@@ -547,8 +560,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     auto packed = [](int T) { return static_cast<long long>(T) | (static_cast<long long>(T > 0) << 32); };
     long long loc = 0;
     // L_first (read above) is reused by the segment scan below
-    loc += packed(tiles_of(clamp_len(L_first, cap, bad)));
-    for (int b = tid + kThreads; b < p.batch; b += kThreads) loc += packed(tiles_of(clamp_len(p.seq_lens[b], cap, bad)));
+    loc += packed(tiles_of(tid < p.batch ? vlen_from(L_first, p.tokens, tid, cap, bad) : 0));
+    for (int b = tid + kThreads; b < p.batch; b += kThreads)
+      loc += packed(tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, bad)));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     long long tot0 = 0;
     const long long incl0 = block_incl_scan<kThreads, long long>(loc, scratch, tot0);
@@ -582,7 +596,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       // one sequence per thread: its tiles are [S, S + T) of the first scan; the sequences
       // overlapping the CTA are numbered by a ballot count
       bool dummy = false;
-      const int L = (tid < p.batch) ? clamp_len(L_first, cap, dummy) : 0;
+      const int L = (tid < p.batch) ? vlen_from(L_first, p.tokens, tid, cap, dummy) : 0;
       const int T = tiles_of(L);
       const long long ex = incl0 - packed(T);
       const int S = static_cast<int>(ex & 0xFFFFFFFFll), Nb = static_cast<int>(ex >> 32);
@@ -617,7 +631,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       for (int c0 = 0; c0 < p.batch && cost_of(carry) <= X1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
-        const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
+        const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) : 0;
         const int T = tiles_of(L);
         long long tot = 0;
         const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -635,7 +649,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         for (int c0 = 0; c0 < p.batch && (carry & 0xFFFFFFFFll) < t1; c0 += kThreads) {
           const int b = c0 + tid;
           bool dummy = false;
-          const int L = (b < p.batch) ? clamp_len(c0 == 0 ? L_first : p.seq_lens[b], cap, dummy) : 0;
+          const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) : 0;
           const int T = tiles_of(L);
           long long tot = 0;
           const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -675,7 +689,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       const int4 sg = seg[s];
       const int j = sg.y + (n - seg_n0[s]);
       const int r0 = min(kPage, sg.w - kTile * j), r1 = min(kPage, sg.w - kTile * j - kPage);
-      const int32_t* row = p.block_table + static_cast<size_t>(sg.x) * p.max_pages;
+      const int32_t* row = p.block_table + static_cast<size_t>(sg.x / p.tokens) * p.max_pages;
       int b0 = row[2 * j];
       int b1 = (r1 > 0) ? row[2 * j + 1] : 0;
       // an id outside the pool is reported and replaced by page 0, so every TMA coordinate
@@ -983,7 +997,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       bool dummy = false;
-      if (clamp_len(p.seq_lens[b], cap, dummy) != 0) continue;
+      if (vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) != 0) continue;
       const int esz = p.out_f32 ? 4 : 2;
       uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * kH * kD * esz);
       for (int i = ts; i < kH * kD * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
@@ -1446,7 +1460,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   int before = 0, total = 0, nb = 0, nt = 0;
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
     bool dummy = false;
-    const int T = tiles_of(clamp_len(p.seq_lens[i], cap, dummy));
+    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, i), p.tokens, i, cap, dummy));
     total += T;
     nt += (T > 0);
     before += (i < b) ? T : 0;
@@ -1474,7 +1488,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
     nt += red_nt[w];
   }
   bool dummy = false;
-  const int Tb = tiles_of(clamp_len(p.seq_lens[b], cap, dummy));
+  const int Tb = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy));
   if (Tb == 0) return;
   const long long C = 4LL * total + 3LL * max(nt - 1, 0);
   const long long base = 4LL * before + 3LL * nb;   // cost of sequence b's first tile
@@ -1670,22 +1684,29 @@ static long long max_cta_tiles(const std::vector<long long>& Tall, long long G) 
   return most;
 }
 
+// The (sequence, new query token) pairs the kernels treat as sequences: B * T.
+static long long vbatch(const mfa_problem* pr) {
+  return static_cast<long long>(pr->batch) * pr->tokens_per_seq;
+}
+
 mfa_status check_problem(const mfa_problem* pr) {
   if (pr == nullptr) return MFA_ERR_INVALID_ARG;
+  if (pr->tokens_per_seq < 1 || pr->tokens_per_seq > kMaxTokensPerSeq) return MFA_ERR_INVALID_ARG;
   if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
   if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;
   if (pr->out_dtype != MFA_OUT_BF16 && pr->out_dtype != MFA_OUT_FP32) return MFA_ERR_INVALID_ARG;
   if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
   if (pr->num_q_heads != kH || pr->head_dim != kD || pr->page_size != kPage) return MFA_ERR_UNSUPPORTED;
   if (static_cast<long long>(pr->max_pages_per_seq) * kPage > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
-  if (static_cast<long long>(pr->batch) * kH > INT_MAX) return MFA_ERR_INVALID_ARG;
+  if (vbatch(pr) * kH > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   return MFA_OK;
 }
 
 static mfa_status check_plan(const mfa_plan* pl, const mfa_problem* pr) {
   if (pl == nullptr) return MFA_ERR_INVALID_ARG;
-  if (pl->batch != pr->batch || pl->kv_dtype != pr->kv_dtype) return MFA_ERR_INVALID_ARG;
-  if (pl->num_ctas < 1 || pl->num_partials != pr->batch + pl->num_ctas - 1) return MFA_ERR_INVALID_ARG;
+  if (pl->batch != pr->batch || pl->kv_dtype != pr->kv_dtype || pl->tokens_per_seq != pr->tokens_per_seq)
+    return MFA_ERR_INVALID_ARG;
+  if (pl->num_ctas < 1 || pl->num_partials != vbatch(pr) + pl->num_ctas - 1) return MFA_ERR_INVALID_ARG;
   if (pl->workspace_bytes != workspace_bytes_for(pl->num_partials)) return MFA_ERR_INVALID_ARG;
   return MFA_OK;
 }
@@ -1695,7 +1716,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   auto enc = encode_fn();
   if (enc == nullptr) return cuda_fail_msg("cuTensorMapEncodeTiled is not available from the driver");
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(pr->batch) * kH};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(vbatch(pr)) * kH};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
     cuuint32_t box[2] = {64, 64};
     cuuint32_t es[2] = {1, 1};
@@ -1735,15 +1756,15 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.out = out;
   cp.out_f32 = pr->out_dtype == MFA_OUT_FP32 ? 1 : 0;
   cp.lse = lse;
-  cp.batch = pr->batch;
+  cp.batch = static_cast<int>(vbatch(pr));
+  cp.tokens = pr->tokens_per_seq;
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
   cudaLaunchConfig_t cfg = {};
   // about two CTAs per SM: many sequences -> more heads per CTA
   const long long want = 2LL * (pl->num_sms > 0 ? pl->num_sms : 148);
-  cp.heads_per_cta = (static_cast<long long>(pr->batch) * kH >= 16 * want) ? 16
-                     : (static_cast<long long>(pr->batch) * kH >= 4 * want) ? 4 : 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(pr->batch), kH / cp.heads_per_cta, 1);
+  cp.heads_per_cta = (vbatch(pr) * kH >= 16 * want) ? 16 : (vbatch(pr) * kH >= 4 * want) ? 4 : 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(vbatch(pr)), kH / cp.heads_per_cta, 1);
   cfg.blockDim = dim3(kCombineThreads, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
@@ -1785,18 +1806,25 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   if (st != MFA_OK) return st;
   if (plan == nullptr || force_ctas < 0) return MFA_ERR_INVALID_ARG;
   const long long cap = static_cast<long long>(pr->max_pages_per_seq) * kPage;
-  std::vector<long long> T(static_cast<size_t>(pr->batch));
+  const int nt = pr->tokens_per_seq;
+  const long long Bv = vbatch(pr);
+  // tiles of each (sequence, new token) pair: query token i of a sequence of L tokens attends
+  // to its first L - T + 1 + i
+  std::vector<long long> T(static_cast<size_t>(Bv));
   long long W = 0;
   if (host_seq_lens != nullptr) {
     for (int b = 0; b < pr->batch; ++b) {
       if (host_seq_lens[b] < 0 || host_seq_lens[b] > cap) return MFA_ERR_INVALID_ARG;
-      T[b] = (host_seq_lens[b] + kTile - 1) / kTile;
-      W += T[b];
+      for (int i = 0; i < nt; ++i) {
+        const long long L = std::max(0ll, static_cast<long long>(host_seq_lens[b]) - (nt - 1 - i));
+        T[static_cast<size_t>(b) * nt + i] = (L + kTile - 1) / kTile;
+        W += T[static_cast<size_t>(b) * nt + i];
+      }
     }
   } else {
     if (max_seq_len < 0 || max_seq_len > cap) return MFA_ERR_INVALID_ARG;
-    for (int b = 0; b < pr->batch; ++b) T[b] = (max_seq_len + kTile - 1) / kTile;
-    W = static_cast<long long>(pr->batch) * ((max_seq_len + kTile - 1) / kTile);
+    for (long long x = 0; x < Bv; ++x) T[static_cast<size_t>(x)] = (max_seq_len + kTile - 1) / kTile;
+    W = Bv * ((max_seq_len + kTile - 1) / kTile);
   }
   if (num_sms <= 0) {
     int dev = 0;
@@ -1815,7 +1843,7 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   }
   // planned from a bound, any shorter mix must fit too: a CTA's cost range of at most
   // ceil(C / G) units holds at most ceil(ceil(C / G) / 4) tiles
-  const long long Cb = 4 * W + 3 * std::max(static_cast<long long>(pr->batch) - 1, 0ll);
+  const long long Cb = 4 * W + 3 * std::max(Bv - 1, 0ll);
   auto worst = [&](long long g) {
     const long long exact = max_cta_tiles(T, g);
     return host_seq_lens != nullptr ? exact : std::max(exact, ((Cb + g - 1) / g + 3) / 4);
@@ -1826,13 +1854,14 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
     ++G;
     most = worst(G);
   }
-  if (G > INT_MAX / 2 || static_cast<long long>(pr->batch) + G - 1 > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
+  if (G > INT_MAX / 2 || Bv + G - 1 > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_ctas = static_cast<int32_t>(G);
   plan->tile_tokens = kTile;
   plan->max_tiles_per_cta = static_cast<int32_t>(most);
-  plan->num_partials = static_cast<int32_t>(pr->batch + G - 1);
+  plan->num_partials = static_cast<int32_t>(Bv + G - 1);
   plan->batch = pr->batch;
+  plan->tokens_per_seq = pr->tokens_per_seq;
   plan->kv_dtype = pr->kv_dtype;
   plan->flags = flags;
   plan->num_sms = num_sms;
@@ -1889,7 +1918,8 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.part_o = reinterpret_cast<float*>(ws + partial_o_offset());
   prm.part_lse = reinterpret_cast<float*>(ws + partial_lse_offset(plan->num_partials));
   prm.status = reinterpret_cast<unsigned int*>(ws);
-  prm.batch = pr->batch;
+  prm.batch = static_cast<int>(vbatch(pr));
+  prm.tokens = pr->tokens_per_seq;
   prm.max_pages = pr->max_pages_per_seq;
   prm.num_blocks = pr->num_blocks;
   prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
@@ -1940,9 +1970,9 @@ mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* pr, cons
   if (st != MFA_OK || pr->batch == 0) return st;
   if (!q_host || !block_table_host || !seq_lens_host || !out_host) return MFA_ERR_INVALID_ARG;
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return MFA_ERR_INVALID_ARG;
-  const size_t B = static_cast<size_t>(pr->batch);
-  const size_t q_bytes = B * kH * kD * 2, table_bytes = B * pr->max_pages_per_seq * 4, lens_bytes = B * 4;
-  const size_t out_bytes = B * kH * kD * (pr->out_dtype == MFA_OUT_FP32 ? 4 : 2), lse_bytes = B * kH * 4;
+  const size_t B = static_cast<size_t>(pr->batch), Bv = static_cast<size_t>(vbatch(pr));
+  const size_t q_bytes = Bv * kH * kD * 2, table_bytes = B * pr->max_pages_per_seq * 4, lens_bytes = B * 4;
+  const size_t out_bytes = Bv * kH * kD * (pr->out_dtype == MFA_OUT_FP32 ? 4 : 2), lse_bytes = Bv * kH * 4;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
   if ((e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||

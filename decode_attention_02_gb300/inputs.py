@@ -13,7 +13,7 @@ with 64-token pages.
 Recipe (fixed seeds, numpy PCG64 via ``default_rng``), in draw order:
   1. lengths: given, or uniform integers in [lo, hi] inclusive;
   2. physical page order: identity ("contiguous") or ``rng.permutation``;
-  3. q ~ N(0,1) fp32 [B, H, d];
+  3. q ~ N(0,1) fp32 [B*T, H, d] (T new query tokens per sequence, 1 unless stated);
   4. K pool ~ N(0,1) fp32 [num_blocks, page, d], drawn in chunks of
      ``_CHUNK_BLOCKS`` pages; optionally each scalar K element is multiplied
      by ``k_spike_mult`` with independent probability ``k_spike_frac``
@@ -62,6 +62,7 @@ class Workload:
     head_dim: int = HEAD_DIM
     page_size: int = PAGE_SIZE
     softmax_scale: Optional[float] = None       # None -> 1/sqrt(head_dim)
+    tokens_per_seq: int = 1                     # T new query tokens per sequence (multi-token decode)
 
     def scale(self) -> float:
         if self.softmax_scale is not None:
@@ -87,6 +88,9 @@ WORKLOADS = {
     "long_b4_l131072_fp8": Workload(
         "long_b4_l131072_fp8", batch=4, lens=(131072, 131072, 65536, 16384),
         kv_dtype="fp8_e4m3", seed=6),
+    # multi-token decode: two new query tokens per sequence, causal among them
+    "mtp2_b32_l4096_bf16": Workload(
+        "mtp2_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=7, tokens_per_seq=2),
 }
 
 
@@ -94,7 +98,7 @@ WORKLOADS = {
 class Case:
     """Host tensors of one decode step (all torch CPU tensors, contiguous)."""
     workload: Workload
-    q: torch.Tensor             # bf16 [B, H, d]
+    q: torch.Tensor             # bf16 [B*T, H, d] (T = workload.tokens_per_seq)
     k_cache: torch.Tensor       # bf16 [nb, page, d] or uint8 e4m3 codes
     v_cache: torch.Tensor
     k_scale: Optional[torch.Tensor]   # fp32 [nb, page] (FP8 only)
@@ -163,7 +167,7 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
     else:
         perm = rng.permutation(nb)
 
-    q = rng.standard_normal((B, H, d), dtype=np.float32)
+    q = rng.standard_normal((B * w.tokens_per_seq, H, d), dtype=np.float32)
     kf = _draw_pool(rng, nb, page, d, w.k_spike_frac, w.k_spike_mult)
     vf = _draw_pool(rng, nb, page, d, 0.0, 1.0)
 
@@ -228,12 +232,13 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
 def small(name: str, batch: int, lens: Sequence[int], kv_dtype: str = "bf16", seed: int = 100,
           layout: str = "shuffled", extra_blocks: int = 2, k_spike_frac: float = 0.0,
           softmax_scale: Optional[float] = None, num_q_heads: int = NUM_Q_HEADS,
-          head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE) -> Case:
+          head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, tokens_per_seq: int = 1) -> Case:
     """A small poisoned case for parity tests (explicit lengths)."""
     w = Workload(name, batch=batch, lens=tuple(int(x) for x in lens), kv_dtype=kv_dtype,
                  layout=layout, seed=seed, extra_blocks=extra_blocks,
                  k_spike_frac=k_spike_frac, softmax_scale=softmax_scale,
-                 num_q_heads=num_q_heads, head_dim=head_dim, page_size=page_size)
+                 num_q_heads=num_q_heads, head_dim=head_dim, page_size=page_size,
+                 tokens_per_seq=tokens_per_seq)
     return generate(w)
 
 

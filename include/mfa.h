@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MFA_ABI_VERSION 1
+#define MFA_ABI_VERSION 2
 
 typedef enum mfa_status {
     MFA_OK = 0,
@@ -98,19 +98,34 @@ typedef struct mfa_problem {
     int32_t kv_dtype;          /* mfa_kv_dtype */
     float softmax_scale;       /* finite, > 0; 1/sqrt(256) = 0.0625 for MFA */
     int32_t out_dtype;         /* mfa_out_dtype */
+    int32_t tokens_per_seq;    /* T new query tokens per sequence, 1..4 (see below) */
 } mfa_problem;
+
+/*
+ * Multi-token decode (tokens_per_seq = T > 1, as in multi-token prediction or speculative
+ * decoding; Step-3 page section 5 "Model-System Co-design": MTP raises the arithmetic
+ * intensity).  The T new tokens of sequence b are the last T of its L_b cached tokens (their
+ * K and V already appended), and query token i (0 <= i < T) attends to the cached tokens
+ * 0 .. L_b - T + i: each new token sees the cache and the new tokens up to itself (causal).
+ * q and out are [B, T, 64, 256] (equivalently [B*T, 64, 256]) and lse is [B, T, 64];
+ * block_table and seq_lens stay per sequence.  A query token whose range is empty
+ * (L_b - T + i < 0) gets out = 0 and lse = -inf.  The pair (b, i) is computed as its own
+ * sequence of length L_b - T + 1 + i over b's block-table row, so its KV pages are read once
+ * per query token (mostly from L2, the T pairs being adjacent in the schedule).
+ */
 
 typedef struct mfa_plan {
     int32_t num_ctas;          /* decode grid size G (persistent CTAs) */
     int32_t tile_tokens;       /* tokens per pipeline tile (128) */
     int32_t max_tiles_per_cta; /* most tiles one CTA gets for the lengths planned with (<= 128) */
-    int32_t num_partials;      /* partial-result slots in the workspace: B + G - 1 */
+    int32_t num_partials;      /* partial-result slots in the workspace: B*T + G - 1 */
     int32_t batch;             /* copy of problem->batch (checked by run) */
     int32_t kv_dtype;          /* copy of problem->kv_dtype (checked by run) */
     uint32_t flags;            /* MFA_PLAN_* */
     int32_t num_sms;           /* SM count the plan was made for */
     uint64_t total_tiles;      /* 128-token tiles of the batch as planned */
     uint64_t workspace_bytes;  /* device bytes the caller must pass to run/combine */
+    int32_t tokens_per_seq;    /* copy of problem->tokens_per_seq (checked by run) */
 } mfa_plan;
 
 /*

@@ -147,7 +147,9 @@ def _ptr(a):
 def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
            softmax_scale: Optional[float] = None, batch_slice: Optional[slice] = None,
            lib=None):
-    """Oracle decode of ``case`` -> (out float64 [B,H,d], lse float64 [B,H]).
+    """Oracle decode of ``case`` -> (out float64 [B*T,H,d], lse float64 [B*T,H]).
+
+    T = case.workload.tokens_per_seq new query tokens per sequence (1: one each).
 
     ``t_begin``/``t_end`` (int sequences of length B) restrict each sequence to
     a token range; ``batch_slice`` restricts the batch (for bounded samples).
@@ -157,6 +159,14 @@ def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
     q = _np(case.q)
     table = _np(case.block_table).astype(np.int32)
     lens = _np(case.seq_lens).astype(np.int32)
+    T = int(getattr(w, "tokens_per_seq", 1))
+    if T > 1:
+        # multi-token decode: the T new tokens are the last T cached ones, and query token i
+        # of sequence b attends to its cached tokens 0 .. L_b - T + i (causal among the new
+        # tokens).  Each (b, i) is then an ordinary decode over b's block-table row.
+        i = np.tile(np.arange(T), len(lens))
+        table = np.ascontiguousarray(np.repeat(table, T, axis=0))
+        lens = np.ascontiguousarray(np.maximum(0, np.repeat(lens, T) - (T - 1 - i)).astype(np.int32))
     if batch_slice is not None:
         q, table, lens = q[batch_slice], table[batch_slice], lens[batch_slice]
         q, table, lens = (np.ascontiguousarray(x) for x in (q, table, lens))

@@ -28,7 +28,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(mfa.EXPORTED_SYMBOLS)
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
-    assert lib.mfa_abi_version() == 1
+    assert lib.mfa_abi_version() == 2
 
 
 def test_status_strings(lib):

@@ -352,3 +352,46 @@ def test_host_buffer_steps_on_two_streams_match_the_device_path(kv_dtype):
     for o_h, l_h in outs:
         assert torch.equal(o_h.view(torch.int16), ref_out.cpu().view(torch.int16))
         assert torch.equal(l_h, ref_lse.cpu())
+
+
+def gpu_decode_mtp(case, force_ctas=0, out_dtype=mfa.MFA_OUT_FP32, flags=mfa.MFA_PLAN_CHECK):
+    t = to_dev(case)
+    kv = mfa.MFA_KV_FP8_E4M3 if case.workload.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    T = case.workload.tokens_per_seq
+    dec = mfa.Decoder(case.seq_lens.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv,
+                      softmax_scale=case.workload.scale(), host_seq_lens=case.seq_lens.tolist(),
+                      force_ctas=force_ctas, flags=flags, out_dtype=out_dtype, tokens_per_seq=T)
+    out, lse = dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
+                   k_scale=t["k_scale"], v_scale=t["v_scale"])
+    torch.cuda.synchronize()
+    return out, lse, dec
+
+
+@pytest.mark.parametrize("T", [2, 3, 4])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("force_ctas", [0, 1, 7])
+def test_multi_token_decode(T, kv_dtype, force_ctas):
+    """T new query tokens per sequence, causal among themselves: lengths below T leave some
+    query tokens with nothing to attend to (out 0, lse -inf)."""
+    lens = [1, 2, 3, 0, 64, 65, 130, 257, 700, 4]
+    case = inputs.small("mtp", len(lens), lens, kv_dtype=kv_dtype, seed=80 + T, tokens_per_seq=T)
+    out, lse, dec = gpu_decode_mtp(case, force_ctas=force_ctas)
+    assert out.shape[0] == len(lens) * T
+    if kv_dtype == "bf16":
+        check_parity(case, out, lse)
+    else:
+        check_parity(case, out, lse, max_abs=3e-2, rel_l2=1.5e-2)
+
+
+def test_multi_token_decode_full_size():
+    """Two new tokens for each of 32 sequences of 4096: the benchmark's MTP workload, checked
+    on a sample of sequences (the oracle runs per (sequence, token) pair)."""
+    case = inputs.generate(inputs.WORKLOADS["mtp2_b32_l4096_bf16"])
+    out, lse, dec = gpu_decode_mtp(case, flags=mfa.MFA_PLAN_CHECK | mfa.MFA_PLAN_EARLY_METADATA)
+    sample = slice(0, 8)   # the first four sequences' two tokens each
+    ref_o, ref_lse = oracle.decode(case, batch_slice=sample)
+    got = out[sample].cpu().double().numpy()
+    err = np.abs(got - ref_o)
+    assert err.max() <= BF16_MAX_ABS
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= BF16_REL_L2
+    assert np.abs(lse[sample].cpu().double().numpy() - ref_lse).max() <= LSE_ABS

@@ -363,3 +363,56 @@ def test_mutants_are_caught():
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
                                    "-o", so, path, "-lm"])
             assert not _run_pins(oracle.load_library(so)), f"mutant {name} survived the pins"
+
+
+# ------------------------------------------------------------- multi-token decode
+
+def dense_mtp_reference(case):
+    """Multi-token decode written with an explicit causal mask over a dense gather: the T new
+    tokens are the last T cached ones, and query token i may see key t only if t <= L - T + i."""
+    w = case.workload
+    T = w.tokens_per_seq
+    B = case.seq_lens.shape[0]
+    H, d = case.q.shape[1], case.q.shape[2]
+    out = np.zeros((B * T, H, d))
+    lse = np.full((B * T, H), -np.inf)
+    for b in range(B):
+        L = int(case.seq_lens[b])
+        if L == 0:
+            continue
+        K, V = dense_kv(case, b)
+        K, V = K.numpy(), V.numpy()
+        for i in range(T):
+            q = case.q[b * T + i].to(torch.float64).numpy()
+            s = (q @ K.T) * w.scale()                      # [H, L]
+            visible = np.arange(L) <= L - T + i
+            if not visible.any():
+                continue
+            s = np.where(visible[None, :], s, -np.inf)
+            lse[b * T + i] = scipy.special.logsumexp(s, axis=1)
+            out[b * T + i] = np.exp(s - lse[b * T + i][:, None]) @ V
+    return out, lse
+
+
+@pytest.mark.parametrize("T", [2, 3, 4])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_multi_token_decode_matches_an_explicit_causal_mask(T, kv):
+    case = inputs.small("mtp", 5, [1, 2, 65, 130, 3], kv_dtype=kv, seed=170 + T, tokens_per_seq=T)
+    out, lse = oracle.decode(case)
+    ro, rl = dense_mtp_reference(case)
+    assert_close(out, ro)
+    assert np.array_equal(np.isneginf(lse), np.isneginf(rl))
+    fin = np.isfinite(rl)
+    assert np.abs(lse[fin] - rl[fin]).max() <= TOL
+
+
+def test_multi_token_decode_last_token_is_the_ordinary_decode():
+    """Query token T - 1 sees the whole cache: it is the single-token decode of its q."""
+    T = 3
+    case = inputs.small("mtp_last", 4, [7, 64, 200, 129], seed=183, tokens_per_seq=T)
+    out, lse = oracle.decode(case)
+    single = inputs.Case(workload=inputs.Workload("single", batch=4, lens=(7, 64, 200, 129)),
+                         q=case.q[T - 1::T].contiguous(), k_cache=case.k_cache, v_cache=case.v_cache,
+                         k_scale=None, v_scale=None, block_table=case.block_table, seq_lens=case.seq_lens)
+    o1, l1 = oracle.decode(single)
+    assert np.array_equal(out[T - 1::T], o1) and np.array_equal(lse[T - 1::T], l1)
