@@ -712,7 +712,11 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     // lane; groups go out strictly in ring order, so every slot's phases stay in step.
     if (ntiles > 0) {
       if (p.early_metadata) grid_dep_wait();
-      const uint64_t pol = l2_policy_evict_first();
+      // KV is streamed once: evict first.  Multi-token decode reads a sequence's pages once
+      // per query token, the pairs back to back, so all but the last query token's reads keep
+      // the lines (evict last) for the next one.
+      const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_last();
+      int seg_k = 0, seg_v = 0;   // segment of the producer's current K and V tiles
       const bool act = lane < 4;
       const int c = lane & 3;
       bool ok = true;
@@ -723,6 +727,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       // d-half c >> 1; V: page c >> 1, d-half c & 1)
       auto group = [&](bool is_v, int t) -> bool {
         bool okl = true;
+        int& sc_ = is_v ? seg_v : seg_k;
+        while (sc_ + 1 < nseg && seg_n0[sc_ + 1] <= t) ++sc_;
+        const uint64_t pol = (p.tokens > 1 && seg[sc_].x % p.tokens != p.tokens - 1) ? pol_again : pol_once;
         if (act) {
           const int4 ti = tile_info[t];
           const uint32_t u = ring_use(t, ntiles, is_v, 0, 0) + c;
