@@ -248,7 +248,8 @@ def mfa_kv_append(problem: MfaProblem, k_new, v_new, positions, block_table, k_c
                   v_scale=None, device_status=None, stream=None) -> None:
     """Write each sequence's new key/value row into the paged cache (FP8: quantised).
 
-    k_new/v_new: bf16 [B, 256]; positions: int32 [B] (token index, < 0 = none);
+    k_new/v_new: bf16 [B*T, 256] (T = problem.tokens_per_seq new rows per sequence);
+    positions: int32 [B] (index of each sequence's first new row, < 0 = none);
     device_status: a uint32 device tensor (or a decode workspace, whose first word is
     the status word) that collects bad-position / bad-page bits, or None.
     """

@@ -6,7 +6,7 @@
 // scale per row, s = absmax / 448 (1 for an all-zero row), and e4m3 codes of x / s, rounded
 // to nearest even and saturated to +-448; the format the decode kernel reads.
 //
-// The work is 2B independent rows of 256 values (512 bytes of bf16 in; 512 bytes of bf16
+// The work is 2BT independent rows of 256 values (T new tokens per sequence) (512 bytes of bf16 in; 512 bytes of bf16
 // or 260 bytes of codes and scale out), so it is a latency-bound scatter: one warp per
 // row, one 16-byte load and one 16- or 8-byte store per lane, a warp max for the scale;
 // the row's load is issued before the dependent position and page-id loads.
@@ -37,6 +37,7 @@ struct AppendParams {
   float* v_scale;
   unsigned int* status;    // may be null
   int batch;
+  int tokens;              // new rows per sequence T: row pairs (b, i) = (x / T, x % T)
   int max_pages;
   int num_blocks;
   int fp8;
@@ -59,15 +60,16 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mfa_kv_append_kernel(const 
   grid_dep_wait();
   grid_dep_launch();
   const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);   // row: sequence r / 2, K or V
-  if (r >= 2 * p.batch) return;
-  const int b = r >> 1;
+  const int r = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);   // row: new token r / 2, K or V
+  if (r >= 2 * p.batch * p.tokens) return;
+  const int xr = r >> 1, b = xr / p.tokens, i = xr % p.tokens;   // token i of sequence b
   const bool is_v = (r & 1) != 0;
   // lane l holds elements 8l .. 8l+7 of the row; the load is issued first, so that it
   // overlaps the position -> page id chain
-  const uint4 x = __ldg((is_v ? p.v_new : p.k_new) + static_cast<size_t>(b) * (kAppendRowLen / 8) + lane);
-  const int t = p.positions[b];
-  if (t < 0) return;                                    // no new token for this sequence
+  const uint4 x = __ldg((is_v ? p.v_new : p.k_new) + static_cast<size_t>(xr) * (kAppendRowLen / 8) + lane);
+  const int t0 = p.positions[b];
+  if (t0 < 0) return;                                   // no new token for this sequence
+  const int t = t0 + i;
   if (t >= p.max_pages * kAppendPage) {
     if (lane == 0 && !is_v && p.status) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     return;
@@ -128,11 +130,12 @@ extern "C" mfa_status mfa_kv_append(const mfa_problem* pr, const void* k_new, co
   p.v_scale = fp8 ? v_scale : nullptr;
   p.status = device_status;
   p.batch = pr->batch;
+  p.tokens = pr->tokens_per_seq;
   p.max_pages = pr->max_pages_per_seq;
   p.num_blocks = pr->num_blocks;
   p.fp8 = fp8 ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
-  const long long rows = 2LL * pr->batch;
+  const long long rows = 2LL * pr->batch * pr->tokens_per_seq;
   cfg.gridDim = dim3(static_cast<unsigned>((rows + kAppendWarps - 1) / kAppendWarps), 1, 1);
   cfg.blockDim = dim3(32 * kAppendWarps, 1, 1);
   cfg.dynamicSmemBytes = 0;

@@ -292,22 +292,25 @@ def new_token_rows(batch: int, d: int = HEAD_DIM, seed: int = 0, kinds: Sequence
 
 
 def append_step(case: Case, seed: int = 0, inactive_every: int = 0,
-                kinds: Sequence[str] = ROW_KINDS) -> AppendStep:
-    """New rows for every sequence of ``case``, written at position seq_lens[b] - 1.
+                kinds: Sequence[str] = ROW_KINDS, tokens_per_seq: int = 1) -> AppendStep:
+    """New rows for every sequence of ``case``, written at its last position(s).
 
     Build ``case`` for the lengths after the append (each sequence one token longer), so
     its block table already holds the page of the new token, as a serving system
     allocates it before the step; the slot's old contents are then overwritten.  With
     inactive_every = n > 0, every n-th sequence (b % n == n - 1) has no new token
     (position -1).  k rows use ``seed``, v rows ``seed + 1``; ``kinds`` as for
-    new_token_rows (("normal",) for rows inside the FP8 decode's V-scale range).
+    new_token_rows (("normal",) for rows inside the FP8 decode's V-scale range).  With
+    tokens_per_seq = T, each sequence gets T new rows ([B*T, d], sequence-major) at positions
+    L - T .. L - 1; positions[b] is the first of them.
     """
-    B = case.q.shape[0]
+    B = case.seq_lens.shape[0]
     d = case.q.shape[2]
-    pos = case.seq_lens.to(torch.int64) - 1
+    T = int(tokens_per_seq)
+    pos = case.seq_lens.to(torch.int64) - T
     if inactive_every > 0:
         idx = torch.arange(B)
         pos[idx % inactive_every == inactive_every - 1] = -1
-    pos[case.seq_lens <= 0] = -1
-    return AppendStep(k_new=new_token_rows(B, d, seed, kinds), v_new=new_token_rows(B, d, seed + 1, kinds),
+    pos[case.seq_lens < T] = -1
+    return AppendStep(k_new=new_token_rows(B * T, d, seed, kinds), v_new=new_token_rows(B * T, d, seed + 1, kinds),
                       positions=pos.to(torch.int32).contiguous())

@@ -273,9 +273,10 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  * Enqueue the KV-cache append of one decode step: each sequence's new key row and
  * value row go into the paged cache (the attention instances own and fill their KV
  * caches, Step-3 page section 7 "Implementation and Results"; the cache holds 8-bit
- * KV, section 5 "Model-System Co-design").  For every b with t = positions[b] >= 0,
- * row k_new[b] goes to K slot t % 64 of page block_table[b][t / 64], v_new[b] to the
- * same V slot:
+ * KV, section 5 "Model-System Co-design").  With T = problem->tokens_per_seq new tokens
+ * per sequence, for every b with positions[b] >= 0 and every i < T, row k_new[b*T + i]
+ * goes to K slot t % 64 of page block_table[b][t / 64], t = positions[b] + i, and
+ * v_new[b*T + i] to the same V slot:
  *   - bf16 cache: the bf16 bits, unchanged;
  *   - e4m3 cache (quantisation fused in the same pass): the row's scale
  *     s = absmax / 448 in fp32 (s = 1 for an all-zero row) goes to
@@ -285,9 +286,9 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  *     the code 0x80).  The row maximum always lands on code +-448.
  *   problem      : the decode's problem description (kv_dtype, batch, table width and
  *                  pool size are used); validated as for mfa_decode_plan.
- *   k_new, v_new : device bf16 [B, 256], 16-byte aligned, finite values (non-finite
+ *   k_new, v_new : device bf16 [B, T, 256], 16-byte aligned, finite values (non-finite
  *                  values give unspecified codes and scales).
- *   positions    : device int32 [B]: the token index each sequence's new row takes
+ *   positions    : device int32 [B]: the token index of each sequence's first new row
  *                  (usually its length before the step); a negative entry means no
  *                  new token for that sequence (nothing is written).
  *   block_table  : device int32 [B, max_pages_per_seq]: must already hold the page of
@@ -296,7 +297,7 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  *                  only the target slots change.  Scales NULL for a bf16 cache.
  *   device_status: device uint32, or NULL.  A position >= max_pages_per_seq * 64 sets
  *                  MFA_DEV_BAD_LENGTH, a page id outside [0, num_blocks) sets
- *                  MFA_DEV_BAD_BLOCK; that sequence's rows are then not written.  The
+ *                  MFA_DEV_BAD_BLOCK; that token's rows are then not written.  The
  *                  status word of a decode workspace (offset 0) may be passed, so that
  *                  mfa_read_device_status() reports both steps.
  *   stream       : cudaStream_t.  The kernel is launched as a programmatic dependent

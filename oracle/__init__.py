@@ -61,7 +61,7 @@ def load_library(path: str):
     lib.mfa_oracle_e4m3_from_float.restype = ctypes.c_uint8
     lib.mfa_oracle_e4m3_from_float_array.argtypes = [P, ctypes.c_long, P]
     lib.mfa_oracle_e4m3_from_float_array.restype = None
-    lib.mfa_oracle_kv_append.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+    lib.mfa_oracle_kv_append.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
     lib.mfa_oracle_kv_append.restype = I
     return lib
 
@@ -100,17 +100,19 @@ APPEND_BAD_POSITION = 2
 
 
 def kv_append(k_new, v_new, positions, block_table, k_cache, v_cache, k_scale=None, v_scale=None,
-              page_size: int = 64, lib=None):
+              page_size: int = 64, tokens_per_seq: int = 1, lib=None):
     """Oracle KV append: returns (k_cache, v_cache, k_scale, v_scale, mask), updated copies.
 
-    k_new/v_new: bf16 [B, d] (torch) or uint16 bit arrays; positions: int [B], the token
-    index each sequence's new row goes to (< 0: none); block_table int32 [B, max_pages];
+    k_new/v_new: bf16 [B*T, d] (torch) or uint16 bit arrays, T = tokens_per_seq new rows
+    per sequence; positions: int [B], the token index of each sequence's first new row
+    (row i goes to positions[b] + i; < 0: none); block_table int32 [B, max_pages];
     caches as produced by the input generator (bf16 [nb, page, d], or uint8 e4m3 codes with
     fp32 scales [nb, page]).  The inputs are not modified.
     """
     kn = np.ascontiguousarray(_np(k_new)).view(np.uint16)
     vn = np.ascontiguousarray(_np(v_new)).view(np.uint16)
-    B, d = kn.shape
+    T = int(tokens_per_seq)
+    B, d = kn.shape[0] // T, kn.shape[1]
     pos = np.ascontiguousarray(np.asarray(_np(positions), dtype=np.int32))
     table = np.ascontiguousarray(_np(block_table).astype(np.int32))
     kc = np.array(_np(k_cache), copy=True)
@@ -121,7 +123,7 @@ def kv_append(k_new, v_new, positions, block_table, k_cache, v_cache, k_scale=No
         ks = np.array(_np(k_scale), dtype=np.float32, copy=True)
         vs = np.array(_np(v_scale), dtype=np.float32, copy=True)
     mask = (lib or _load()).mfa_oracle_kv_append(
-        B, d, page_size, table.shape[1], kc.shape[0], 1 if fp8 else 0, _ptr(kn), _ptr(vn), _ptr(pos),
+        B, T, d, page_size, table.shape[1], kc.shape[0], 1 if fp8 else 0, _ptr(kn), _ptr(vn), _ptr(pos),
         _ptr(table), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs))
     if mask < 0:
         raise ValueError("mfa_oracle_kv_append: bad argument")

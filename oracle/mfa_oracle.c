@@ -285,16 +285,17 @@ int mfa_oracle_combine(int S, long R, int d, const double *part_o, const double 
  * attention instances own and fill their KV caches, Step-3 page section 7 "Implementation
  * and Results"; the cache holds 8-bit KV, section 5 "Model-System Co-design").
  *
- * For every sequence b with positions[b] = t >= 0, the new token's key row k_new[b][:] and
- * value row v_new[b][:] (bf16) go to slot t % page of page block_table[b][t / page]:
+ * For every sequence b with positions[b] = t0 >= 0, its T new tokens' key rows
+ * k_new[b*T + i][:] and value rows v_new[b*T + i][:] (bf16), i < T, go to position
+ * t = t0 + i: slot t % page of page block_table[b][t / page]:
  *   - bf16 cache: the bf16 bits unchanged;
  *   - e4m3 cache: one fp32 scale per row, s = absmax / 448 (s = 1 for an all-zero row), and
  *     codes e4m3(x_i / s), x_i the row's bf16 values; both divisions are fp32 divisions
  *     rounded to nearest, and the e4m3 rounding is to the nearest value, ties to the even
  *     code, with magnitudes above 448 saturating to 448.
  * positions[b] < 0: no token for b (nothing written).  t >= max_pages * page, or a page id
- * outside [0, num_blocks): nothing written for b, and bit 1 (position) or bit 0 (page id)
- * of the return mask is set.
+ * outside [0, num_blocks): nothing written for that token, and bit 1 (position) or bit 0
+ * (page id) of the return mask is set.
  */
 
 static float bf16_to_float(uint16_t bits) {
@@ -343,23 +344,24 @@ static void quantise_row(const uint16_t *x, int d, uint8_t *codes, float *scale)
 }
 
 /*
- * k_new/v_new: bf16 bits [B,d]; positions: int32 [B]; block_table: int32 [B,max_pages];
+ * k_new/v_new: bf16 bits [B*T,d]; positions: int32 [B]; block_table: int32 [B,max_pages];
  * k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,d], updated in place;
  * k_scale/v_scale: fp32 [num_blocks,page] (FP8 only), updated in place.
  * Returns the error mask described above (0 = every row written or skipped by choice),
  * or -1 on a bad argument.
  */
-int mfa_oracle_kv_append(int B, int d, int page, int max_pages, int num_blocks, int kv_fp8,
+int mfa_oracle_kv_append(int B, int T, int d, int page, int max_pages, int num_blocks, int kv_fp8,
                          const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
                          const int32_t *block_table, void *k_cache, void *v_cache,
                          float *k_scale, float *v_scale) {
-    if (B < 0 || d <= 0 || page <= 0 || max_pages <= 0 || num_blocks <= 0) return -1;
+    if (B < 0 || T < 1 || d <= 0 || page <= 0 || max_pages <= 0 || num_blocks <= 0) return -1;
     if (!k_new || !v_new || !positions || !block_table || !k_cache || !v_cache) return -1;
     if (kv_fp8 && (!k_scale || !v_scale)) return -1;
     int mask = 0;
-    for (int b = 0; b < B; ++b) {
-        const int t = positions[b];
-        if (t < 0) continue;
+    for (int x = 0; x < B * T; ++x) {
+        const int b = x / T;
+        if (positions[b] < 0) continue;
+        const int t = positions[b] + x % T;
         if (t >= max_pages * page) {
             mask |= 2;
             continue;
@@ -371,11 +373,11 @@ int mfa_oracle_kv_append(int B, int d, int page, int max_pages, int num_blocks, 
         }
         const size_t row = (size_t)blk * page + (size_t)(t % page);
         if (kv_fp8) {
-            quantise_row(k_new + (size_t)b * d, d, (uint8_t *)k_cache + row * d, k_scale + row);
-            quantise_row(v_new + (size_t)b * d, d, (uint8_t *)v_cache + row * d, v_scale + row);
+            quantise_row(k_new + (size_t)x * d, d, (uint8_t *)k_cache + row * d, k_scale + row);
+            quantise_row(v_new + (size_t)x * d, d, (uint8_t *)v_cache + row * d, v_scale + row);
         } else {
-            memcpy((uint16_t *)k_cache + row * d, k_new + (size_t)b * d, (size_t)d * sizeof(uint16_t));
-            memcpy((uint16_t *)v_cache + row * d, v_new + (size_t)b * d, (size_t)d * sizeof(uint16_t));
+            memcpy((uint16_t *)k_cache + row * d, k_new + (size_t)x * d, (size_t)d * sizeof(uint16_t));
+            memcpy((uint16_t *)v_cache + row * d, v_new + (size_t)x * d, (size_t)d * sizeof(uint16_t));
         }
     }
     return mask;

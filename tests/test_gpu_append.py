@@ -22,9 +22,10 @@ def kv_of(case):
     return mfa.MFA_KV_FP8_E4M3 if case.workload.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
 
 
-def gpu_append(case, step, positions=None, block_table=None, status=None):
+def gpu_append(case, step, positions=None, block_table=None, status=None, tokens_per_seq=1):
     dev = "cuda"
-    pr = mfa.make_problem(case.q.shape[0], case.max_pages, case.num_blocks, kv_of(case))
+    pr = mfa.make_problem(case.seq_lens.shape[0], case.max_pages, case.num_blocks, kv_of(case),
+                          tokens_per_seq=tokens_per_seq)
     kc, vc = case.k_cache.to(dev), case.v_cache.to(dev)
     ks = None if case.k_scale is None else case.k_scale.to(dev)
     vs = None if case.v_scale is None else case.v_scale.to(dev)
@@ -47,10 +48,10 @@ def as_bits(t):
     return t.numpy()
 
 
-def oracle_append(case, step, positions=None, block_table=None):
+def oracle_append(case, step, positions=None, block_table=None, tokens_per_seq=1):
     return oracle.kv_append(step.k_new, step.v_new, step.positions if positions is None else positions,
                             case.block_table if block_table is None else block_table, case.k_cache, case.v_cache,
-                            case.k_scale, case.v_scale)
+                            case.k_scale, case.v_scale, tokens_per_seq=tokens_per_seq)
 
 
 def assert_pools_equal(got, want):
@@ -148,3 +149,54 @@ def test_append_then_decode_sees_the_new_token(kv_dtype, flags):
     assert np.abs(got - ref_o).max() <= tol[0]
     assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= tol[1]
     assert np.abs(lse.cpu().double().numpy() - ref_lse).max() <= 2e-3
+
+
+@pytest.mark.parametrize("T", [2, 3])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_append_of_several_tokens_matches_oracle(T, kv_dtype):
+    """Multi-token step: T new rows per sequence at positions[b] .. positions[b] + T - 1, some
+    across a page boundary, some sequences too short to hold T (skipped)."""
+    lens = [1, 2, 64, 65, 66, 128, 130, 300, 3, 0]
+    case = inputs.small("append_t", len(lens), lens, kv_dtype=kv_dtype, seed=93 + T, tokens_per_seq=T)
+    step = inputs.append_step(case, seed=94, tokens_per_seq=T)
+    want = oracle_append(case, step, tokens_per_seq=T)
+    assert want[4] == 0
+    assert_pools_equal(gpu_append(case, step, tokens_per_seq=T), want)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_multi_token_append_then_decode(kv_dtype):
+    """A multi-token step on one stream: append the T new rows, then decode the T query tokens
+    (causal among them), against the oracle's decode over the oracle-appended cache."""
+    T = 2
+    case = inputs.small("mtp_step", len(RAGGED), RAGGED, kv_dtype=kv_dtype, seed=95, tokens_per_seq=T)
+    step = inputs.append_step(case, seed=96, tokens_per_seq=T, kinds=("normal",))
+    kc, vc, ks, vs, mask = oracle_append(case, step, tokens_per_seq=T)
+    assert mask == 0
+    appended = inputs.Case(workload=case.workload, q=case.q,
+                           k_cache=torch.from_numpy(kc).view(case.k_cache.dtype),
+                           v_cache=torch.from_numpy(vc).view(case.v_cache.dtype),
+                           k_scale=None if ks is None else torch.from_numpy(ks),
+                           v_scale=None if vs is None else torch.from_numpy(vs),
+                           block_table=case.block_table, seq_lens=case.seq_lens)
+    ref_o, ref_lse = oracle.decode(appended)
+    dev = "cuda"
+    t = dict(q=case.q.to(dev), k=case.k_cache.to(dev), v=case.v_cache.to(dev), table=case.block_table.to(dev),
+             lens=case.seq_lens.to(dev), ks=None if case.k_scale is None else case.k_scale.to(dev),
+             vs=None if case.v_scale is None else case.v_scale.to(dev))
+    dec = mfa.Decoder(case.seq_lens.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv_of(case),
+                      host_seq_lens=case.seq_lens.tolist(), flags=mfa.MFA_PLAN_EARLY_METADATA,
+                      out_dtype=mfa.MFA_OUT_FP32, tokens_per_seq=T)
+    mfa.mfa_read_device_status(dec.workspace, clear=True)
+    mfa.mfa_kv_append(dec.problem, step.k_new.to(dev), step.v_new.to(dev), step.positions.to(dev), t["table"],
+                      t["k"], t["v"], t["ks"], t["vs"], device_status=dec.workspace)
+    out, lse = dec(t["q"], t["k"], t["v"], t["table"], t["lens"], k_scale=t["ks"], v_scale=t["vs"])
+    torch.cuda.synchronize()
+    assert mfa.mfa_read_device_status(dec.workspace) == 0
+    got = out.cpu().double().numpy()
+    tol = (1e-2, 5e-3) if kv_dtype == "bf16" else (3e-2, 1.5e-2)
+    assert np.abs(got - ref_o).max() <= tol[0]
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= tol[1]
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isneginf(lse.cpu().numpy()), np.isneginf(ref_lse))
+    assert np.abs(lse.cpu().double().numpy()[fin] - ref_lse[fin]).max() <= 2e-3

@@ -184,8 +184,38 @@ def check_error_masks(lib=None):
     assert np.array_equal(ks2.view(np.uint32), case.k_scale.numpy().view(np.uint32))
 
 
+def check_multi_token_append(lib=None):
+    """T new rows per sequence land at positions[b] .. positions[b] + T - 1: the same bytes
+    as T single-row appends at those positions (the single-row append is pinned above)."""
+    for kv in ("bf16", "fp8_e4m3"):
+        T = 3
+        case = inputs.small("append_t", 6, [3, 64, 66, 130, 2, 200], kv_dtype=kv, seed=91, tokens_per_seq=T)
+        step = inputs.append_step(case, seed=92, tokens_per_seq=T)
+        many = oracle.kv_append(step.k_new, step.v_new, step.positions, case.block_table, case.k_cache,
+                                case.v_cache, case.k_scale, case.v_scale, tokens_per_seq=T, lib=lib)
+        kc, vc, ks, vs = case.k_cache, case.v_cache, case.k_scale, case.v_scale
+        for i in range(T):
+            pos_i = torch.where(step.positions >= 0, step.positions + i, step.positions)
+            kc, vc, ks, vs, mask = oracle.kv_append(step.k_new[i::T].contiguous(), step.v_new[i::T].contiguous(),
+                                                    pos_i, case.block_table, kc, vc, ks, vs, lib=lib)
+            kc, vc = torch.from_numpy(kc).view(case.k_cache.dtype), torch.from_numpy(vc).view(case.v_cache.dtype)
+            if ks is not None:
+                ks, vs = torch.from_numpy(ks), torch.from_numpy(vs)
+            assert mask == 0
+        assert many[4] == 0
+        assert np.array_equal(many[0], kc.view(torch.uint8 if kv != "bf16" else torch.int16).numpy())
+        assert np.array_equal(many[1], vc.view(torch.uint8 if kv != "bf16" else torch.int16).numpy())
+        if ks is not None:
+            assert np.array_equal(many[2].view(np.uint32), ks.numpy().view(np.uint32))
+            assert np.array_equal(many[3].view(np.uint32), vs.numpy().view(np.uint32))
+
+
+def test_append_of_several_tokens_equals_single_token_appends():
+    check_multi_token_append()
+
+
 PINS = (check_encoder, check_round_trip, check_saturation_and_zeros, check_bf16_append, check_fp8_append,
-        check_error_masks)
+        check_error_masks, check_multi_token_append)
 
 
 def test_encoder_matches_torch_on_every_rounding_boundary():
@@ -230,7 +260,8 @@ _MUTANTS = {
     "absmax_first": ("if (a > absmax) absmax = a;", "if (i == 0) absmax = a;"),
     "wrong_slot": ("(size_t)(t % page)", "(size_t)((t + 1) % page)"),
     "wrong_page": ("t / page]", "(t / page + 1) % max_pages]"),
-    "k_for_v": ("quantise_row(v_new + (size_t)b * d", "quantise_row(k_new + (size_t)b * d"),
+    "k_for_v": ("quantise_row(v_new + (size_t)x * d", "quantise_row(k_new + (size_t)x * d"),
+    "token_offset_dropped": ("positions[b] + x % T;", "positions[b];"),
     "bf16_v_from_k": ("memcpy((uint16_t *)v_cache + row * d, v_new", "memcpy((uint16_t *)v_cache + row * d, k_new"),
     "position_not_reported": ("mask |= 2;", "mask |= 0;"),
     "block_not_reported": ("mask |= 1;", "mask |= 0;"),
@@ -259,3 +290,5 @@ def test_append_mutants_are_caught():
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
                                    "-fno-fast-math", "-ffp-contract=off", "-o", so, path, "-lm"])
             assert not _pins_pass(oracle.load_library(so)), f"mutant {name} survived the pins"
+
+
