@@ -441,8 +441,10 @@ def run_native(args, case, rank: int, world: int):
     e0.record(stream)
     for _, st_k, _, _ in lanes:
         st_k.wait_event(e0)
+    t_enq = time.perf_counter()
     for i in range(args.steps):
         e2e_step(i)
+    enqueue_ms = (time.perf_counter() - t_enq) * 1e3 / args.steps   # host time to issue one step
     join_lanes()
     e1.record(stream)
     barrier()
@@ -528,7 +530,8 @@ def run_native(args, case, rank: int, world: int):
                      "algorithmic_bytes_per_launch": acct["total"], "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": whole_job_gbs(acct["kv"], world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "path": "mfa_decode_run_host (pinned host buffers in and out), two streams alternating"},
+                "path": "mfa_decode_run_host (pinned host buffers in and out), two streams alternating",
+                "host_enqueue_ms_per_step": enqueue_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "device_status": status,

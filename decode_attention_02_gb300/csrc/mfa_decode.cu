@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -1718,8 +1719,8 @@ static mfa_status check_plan(const mfa_plan* pl, const mfa_problem* pr) {
   return MFA_OK;
 }
 
-static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const void* q, const void* k,
-                              const void* v) {
+static mfa_status encode_maps_uncached(DecodeParams& prm, const mfa_problem* pr, const void* q, const void* k,
+                                       const void* v) {
   auto enc = encode_fn();
   if (enc == nullptr) return cuda_fail_msg("cuTensorMapEncodeTiled is not available from the driver");
   {
@@ -1749,6 +1750,67 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cuda_fail_msg("cuTensorMapEncodeTiled rejected a tensor map");
   }
+  return MFA_OK;
+}
+
+// The three tensor maps depend only on the q, K and V addresses and the problem's shapes and
+// KV dtype, so a host thread keeps its last few encodings: a decode loop over a handful of
+// buffers then encodes each set once.  (Host memory only; it changes no result.)
+static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const void* q, const void* k,
+                              const void* v) {
+  struct Entry {
+    const void* q;
+    const void* k;
+    const void* v;
+    long long rows;
+    int num_blocks, kv_dtype;
+    CUtensorMap tq, tk, tv;
+  };
+  constexpr int kEntries = 8;
+  static thread_local Entry cache[kEntries];
+  static thread_local int used = 0, next = 0;
+  const long long rows = vbatch(pr) * kH;
+  for (int i = 0; i < used; ++i) {
+    const Entry& e = cache[i];
+    if (e.q == q && e.k == k && e.v == v && e.rows == rows && e.num_blocks == pr->num_blocks &&
+        e.kv_dtype == pr->kv_dtype) {
+      prm.tm_q = e.tq;
+      prm.tm_k = e.tk;
+      prm.tm_v = e.tv;
+      return MFA_OK;
+    }
+  }
+  const mfa_status st = encode_maps_uncached(prm, pr, q, k, v);
+  if (st != MFA_OK) return st;
+  Entry& e = cache[next];
+  e.q = q;
+  e.k = k;
+  e.v = v;
+  e.rows = rows;
+  e.num_blocks = pr->num_blocks;
+  e.kv_dtype = pr->kv_dtype;
+  e.tq = prm.tm_q;
+  e.tk = prm.tm_k;
+  e.tv = prm.tm_v;
+  next = (next + 1) % kEntries;
+  if (used < kEntries) ++used;
+  return MFA_OK;
+}
+
+// cudaFuncSetAttribute for a kernel's dynamic shared memory, once per device and kernel.
+static mfa_status ensure_smem_attribute(bool fp8) {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<bool> done[2][kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const bool cacheable = dev >= 0 && dev < kMaxDevices;
+  if (cacheable && done[fp8][dev].load(std::memory_order_acquire)) return MFA_OK;
+  auto kernel = fp8 ? mfa_decode_kernel<true> : mfa_decode_kernel<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fp8 ? smem_bytes<true>() : smem_bytes<false>());
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  if (cacheable) done[fp8][dev].store(true, std::memory_order_release);
   return MFA_OK;
 }
 
@@ -1938,8 +2000,8 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
   auto kernel = fp8 ? mfa_decode_kernel<true> : mfa_decode_kernel<false>;
   const int smem = fp8 ? smem_bytes<true>() : smem_bytes<false>();
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  st = ensure_smem_attribute(fp8);
+  if (st != MFA_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
   cfg.blockDim = dim3(fp8 ? threads_of<true>() : threads_of<false>(), 1, 1);

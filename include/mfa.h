@@ -27,7 +27,9 @@
  *
  * Conventions for every call:
  *   - All device pointers are caller-owned (allocate them with any allocator);
- *     the library allocates no device memory and keeps no state between calls.
+ *     the library allocates no device memory and keeps no device state between calls
+ *     (host-side it remembers, per thread, its last few tensor-map encodings, and sets each
+ *     kernel's shared-memory attribute once per device; neither changes any result).
  *   - All tensors are dense, row-major, contiguous, with the strides implied by
  *     their shapes below.
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
