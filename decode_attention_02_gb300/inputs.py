@@ -91,6 +91,8 @@ WORKLOADS = {
     # multi-token decode: two new query tokens per sequence, causal among them
     "mtp2_b32_l4096_bf16": Workload(
         "mtp2_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=7, tokens_per_seq=2),
+    "mtp2_b32_l4096_fp8": Workload(
+        "mtp2_b32_l4096_fp8", batch=32, lens=(4096,) * 32, kv_dtype="fp8_e4m3", seed=8, tokens_per_seq=2),
 }
 
 

@@ -395,3 +395,17 @@ def test_multi_token_decode_full_size():
     assert err.max() <= BF16_MAX_ABS
     assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= BF16_REL_L2
     assert np.abs(lse[sample].cpu().double().numpy() - ref_lse).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_multi_token_decode_beyond_one_thread_per_pair(kv_dtype):
+    """150 sequences x 3 query tokens = 450 (sequence, token) pairs: more than the bf16 kernel's
+    352 threads, so its schedule takes the chunked path (e4m3, 512 threads, the per-thread one)."""
+    rng = np.random.default_rng(97)
+    lens = [int(x) for x in rng.integers(0, 200, size=150)]
+    case = inputs.small("mtp_many", len(lens), lens, kv_dtype=kv_dtype, seed=98, tokens_per_seq=3)
+    out, lse, dec = gpu_decode_mtp(case)
+    if kv_dtype == "bf16":
+        check_parity(case, out, lse)
+    else:
+        check_parity(case, out, lse, max_abs=3e-2, rel_l2=1.5e-2)
