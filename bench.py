@@ -64,11 +64,12 @@ def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int 
     return {"kv": kv, "total": kv + other}
 
 
-def append_bytes(batch: int, kv_dtype: str, d: int = 256) -> int:
-    """Algorithmic bytes of one KV append: per sequence the new bf16 K and V rows, its
-    position and page id in, and the stored rows out (bf16, or e4m3 codes + fp32 scale)."""
+def append_bytes(batch: int, kv_dtype: str, d: int = 256, T: int = 1) -> int:
+    """Algorithmic bytes of one KV append: per sequence its position in, and per new token
+    (T of them) the bf16 K and V rows and the page id in, and the stored rows out (bf16, or
+    e4m3 codes + fp32 scale)."""
     out_row = 2 * d if kv_dtype == "bf16" else d + 4
-    return batch * (2 * 2 * d + 4 + 4 + 2 * out_row)
+    return batch * (4 + T * (2 * 2 * d + 4 + 2 * out_row))
 
 
 def algorithmic_flops(lens, H: int = 64, d: int = 256, T: int = 1) -> int:
@@ -340,6 +341,8 @@ def run_native(args, case, rank: int, world: int):
     step(0)
     torch.cuda.synchronize()
     status = mfa.mfa_read_device_status(dec.workspace)
+    if status != 0:
+        raise RuntimeError(f"decode step set device status bits {status:#x} on {w.name}")
 
     sampler = ClockSampler(dev.index)
     sampler.start()
@@ -451,12 +454,12 @@ def run_native(args, case, rank: int, world: int):
     windows.append((t_start, time.time()))
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
 
-    # --- the KV append of the same batch (each sequence's new row at its last position),
+    # --- the KV append of the same batch (each sequence's T new rows at its last T positions),
     #     alone (per-launch events behind a GPU sleep) and chained in front of the decode
     #     step (append -> decode -> combine, K steps from one CUDA graph)
-    k_new = inputs.new_token_rows(B, seed=w.seed + 101, kinds=("normal",)).to(dev)
-    v_new = inputs.new_token_rows(B, seed=w.seed + 102, kinds=("normal",)).to(dev)
-    positions = (case.seq_lens.to(torch.int32) - 1).to(dev)
+    k_new = inputs.new_token_rows(B * T, seed=w.seed + 101, kinds=("normal",)).to(dev)
+    v_new = inputs.new_token_rows(B * T, seed=w.seed + 102, kinds=("normal",)).to(dev)
+    positions = (case.seq_lens.to(torch.int32) - T).to(dev)
 
     def append(i):
         s = sets[i % nsets]
@@ -489,7 +492,9 @@ def run_native(args, case, rank: int, world: int):
     barrier()
     ms_step_append = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
     app_status = mfa.mfa_read_device_status(dec.workspace)
-    app_bytes = append_bytes(B, w.kv_dtype)
+    if app_status != 0:
+        raise RuntimeError(f"append + decode steps set device status bits {app_status:#x} on {w.name}")
+    app_bytes = append_bytes(B, w.kv_dtype, T=T)
 
     # keep sampling clocks until the windows hold enough samples
     clocks = sampler.summary(windows)

@@ -10,7 +10,8 @@
 //
 //  * One CTA per SM (persistent).  The batch's 128-token tiles are laid end to end
 //    and CTA g owns an equal share of their cost, a sequence boundary counting as 3/4
-//    of a tile, so the load is even for any length mix; a sequence cut by a CTA
+//    of a tile (bf16) or 2.5 tiles (e4m3), so the load is even for any length mix; a
+//    sequence cut by a CTA
 //    boundary yields partial results that the combine kernel merges (split-KV with a
 //    log-sum-exp merge).
 //  * Each CTA holds all 64 heads of its sequence, so K and V are read once.
@@ -35,6 +36,15 @@
 //  * The ragged last page is loaded with its valid rows shifted to the end of the
 //    box (negative row start; TMA fills the rest with zeros), so NaN or stale data
 //    in unused page slots never enters an MMA.
+//  * K and V uses share the ring.  With the two MMA streams in different threads, each
+//    stream publishes in shared memory how many tiles of its uses have landed, and the
+//    other waits on that count before it reuses a slot (an mbarrier parity would be
+//    ambiguous for a waiter two phases behind).
+//  * Multi-token decode (T new query tokens per sequence, causal among them): each
+//    (sequence, token) pair is scheduled as its own sequence of length L - T + 1 + i
+//    over the sequence's block-table row; its pages are read once per query token, all
+//    but the last token's reads kept in L2 for the next.
+//  * mfa_decode_run_host wraps one step with the copies of its host inputs and outputs.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -79,6 +89,12 @@ constexpr uint32_t kRegsCtl = 80, kRegsSoftmax = 168, kRegsDequant = 96;
 static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsDequant == 4 * (65536 / 512),
               "e4m3 register split must add up to the launch budget (4 warpgroups x 128)");
 constexpr int kMaxTilesPerCta = 128;
+// Schedule cost units: a 128-token tile weighs kCostTile, a sequence boundary inside a CTA's
+// range cost_seq (the next sequence's q and one more epilogue).  Measured per sequence switch:
+// under a tile period for bf16, about two tile periods for e4m3 (whose q is converted and
+// whose epilogue is not overlapped).
+constexpr int kCostTile = 4;
+__host__ __device__ constexpr int cost_seq(bool fp8) { return fp8 ? 10 : 3; }
 constexpr int kMaxTokensPerSeq = 4;   // new query tokens per sequence (multi-token decode)
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
@@ -210,6 +226,7 @@ struct CombineParams {
   int out_f32;
   int heads_per_cta;  // 1, 4 or 16
   int tokens;         // as DecodeParams::tokens
+  int seq_cost;       // cost_seq of the KV format: the decode kernel's split
 };
 
 // ------------------------------------------------------------------ helpers
@@ -547,12 +564,13 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   }
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
-  // Cost-balanced split: tile k of sequence b sits at cost 4 (S_b + k) + 3 N_b, S_b being the
-  // tiles and N_b the non-empty sequences before b, so a sequence boundary inside a CTA's
-  // range weighs 3/4 of a tile (the next sequence's q load and one more epilogue).  CTA g owns
-  // the tiles whose cost lies in [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1):
-  // a contiguous run of tiles, in sequence order across CTAs.  Tile counts and non-empty
-  // counts are scanned together (low and high 32 bits).
+  // Cost-balanced split: tile k of sequence b sits at cost 4 (S_b + k) + c N_b, S_b being the
+  // tiles and N_b the non-empty sequences before b, c = cost_seq: a sequence boundary inside
+  // a CTA's range weighs c/4 of a tile.  CTA g owns the tiles whose cost lies in
+  // [floor(g C / G), floor((g + 1) C / G)), C = 4 W + c (N - 1): a contiguous run of tiles, in
+  // sequence order across CTAs.  Tile counts and non-empty counts are scanned together (low
+  // and high 32 bits).
+  constexpr long long kSeqW = cost_seq(kFp8);
   const int cap = p.max_pages * kPage;
   {
     long long* scratch = reinterpret_cast<long long*>(smem + kOffRed);   // idle until the softmax
@@ -569,7 +587,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     const long long incl0 = block_incl_scan<kThreads, long long>(loc, scratch, tot0);
     const int W = static_cast<int>(tot0 & 0xFFFFFFFFll), N = static_cast<int>(tot0 >> 32);
     const int G = gridDim.x, g = blockIdx.x;
-    const long long C = 4LL * W + 3LL * max(N - 1, 0);
+    const long long C = kCostTile * static_cast<long long>(W) + kSeqW * max(N - 1, 0);
     long long X0, X1;
     if (C <= 0x7FFFFFFFll / G) {   // (g + 1) C fits in 32 bits: the short division
       const uint32_t Cu = static_cast<uint32_t>(C), Gu = static_cast<uint32_t>(G), gu = static_cast<uint32_t>(g);
@@ -581,14 +599,14 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     }
     // sequence with first-tile cost `base` and T tiles: first of its tiles at cost >= X
     auto first_at = [](long long X, long long base, int T) -> int {
-      return X <= base ? 0 : static_cast<int>(min(static_cast<long long>(T), (X - base + 3) / 4));
+      return X <= base ? 0 : static_cast<int>(min(static_cast<long long>(T), (X - base + kCostTile - 1) / kCostTile));
     };
     // this sequence's contribution to the CTA's [first, end) tiles: the non-empty sequence
     // whose cost span [base, next base) holds X0 (X1) fixes the first (end) tile.  Those spans
     // tile [0, C) exactly, so only X = C (X1 of the last CTA) has no owner: it stands for W.
     auto mark_bounds = [&](long long base, int S, int T) {
       if (T == 0) return;
-      const long long nxt = base + 4LL * T + 3;
+      const long long nxt = base + kCostTile * static_cast<long long>(T) + kSeqW;
       if (base <= X0 && X0 < nxt) tb[0] = S + first_at(X0, base, T);
       if (base <= X1 && X1 < nxt) tb[1] = S + first_at(X1, base, T);
     };
@@ -601,7 +619,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       const int T = tiles_of(L);
       const long long ex = incl0 - packed(T);
       const int S = static_cast<int>(ex & 0xFFFFFFFFll), Nb = static_cast<int>(ex >> 32);
-      const long long base = 4LL * S + 3LL * Nb;
+      const long long base = kCostTile * static_cast<long long>(S) + kSeqW * Nb;
       if (tid < p.batch) mark_bounds(base, S, T);
       const int k_lo = first_at(X0, base, T), k_hi = first_at(X1, base, T);
       const bool f = (tid < p.batch) && (k_lo < k_hi);
@@ -628,7 +646,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     } else {
       // pass 1: the CTA's first and end tiles (sequences beyond cost X1 cannot matter)
       long long carry = 0;
-      auto cost_of = [](long long pk) { return 4LL * (pk & 0xFFFFFFFFll) + 3LL * (pk >> 32); };
+      auto cost_of = [](long long pk) { return kCostTile * (pk & 0xFFFFFFFFll) + kSeqW * (pk >> 32); };
       for (int c0 = 0; c0 < p.batch && cost_of(carry) <= X1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
@@ -1433,8 +1451,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
 // ------------------------------------------------------------------ combine kernel
 
 // Largest g with floor(g C / G) <= c: the CTA owning cost position c (see the decode
-// kernel's cost-balanced split: tile k of sequence b at cost 4 (S_b + k) + 3 N_b, N_b the
-// non-empty sequences before b, C = 4 W + 3 (N - 1)).
+// kernel's cost-balanced split: tile k of sequence b at cost 4 (S_b + k) + c N_b, N_b the
+// non-empty sequences before b, C = 4 W + c (N - 1), c = cost_seq).
 __device__ __forceinline__ int cta_of_cost(long long c, long long C, long long G) {
   return static_cast<int>(((c + 1) * G + C - 1) / C - 1);
 }
@@ -1498,10 +1516,11 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   bool dummy = false;
   const int Tb = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy));
   if (Tb == 0) return;
-  const long long C = 4LL * total + 3LL * max(nt - 1, 0);
-  const long long base = 4LL * before + 3LL * nb;   // cost of sequence b's first tile
+  const long long sw = p.seq_cost;
+  const long long C = kCostTile * static_cast<long long>(total) + sw * max(nt - 1, 0);
+  const long long base = kCostTile * static_cast<long long>(before) + sw * nb;   // cost of sequence b's first tile
   const int g0 = cta_of_cost(base, C, p.num_ctas);
-  const int g1 = cta_of_cost(base + 4LL * (Tb - 1), C, p.num_ctas);
+  const int g1 = cta_of_cost(base + kCostTile * static_cast<long long>(Tb - 1), C, p.num_ctas);
   if (g0 == g1) return;  // written whole by the decode kernel
 
   const int quad = threadIdx.x >> 6;
@@ -1524,8 +1543,8 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
           if (g < ge) {
             const long long x0 = (static_cast<long long>(g) * C) / p.num_ctas;
             const long long x1 = (static_cast<long long>(g + 1) * C) / p.num_ctas;
-            const long long k_lo = x0 <= base ? 0 : (x0 - base + 3) / 4;
-            const long long k_hi = x1 <= base ? 0 : (x1 - base + 3) / 4;
+            const long long k_lo = x0 <= base ? 0 : (x0 - base + kCostTile - 1) / kCostTile;
+            const long long k_hi = x1 <= base ? 0 : (x1 - base + kCostTile - 1) / kCostTile;
             live = k_lo < min(k_hi, static_cast<long long>(Tb));
           }
           const unsigned m = __ballot_sync(0xffffffffu, live);
@@ -1663,25 +1682,25 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Most tiles any CTA gets under the decode kernel's cost-balanced split (tile k of sequence b
-// at cost 4 (S_b + k) + 3 N_b, N_b the non-empty sequences before b; CTA g owns costs
-// [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1)) for sequences of T[b] tiles:
-// the CTA boundaries walked in order over the non-empty sequences.
-static long long max_cta_tiles(const std::vector<long long>& Tall, long long G) {
+// at cost 4 (S_b + k) + c N_b, N_b the non-empty sequences before b, c = cost_seq; CTA g owns
+// costs [floor(g C / G), floor((g + 1) C / G)), C = 4 W + c (N - 1)) for sequences of T[b]
+// tiles: the CTA boundaries walked in order over the non-empty sequences.
+static long long max_cta_tiles(const std::vector<long long>& Tall, long long G, long long c) {
   std::vector<long long> T;
   for (long long t : Tall)
     if (t > 0) T.push_back(t);
   const long long B = static_cast<long long>(T.size());
   long long W = 0;
   for (long long t : T) W += t;
-  const long long C = 4 * W + 3 * std::max(B - 1, 0ll);
+  const long long C = kCostTile * W + c * std::max(B - 1, 0ll);
   if (C == 0 || G <= 0) return 0;
   long long b = 0, S = 0;
   // first tile with cost >= X, for non-decreasing X
   auto tile_at = [&](long long X) -> long long {
     if (X >= C) return W;
-    while (b + 1 < B && 4 * (S + T[b]) + 3 * (b + 1) <= X) { S += T[b]; ++b; }
-    const long long base = 4 * S + 3 * b;
-    return S + (X <= base ? 0 : std::min(T[b], (X - base + 3) / 4));
+    while (b + 1 < B && kCostTile * (S + T[b]) + c * (b + 1) <= X) { S += T[b]; ++b; }
+    const long long base = kCostTile * S + c * b;
+    return S + (X <= base ? 0 : std::min(T[b], (X - base + kCostTile - 1) / kCostTile));
   };
   long long prev = tile_at(0), most = 0;
   for (long long g = 0; g < G; ++g) {
@@ -1827,6 +1846,7 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.lse = lse;
   cp.batch = static_cast<int>(vbatch(pr));
   cp.tokens = pr->tokens_per_seq;
+  cp.seq_cost = cost_seq(pr->kv_dtype == MFA_KV_FP8_E4M3);
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
   cudaLaunchConfig_t cfg = {};
@@ -1912,10 +1932,12 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   }
   // planned from a bound, any shorter mix must fit too: a CTA's cost range of at most
   // ceil(C / G) units holds at most ceil(ceil(C / G) / 4) tiles
-  const long long Cb = 4 * W + 3 * std::max(Bv - 1, 0ll);
+  const long long cs = cost_seq(pr->kv_dtype == MFA_KV_FP8_E4M3);
+  const long long Cb = kCostTile * W + cs * std::max(Bv - 1, 0ll);
   auto worst = [&](long long g) {
-    const long long exact = max_cta_tiles(T, g);
-    return host_seq_lens != nullptr ? exact : std::max(exact, ((Cb + g - 1) / g + 3) / 4);
+    const long long exact = max_cta_tiles(T, g, cs);
+    return host_seq_lens != nullptr ? exact
+                                    : std::max(exact, ((Cb + g - 1) / g + kCostTile - 1) / kCostTile);
   };
   long long most = worst(G);
   while (most > kMaxTilesPerCta) {

@@ -6,10 +6,11 @@
 // scale per row, s = absmax / 448 (1 for an all-zero row), and e4m3 codes of x / s, rounded
 // to nearest even and saturated to +-448; the format the decode kernel reads.
 //
-// The work is 2BT independent rows of 256 values (T new tokens per sequence) (512 bytes of bf16 in; 512 bytes of bf16
-// or 260 bytes of codes and scale out), so it is a latency-bound scatter: one warp per
-// row, one 16-byte load and one 16- or 8-byte store per lane, a warp max for the scale;
-// the row's load is issued before the dependent position and page-id loads.
+// The work is 2BT independent rows of 256 values, T new tokens per sequence.  Each row is
+// 512 bytes of bf16 in and 512 bytes of bf16, or 260 bytes of codes and scale, out, so it
+// is a latency-bound scatter: one warp per row, one 16-byte load and one 16- or 8-byte
+// store per lane, a warp max for the scale; the row's load is issued before the dependent
+// position and page-id loads.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

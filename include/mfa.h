@@ -144,12 +144,13 @@ typedef struct mfa_plan {
  *   flags          : MFA_PLAN_* copied into the plan.
  *   plan (out)     : filled on MFA_OK.
  * The work is 128-token tiles laid end to end in sequence order.  Tile k of sequence b
- * sits at cost 4 (S_b + k) + 3 N_b, with S_b the tiles and N_b the non-empty sequences
+ * sits at cost 4 (S_b + k) + c N_b, with S_b the tiles and N_b the non-empty sequences
  * before b, and CTA g of G takes the tiles whose cost lies in
- * [floor(g*C/G), floor((g+1)*C/G)), C = 4 W + 3 (N - 1) for W tiles in N non-empty
+ * [floor(g*C/G), floor((g+1)*C/G)), C = 4 W + c (N - 1) for W tiles in N non-empty
  * sequences: every CTA gets the same share whatever the length mix, a sequence boundary
- * inside a CTA's range counting as 3/4 of a tile (the next sequence's q and one more
- * epilogue).  A sequence is split once per CTA boundary that falls inside it.  Planned
+ * inside a CTA's range (the next sequence's q and one more epilogue) counting as c/4 of a
+ * tile, c = 3 for bf16 KV and c = 10 for e4m3 KV.  A sequence is split once per CTA
+ * boundary that falls inside it.  Planned
  * from a length bound (host_seq_lens NULL), the grid keeps every CTA within 128 tiles
  * for any lengths up to the bound.
  */

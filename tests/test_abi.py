@@ -55,6 +55,43 @@ def test_plan_one_cta_per_sm_when_enough_tiles(lib):
     assert o_off == 256 and l_off % 256 == 0 and plan.workspace_bytes % 256 == 0
 
 
+def split_tiles_brute_force(lens, G, c):
+    """Tiles per CTA under the documented split, by enumerating every tile: tile k of sequence
+    b at cost 4 (S_b + k) + c N_b, owned by the largest g with floor(g C / G) <= its cost."""
+    tiles = [(L + 127) // 128 for L in lens]
+    W, N = sum(tiles), sum(1 for t in tiles if t > 0)
+    C = 4 * W + c * max(N - 1, 0)
+    per = [0] * G
+    before = nonempty = 0
+    for t in tiles:
+        for k in range(t):
+            x = 4 * (before + k) + c * nonempty
+            per[max(g for g in range(G) if (g * C) // G <= x)] += 1
+        before += t
+        nonempty += t > 0
+    return per
+
+
+@pytest.mark.parametrize("kv, c", [(mfa.MFA_KV_BF16, 3), (mfa.MFA_KV_FP8_E4M3, 10)])
+def test_plan_tile_counts_follow_the_documented_split(lib, kv, c):
+    import random
+    rng = random.Random(5)
+    for trial in range(40):
+        B = rng.randint(1, 40)
+        lens = [rng.choice([0, 1, 64, 128, 129, rng.randint(0, 4096)]) for _ in range(B)]
+        G = rng.randint(1, 60)
+        plan = mfa.mfa_decode_plan(problem(batch=B, max_pages_per_seq=64, num_blocks=4096, kv_dtype=kv), lens,
+                                   num_sms=152, force_ctas=G)
+        per = split_tiles_brute_force(lens, G, c)
+        assert sum(per) == plan.total_tiles
+        assert plan.max_tiles_per_cta == max(per), (lens, G)
+    # the boundary weight moves tiles away from CTAs that hold a sequence switch
+    lens = [4096] * 32
+    plan = mfa.mfa_decode_plan(problem(batch=32, max_pages_per_seq=64, num_blocks=2048, kv_dtype=kv), lens,
+                               num_sms=152)
+    assert plan.max_tiles_per_cta == max(split_tiles_brute_force(lens, 152, c))
+
+
 def test_plan_fewer_ctas_than_sms_for_short_batches(lib):
     plan = mfa.mfa_decode_plan(problem(batch=1), [512], num_sms=152)
     assert plan.num_ctas == 4 and plan.max_tiles_per_cta == 1

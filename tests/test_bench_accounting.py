@@ -35,3 +35,5 @@ def test_append_bytes():
     # per sequence: two bf16 rows in, position and page id, two rows out
     assert bench.append_bytes(3, "bf16") == 3 * (2 * 2 * D + 4 + 4 + 2 * 2 * D)
     assert bench.append_bytes(3, "fp8_e4m3") == 3 * (2 * 2 * D + 4 + 4 + 2 * (D + 4))
+    # T new tokens per sequence: one position per sequence, rows and page ids per token
+    assert bench.append_bytes(3, "bf16", T=2) == 3 * (4 + 2 * (2 * 2 * D + 4 + 2 * 2 * D))

@@ -153,11 +153,12 @@ def test_separate_combine_matches_fused_run():
     assert torch.equal(lse1, lse2)
 
 
-def test_combine_kernel_against_oracle_merge():
+@pytest.mark.parametrize("kv", [mfa.MFA_KV_BF16, mfa.MFA_KV_FP8_E4M3])
+def test_combine_kernel_against_oracle_merge(kv):
     """mfa_combine alone on random partials laid out as include/mfa.h documents."""
     lens = [129, 1000, 5, 640]
     B, G = len(lens), 6
-    prob = mfa.make_problem(B, 16, 64)
+    prob = mfa.make_problem(B, 16, 64, kv)
     plan = mfa.mfa_decode_plan(prob, lens, force_ctas=G, num_sms=152)
     ws = torch.zeros(int(plan.workspace_bytes), dtype=torch.uint8, device="cuda")
     o_off, l_off = mfa.workspace_layout(plan)
@@ -173,14 +174,15 @@ def test_combine_kernel_against_oracle_merge():
     assert prob.out_dtype == mfa.MFA_OUT_BF16
     mfa.mfa_combine(plan, prob, ws, seq, out, lse)
     torch.cuda.synchronize()
-    # the documented split: tile k of sequence b at cost 4 (S_b + k) + 3 N_b; CTA g owns
-    # costs [floor(g C / G), floor((g + 1) C / G)), C = 4 W + 3 (N - 1)
+    # the documented split: tile k of sequence b at cost 4 (S_b + k) + c N_b; CTA g owns
+    # costs [floor(g C / G), floor((g + 1) C / G)), C = 4 W + c (N - 1); c = 3 (bf16 KV) or 10
+    c = 10 if kv == mfa.MFA_KV_FP8_E4M3 else 3
     tiles = [(L + 127) // 128 for L in lens]
     W, N = sum(tiles), sum(1 for t in tiles if t > 0)
-    C = 4 * W + 3 * max(N - 1, 0)
+    C = 4 * W + c * max(N - 1, 0)
     before = nonempty = 0
     for b in range(B):
-        base = 4 * before + 3 * nonempty
+        base = 4 * before + c * nonempty
         costs = [base + 4 * k for k in range(tiles[b])]
         covering = sorted({max(gg for gg in range(G) if (gg * C) // G <= c) for c in costs})
         before += tiles[b]
