@@ -95,6 +95,10 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+# GB300's nominal HBM3e bandwidth (the measured copy bandwidth is the roofline's peak; the
+# fraction of this nominal figure is reported beside it)
+NOMINAL_HBM_GBS = 7900.0
+
 # Streams of the end-to-end leg: with two, a step's copies are not fully hidden (35.4 against
 # 32.1 us per step at bf16 4K); with three they are; with four, concurrent steps also fill the
 # SMs that one step's tail leaves idle, and e2e exceeds the single-stream device number.
@@ -538,7 +542,8 @@ def run_native(args, case, rank: int, world: int):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic(w.name),
                      "kernel": "mfa_decode_kernel", "mean_launch_ms": kern_mean_ms,
-                     "algorithmic_bytes_per_launch": acct["total"], "peak_source": f"{peak_src} hbm_gbs"},
+                     "algorithmic_bytes_per_launch": acct["total"], "peak_source": f"{peak_src} hbm_gbs",
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "e2e": {"value": whole_job_gbs(acct["kv"], world, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": f"mfa_decode_run_host (pinned host buffers in and out), {E2E_LANES} streams in rotation",
@@ -592,9 +597,12 @@ def main():
             import oracle
             oracle.build()
             v, dt, k, reps = cpu_oracle_sample(case)
+            v1, dt1, k1, reps1 = cpu_oracle_sample(case, target_s=4.0, nthreads=1)
             res["cpu_baseline"] = {"value": v, "unit": "GB/s", "cores": oracle.num_cpus(), "kind": "oracle",
                                    "sample": f"{k} of {len(case.seq_lens)} sequences x {reps} passes, "
-                                             f"fp64, {dt:.1f} s"}
+                                             f"fp64, {dt:.1f} s",
+                                   "single_thread": {"value": v1, "unit": "GB/s", "cores": 1,
+                                                     "sample": f"{k1} sequences x {reps1} passes, {dt1:.1f} s"}}
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist
