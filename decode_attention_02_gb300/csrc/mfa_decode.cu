@@ -131,6 +131,9 @@ struct KvLayout<true> {
 };
 static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
 static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
+// The e4m3 QK^T reads a d-half's two pages as one 128-row operand from two adjacent slots
+// (uses 2k and 2k + 1 of an aligned group of four): they stay adjacent only for an even count.
+static_assert(KvLayout<true>::kNumSlots % 2 == 0, "e4m3 ring: page pairs must not wrap");
 constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan
                                          //      [20..21] CTA tile range [24..31] q maxima
 // Ring-order counts.  K and V uses share one ring, and a consumer may only wait on a slot's
