@@ -90,3 +90,15 @@ def test_fp8_full_size_workload(name):
     assert dec.plan.num_ctas == min(torch.cuda.get_device_properties(0).multi_processor_count,
                                     int(dec.plan.total_tiles))
     check_parity(case, out, lse, **FP8)
+
+
+def test_fp8_ragged_full_size_mix():
+    """128 sequences of 1,024..8,192 tokens in e4m3 (ragged last pages, 1% of K elements x20):
+    many sequence switches per CTA under the e4m3 schedule's boundary weight."""
+    import dataclasses
+    w = dataclasses.replace(inputs.WORKLOADS["ragged_b128_l1024_8192_bf16"], name="ragged_b128_l1024_8192_fp8",
+                            kv_dtype="fp8_e4m3", seed=12)
+    case = inputs.generate(w)
+    out, lse, dec = gpu_decode(case)
+    assert dec.plan.num_ctas == torch.cuda.get_device_properties(0).multi_processor_count
+    check_parity(case, out, lse, **FP8)
