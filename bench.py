@@ -419,6 +419,24 @@ def run_native(args, case, rank: int, world: int):
     kern_ms = [a.elapsed_time(b) for a, b in evs]
     kern_mean_ms = max_over_ranks(sum(kern_ms) / len(kern_ms), dist, dev)
 
+    # --- the combine kernel alone, on the partials the last decode-only launch left in the
+    #     workspace (same method), so that one step's kernel shares can be set beside the
+    #     ncu launch list's
+    comb_lens = sets[(nk - 1) % nsets]["lens"]
+    for i in range(3):
+        mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse)
+    barrier()
+    cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
+    t_start = time.time()
+    torch.cuda._sleep(int(2e7))
+    for i in range(nk):
+        cevs[i][0].record(stream)
+        mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse)
+        cevs[i][1].record(stream)
+    barrier()
+    windows.append((t_start, time.time()))
+    comb_mean_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in cevs) / nk, dist, dev)
+
     # --- end to end through the C ABI with host buffers (mfa_decode_run_host): every step
     #     copies its pinned host inputs (q, block table, lengths) in and its outputs (out, lse)
     #     back inside the timed region.  Three streams rotate, each with its own device
@@ -551,6 +569,13 @@ def run_native(args, case, rank: int, world: int):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "device_status": status,
+        "kernels_live": {
+            "mean_launch_ms": {"mfa_decode_kernel": kern_mean_ms, "mfa_combine_kernel": comb_mean_ms,
+                               "mfa_kv_append_kernel": app_mean_ms},
+            "share_of_one_step": {k: v / (kern_mean_ms + comb_mean_ms + app_mean_ms) for k, v in
+                                  (("mfa_decode_kernel", kern_mean_ms), ("mfa_combine_kernel", comb_mean_ms),
+                                   ("mfa_kv_append_kernel", app_mean_ms))},
+            "timing": "each kernel alone, per-launch events behind a GPU sleep (launch latency included)"},
         "kv_append": {"kernel": "mfa_kv_append_kernel", "mean_launch_ms": app_mean_ms,
                       "algorithmic_bytes_per_launch": app_bytes,
                       "achieved_gbs": app_bytes / (app_mean_ms * 1e-3) / 1e9,
