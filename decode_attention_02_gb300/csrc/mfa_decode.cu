@@ -441,6 +441,26 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   const bool ok = wait_bar(bar, parity, abort_flag);
   return __all_sync(0xffffffffu, ok);
 }
+// The same bounded wait, sleeping 128 ns between polls: for waits off the critical chain (the
+// e4m3 softmax's, whose P has about 1 us of slack before the dequantised V it meets), so that
+// the waiting warps leave issue slots to the dequant warps that share their SM sub-partitions.
+__device__ __forceinline__ bool wait_lazy(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(128);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort_flag != nullptr && *abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (abort_flag != nullptr) *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool wait_warp_lazy(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = wait_lazy(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
 
 // ------------------------------------------------------------------ decode kernel
 
@@ -1224,7 +1244,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       for (int j = sg.y; j < sg.z; ++j, ++n) {
         const bool first = (j == sg.y);
         const uint32_t s_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1) + h0 + lane_base;
-        const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
+        const bool okS = kFp8 ? wait_warp_lazy(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag)
+                              : wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
         aborted = aborted || !okS;
         bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
         const int rp = page_rows(L, j, rpg);
@@ -1366,7 +1387,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           // the next segment's q, as soon as this segment's last scores are read
           if (j + 1 == sg.z && s + 1 < nseg) convert_q(s + 1);
         }
-        if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
+        if (!pv_waited && !(kFp8 ? wait_warp_lazy(bar(kBarPvDone), (n - 1) & 1, abort_flag)
+                                 : wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)))
+          aborted = true;
         // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
         uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
