@@ -1,9 +1,13 @@
 """Benchmark of the MFA decode step on GB300 (one JSON line on rank 0).
 
 A step is one pass of the whole hot path -- decode kernel plus log-sum-exp
-combine -- over one batch of synthetic decode inputs.  The default workload is
-B=32 sequences of 4096 tokens, bf16 KV, 64 query heads of width 256 over one
-shared K/V head in 64-token pages whose physical order is a seeded permutation.
+combine -- over one batch of synthetic decode inputs.  The headline workload is
+the largest one that fits a GPU: B=128 sequences of 1,024-8,192 tokens (seeded,
+uniform), bf16 KV with 1% of the key elements x20, 64 query heads of width 256
+over one shared K/V head in 64-token pages whose physical order is a seeded
+permutation.  Every other target workload (4K and 64K+ contexts in bf16 and
+e4m3, multi-token decode, the tiny case) is measured on the same run and
+reported under "workloads" with its own value, roofline and e2e.
 
 value      : KV-cache bytes read per second over the timed steps (GB/s), inputs
              resident in HBM; several input copies rotate so that each step reads
@@ -39,7 +43,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "b32_l4096_bf16"
+DEFAULT_WORKLOAD = "ragged_b128_l1024_8192_bf16"
+# The other target workloads, measured on the same run and reported under "workloads".
+SIDE_WORKLOADS = ("tiny_b1_l512_bf16", "b32_l4096_bf16", "b128_l4096_fp8", "long_b4_l131072_bf16",
+                  "b32_l4096_fp8", "long_b4_l131072_fp8", "mtp2_b32_l4096_bf16", "mtp2_b32_l4096_fp8")
+SIDE_STEPS = 100
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -298,14 +306,70 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
     return bytes_per_rank * world / (ms * 1e-3) / 1e9
 
 
-def run_native(args, case, rank: int, world: int):
+class _Timer:
+    """Device timing helpers shared by the workloads: CUDA events on the launching stream,
+    barrier + synchronize on both sides of every timed region, max over ranks."""
+
+    def __init__(self, dev, dist, windows):
+        import torch
+        self.torch = torch
+        self.dev = dev
+        self.dist = dist
+        self.windows = windows
+        self.stream = torch.cuda.current_stream(dev)
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+        self.torch.cuda.synchronize()
+
+    def graph_ms(self, fn, steps):
+        """Mean ms per call of fn(i), i < steps, replayed from one CUDA graph of exactly
+        `steps` calls (the first replay, which uploads the graph, is untimed)."""
+        torch = self.torch
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(steps):
+                fn(i)
+        graph.replay()
+        self.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start = time.time()
+        e0.record(self.stream)
+        graph.replay()
+        e1.record(self.stream)
+        self.barrier()
+        self.windows.append((t_start, time.time()))
+        return max_over_ranks(e0.elapsed_time(e1), self.dist, self.dev) / steps, graph
+
+    def per_launch_ms(self, fn, n):
+        """Mean ms of fn(i) alone: per-launch events, queued behind a GPU sleep so that the
+        launches run back to back whatever the host-side cost of enqueueing them."""
+        torch = self.torch
+        for i in range(3):
+            fn(i)
+        self.barrier()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        t_start = time.time()
+        torch.cuda._sleep(int(2e7))
+        for i in range(n):
+            evs[i][0].record(self.stream)
+            fn(i)
+            evs[i][1].record(self.stream)
+        self.barrier()
+        self.windows.append((t_start, time.time()))
+        return max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / n, self.dist, self.dev)
+
+
+def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
+    """Time one workload: the whole step (decode + combine) from a CUDA graph, the decode
+    kernel alone, and the step end to end through the host-buffer C ABI call.  The headline
+    workload also gets the step without early metadata, each kernel alone and the KV append."""
     import torch
     import decode_attention_02_gb300 as mfa
-    from decode_attention_02_gb300 import build, inputs
+    from decode_attention_02_gb300 import inputs
 
-    build.build_library()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
+    dev = tm.dev
     w = case.workload
     lens = case.seq_lens.tolist()
     kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
@@ -326,19 +390,17 @@ def run_native(args, case, rank: int, world: int):
             table=case.block_table.to(dev), lens=case.seq_lens.to(dev)))
     out = torch.empty(B * T, 64, 256, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B * T, 64, dtype=torch.float32, device=dev)
+
+    def decoder(flags):
+        return mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
+                           host_seq_lens=lens, flags=flags, device=dev, tokens_per_seq=T)
+
     # the timed steps are back-to-back decode steps whose lengths and block table are
     # filled once, before the loop: each step's decode may therefore read them while the
     # previous step's combine is still running (q, K, V and all outputs stay ordered)
-    dec = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                      host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev,
-                      tokens_per_seq=T)
-    dec_strict = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                             host_seq_lens=lens, device=dev, tokens_per_seq=T)
+    dec = decoder(mfa.MFA_PLAN_EARLY_METADATA)
     # the decode kernel alone, in the configuration the timed steps launch it with
-    dec_only = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                           host_seq_lens=lens, flags=mfa.MFA_PLAN_NO_COMBINE | mfa.MFA_PLAN_EARLY_METADATA,
-                           device=dev, tokens_per_seq=T)
-    stream = torch.cuda.current_stream(dev)
+    dec_only = decoder(mfa.MFA_PLAN_NO_COMBINE | mfa.MFA_PLAN_EARLY_METADATA)
     G = dec.plan.num_ctas
     launches_per_step = 1 + (1 if G > 1 else 0)
 
@@ -347,108 +409,30 @@ def run_native(args, case, rank: int, world: int):
         mfa.mfa_decode_run(d.plan, d.problem, s["q"], s["k"], s["v"], s["ks"], s["vs"], s["table"], s["lens"],
                            out, lse, d.workspace, None)
 
-    # status word of this exact launch configuration must stay clear
+    # the status word of this exact launch configuration must stay clear
     step(0)
     torch.cuda.synchronize()
     status = mfa.mfa_read_device_status(dec.workspace)
     if status != 0:
         raise RuntimeError(f"decode step set device status bits {status:#x} on {w.name}")
 
-    sampler = ClockSampler(dev.index)
-    sampler.start()
-    time.sleep(0.2)
-    windows = []
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    # --- timed steps (decode + combine), replayed from a CUDA graph of exactly K steps
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        for i in range(args.steps):
-            step(i)
-    graph.replay()   # untimed: first replay uploads the graph
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_start = time.time()
-    e0.record(stream)
-    graph.replay()
-    e1.record(stream)
-    barrier()
-    windows.append((t_start, time.time()))
-    ms_total = e0.elapsed_time(e1)
-    ms_total = max_over_ranks(ms_total, dist, dev)
-    ms_step = ms_total / args.steps
+    ms_step, graph = tm.graph_ms(step, steps)
+    kern_mean_ms = tm.per_launch_ms(lambda i: step(i, dec_only), max(min(steps, 400), 50))
 
-    # the same K steps without the early-metadata overlap (every read after the previous step)
-    graph2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph2):
-        for i in range(args.steps):
-            step(i, dec_strict)
-    graph2.replay()
-    barrier()
-    e0.record(stream)
-    graph2.replay()
-    e1.record(stream)
-    barrier()
-    ms_step_strict = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
-
-    # --- decode kernel alone: per-launch CUDA events, queued behind a GPU sleep so
-    #     the launches run back to back whatever the host-side cost of enqueueing them
-    nk = max(min(args.steps, 400), 50)
-    for i in range(3):
-        step(i, dec_only)
-    barrier()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
-    t_start = time.time()
-    torch.cuda._sleep(int(2e7))
-    for i in range(nk):
-        evs[i][0].record(stream)
-        step(i, dec_only)
-        evs[i][1].record(stream)
-    barrier()
-    windows.append((t_start, time.time()))
-    kern_ms = [a.elapsed_time(b) for a, b in evs]
-    kern_mean_ms = max_over_ranks(sum(kern_ms) / len(kern_ms), dist, dev)
-
-    # --- the combine kernel alone, on the partials the last decode-only launch left in the
-    #     workspace (same method), so that one step's kernel shares can be set beside the
-    #     ncu launch list's
-    comb_lens = sets[(nk - 1) % nsets]["lens"]
-    for i in range(3):
-        mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse)
-    barrier()
-    cevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
-    t_start = time.time()
-    torch.cuda._sleep(int(2e7))
-    for i in range(nk):
-        cevs[i][0].record(stream)
-        mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse)
-        cevs[i][1].record(stream)
-    barrier()
-    windows.append((t_start, time.time()))
-    comb_mean_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in cevs) / nk, dist, dev)
-
-    # --- end to end through the C ABI with host buffers (mfa_decode_run_host): every step
-    #     copies its pinned host inputs (q, block table, lengths) in and its outputs (out, lse)
-    #     back inside the timed region.  Three streams rotate, each with its own device
-    #     buffers and workspace, so that one step's copies overlap the other steps' kernels.
+    # end to end through the C ABI with host buffers (mfa_decode_run_host): every step
+    # copies its pinned host inputs (q, block table, lengths) in and its outputs (out, lse)
+    # back inside the timed region.  Three streams rotate, each with its own device buffers
+    # and workspace, so that one step's copies overlap the other steps' kernels.
     q_h = case.q.pin_memory()
     table_h = case.block_table.pin_memory()
     lens_h = case.seq_lens.pin_memory()
     lanes = []
     for _ in range(E2E_LANES):
-        d_k = mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                          host_seq_lens=lens, flags=mfa.MFA_PLAN_EARLY_METADATA, device=dev, tokens_per_seq=T)
-        lanes.append((d_k, torch.cuda.Stream(dev), torch.empty(B * T, 64, 256, dtype=torch.bfloat16).pin_memory(),
+        lanes.append((decoder(mfa.MFA_PLAN_EARLY_METADATA), torch.cuda.Stream(dev),
+                      torch.empty(B * T, 64, 256, dtype=torch.bfloat16).pin_memory(),
                       torch.empty(B * T, 64, dtype=torch.float32).pin_memory()))
     h2d = sum(t.numel() * t.element_size() for t in (q_h, table_h, lens_h))
     d2h = sum(t.numel() * t.element_size() for t in lanes[0][2:])
@@ -462,101 +446,34 @@ def run_native(args, case, rank: int, world: int):
         for _, st_k, _, _ in lanes:
             ev = torch.cuda.Event()
             ev.record(st_k)
-            stream.wait_event(ev)
+            tm.stream.wait_event(ev)
 
     for i in range(args.warmup):
         e2e_step(i)
     join_lanes()
-    barrier()
+    tm.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_start = time.time()
-    e0.record(stream)
+    e0.record(tm.stream)
     for _, st_k, _, _ in lanes:
         st_k.wait_event(e0)
     t_enq = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         e2e_step(i)
-    enqueue_ms = (time.perf_counter() - t_enq) * 1e3 / args.steps   # host time to issue one step
+    enqueue_ms = (time.perf_counter() - t_enq) * 1e3 / steps   # host time to issue one step
     join_lanes()
-    e1.record(stream)
-    barrier()
-    windows.append((t_start, time.time()))
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
+    e1.record(tm.stream)
+    tm.barrier()
+    tm.windows.append((t_start, time.time()))
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), tm.dist, dev) / steps
 
-    # --- the KV append of the same batch (each sequence's T new rows at its last T positions),
-    #     alone (per-launch events behind a GPU sleep) and chained in front of the decode
-    #     step (append -> decode -> combine, K steps from one CUDA graph)
-    k_new = inputs.new_token_rows(B * T, seed=w.seed + 101, kinds=("normal",)).to(dev)
-    v_new = inputs.new_token_rows(B * T, seed=w.seed + 102, kinds=("normal",)).to(dev)
-    positions = (case.seq_lens.to(torch.int32) - T).to(dev)
-
-    def append(i):
-        s = sets[i % nsets]
-        mfa.mfa_kv_append(dec.problem, k_new, v_new, positions, s["table"], s["k"], s["v"], s["ks"], s["vs"],
-                          device_status=dec.workspace)
-
-    for i in range(3):
-        append(i)
-    barrier()
-    aevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nk)]
-    t_start = time.time()
-    torch.cuda._sleep(int(2e7))
-    for i in range(nk):
-        aevs[i][0].record(stream)
-        append(i)
-        aevs[i][1].record(stream)
-    barrier()
-    windows.append((t_start, time.time()))
-    app_mean_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in aevs) / nk, dist, dev)
-    graph3 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph3):
-        for i in range(args.steps):
-            append(i)
-            step(i)
-    graph3.replay()
-    barrier()
-    e0.record(stream)
-    graph3.replay()
-    e1.record(stream)
-    barrier()
-    ms_step_append = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.steps
-    app_status = mfa.mfa_read_device_status(dec.workspace)
-    if app_status != 0:
-        raise RuntimeError(f"append + decode steps set device status bits {app_status:#x} on {w.name}")
-    app_bytes = append_bytes(B, w.kv_dtype, T=T)
-
-    # keep sampling clocks until the windows hold enough samples
-    clocks = sampler.summary(windows)
-    if clocks["samples"] < 5:
-        t_start = time.time()
-        i = 0
-        while time.time() - t_start < 0.6:
-            graph.replay()
-            torch.cuda.synchronize()
-        windows.append((t_start, time.time()))
-        time.sleep(0.1)
-        clocks = sampler.summary(windows)
-        clocks["window"] = "timed regions plus 0.6 s of identical steps"
-    sampler.stop()
-
-    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
-    kv_gbs = whole_job_gbs(acct["kv"], world, ms_step)
+    hbm_peak, bf16_peak, _, peak_src = load_peaks()
     achieved = acct["total"] / (kern_mean_ms * 1e-3) / 1e9
-    tflops = flops * world / (ms_step * 1e-3) / 1e12
-    t_hbm = acct["total"] / (hbm_peak * 1e9)
-    t_tc = flops / (bf16_peak * 1e12)
-    result = {
-        "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV, f16 MMA",
-        "data": "synthetic",
-        "config": workload_config(case, {"l2": f"{nsets} rotating input copies ({nsets * set_bytes / 1e6:.0f} MB "
-                                               f"of KV) so no step reads KV left in L2 by the previous one",
-                                         "num_ctas": G, "timing": "K steps replayed from one CUDA graph",
-                                         "flags": "MFA_PLAN_EARLY_METADATA"}),
-        "tflops": tflops,
-        "ms_per_step_without_early_metadata": ms_step_strict,
-        "hbm_roofline_frac": (t_hbm / (ms_step * 1e-3)),
-        "tensor_roofline_frac": (t_tc / (ms_step * 1e-3)),
+    res = {
+        "value": whole_job_gbs(acct["kv"], world, ms_step), "unit": "GB/s", "ms_per_step": ms_step,
+        "tflops": flops * world / (ms_step * 1e-3) / 1e12,
+        "hbm_roofline_frac": (acct["total"] / (hbm_peak * 1e9)) / (ms_step * 1e-3),
+        "tensor_roofline_frac": (flops / (bf16_peak * 1e12)) / (ms_step * 1e-3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": profiled_traffic(w.name),
                      "kernel": "mfa_decode_kernel", "mean_launch_ms": kern_mean_ms,
@@ -566,26 +483,127 @@ def run_native(args, case, rank: int, world: int):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "path": f"mfa_decode_run_host (pinned host buffers in and out), {E2E_LANES} streams in rotation",
                 "host_enqueue_ms_per_step": enqueue_ms},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "config": workload_config(case, {"l2": f"{nsets} rotating input copies ({nsets * set_bytes / 1e6:.0f} MB "
+                                               f"of KV) so no step reads KV left in L2 by the previous one",
+                                         "num_ctas": G, "timing": "K steps replayed from one CUDA graph",
+                                         "flags": "MFA_PLAN_EARLY_METADATA"}),
+        "steps": steps,
+        "gpu_launches": launches_per_step * steps,
         "device_status": status,
-        "kernels_live": {
-            "mean_launch_ms": {"mfa_decode_kernel": kern_mean_ms, "mfa_combine_kernel": comb_mean_ms,
-                               "mfa_kv_append_kernel": app_mean_ms},
-            "share_of_one_step": {k: v / (kern_mean_ms + comb_mean_ms + app_mean_ms) for k, v in
-                                  (("mfa_decode_kernel", kern_mean_ms), ("mfa_combine_kernel", comb_mean_ms),
-                                   ("mfa_kv_append_kernel", app_mean_ms))},
-            "timing": "each kernel alone, per-launch events behind a GPU sleep (launch latency included)"},
-        "kv_append": {"kernel": "mfa_kv_append_kernel", "mean_launch_ms": app_mean_ms,
-                      "algorithmic_bytes_per_launch": app_bytes,
-                      "achieved_gbs": app_bytes / (app_mean_ms * 1e-3) / 1e9,
-                      "frac_of_hbm": app_bytes / (app_mean_ms * 1e-3) / 1e9 / hbm_peak,
-                      "bound": "latency: one dependent load chain (position, page id, row) per row",
-                      "ms_per_step_with_append": ms_step_append,
-                      "timing": "append alone: per-launch events behind a GPU sleep; with append: "
-                                "K steps of append + decode + combine from one CUDA graph",
-                      "device_status": app_status},
     }
+    if not headline:
+        del sets, lanes, graph
+        return res
+
+    # --- the same K steps without the early-metadata overlap (every read after the previous step)
+    dec_strict = decoder(0)
+    res["ms_per_step_without_early_metadata"], _ = tm.graph_ms(lambda i: step(i, dec_strict), steps)
+
+    # --- the combine kernel alone, on the partials the last decode-only launch left in the
+    #     workspace, so that one step's kernel shares can be set beside the ncu launch list's
+    comb_lens = sets[0]["lens"]
+    step(0, dec_only)
+    comb_mean_ms = tm.per_launch_ms(
+        lambda i: mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse),
+        max(min(steps, 400), 50))
+
+    # --- the KV append of the same batch (each sequence's T new rows at its last T positions),
+    #     alone and chained in front of the decode step (append -> decode -> combine)
+    k_new = inputs.new_token_rows(B * T, seed=w.seed + 101, kinds=("normal",)).to(dev)
+    v_new = inputs.new_token_rows(B * T, seed=w.seed + 102, kinds=("normal",)).to(dev)
+    positions = (case.seq_lens.to(torch.int32) - T).to(dev)
+
+    def append(i):
+        s = sets[i % nsets]
+        mfa.mfa_kv_append(dec.problem, k_new, v_new, positions, s["table"], s["k"], s["v"], s["ks"], s["vs"],
+                          device_status=dec.workspace)
+
+    app_mean_ms = tm.per_launch_ms(append, max(min(steps, 400), 50))
+
+    def append_and_step(i):
+        append(i)
+        step(i)
+
+    ms_step_append, _ = tm.graph_ms(append_and_step, steps)
+    app_status = mfa.mfa_read_device_status(dec.workspace)
+    if app_status != 0:
+        raise RuntimeError(f"append + decode steps set device status bits {app_status:#x} on {w.name}")
+    app_bytes = append_bytes(B, w.kv_dtype, T=T)
+    res["kernels_live"] = {
+        "mean_launch_ms": {"mfa_decode_kernel": kern_mean_ms, "mfa_combine_kernel": comb_mean_ms,
+                           "mfa_kv_append_kernel": app_mean_ms},
+        "share_of_one_step": {k: v / (kern_mean_ms + comb_mean_ms + app_mean_ms) for k, v in
+                              (("mfa_decode_kernel", kern_mean_ms), ("mfa_combine_kernel", comb_mean_ms),
+                               ("mfa_kv_append_kernel", app_mean_ms))},
+        "timing": "each kernel alone, per-launch events behind a GPU sleep (launch latency included)"}
+    res["kv_append"] = {
+        "kernel": "mfa_kv_append_kernel", "mean_launch_ms": app_mean_ms,
+        "algorithmic_bytes_per_launch": app_bytes,
+        "achieved_gbs": app_bytes / (app_mean_ms * 1e-3) / 1e9,
+        "frac_of_hbm": app_bytes / (app_mean_ms * 1e-3) / 1e9 / hbm_peak,
+        "bound": "latency: one dependent load chain (position, page id, row) per row",
+        "ms_per_step_with_append": ms_step_append,
+        "added_ms_per_step": ms_step_append - ms_step,
+        "timing": "append alone: per-launch events behind a GPU sleep; with append: "
+                  "K steps of append + decode + combine from one CUDA graph",
+        "device_status": app_status}
+    return res
+
+
+def run_native(args, case, rank: int, world: int, side_names=()):
+    import torch
+    from decode_attention_02_gb300 import build, inputs
+
+    build.build_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    windows = []
+    tm = _Timer(dev, dist, windows)
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.2)
+
+    head = measure_workload(args, case, tm, world, args.steps, headline=True)
+    side = {}
+    for name in side_names:
+        c = inputs.generate(rank_workload(inputs.WORKLOADS[name], rank))
+        r = measure_workload(args, c, tm, world, min(args.steps, SIDE_STEPS), headline=False)
+        side[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "tflops", "hbm_roofline_frac", "roofline",
+                                        "e2e", "steps", "device_status")}
+        side[name]["config"] = {k: r["config"][k] for k in ("batch", "total_tokens", "kv_dtype", "num_ctas",
+                                                             "new_tokens_per_seq")}
+        del c, r
+        torch.cuda.empty_cache()
+
+    # keep sampling clocks until the windows hold enough samples
+    clocks = sampler.summary(windows)
+    if clocks["samples"] < 5:
+        t_start = time.time()
+        while time.time() - t_start < 0.6:
+            tm.barrier()
+            time.sleep(0.01)
+        windows.append((t_start, time.time()))
+        time.sleep(0.1)
+        clocks = sampler.summary(windows)
+        clocks["window"] = "timed regions plus 0.6 s idle"
+    sampler.stop()
+
+    w = case.workload
+    result = {
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV, f16 MMA",
+        "data": "synthetic", "config": head["config"],
+    }
+    for k in ("tflops", "ms_per_step_without_early_metadata", "hbm_roofline_frac", "tensor_roofline_frac",
+              "roofline", "e2e", "gpu_launches", "device_status", "kernels_live", "kv_append"):
+        result[k] = head[k]
+    result["clocks"] = clocks
+    if side:
+        result["workloads"] = side
     return result
 
 
@@ -597,6 +615,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workloads", default="all",
+                    help="side workloads measured after the headline: all, none, or a comma list")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -616,7 +636,13 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.init_process_group("nccl")
-    res = run_native(args, case, rank, world)
+    if args.workloads == "all":
+        side_names = [n for n in SIDE_WORKLOADS if n != args.workload]
+    elif args.workloads == "none":
+        side_names = []
+    else:
+        side_names = [n for n in args.workloads.split(",") if n]
+    res = run_native(args, case, rank, world, side_names)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             import oracle

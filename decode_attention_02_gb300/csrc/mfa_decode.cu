@@ -502,12 +502,13 @@ __device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uin
 }
 
 // e4m3: per-token scale of box row ri of page pg of tile `ti` ({page 0, page 1, rows 0,
-// rows 1}); 0 for rows past the sequence end (the last page's valid rows sit at the end of
+// rows 1}); 0 for rows past the sequence end and for a page id outside the pool (the last page's valid rows sit at the end of
 // the box, so box row ri holds page row ri - (64 - rows)).
 __device__ __forceinline__ float token_scale(const float* __restrict__ sc, const int4 ti, int pg, int ri) {
   const int r = pg ? ti.w : ti.z;
-  if (r <= 0 || ri < kPage - r) return 0.f;
-  return __ldg(sc + static_cast<size_t>(pg ? ti.y : ti.x) * kPage + ri - (kPage - r));
+  const int blk = pg ? ti.y : ti.x;   // -1: an id outside the pool (its page reads as zeros)
+  if (r <= 0 || ri < kPage - r || blk < 0) return 0.f;
+  return __ldg(sc + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
 }
 
 // e4m3 ring use index of the K (is_v = false) or V part (page pg, d-half dh) of tile t of a
@@ -734,10 +735,11 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       const int32_t* row = p.block_table + static_cast<size_t>(sg.x / p.tokens) * p.max_pages;
       int b0 = row[2 * j];
       int b1 = (r1 > 0) ? row[2 * j + 1] : 0;
-      // an id outside the pool is reported and replaced by page 0, so every TMA coordinate
-      // stays inside the pool (the output of that sequence is then wrong)
-      if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = 0; }
-      if (r1 > 0 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = 0; }
+      // an id outside the pool is reported and replaced by -1: the TMA box then lies wholly
+      // outside the pool and lands as zeros, and an e4m3 page's scales read as 0, so that
+      // page contributes zero keys and zero values and no other page's data
+      if (b0 < 0 || b0 >= p.num_blocks) { bad_blk = true; b0 = -1; }
+      if (r1 > 0 && (b1 < 0 || b1 >= p.num_blocks)) { bad_blk = true; b1 = -1; }
       tile_info[n] = make_int4(b0, b1, r0, r1);
     }
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
@@ -2159,6 +2161,9 @@ extern "C" mfa_status mfa_decode_run_static_workspace(
   st = check_plan(plan, pr);
   if (st != MFA_OK) return st;
   if (plan->workspace_bytes > MFA_STATIC_WORKSPACE_BYTES) return MFA_ERR_WORKSPACE;
+  // the partials of a split plan live in the library's array, which the caller cannot name:
+  // without the combine they could never be merged, so such a plan is refused
+  if ((plan->flags & MFA_PLAN_NO_COMBINE) != 0 && plan->num_ctas > 1) return MFA_ERR_INVALID_ARG;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -2174,6 +2179,11 @@ extern "C" mfa_status mfa_decode_run_static_workspace(
     }
     ws = g_static_ptr[dev];
   }
+  // every argument is validated before anything is enqueued, so a refused call leaves
+  // nothing on the stream
+  st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse, ws,
+                 MFA_STATIC_WORKSPACE_BYTES);
+  if (st != MFA_OK || pr->batch == 0) return st;
   // the status word is the only part that must start at zero; partial results are
   // always written before they are read
   e = cudaMemsetAsync(ws, 0, 4, static_cast<cudaStream_t>(stream_ptr));

@@ -255,14 +255,22 @@ const char* mfa_status_string(mfa_status status);
  * created on every device that loads it and kept until the process exits.  This
  * call allocates nothing.  Its first call on a device looks the array's device
  * address up (cudaGetSymbolAddress, with that device current); make that first
- * call before any stream capture.  Each call clears the array's status word,
- * then enqueues exactly what mfa_decode_run enqueues (MFA_PLAN_CHECK included).
- * All calls on a device share the one array and it keeps the last call's
- * contents, so two calls whose kernels may overlap on the GPU (different
+ * call before any stream capture.  Every argument is validated first; a call
+ * that is refused enqueues nothing.  A valid call clears the array's status
+ * word, then enqueues exactly what mfa_decode_run enqueues (MFA_PLAN_CHECK
+ * included).  All calls on a device share the one array and it keeps the last
+ * call's contents, so two calls whose kernels may overlap on the GPU (different
  * streams, no ordering between them) race on it: order them on one stream.
- * Plans whose workspace_bytes exceed MFA_STATIC_WORKSPACE_BYTES are rejected
- * with MFA_ERR_WORKSPACE; at the default 24 MiB that covers
- * batch + num_ctas - 1 <= 382 partial slots (for example B <= 231 on 152 SMs).
+ *   - Plans whose workspace_bytes exceed MFA_STATIC_WORKSPACE_BYTES are rejected
+ *     with MFA_ERR_WORKSPACE; at the default 24 MiB that covers
+ *     batch + num_ctas - 1 <= 382 partial slots (for example B <= 231 on 152 SMs).
+ *   - A plan with MFA_PLAN_NO_COMBINE and more than one CTA is rejected with
+ *     MFA_ERR_INVALID_ARG: its partial results would stay in the library's
+ *     array, which no caller can pass to mfa_combine().
+ *   - The array's address is never handed out, so mfa_read_device_status()
+ *     cannot read this path's status word.  Its device-side checks (a block id
+ *     outside the pool, a bad length, a timed-out wait) are reported only
+ *     through MFA_PLAN_CHECK, as MFA_ERR_DEVICE_CHECK.
  * Arguments are those of mfa_decode_run without the workspace.
  */
 #define MFA_STATIC_WORKSPACE_BYTES (24u * 1024u * 1024u)

@@ -203,6 +203,30 @@ def test_bad_block_id_is_reported_not_faulted():
     assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("bad_id", [-3, 10 ** 6])
+def test_bad_block_id_reads_as_a_page_of_zeros(kv, bad_id):
+    """A block id outside the pool is reported, and its page contributes zero keys and zero
+    values: the output equals the oracle's over a cache whose entry points at a zero page."""
+    case = inputs.small("badblk0", 3, [100, 200, 150], kv_dtype=kv, seed=15)
+    ref_case = inputs.small("badblk0", 3, [100, 200, 150], kv_dtype=kv, seed=15)
+    case.block_table[1, 2] = bad_id
+    # the oracle's input: one more physical page, all zeros (e4m3 code 0 with scale 1)
+    nb = ref_case.num_blocks
+    zero_k = torch.zeros((1,) + tuple(ref_case.k_cache.shape[1:]), dtype=ref_case.k_cache.dtype)
+    ref_case.k_cache = torch.cat([ref_case.k_cache, zero_k]).contiguous()
+    ref_case.v_cache = torch.cat([ref_case.v_cache, zero_k.clone()]).contiguous()
+    if ref_case.k_scale is not None:
+        one = torch.ones((1, ref_case.k_scale.shape[1]), dtype=torch.float32)
+        ref_case.k_scale = torch.cat([ref_case.k_scale, one]).contiguous()
+        ref_case.v_scale = torch.cat([ref_case.v_scale, one.clone()]).contiguous()
+    ref_case.block_table[1, 2] = nb
+    out, lse, dec = gpu_decode(case, flags=0)
+    assert mfa.mfa_read_device_status(dec.workspace) == mfa.MFA_DEV_BAD_BLOCK
+    lim = (3e-2, 1.5e-2) if kv == "fp8_e4m3" else (BF16_MAX_ABS, BF16_REL_L2)
+    check_parity(case, out, lse, *lim, ref=oracle.decode(ref_case))
+
+
 def test_length_beyond_table_is_reported():
     case = inputs.small("badlen", 2, [100, 200], seed=16)
     t = to_dev(case)
