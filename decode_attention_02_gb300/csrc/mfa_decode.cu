@@ -72,22 +72,14 @@ constexpr int kD = 256;            // head width
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
-constexpr int kDequantThreads = 128;  // e4m3: one thread per token row of a tile
-// bf16 : warp 0 TMA, warp 1 QK^T MMAs, warps 2..9 softmax, warp 10 PV MMAs (352 threads,
-//        168 registers each).
-// e4m3 : warpgroup 0 = warp 0 TMA, warp 1 QK^T MMAs, warp 2 PV MMAs (warp 3 idle), warpgroups 1-2 = warps
-//        4..11 softmax, warpgroup 3 = warps 12..15 V dequantisation; launched with 128
-//        registers per thread and rebalanced to 80 / 168 / 168 / 96 (sum 4 x 128).
+// Both KV formats: warp 0 TMA, warp 1 QK^T MMAs, warps 2..9 softmax, warp 10 PV MMAs (352
+// threads, 168 registers each).
 template <bool kFp8>
-__host__ __device__ constexpr int threads_of() { return kFp8 ? 512 : 352; }
+__host__ __device__ constexpr int threads_of() { return 352; }
 template <bool kFp8>
-__host__ __device__ constexpr int pv_warp() { return kFp8 ? 2 : 10; }   // issues the PV MMAs
+__host__ __device__ constexpr int pv_warp() { return 10; }   // issues the PV MMAs
 template <bool kFp8>
-__host__ __device__ constexpr int softmax_warp0() { return kFp8 ? 4 : 2; }
-constexpr int kDequantWarp0 = 12;
-constexpr uint32_t kRegsCtl = 80, kRegsSoftmax = 168, kRegsDequant = 96;
-static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsDequant == 4 * (65536 / 512),
-              "e4m3 register split must add up to the launch budget (4 warpgroups x 128)");
+__host__ __device__ constexpr int softmax_warp0() { return 2; }
 constexpr int kMaxTilesPerCta = 128;
 // Schedule cost units: a 128-token tile weighs kCostTile, a sequence boundary inside a CTA's
 // range cost_seq (the next sequence's q and one more epilogue).  Measured per sequence switch:
@@ -98,7 +90,17 @@ __host__ __device__ constexpr int cost_seq(bool fp8) { return fp8 ? 10 : 3; }
 constexpr int kMaxTokensPerSeq = 4;   // new query tokens per sequence (multi-token decode)
 constexpr int kMaxSeg = kMaxTilesPerCta;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 domain: p <= 2^8 between rescales
+// Lazy running max (log2 domain): a head's reference max moves only when a score exceeds it
+// by this much, so p <= 2^8 (bf16 weights) or p <= 2^3 (e4m3: the weight times the token's
+// scaled V scale, below 2^5, must stay inside e4m3's 448) between rescales.
+template <bool kFp8>
+__host__ __device__ constexpr float rescale_threshold() { return kFp8 ? 3.0f : 8.0f; }
+// e4m3: each token's V scale s_v is folded into its weights as s_v 2^(kPvShift - E), E the
+// segment's reference exponent (every s_v so far below 2^(E + 1)); the output is scaled back by
+// 2^(E - kPvShift).  kPvShift = 4 puts typical weights near 1, where both e4m3 parts of the
+// weight are normal numbers, and keeps the largest (< 2^3 * 2 * 2^4) under 448.
+constexpr int kPvShift = 4;
+constexpr int kEMin = -120;   // floor of E (2^(kPvShift - E) stays a normal fp32 number)
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an abort
@@ -106,9 +108,9 @@ constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an a
 // Shared-memory map (offsets from a 1024-byte aligned base).  Both KV formats put the
 // barriers at the same offset; they differ below it:
 //   bf16 : Q 32 KB | P 16 KB | ring 10 x 16 KB (K/V operand tiles as TMA writes them)
-//   e4m3 : Q 32 KB (e4m3 hi and lo parts) | P 16 KB | V f16 64 KB (dequantised PV operand) |
-//          ring 12 x 8 KB (raw e4m3 boxes, K read by the MMA as they are); the per-token
-//          scales are read from global memory by the threads that apply them
+//   e4m3 : Q 32 KB (e4m3 hi and lo parts) | P 16 KB (e4m3 weights: hi part 8 KB, lo part 8 KB) |
+//          ring 20 x 8 KB (raw e4m3 boxes: both MMAs read K and V as TMA wrote them); the
+//          per-token scales are read from global memory by the threads that apply them
 constexpr int kOffQ = 0;                                     // 4 x [64 heads x 128 B]
 constexpr int kOffP = 32768;                                 // [128 tokens x 128 B]
 constexpr int kOffBar = 212992;                              // mbarriers
@@ -123,9 +125,8 @@ struct KvLayout<false> {
 };
 template <>
 struct KvLayout<true> {
-  static constexpr int kOffVh = 49152;              // 4 x 16 KB: (page, d-half) f16 tiles
-  static constexpr int kOffRing = 114688;
-  static constexpr int kNumSlots = 12;
+  static constexpr int kOffRing = 49152;
+  static constexpr int kNumSlots = 20;
   static constexpr int kSlotBytes = 8192;
   static constexpr int kExtraSmem = 0;
 };
@@ -139,22 +140,17 @@ constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nse
 // Ring-order counts.  K and V uses share one ring, and a consumer may only wait on a slot's
 // Full barrier once the slot's previous use has landed: a waiter two phases behind would see
 // the parity it wants and read a slot still being written.  With the QK^T and PV streams in
-// different threads, a tile's K uses follow the V uses of three tiles earlier in some slots
-// (and, for e4m3, its V uses follow its own K uses), with no barrier between the two streams
-// that orders them.  So each stream publishes how many tiles of its uses have landed:
-//   cnt[0]: K tiles whose four uses the QK^T issuer has seen land (the e4m3 issuer waits
-//           for a tile's K before it waits for the softmax, so that the count does not
-//           lag behind the softmax);
-//   cnt[1], cnt[2]: V tiles whose uses the V consumer (bf16: the PV issuer after its waits;
-//           e4m3: the dequant warps after the tile) has seen land, for page 0 and page 1
-//           (both written together).
-// The QK^T issuer waits for both V counts >= n - 2 before tile n's K uses; the e4m3
-// dequant warps wait for the K count >= n + 1 before tile n's V uses.  (A bf16 PV of tile n
-// already follows tile n's K through the softmax's P.)
-//   cnt[3]: e4m3 PV tiles issued.  The e4m3 QK^T issuer issues tile n only after PV(n - 2),
-//           so that a ready PV is not queued behind the next QK^T in the tensor pipe (the
-//           softmax cannot start tile n before PV(n - 2) completes anyway).
-constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1, PV tiles
+// different threads, some slots of tile n's K uses last held the V uses of an earlier tile
+// (bf16, 10 slots: V(n - 3); e4m3, 20 slots: V(n - 4)), with no barrier between the two
+// streams that orders them.  So the PV issuer publishes, after its Full waits, how many
+// tiles of V uses have landed (cnt[1], cnt[2]: page 0 and page 1, written together), and
+// the QK^T issuer waits for both counts >= n - kVLag + 1 before tile n's K uses.  The other
+// direction needs no count: tile n's V slots last held K uses of tile n - 1 or earlier, and
+// a PV of tile n follows tile n's K through the softmax's P.  cnt[0] counts the K tiles the
+// QK^T issuer has issued (diagnostic).
+template <bool kFp8>
+__host__ __device__ constexpr int v_lag() { return kFp8 ? 4 : 3; }
+constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1, spare
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -169,8 +165,8 @@ static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
 
 enum Bar : int {
   kBarFull = 0,
-  kBarEmpty = kBarFull + 12,   // room for the larger ring
-  kBarQFull = kBarEmpty + 12,
+  kBarEmpty = kBarFull + 20,   // room for the larger ring
+  kBarQFull = kBarEmpty + 20,
   kBarQEmpty,
   kBarSFull,   // 2
   kBarSEmpty = kBarSFull + 2,
@@ -180,7 +176,6 @@ enum Bar : int {
   kBarOEmpty = kBarOFull + 2,
   kBarDrain = kBarOEmpty + 2,
   kBarQReady,   // e4m3: q split in place into e4m3 hi and lo parts
-  kBarVhFull,   // e4m3: a tile's V is in the f16 operand tile
   kBarCount
 };
 static_assert(kBarCount * 8 <= kOffCnt - kOffBar, "barrier area (the ring-order counts follow it)");
@@ -241,6 +236,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+// The same with the 64-byte swizzle (layout code 4): 64-byte rows, 8-row atoms of 512 bytes,
+// 16-byte chunk c of row r stored at chunk c ^ ((r >> 1) & 3).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
 
 // tcgen05 instruction descriptor for kind::f16: fp32 D, bf16 or f16 A/B,
 // K-major (0) or MN-major (1) operands, N>>3 at bit 17, M>>4 at bit 24.
@@ -251,10 +253,10 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn, bool b_mn
 }
 
 // tcgen05 instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0),
-// fp32 D, both operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3(int m, int n) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-         (static_cast<uint32_t>(m >> 4) << 24);
+// fp32 D, K-major (0) or MN-major (1) operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3(bool a_mn, bool b_mn, int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 __device__ __forceinline__ int clamp_len(int L, int cap, bool& bad) {
@@ -441,43 +443,12 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   const bool ok = wait_bar(bar, parity, abort_flag);
   return __all_sync(0xffffffffu, ok);
 }
-// The same bounded wait, sleeping 128 ns between polls: for waits off the critical chain (the
-// e4m3 softmax's, whose P has about 1 us of slack before the dequantised V it meets), so that
-// the waiting warps leave issue slots to the dequant warps that share their SM sub-partitions.
-__device__ __forceinline__ bool wait_lazy(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(128);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      if (abort_flag != nullptr) *abort_flag = 1;
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ bool wait_warp_lazy(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  const bool ok = wait_lazy(bar, parity, abort_flag);
-  return __all_sync(0xffffffffu, ok);
-}
-
 // ------------------------------------------------------------------ decode kernel
 
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t r;
   const uint16_t v = static_cast<uint16_t>(two_codes);
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 // Two floats to two e4m3 codes (round to nearest even, saturating); lo in the low byte.
@@ -501,6 +472,19 @@ __device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uin
   lo = pack_e4m3_sat(x0 - f16_lo(back), x1 - f16_hi(back));
 }
 
+// Split two PV weights x >= 0 (below 448) into e4m3 pairs hi + lo: hi = e4m3(x) rounded to
+// nearest, lo = e4m3(x - hi).  hi is read back exactly from its code: a 7-bit code b placed
+// at bit 20 of an fp32 word is the code's value times 2^-120 (subnormal codes included, as
+// fp32 subnormals), so one multiply by 2^120 restores it.  x - hi is exact in fp32, and
+// hi + lo matches x to 2^-9 of x where lo is a normal e4m3 number (x above about 2^-1), and
+// to 2^-10 absolute below that.
+__device__ __forceinline__ void split_weights_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_e4m3_sat(x0, x1);
+  const float f0 = __uint_as_float((hi & 0x7Fu) << 20) * 0x1p120f;
+  const float f1 = __uint_as_float(((hi >> 8) & 0x7Fu) << 20) * 0x1p120f;
+  lo = pack_e4m3_sat(x0 - f0, x1 - f1);
+}
+
 // e4m3: per-token scale of box row ri of page pg of tile `ti` ({page 0, page 1, rows 0,
 // rows 1}); 0 for rows past the sequence end and for a page id outside the pool (the last page's valid rows sit at the end of
 // the box, so box row ri holds page row ri - (64 - rows)).
@@ -515,8 +499,8 @@ __device__ __forceinline__ float token_scale(const float* __restrict__ sc, const
 // CTA with `ntiles` tiles.  The producer issues K(0), then K(t) and V(t-1) for t = 1..N-1,
 // then V(N-1), four uses each: K(0) = 0..3, K(t) = 8t-4.., V(t) = 8t+8.. except the last
 // tile's V, which directly follows its K: V(N-1) = 8N-4...  Every group of four starts at
-// a multiple of 4 and the ring has 12 slots, so a group never wraps: K's two pages of one
-// d-half sit in adjacent slots and form one 128-row MMA operand.
+// a multiple of 4 and the e4m3 ring has 20 slots, so a group never wraps: K's two pages of
+// one d-half sit in adjacent slots and form one 128-row MMA operand.
 __device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v, int pg, int dh) {
   const uint32_t base = is_v ? (t + 1 < ntiles ? 8u * t + 8u : 8u * t + 4u) : (t == 0 ? 0u : 8u * t - 4u);
   return base + (is_v ? 2u * pg + dh : 2u * dh + pg);
@@ -549,15 +533,13 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // ---------------- set-up: barriers (one per lane of warp 0), tensor memory
   if (warp == 0) {
     for (int i = lane; i < kBarCount; i += 32) {
-      // arrivals per phase: the softmax threads for the barriers they release, the dequant
-      // threads for the f16 V tile, one commit from each MMA issuer for the drain, and one
-      // (a commit, an expect_tx arrive, or the dequant warps' leader) for the others
+      // arrivals per phase: the softmax threads for the barriers they release, one commit
+      // from each MMA issuer for the drain, and one (a commit or an expect_tx arrive) for
+      // the others
       uint32_t count = 1;
       if (i == kBarSEmpty || i == kBarSEmpty + 1 || i == kBarOEmpty || i == kBarOEmpty + 1 ||
           i == kBarPFull || i == kBarQReady)
         count = kSoftmaxThreads;
-      else if (i == kBarVhFull)
-        count = kDequantThreads;
       else if (i == kBarDrain)
         count = 2;
       mbar_init(bar(i), count);
@@ -746,11 +728,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   }
   __syncthreads();
 
-  // e4m3 warpgroup register split (see threads_of), at the top of each role so that the
-  // role's budget covers all of its code: control warps give registers up, the softmax
-  // warpgroups take them; the four budgets add up to the launch's 4 x 128
   if (warp == 0) {
-    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
     // ---------------- producer: TMA loads of Q, K and V in ring order.  Each group of four
     // ring uses (a tile's K, or a tile's V) is issued by lanes 0..3 together, one use per
     // lane; groups go out strictly in ring order, so every slot's phases stay in step.
@@ -843,7 +821,6 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       }
     }
   } else if (warp == 1 || warp == pv_warp<kFp8>()) {
-    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
     // ---------------- MMA issuers: QK^T of tile n, then PV of tile n - 1, so the next tile's
     // scores are computed while the softmax works on the current one.  Warp 1 issues the
     // QK^T stream and warp pv_warp the PV stream (they share no operand, accumulator or
@@ -852,8 +829,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     // tensor memory is released.
     if (lane == 0 && ntiles > 0) {
       constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
-      constexpr uint32_t kIdescQK8 = idesc_e4m3(128, 128);
+      constexpr uint32_t kIdescQK8 = idesc_e4m3(false, false, 128, 128);
       constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, 64);
+      constexpr uint32_t kIdescPV8 = idesc_e4m3(true, true, 128, 64);
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
       for (int n = 0; n <= ntiles && ok; ++n) {
@@ -861,18 +839,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
           const uint32_t u0 = ring_use(n, ntiles, false, 0, 0);
-          // the slots of tile n's K last held V(n - 3): it must have landed (ring-order counts)
-          if (n >= 3) ok = wait_count(cnt + 1, n - 2, abort_flag) && wait_count(cnt + 2, n - 2, abort_flag);
-          if constexpr (kFp8) {
-            // e4m3: the tile's K first, so that its count reaches the dequant warps without
-            // waiting for the softmax
-            for (int c = 0; c < 4 && ok; ++c)
-              ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
-            if (ok) st_release_cta(cnt, n + 1);
-          }
+          // some slots of tile n's K last held V(n - v_lag): it must have landed (ring-order counts)
+          constexpr int kLag = v_lag<kFp8>();
+          if (n >= kLag)
+            ok = wait_count(cnt + 1, n - kLag + 1, abort_flag) && wait_count(cnt + 2, n - kLag + 1, abort_flag);
           if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
-          if (kFp8 && ok && n >= 2) ok = wait_count(cnt + 3, n - 1, abort_flag);   // PV(n - 2) issued first
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
@@ -891,22 +863,28 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               umma_commit(bar(kBarEmpty + slot));
             }
             if (!ok) break;
-            st_release_cta(cnt, n + 1);
           } else {
             // e4m3 K boxes as TMA wrote them: the two pages of d-half dh are adjacent slots,
             // one 128-row A operand; B stacks q's e4m3 hi part (rows 0..63) over its lo part
-            // (rows 64..127), so each K step (32) reads K once for both (its Full waits are above)
+            // (rows 64..127), so each K step (32) reads K once for both
 #pragma unroll
             for (int dh = 0; dh < 2; ++dh) {
+              for (int c = 2 * dh; c < 2 * dh + 2 && ok; ++c)
+                ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
               const uint32_t a0 = sbase + kOffRing + ((u0 + 2 * dh) % kNumSlots) * kSlotBytes;
               const uint32_t b0 = sbase + kOffQ + dh * 16384;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_f8_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
                            kIdescQK8, (dh | kk) != 0);
+              umma_commit(bar(kBarEmpty + (u0 + 2 * dh) % kNumSlots));
+              umma_commit(bar(kBarEmpty + (u0 + 2 * dh + 1) % kNumSlots));
             }
-            for (int c = 0; c < 4; ++c) umma_commit(bar(kBarEmpty + (u0 + c) % kNumSlots));
+            if (!ok) break;
           }
+          st_release_cta(cnt, n + 1);
           umma_commit(bar(kBarSFull + (n & 1)));
           if (last) umma_commit(bar(kBarQEmpty));
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
@@ -919,43 +897,50 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           const int4 ti = tile_info[m];
           const uint32_t uv = ring_use(m, ntiles, true, 0, 0);
           ok = wait_bar(bar(kBarPFull), m & 1, abort_flag);
-          if (kFp8 && ok) ok = wait_bar(bar(kBarVhFull), m & 1, abort_flag);
           if (ok && first && sv >= 2) ok = wait_bar(bar(kBarOEmpty + kb), ((sv >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           for (int pg = 0; pg < 2 && ok; ++pg) {
             const int r = pg ? ti.w : ti.z;
             for (int hh = 0; hh < 2; ++hh) {
-              uint32_t a0;
-              if constexpr (!kFp8) {
-                const uint32_t u = uv + 2 * pg + hh;
-                ok = wait_bar(bar(kBarFull + u % kNumSlots), (u / kNumSlots) & 1, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                a0 = sbase + kOffRing + (u % kNumSlots) * kSlotBytes;
-              } else {
-                a0 = sbase + KvLayout<true>::kOffVh + (2 * pg + hh) * 16384;   // filled by the dequant warps
-              }
+              const uint32_t u = uv + 2 * pg + hh;
+              ok = wait_bar(bar(kBarFull + u % kNumSlots), (u / kNumSlots) & 1, abort_flag);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t a0 = sbase + kOffRing + (u % kNumSlots) * kSlotBytes;
+              const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 128u * kb + 64u * hh;
               if (r > 0) {
-                const uint32_t b0 = sbase + kOffP + pg * 8192;
-                const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 128u * kb + 64u * hh;
+                if constexpr (!kFp8) {
+                  const uint32_t b0 = sbase + kOffP + pg * 8192;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  umma_f16_ss(d_tmem, smem_desc(a0 + 2048 * kk, 8192, 1024),
-                              smem_desc(b0 + 2048 * kk, 1024, 1024), kIdescPV,
-                              !(first && pg == 0 && kk == 0));
+                  for (int kk = 0; kk < 4; ++kk)
+                    umma_f16_ss(d_tmem, smem_desc(a0 + 2048 * kk, 8192, 1024),
+                                smem_desc(b0 + 2048 * kk, 1024, 1024), kIdescPV,
+                                !(first && pg == 0 && kk == 0));
+                } else {
+                  // A = V^T straight from the e4m3 box ([64 tokens][128 d], MN-major, one
+                  // 128-element swizzle atom along d); B = the weights' hi part, then their
+                  // lo part ([128 tokens][64 heads] each, MN-major, 64-byte swizzle); K = 32
+                  // tokens per MMA, both parts into one accumulator
+                  const uint32_t bh = sbase + kOffP + pg * 4096;
+#pragma unroll
+                  for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ad = smem_desc(a0 + 4096 * kk, 8192, 1024);
+                    umma_f8_ss(d_tmem, ad, smem_desc_sw64(bh + 2048 * kk, 4096, 512), kIdescPV8,
+                               !(first && pg == 0 && kk == 0));
+                    umma_f8_ss(d_tmem, ad, smem_desc_sw64(bh + 8192 + 2048 * kk, 4096, 512), kIdescPV8, 1u);
+                  }
+                }
               }
-              if constexpr (!kFp8) umma_commit(bar(kBarEmpty + (uv + 2 * pg + hh) % kNumSlots));
+              umma_commit(bar(kBarEmpty + u % kNumSlots));
             }
           }
           if (!ok) break;
-          if constexpr (!kFp8) {   // V(m) has landed
-            st_release_cta(cnt + 1, m + 1);
-            st_release_cta(cnt + 2, m + 1);
-          }
+          // V(m) has landed
+          st_release_cta(cnt + 1, m + 1);
+          st_release_cta(cnt + 2, m + 1);
           umma_commit(bar(kBarPvDone));
           if (last) umma_commit(bar(kBarOFull + kb));
-          if constexpr (kFp8) st_release_cta(cnt + 3, m + 1);   // PV(m) issued
           if (++jv == sg.z && ++sv < nseg) jv = seg[sv].y;
         }
       }
@@ -964,73 +949,11 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       umma_commit(bar(kBarDrain));
       wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
     }
-  } else if (kFp8 && warp < softmax_warp0<kFp8>()) {
-    // e4m3: warp 3 completes warpgroup 0 and has no role
-    if constexpr (kFp8) reg_dealloc<kRegsCtl>();
-  } else if (kFp8 && warp >= kDequantWarp0) {
-    if constexpr (kFp8) {
-      reg_dealloc<kRegsDequant>();
-      // ---------------- e4m3 V -> f16 PV operand (warps 12..15; thread = token row of a tile)
-      // The token's V scale multiplies its row here (P keeps plain weights).  Scales above
-      // 146 would let 448 * scale leave the f16 range: they are clamped and reported.
-      using L8 = KvLayout<true>;
-      const int dt = tid - 32 * kDequantWarp0;   // 0..127
-      const int pg = dt >> 6, ri = dt & 63;       // page of the tile (warp-uniform), row
-      bool aborted = false, range_bad = false;
-      if (p.early_metadata) grid_dep_wait();      // v_scale may be written by the preceding kernel
-      float sv_next = (ntiles > 0) ? token_scale(p.v_scale, tile_info[0], pg, ri) : 0.f;
-      for (int n = 0; n < ntiles; ++n) {
-        const int4 ti = tile_info[n];
-        const int rp = pg ? ti.w : ti.z;
-        float sv = sv_next;                      // loaded one tile ahead
-        if (n + 1 < ntiles) sv_next = token_scale(p.v_scale, tile_info[n + 1], pg, ri);
-        range_bad |= !(sv <= 146.f);
-        sv = fminf(sv, 146.f);
-        const uint32_t sv2 = pack_f16_sat(sv, sv);
-        auto cv = [&](uint32_t two) { return hmul2(e4m3x2_to_f16x2(two), sv2); };
-        // the f16 tile is free once the previous tile's PV has read it
-        bool ok = (n == 0) || wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag);
-        // tile n's V uses follow its K uses in the ring: K(n) must have landed first
-        if (ok) ok = wait_count_warp(cnt, n + 1, abort_flag);
-        for (int dh = 0; dh < 2 && ok; ++dh) {
-          const uint32_t use = ring_use(n, ntiles, true, pg, dh);
-          ok = wait_warp(bar(kBarFull + use % kNumSlots), (use / kNumSlots) & 1, abort_flag);
-          if (!ok || rp <= 0) continue;
-          const uint8_t* box = smem + kOffRing + (use % kNumSlots) * kSlotBytes + ri * 128;
-          uint4 rw[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) rw[q] = *reinterpret_cast<const uint4*>(box + ((q ^ (ri & 7)) << 4));
-          // [64 tokens x 64 d] f16 boxes, 128 B rows, 128B swizzle (as TMA would lay them out)
-          uint8_t* vh = smem + L8::kOffVh + (2 * pg + dh) * 16384 + ri * 128;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 w = rw[q];
-            const uint4 lo = make_uint4(cv(w.x), cv(w.x >> 16), cv(w.y), cv(w.y >> 16));
-            const uint4 hi = make_uint4(cv(w.z), cv(w.z >> 16), cv(w.w), cv(w.w >> 16));
-            const int j0 = 2 * q, j1 = 2 * q + 1;   // 16-byte f16 chunks 0..15 of the 128-d row
-            *reinterpret_cast<uint4*>(vh + (j0 >> 3) * 8192 + (((j0 & 7) ^ (ri & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(vh + (j1 >> 3) * 8192 + (((j1 & 7) ^ (ri & 7)) << 4)) = hi;
-          }
-        }
-        // the four warps agree; past this point every ring read of the tile is done
-        if (named_bar_or(4, kDequantThreads, !ok || *abort_flag)) { aborted = true; break; }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(kBarVhFull));
-        if (dt == 0) {
-          st_release_cta(cnt + 1, n + 1);   // V(n) landed (and is read)
-          st_release_cta(cnt + 2, n + 1);
-          for (int c = 0; c < 4; ++c) mbar_arrive(bar(kBarEmpty + ring_use(n, ntiles, true, c >> 1, c & 1) % kNumSlots));
-        }
-      }
-      if (range_bad) atomicOr(p.status, MFA_DEV_RANGE);
-      if (aborted && dt == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
-    }
   } else {
-    if constexpr (kFp8) reg_alloc<kRegsSoftmax>();
     // ---------------- softmax + epilogue (256 threads: two warps per TMEM lane quarter)
     const int ts = tid - 32 * softmax_warp0<kFp8>();   // 0..255
     const int sw = warp - softmax_warp0<kFp8>();       // 0..7
-    const int grp = sw >> 2;                       // head half [32*grp, +32); e4m3 dequant: d-half
+    const int grp = sw >> 2;                       // head half [32*grp, +32)
     const int h0 = 32 * grp;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
     const int row = wq * 32 + lane;                // token row of a tile / d within an O half
@@ -1221,10 +1144,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       mbar_arrive(bar(kBarQReady));
     };
 
-    float sk_next = 0.f;                            // e4m3: K scale of this row in the next tile
+    float sk_next = 0.f, sv_next = 0.f;            // e4m3: K and V scales of this row in the next tile
+    int e_ref = kEMin;                              // e4m3: the segment's reference exponent of V scales
     if constexpr (kFp8) {
       if (ntiles > 0) {
         sk_next = token_scale(p.k_scale, tile_info[0], rpg, ri);
+        sv_next = token_scale(p.v_scale, tile_info[0], rpg, ri);
         convert_q(0);
       }
     }
@@ -1238,6 +1163,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       if (ts < kH) m_ref[ts] = -INFINITY;
       if constexpr (kFp8) {
         qinv = qinv_next;
+        e_ref = kEMin;
 #pragma unroll
         for (int h = 0; h < 32; ++h) lreg[h] = 0.f;
       }
@@ -1246,23 +1172,30 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       for (int j = sg.y; j < sg.z; ++j, ++n) {
         const bool first = (j == sg.y);
         const uint32_t s_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1) + h0 + lane_base;
-        const bool okS = kFp8 ? wait_warp_lazy(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag)
-                              : wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
+        const bool okS = wait_warp(bar(kBarSFull + (n & 1)), (n >> 1) & 1, abort_flag);
         aborted = aborted || !okS;
         bool pv_waited = (n == 0);   // PV of the previous tile must be done before P or O are touched
         const int rp = page_rows(L, j, rpg);
         const bool valid = okS && rp > 0 && ri >= kPage - rp;
         // score multiplier of this row: scale*log2(e), times (e4m3) the token's K scale and
-        // the 2^-sigma that undoes q's split scaling
-        float ck = c;
+        // the 2^-sigma that undoes q's split scaling; e4m3 also takes the token's V scale
+        float ck = c, svt = 0.f;
+        int sv_e = kEMin;   // e4m3: unbiased exponent of the token's V scale
         if constexpr (kFp8) {
           ck = c * qinv * sk_next;                 // loaded one tile ahead
-          if (n + 1 < ntiles) sk_next = token_scale(p.k_scale, tile_info[n + 1], rpg, ri);
+          svt = sv_next;
+          if (n + 1 < ntiles) {
+            sk_next = token_scale(p.k_scale, tile_info[n + 1], rpg, ri);
+            sv_next = token_scale(p.v_scale, tile_info[n + 1], rpg, ri);
+          }
+          sv_e = static_cast<int>((__float_as_uint(svt) >> 23) & 0xFFu) - 127;
         }
         // --- this row's 32 scores, read from tensor memory once per tile; does any exceed
-        //     its head's reference max by > 2^8?
+        //     its head's reference max by more than the threshold (e4m3: or does the token's
+        //     V scale reach past the segment's reference exponent)?
         // (bf16 keeps the scores in registers for the exponentials; e4m3, whose row sums
         // already live in registers, reads them again there)
+        constexpr float kThr = rescale_threshold<kFp8>();
         bool need = false;
         uint32_t sc[32];
         if (okS) {
@@ -1271,11 +1204,12 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
 #pragma unroll
           for (int h = 0; h < 32; h += 4) {
             const float4 m4 = *reinterpret_cast<const float4*>(m_ref + h0 + h);
-            need |= (fmaf(__uint_as_float(sc[h + 0]), ck, -m4.x) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sc[h + 1]), ck, -m4.y) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sc[h + 2]), ck, -m4.z) > kRescaleThreshold) |
-                    (fmaf(__uint_as_float(sc[h + 3]), ck, -m4.w) > kRescaleThreshold);
+            need |= (fmaf(__uint_as_float(sc[h + 0]), ck, -m4.x) > kThr) |
+                    (fmaf(__uint_as_float(sc[h + 1]), ck, -m4.y) > kThr) |
+                    (fmaf(__uint_as_float(sc[h + 2]), ck, -m4.z) > kThr) |
+                    (fmaf(__uint_as_float(sc[h + 3]), ck, -m4.w) > kThr);
           }
+          if constexpr (kFp8) need |= sv_e > e_ref;
           need = need && valid;
         } else {
 #pragma unroll
@@ -1284,24 +1218,40 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         const bool any_need = named_bar_or(1, kSoftmaxThreads, need || aborted || *abort_flag);
         if (any_need) {
           if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) { stop = true; break; }
-          // --- rare path: new reference max for heads whose scores jumped by > 2^8
+          // --- rare path: new reference max for heads whose scores jumped past the threshold
+          //     (e4m3: and a new reference exponent for the V scales)
+          int* red_e = reinterpret_cast<int*>(red + 256);   // e4m3: per-warp maximum exponent
           {
             if constexpr (kFp8) ld_s32(s_tmem, sc);
             float mv[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) mv[h] = valid ? __uint_as_float(sc[h]) * ck : -INFINITY;
             red[wq * 64 + h0 + lane] = warp_reduce_scatter32<true>(mv);
+            if constexpr (kFp8) {
+              const int em = __reduce_max_sync(0xffffffffu, (valid && svt > 0.f) ? sv_e : kEMin);
+              if (lane == 0) red_e[sw] = em;
+            }
           }
           named_bar_sync(1, kSoftmaxThreads);
           if (ts < kH) {
             const float mt = fmaxf(fmaxf(red[ts], red[64 + ts]), fmaxf(red[128 + ts], red[192 + ts]));
             const float mo = m_ref[ts];
             float a = 1.f;
-            if (mt > mo + kRescaleThreshold) {
+            if (mt > mo + kThr) {
               a = exp2f(mo - mt);
               m_ref[ts] = mt;
             }
             alpha_s[ts] = a;
+          }
+          // e4m3: every thread takes the same new reference exponent; the O accumulated so far
+          // was weighted by 2^(kPvShift - e_ref) and is rescaled to the new one
+          float o_extra = 1.f;
+          if constexpr (kFp8) {
+            int em = e_ref;
+#pragma unroll
+            for (int w8 = 0; w8 < 8; ++w8) em = max(em, red_e[w8]);
+            o_extra = exp2f(static_cast<float>(e_ref - em));
+            e_ref = em;
           }
           named_bar_sync(1, kSoftmaxThreads);
           if (!pv_waited) {
@@ -1319,18 +1269,27 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             for (int k3 = 0; k3 < (kFp8 ? 2 : 4); ++k3) {
               uint32_t ov[32];
               const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem : o_tmem + 64u * k3;
+              const float ox = (k3 < 2) ? o_extra : 1.f;
               tmem_ld32(ta, ov);
               tmem_ld_wait(ov);
 #pragma unroll
-              for (int h = 0; h < 32; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha_s[h0 + h]);
+              for (int h = 0; h < 32; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * (alpha_s[h0 + h] * ox));
               tmem_st32(ta, ov);
             }
             tmem_st_wait();
           }
         }
         // --- probabilities and row sums; the P^T row piece stays in registers until the
-        //     previous tile's PV has released the P buffer
+        //     previous tile's PV has released the P buffer.  e4m3: the weight times the
+        //     token's scaled V scale, u = s_v 2^(kPvShift - e_ref) < 2^(kPvShift + 1), split into
+        //     an e4m3 hi part and an e4m3 lo part (pk[0..7] and pk[8..15], four heads a word)
         uint32_t pk[16];
+        float u = 0.f;
+        if constexpr (kFp8) {
+          u = svt * __uint_as_float(static_cast<uint32_t>(127 + kPvShift - e_ref) << 23);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t lv[16], lx[16], sf[16];
@@ -1363,7 +1322,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), ck, -m2.x)) : 0.f;
             const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), ck, -m2.y)) : 0.f;
             if constexpr (kFp8) {
-              pk[8 * half + e] = pack_f16_sat(p0, p1);   // p <= 2^8: inside the f16 range
+              uint32_t hi, lo;
+              split_weights_e4m3(p0 * u, p1 * u, hi, lo);
+              pk[4 * half + (e >> 1)] |= hi << (16 * (e & 1));
+              pk[8 + 4 * half + (e >> 1)] |= lo << (16 * (e & 1));
               lreg[h] += p0;
               lreg[h + 1] += p1;
             } else {
@@ -1389,15 +1351,27 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           // the next segment's q, as soon as this segment's last scores are read
           if (j + 1 == sg.z && s + 1 < nseg) convert_q(s + 1);
         }
-        if (!pv_waited && !(kFp8 ? wait_warp_lazy(bar(kBarPvDone), (n - 1) & 1, abort_flag)
-                                 : wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)))
-          aborted = true;
-        // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
-        uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
+        if (!pv_waited && !wait_warp(bar(kBarPvDone), (n - 1) & 1, abort_flag)) aborted = true;
+        if constexpr (kFp8) {
+          // hi and lo parts: [128 tokens][64 heads] e4m3 each, 64-byte rows with the 64-byte
+          // swizzle; this thread's 32 heads are 16-byte chunks 2*grp and 2*grp+1 of its row
+          uint8_t* prow = smem + kOffP + row * 64;
+          const int swz = (row >> 1) & 3;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(prow + (((4 * grp + q) ^ (row & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 2; ++q) {
+            const int off = ((2 * grp + q) ^ swz) << 4;
+            *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            *reinterpret_cast<uint4*>(prow + 8192 + off) =
+                make_uint4(pk[8 + 4 * q], pk[9 + 4 * q], pk[10 + 4 * q], pk[11 + 4 * q]);
+          }
+        } else {
+          // this thread's 32 heads are 16-byte chunks 4*grp .. 4*grp+3 of the 128-byte P^T row
+          uint8_t* prow = smem + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(prow + (((4 * grp + q) ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarPFull));
         // bf16: the second-to-last segment's output, once the last segment's first P is out:
@@ -1431,7 +1405,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       named_bar_sync(1, kSoftmaxThreads);
       if (ts < kH) {
         const float l = (red[ts] + red[64 + ts]) + (red[128 + ts] + red[192 + ts]);
-        linv[kb * kH + ts] = 1.f / l;
+        // e4m3: the weights carried 2^(kPvShift - e_ref), undone here
+        const float oscale = kFp8 ? __uint_as_float(static_cast<uint32_t>(127 + e_ref - kPvShift) << 23) : 1.f;
+        linv[kb * kH + ts] = oscale / l;
         const float lx = kFp8 ? l : (red[256 + ts] + red[320 + ts]) + (red[384 + ts] + red[448 + ts]);
         const float lse_v = (m_ref[ts] + log2f(lx)) * 0.69314718055994531f;
         if (whole) {

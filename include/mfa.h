@@ -78,7 +78,7 @@ typedef enum mfa_out_dtype {
 #define MFA_DEV_BAD_BLOCK    0x2u  /* a block_table entry outside [0, num_blocks) was used */
 #define MFA_DEV_BAD_LENGTH   0x4u  /* a seq_lens entry outside [0, max_pages_per_seq*64] (clamped) */
 #define MFA_DEV_SCHEDULE     0x8u  /* device lengths need more tiles per CTA than the plan allows */
-#define MFA_DEV_RANGE        0x10u /* e4m3 path: a V scale left the f16 range (saturated) */
+#define MFA_DEV_RANGE        0x10u /* reserved: no longer set (e4m3 scales have no range limit) */
 
 /* Plan flags. */
 #define MFA_PLAN_CHECK       0x1u  /* run: clear the status word, then read it back (synchronises) */
@@ -165,12 +165,12 @@ mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_l
  *   k_cache      : device [num_blocks, 64, 256], bf16 or e4m3 codes (uint8), 16-byte aligned.
  *   v_cache      : same layout as k_cache.
  *   k_scale      : device fp32 [num_blocks, 64], 16-byte aligned (e4m3 only; NULL for bf16):
- *                  value = code * scale.  The e4m3 path computes q.K^T on the e4m3
- *                  codes (q split exactly into two e4m3 parts under one power-of-two
- *                  scale per sequence; K scales applied to the fp32 scores, no limit)
- *                  and P.V in f16 with fp32 accumulation on V dequantised to f16: V
- *                  scales must lie within (0, 146] (448 * scale within the f16 range);
- *                  larger ones saturate and set MFA_DEV_RANGE.
+ *                  value = code * scale, any positive finite scale.  The e4m3 path runs
+ *                  both contractions on the e4m3 codes as stored: q.K^T against q split
+ *                  exactly into two e4m3 parts under one power-of-two scale per sequence,
+ *                  with the K scales applied to the fp32 scores; P.V with each token's V
+ *                  scale folded into its weights, which are split into two e4m3 parts under
+ *                  one power-of-two reference per sequence segment (fp32 accumulation).
  *   v_scale      : same for V.
  *   block_table  : device int32 [B, max_pages_per_seq]; entries past ceil(L_b/64) are never read.
  *   seq_lens     : device int32 [B].
