@@ -445,20 +445,19 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 // ------------------------------------------------------------------ decode kernel
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  const uint16_t v = static_cast<uint16_t>(two_codes);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-  return r;
-}
 // Two floats to two e4m3 codes (round to nearest even, saturating); lo in the low byte.
 __device__ __forceinline__ uint32_t pack_e4m3_sat(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ float f16_lo(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2))); }
-__device__ __forceinline__ float f16_hi(uint32_t h2) { return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16))); }
+
+// Value of the e4m3 code in the low byte of b, exactly: the 7 magnitude bits placed at bit 20
+// of an fp32 word are the code's value times 2^-120 (subnormal codes included, as fp32
+// subnormals), so one multiply by 2^120 restores it; the sign bit moves to bit 31.
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+  return __uint_as_float(((b & 0x7Fu) << 20) | ((b & 0x80u) << 24)) * 0x1p120f;
+}
 
 // Split two scaled q values x into e4m3 pairs hi + lo with hi = e4m3(x) and lo = e4m3(x - hi).
 // x is a bf16 value times a power of two (8 significant bits) and the largest |x| of the
@@ -466,23 +465,24 @@ __device__ __forceinline__ float f16_hi(uint32_t h2) { return __half2float(__ush
 // it fits e4m3's 4 significant bits: hi + lo = x exactly when ulp(x) >= 2^-9 (the e4m3
 // subnormal step), i.e. for |x| >= 2^-2, which covers every element at least 2^-9 of the
 // largest.  Smaller elements err by at most 2^-10, under 2^-16 of the largest.
+// (The hi part is read back through the f16 conversion rather than e4m3_value: the same
+// bits, but the slower read-back measured faster end to end -- finishing a segment's q split
+// earlier moves the CTAs' load streams into a worse phase.)
 __device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   hi = pack_e4m3_sat(x0, x1);
-  const uint32_t back = e4m3x2_to_f16x2(hi);
-  lo = pack_e4m3_sat(x0 - f16_lo(back), x1 - f16_hi(back));
+  uint32_t back;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(static_cast<uint16_t>(hi)));
+  lo = pack_e4m3_sat(x0 - __half2float(__ushort_as_half(static_cast<unsigned short>(back))),
+                     x1 - __half2float(__ushort_as_half(static_cast<unsigned short>(back >> 16))));
 }
 
 // Split two PV weights x >= 0 (below 448) into e4m3 pairs hi + lo: hi = e4m3(x) rounded to
-// nearest, lo = e4m3(x - hi).  hi is read back exactly from its code: a 7-bit code b placed
-// at bit 20 of an fp32 word is the code's value times 2^-120 (subnormal codes included, as
-// fp32 subnormals), so one multiply by 2^120 restores it.  x - hi is exact in fp32, and
-// hi + lo matches x to 2^-9 of x where lo is a normal e4m3 number (x above about 2^-1), and
-// to 2^-10 absolute below that.
+// nearest, lo = e4m3(x - hi), hi read back exactly from its code.  x - hi is exact in fp32,
+// and hi + lo matches x to 2^-9 of x where lo is a normal e4m3 number (x above about 2^-1),
+// and to 2^-10 absolute below that.
 __device__ __forceinline__ void split_weights_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   hi = pack_e4m3_sat(x0, x1);
-  const float f0 = __uint_as_float((hi & 0x7Fu) << 20) * 0x1p120f;
-  const float f1 = __uint_as_float(((hi >> 8) & 0x7Fu) << 20) * 0x1p120f;
-  lo = pack_e4m3_sat(x0 - f0, x1 - f1);
+  lo = pack_e4m3_sat(x0 - e4m3_value(hi), x1 - e4m3_value(hi >> 8));
 }
 
 // e4m3: per-token scale of box row ri of page pg of tile `ti` ({page 0, page 1, rows 0,
