@@ -14,11 +14,12 @@ Recipe (fixed seeds, numpy PCG64 via ``default_rng``), in draw order:
   1. lengths: given, or uniform integers in [lo, hi] inclusive;
   2. physical page order: identity ("contiguous") or ``rng.permutation``;
   3. q ~ N(0,1) fp32 [B*T, H, d] (T new query tokens per sequence, 1 unless stated);
-  4. K pool ~ N(0,1) fp32 [num_blocks, page, d], drawn in chunks of
-     ``_CHUNK_BLOCKS`` pages; optionally each scalar K element is multiplied
-     by ``k_spike_mult`` with independent probability ``k_spike_frac``
-     (uniform draw right after each chunk's normals);
-  5. V pool ~ N(0,1) fp32, same chunking, no spikes.
+  4. K pool ~ N(0,1) fp32 [num_blocks, page, G*d] (G key/value heads per row, 1
+     for MFA), drawn in chunks of ``_CHUNK_BLOCKS`` pages; optionally each
+     scalar K element is multiplied by ``k_spike_mult`` with independent
+     probability ``k_spike_frac`` (uniform draw right after each chunk's normals);
+  5. V pool ~ N(0,1) fp32, same chunking, no spikes -- not drawn when one
+     latent serves as keys and values (``kv_shared``): V is then the K pool.
 Storage: bf16 by round-to-nearest-even, or FP8 e4m3 with one fp32 scale per
 token row (absmax/448, 1 for an all-zero row), codes = e4m3(RNE(x/scale))
 after clamping to +-448.  Unused page slots and unused physical pages are
@@ -63,6 +64,8 @@ class Workload:
     page_size: int = PAGE_SIZE
     softmax_scale: Optional[float] = None       # None -> 1/sqrt(head_dim)
     tokens_per_seq: int = 1                     # T new query tokens per sequence (multi-token decode)
+    num_kv_heads: int = 1                       # G key/value heads of width head_dim per cache row
+    kv_shared: bool = False                     # True: one latent serves as keys and values
 
     def scale(self) -> float:
         if self.softmax_scale is not None:
@@ -93,6 +96,15 @@ WORKLOADS = {
         "mtp2_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=7, tokens_per_seq=2),
     "mtp2_b32_l4096_fp8": Workload(
         "mtp2_b32_l4096_fp8", batch=32, lens=(4096,) * 32, kv_dtype="fp8_e4m3", seed=8, tokens_per_seq=2),
+    # the attention designs the Step-3 page compares MFA with (section 5, "Attention Design";
+    # section 7, attention ablation), at the 4K shape: grouped-query attention with 64 query
+    # heads over 4 key/value heads of width 128 (effective rank 8,192), and a 512-wide latent
+    # shared by keys and values under 128 query heads (intensity 512 with 8-bit KV)
+    "gqa_b32_l4096_bf16": Workload(
+        "gqa_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=9, head_dim=128, num_kv_heads=4),
+    "mla_b32_l4096_bf16": Workload(
+        "mla_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=10, num_q_heads=128, head_dim=512,
+        kv_shared=True),
 }
 
 
@@ -101,8 +113,8 @@ class Case:
     """Host tensors of one decode step (all torch CPU tensors, contiguous)."""
     workload: Workload
     q: torch.Tensor             # bf16 [B*T, H, d] (T = workload.tokens_per_seq)
-    k_cache: torch.Tensor       # bf16 [nb, page, d] or uint8 e4m3 codes
-    v_cache: torch.Tensor
+    k_cache: torch.Tensor       # bf16 [nb, page, G*d] or uint8 e4m3 codes
+    v_cache: torch.Tensor       # the same object as k_cache when the latent is shared
     k_scale: Optional[torch.Tensor]   # fp32 [nb, page] (FP8 only)
     v_scale: Optional[torch.Tensor]
     block_table: torch.Tensor   # int32 [B, max_pages], -1 where unused
@@ -170,8 +182,9 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
         perm = rng.permutation(nb)
 
     q = rng.standard_normal((B * w.tokens_per_seq, H, d), dtype=np.float32)
-    kf = _draw_pool(rng, nb, page, d, w.k_spike_frac, w.k_spike_mult)
-    vf = _draw_pool(rng, nb, page, d, 0.0, 1.0)
+    row = w.num_kv_heads * d                    # cache row: G heads of width d side by side
+    kf = _draw_pool(rng, nb, page, row, w.k_spike_frac, w.k_spike_mult)
+    vf = kf if w.kv_shared else _draw_pool(rng, nb, page, row, 0.0, 1.0)
 
     table = np.full((B, max_pages), -1, dtype=np.int32)
     used = np.zeros(nb, dtype=bool)
@@ -189,7 +202,8 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
                 tails.append((int(table[b, npages[b] - 1]), rem))
 
     if w.kv_dtype == "bf16":
-        k_cache, v_cache = _to_bf16(kf), _to_bf16(vf)
+        k_cache = _to_bf16(kf)
+        v_cache = k_cache if w.kv_shared else _to_bf16(vf)
         k_scale = v_scale = None
         if w.poison:
             kb, vb = k_cache.view(torch.int16), v_cache.view(torch.int16)
@@ -203,7 +217,10 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
                 vb[unused] = nan
     elif w.kv_dtype == "fp8_e4m3":
         k_cache, k_scale = _to_e4m3(kf)
-        v_cache, v_scale = _to_e4m3(vf)
+        if w.kv_shared:
+            v_cache, v_scale = k_cache, k_scale
+        else:
+            v_cache, v_scale = _to_e4m3(vf)
         if w.poison:
             for blk, rem in tails:
                 k_cache[blk, rem:] = E4M3_NAN_CODE
@@ -223,7 +240,7 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
         workload=w,
         q=_to_bf16(q).contiguous(),
         k_cache=k_cache.contiguous(),
-        v_cache=v_cache.contiguous(),
+        v_cache=k_cache if w.kv_shared else v_cache.contiguous(),
         k_scale=None if k_scale is None else k_scale.contiguous(),
         v_scale=None if v_scale is None else v_scale.contiguous(),
         block_table=torch.from_numpy(table).contiguous(),
@@ -234,13 +251,14 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
 def small(name: str, batch: int, lens: Sequence[int], kv_dtype: str = "bf16", seed: int = 100,
           layout: str = "shuffled", extra_blocks: int = 2, k_spike_frac: float = 0.0,
           softmax_scale: Optional[float] = None, num_q_heads: int = NUM_Q_HEADS,
-          head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, tokens_per_seq: int = 1) -> Case:
+          head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, tokens_per_seq: int = 1,
+          num_kv_heads: int = 1, kv_shared: bool = False) -> Case:
     """A small poisoned case for parity tests (explicit lengths)."""
     w = Workload(name, batch=batch, lens=tuple(int(x) for x in lens), kv_dtype=kv_dtype,
                  layout=layout, seed=seed, extra_blocks=extra_blocks,
                  k_spike_frac=k_spike_frac, softmax_scale=softmax_scale,
                  num_q_heads=num_q_heads, head_dim=head_dim, page_size=page_size,
-                 tokens_per_seq=tokens_per_seq)
+                 tokens_per_seq=tokens_per_seq, num_kv_heads=num_kv_heads, kv_shared=kv_shared)
     return generate(w)
 
 

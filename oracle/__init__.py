@@ -5,7 +5,9 @@ leg and its reference arm) may import this package.  The product path
 (``decode_attention_02_gb300``) never imports it and shares no code with it.
 
 ``mfa_oracle.c`` is the plain fp64 definition of softmax(q K^T * scale) V over
-the paged cache (Step-3, paperlayer.ai/abs/2507.19427v1, sections 2 and 5);
+the paged cache (Step-3, paperlayer.ai/abs/2507.19427v1, sections 2 and 5), for
+MFA's one shared key/value head and for the grouped-head (GQA-style) and
+shared-latent (MLA-style) caches of the attention designs the page compares;
 this module compiles it with gcc and calls it through ctypes.
 
 Pins (tests/test_oracle.py): torch SDPA in float64 on a dense gather done by
@@ -48,7 +50,7 @@ def load_library(path: str):
     lib = ctypes.CDLL(path)
     P = ctypes.c_void_p
     I = ctypes.c_int
-    lib.mfa_oracle_decode.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P,
+    lib.mfa_oracle_decode.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P,
                                       ctypes.c_double, P, P, I]
     lib.mfa_oracle_decode.restype = I
     lib.mfa_oracle_combine.argtypes = [I, ctypes.c_long, I, P, P, P, P]
@@ -152,6 +154,8 @@ def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
     """Oracle decode of ``case`` -> (out float64 [B*T,H,d], lse float64 [B*T,H]).
 
     T = case.workload.tokens_per_seq new query tokens per sequence (1: one each).
+    case.workload.num_kv_heads = G key/value heads per cache row (query head h reads head
+    h // (H // G)); case.workload.kv_shared: the values are the key rows (one latent).
 
     ``t_begin``/``t_end`` (int sequences of length B) restrict each sequence to
     a token range; ``batch_slice`` restricts the batch (for bounded samples).
@@ -177,17 +181,23 @@ def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
         if t_end is not None:
             t_end = np.asarray(t_end)[batch_slice]
     B, H, d = q.shape
-    kc, vc = _np(case.k_cache), _np(case.v_cache)
-    ks, vs = _np(case.k_scale), _np(case.v_scale)
+    G = int(getattr(w, "num_kv_heads", 1))
+    shared = bool(getattr(w, "kv_shared", False))
+    kc = _np(case.k_cache)
+    vc = None if shared else _np(case.v_cache)
+    ks = _np(case.k_scale)
+    vs = None if shared else _np(case.v_scale)
     if ks is not None:
-        ks, vs = ks.astype(np.float32), vs.astype(np.float32)
+        ks = ks.astype(np.float32)
+    if vs is not None:
+        vs = vs.astype(np.float32)
     tb = None if t_begin is None else np.ascontiguousarray(np.asarray(t_begin, dtype=np.int32))
     te = None if t_end is None else np.ascontiguousarray(np.asarray(t_end, dtype=np.int32))
     out = np.zeros((B, H, d), dtype=np.float64)
     lse = np.zeros((B, H), dtype=np.float64)
     scale = w.scale() if softmax_scale is None else float(softmax_scale)
     rc = (lib or _load()).mfa_oracle_decode(
-        B, H, d, w.page_size, table.shape[1], 1 if w.kv_dtype == "fp8_e4m3" else 0,
+        B, H, G, d, w.page_size, table.shape[1], 1 if w.kv_dtype == "fp8_e4m3" else 0,
         _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(table), _ptr(lens),
         _ptr(tb), _ptr(te), scale, _ptr(out), _ptr(lse), int(nthreads))
     if rc != 0:

@@ -35,6 +35,16 @@
  * Threads split independent (sequence, group of heads) units; each head's
  * arithmetic runs in the order written above.
  *
+ * The attention designs the Step-3 page compares MFA with (section 5 "Model-System
+ * Co-design", the "Attention Design" items; section 7's attention ablation) are the same
+ * definition over other cache layouts, handled here by two more parameters:
+ *   - G key/value heads per cache row (grouped-query attention): a cache row holds G heads
+ *     of width d side by side, and query head h reads head g(h) = h / (H / G), columns
+ *     [g(h) d, (g(h) + 1) d) of the row, of both pools;
+ *   - one latent shared by keys and values (MLA-style): v_cache NULL means every value row
+ *     is the key row itself.
+ * MFA is G = 1 with separate pools.
+ *
  * mfa_oracle_kv_append() (end of file) writes a decode step's new key and value rows into
  * the paged cache, quantising them to e4m3 with per-row scales for an FP8 cache.
  */
@@ -68,7 +78,7 @@ double mfa_oracle_e4m3_to_double(uint8_t code) {
 }
 
 typedef struct {
-    int B, H, d, page, max_pages, kv_fp8;
+    int B, H, G, d, page, max_pages, kv_fp8;
     const uint16_t *q;
     const void *k_cache, *v_cache;
     const float *k_scale, *v_scale;
@@ -85,21 +95,24 @@ typedef struct {
 
 /* Head groups: the heads of a sequence are split into groups of HEAD_GROUP so
  * that the threads have independent work; a group decodes each key and value row
- * once and uses it for its heads. */
+ * once and uses it for its heads (all of which read the same key/value head). */
 #define HEAD_GROUP 8
 
-/* Row (key or value) of token t of sequence b, decoded to doubles. */
-static void kv_row(const job_t *J, int which_v, int b, int t, double *dst) {
+/* Key/value head g of the row of token t of sequence b (row width G d), decoded to
+ * doubles; a shared latent (v_cache NULL) gives the key row for values too. */
+static void kv_row(const job_t *J, int which_v, int b, int t, int g, double *dst) {
     int32_t blk = J->block_table[(size_t)b * J->max_pages + t / J->page];
     size_t row = (size_t)blk * J->page + (size_t)(t % J->page);
+    size_t base = row * (size_t)J->G * (size_t)J->d + (size_t)g * (size_t)J->d;
+    const void *vpool = J->v_cache ? J->v_cache : J->k_cache;
     if (J->kv_fp8) {
-        const uint8_t *pool = (const uint8_t *)(which_v ? J->v_cache : J->k_cache);
-        const float *sc = which_v ? J->v_scale : J->k_scale;
+        const uint8_t *pool = (const uint8_t *)(which_v ? vpool : J->k_cache);
+        const float *sc = which_v && J->v_cache ? J->v_scale : J->k_scale;
         for (int i = 0; i < J->d; ++i)
-            dst[i] = mfa_oracle_e4m3_to_double(pool[row * J->d + i]) * (double)sc[row];
+            dst[i] = mfa_oracle_e4m3_to_double(pool[base + i]) * (double)sc[row];
     } else {
-        const uint16_t *pool = (const uint16_t *)(which_v ? J->v_cache : J->k_cache);
-        for (int i = 0; i < J->d; ++i) dst[i] = bf16_to_double(pool[row * J->d + i]);
+        const uint16_t *pool = (const uint16_t *)(which_v ? vpool : J->k_cache);
+        for (int i = 0; i < J->d; ++i) dst[i] = bf16_to_double(pool[base + i]);
     }
 }
 
@@ -115,6 +128,7 @@ static void head_group(const job_t *J, int b, int h0, int h1, size_t maxlen, scr
     int t0 = J->t_begin ? J->t_begin[b] : 0;
     int t1 = J->t_end ? J->t_end[b] : L;
     int d = J->d;
+    int g = h0 / (J->H / J->G);   /* the key/value head of every query head in [h0, h1) */
     for (int h = h0; h < h1; ++h) {
         double *o = J->out + ((size_t)b * J->H + h) * d;
         const uint16_t *qh = J->q + ((size_t)b * J->H + h) * d;
@@ -129,7 +143,7 @@ static void head_group(const job_t *J, int b, int h0, int h1, size_t maxlen, scr
     double m[HEAD_GROUP];
     for (int h = h0; h < h1; ++h) m[h - h0] = -INFINITY;
     for (int t = t0; t < t1; ++t) {
-        kv_row(J, 0, b, t, W->row);
+        kv_row(J, 0, b, t, g, W->row);
         for (int h = h0; h < h1; ++h) {
             const double *qv = W->q + (size_t)(h - h0) * d;
             double acc = 0.0;
@@ -143,7 +157,7 @@ static void head_group(const job_t *J, int b, int h0, int h1, size_t maxlen, scr
     double l[HEAD_GROUP];
     for (int h = h0; h < h1; ++h) l[h - h0] = 0.0;
     for (int t = t0; t < t1; ++t) {
-        kv_row(J, 1, b, t, W->row);
+        kv_row(J, 1, b, t, g, W->row);
         for (int h = h0; h < h1; ++h) {
             double p = exp(W->s[(size_t)(h - h0) * maxlen + (size_t)(t - t0)] - m[h - h0]);
             l[h - h0] += p;
@@ -177,11 +191,13 @@ static void *worker(void *arg) {
         free(W.row);
         return (void *)1;
     }
-    int groups = (J->H + HEAD_GROUP - 1) / HEAD_GROUP;
+    int per = J->H / J->G;                           /* query heads per key/value head */
+    int hg = per < HEAD_GROUP ? per : HEAD_GROUP;     /* divides per (checked by the caller) */
+    int groups = J->H / hg;
     long nunits = (long)J->B * groups;
     for (long u = Wk->tid; u < nunits; u += J->nthreads) {
-        int b = (int)(u / groups), g = (int)(u % groups);
-        int h0 = g * HEAD_GROUP, h1 = h0 + HEAD_GROUP < J->H ? h0 + HEAD_GROUP : J->H;
+        int b = (int)(u / groups), gi = (int)(u % groups);
+        int h0 = gi * hg, h1 = h0 + hg;
         head_group(J, b, h0, h1, maxlen, &W);
     }
     free(W.s);
@@ -197,30 +213,34 @@ int mfa_oracle_num_cpus(void) {
 
 /*
  * Returns 0 on success, -1 on a bad argument, -2 on allocation failure.
- * q: bf16 bits [B,H,d]; k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,d];
- * k_scale/v_scale: fp32 [num_blocks,page] (FP8 only); block_table: int32 [B,max_pages];
- * seq_lens: int32 [B]; t_begin/t_end: int32 [B] or NULL; out: double [B,H,d]; lse: double [B,H].
+ * q: bf16 bits [B,H,d]; k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,G*d]
+ * (v_cache NULL: values are the key rows); k_scale/v_scale: fp32 [num_blocks,page] (FP8
+ * only; v_scale unused when v_cache is NULL); G divides H, and H / G is at most HEAD_GROUP
+ * or a multiple of it; block_table: int32 [B,max_pages]; seq_lens: int32 [B];
+ * t_begin/t_end: int32 [B] or NULL; out: double [B,H,d]; lse: double [B,H].
  * nthreads <= 0 uses every online CPU.
  */
-int mfa_oracle_decode(int B, int H, int d, int page, int max_pages, int kv_fp8,
+int mfa_oracle_decode(int B, int H, int G, int d, int page, int max_pages, int kv_fp8,
                       const uint16_t *q, const void *k_cache, const void *v_cache,
                       const float *k_scale, const float *v_scale,
                       const int32_t *block_table, const int32_t *seq_lens,
                       const int32_t *t_begin, const int32_t *t_end,
                       double scale, double *out, double *lse, int nthreads) {
-    if (B < 0 || H <= 0 || d <= 0 || page <= 0 || max_pages <= 0) return -1;
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !lse) return -1;
-    if (kv_fp8 && (!k_scale || !v_scale)) return -1;
+    if (B < 0 || H <= 0 || G <= 0 || H % G != 0 || d <= 0 || page <= 0 || max_pages <= 0) return -1;
+    if (H / G > HEAD_GROUP && (H / G) % HEAD_GROUP != 0) return -1;
+    if (!q || !k_cache || !block_table || !seq_lens || !out || !lse) return -1;
+    if (kv_fp8 && (!k_scale || (v_cache && !v_scale))) return -1;
     for (int b = 0; b < B; ++b) {
         int L = seq_lens[b];
         int t0 = t_begin ? t_begin[b] : 0;
         int t1 = t_end ? t_end[b] : L;
         if (L < 0 || L > max_pages * page || t0 < 0 || t1 > L) return -1;
     }
-    job_t J = {B, H, d, page, max_pages, kv_fp8, q, k_cache, v_cache, k_scale, v_scale,
+    job_t J = {B, H, G, d, page, max_pages, kv_fp8, q, k_cache, v_cache, k_scale, v_scale,
                block_table, seq_lens, t_begin, t_end, scale, out, lse, 0};
     if (nthreads <= 0) nthreads = mfa_oracle_num_cpus();
-    long nunits = (long)B * ((H + HEAD_GROUP - 1) / HEAD_GROUP);
+    int hg = H / G < HEAD_GROUP ? H / G : HEAD_GROUP;
+    long nunits = (long)B * (H / hg);
     if (nunits == 0) return 0;
     if (nthreads > nunits) nthreads = (int)nunits;
     J.nthreads = nthreads;

@@ -25,7 +25,8 @@ TOL = 1e-12
 
 
 def dense_kv(case, b):
-    """Gather sequence b's keys and values by numpy indexing, decoded by torch."""
+    """Gather sequence b's keys and values by numpy indexing, decoded by torch: [L, G*d] rows
+    (G key/value heads side by side; the values are the keys when the latent is shared)."""
     w = case.workload
     L = int(case.seq_lens[b])
     t = np.arange(L)
@@ -39,26 +40,32 @@ def dense_kv(case, b):
             case.k_scale[blk, slot].to(torch.float64)[:, None]
         V = case.v_cache[blk, slot].view(torch.float8_e4m3fn).to(torch.float64) * \
             case.v_scale[blk, slot].to(torch.float64)[:, None]
+    if getattr(w, "kv_shared", False):
+        V = K.clone()
     return K, V
 
 
 def sdpa_reference(case, scale=None):
-    """torch SDPA (float64) on the dense gather, and scipy logsumexp of the scores."""
+    """torch SDPA (float64) on the dense gather, and scipy logsumexp of the scores.  With G
+    key/value heads, the [L, G*d] rows are split into heads and each repeated for its H/G
+    query heads (query head h reads head h // (H/G))."""
     w = case.workload
     scale = w.scale() if scale is None else scale
     B, H, d = case.q.shape
+    G = getattr(w, "num_kv_heads", 1)
     out = np.zeros((B, H, d))
     lse = np.full((B, H), -np.inf)
     for b in range(B):
         K, V = dense_kv(case, b)
         if K.shape[0] == 0:
             continue
+        Kh = K.view(-1, G, d).permute(1, 0, 2).repeat_interleave(H // G, dim=0)   # [H, L, d]
+        Vh = V.view(-1, G, d).permute(1, 0, 2).repeat_interleave(H // G, dim=0)
         q = case.q[b].to(torch.float64)
         o = torch.nn.functional.scaled_dot_product_attention(
-            q[None, :, None, :], K[None, None].expand(1, H, -1, -1),
-            V[None, None].expand(1, H, -1, -1), scale=scale)
+            q[None, :, None, :], Kh[None], Vh[None], scale=scale)
         out[b] = o[0, :, 0, :].numpy()
-        scores = (q.numpy() @ K.numpy().T) * scale
+        scores = np.einsum("hd,hld->hl", q.numpy(), Kh.numpy()) * scale
         lse[b] = scipy.special.logsumexp(scores, axis=1)
     return out, lse
 
@@ -317,7 +324,7 @@ def test_thread_count_does_not_change_results():
 _MUTANTS = {
     "wrong_slot": ("(size_t)(t % J->page)", "(size_t)((t + 1) % J->page)"),
     "wrong_block": ("t / J->page]", "(t / J->page + 1) % J->max_pages]"),
-    "k_for_v": ("kv_row(J, 1, b, t, W->row);", "kv_row(J, 0, b, t, W->row);"),
+    "k_for_v": ("kv_row(J, 1, b, t, g, W->row);", "kv_row(J, 0, b, t, g, W->row);"),
     "sign_flip": ("(t - t0)] - m[h - h0])", "(t - t0)] * -1.0 + m[h - h0])"),
     "no_scale": ("double st = J->scale * acc;", "double st = acc;"),
     "lse_no_log": ("m[h - h0] + log(l[h - h0])", "m[h - h0] + l[h - h0]"),
@@ -327,6 +334,11 @@ _MUTANTS = {
     "fp8_scale_dropped": ("* (double)sc[row]", "* 1.0"),
     "head_index": ("W->q[(size_t)(h - h0) * d + i] = bf16_to_double(qh[i]);",
                    "W->q[(size_t)(h - h0) * d + i] = bf16_to_double(qh[i % 8]);"),
+    # grouped and shared key/value heads
+    "group_interleaved": ("int g = h0 / (J->H / J->G);", "int g = (h0 / HEAD_GROUP) % J->G;"),
+    "row_width_dropped": ("row * (size_t)J->G * (size_t)J->d", "row * (size_t)J->d"),
+    "values_always_keys": ("const void *vpool = J->v_cache ? J->v_cache : J->k_cache;",
+                           "const void *vpool = J->k_cache;"),
 }
 
 
@@ -341,6 +353,12 @@ def _run_pins(lib):
             return False
         for kv in ("bf16", "fp8_e4m3"):
             case = inputs.small("mut", 2, [70, 131], kv_dtype=kv, seed=171)
+            out, lse = oracle.decode(case, lib=lib)
+            ro, rl = sdpa_reference(case)
+            assert_close(out, ro)
+            assert_close(lse, rl)
+        for kw in (dict(num_q_heads=32, head_dim=16, num_kv_heads=2), dict(num_q_heads=8, head_dim=32, kv_shared=True)):
+            case = inputs.small("mutg", 2, [70, 131], seed=172, **kw)
             out, lse = oracle.decode(case, lib=lib)
             ro, rl = sdpa_reference(case)
             assert_close(out, ro)
@@ -416,3 +434,58 @@ def test_multi_token_decode_last_token_is_the_ordinary_decode():
                          k_scale=None, v_scale=None, block_table=case.block_table, seq_lens=case.seq_lens)
     o1, l1 = oracle.decode(single)
     assert np.array_equal(out[T - 1::T], o1) and np.array_equal(lse[T - 1::T], l1)
+
+
+# ------------------------------------------------------------- ablation shapes
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_grouped_query_heads_match_sdpa_with_explicit_grouping(kv):
+    """GQA-style cache at the ablation shape: 64 query heads over 4 key/value heads of width
+    128 (rows of 4 x 128), against torch SDPA with each head's keys and values repeated for
+    its 16 query heads."""
+    case = inputs.small("gqa", 3, [1, 70, 200], kv_dtype=kv, seed=190, head_dim=128, num_kv_heads=4)
+    assert case.k_cache.shape[2] == 4 * 128
+    out, lse = oracle.decode(case)
+    ro, rl = sdpa_reference(case)
+    assert_close(out, ro)
+    assert_close(lse, rl)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_shared_latent_matches_sdpa_with_values_equal_to_keys(kv):
+    """MLA-style cache at the ablation shape: 128 query heads over one 512-wide latent that
+    serves as keys and values (no V pool), against torch SDPA with V = K."""
+    case = inputs.small("mla", 2, [5, 131], kv_dtype=kv, seed=191, num_q_heads=128, head_dim=512,
+                        kv_shared=True)
+    assert case.v_cache is case.k_cache
+    out, lse = oracle.decode(case)
+    ro, rl = sdpa_reference(case)
+    assert_close(out, ro)
+    assert_close(lse, rl)
+
+
+def test_grouped_heads_see_only_their_own_key_value_head():
+    """Changing key/value head 2's columns of every cache row changes exactly query heads
+    32..47 (the 16 heads that read head 2)."""
+    case = inputs.small("gqa_iso", 2, [90, 33], seed=192, head_dim=128, num_kv_heads=4)
+    out, lse = oracle.decode(case)
+    k2 = case.k_cache.clone()
+    v2 = case.v_cache.clone()
+    k2[:, :, 256:384] = k2[:, :, 256:384].flip(1)
+    v2[:, :, 256:384] = -v2[:, :, 256:384]
+    mod = inputs.Case(workload=case.workload, q=case.q, k_cache=k2, v_cache=v2, k_scale=None, v_scale=None,
+                      block_table=case.block_table, seq_lens=case.seq_lens)
+    out2, lse2 = oracle.decode(mod)
+    same = np.array([np.array_equal(out[:, h], out2[:, h]) for h in range(64)])
+    assert same[:32].all() and same[48:].all() and not same[32:48].any()
+
+
+def test_shared_latent_equals_separate_pools_holding_the_same_rows():
+    """A shared latent gives bitwise the same result as a V pool that is a copy of the K pool."""
+    case = inputs.small("mla_eq", 2, [64, 200], seed=193, num_q_heads=16, head_dim=64, kv_shared=True)
+    import dataclasses
+    sep = inputs.Case(workload=dataclasses.replace(case.workload, kv_shared=False), q=case.q,
+                      k_cache=case.k_cache, v_cache=case.k_cache.clone(), k_scale=None, v_scale=None,
+                      block_table=case.block_table, seq_lens=case.seq_lens)
+    a, b = oracle.decode(case), oracle.decode(sep)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
