@@ -44,9 +44,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "ragged_b128_l1024_8192_bf16"
-# The other target workloads, measured on the same run and reported under "workloads".
+# The other target workloads, measured on the same run and reported under "workloads" (the
+# last two are the comparison attention shapes).
 SIDE_WORKLOADS = ("tiny_b1_l512_bf16", "b32_l4096_bf16", "b128_l4096_fp8", "long_b4_l131072_bf16",
-                  "b32_l4096_fp8", "long_b4_l131072_fp8", "mtp2_b32_l4096_bf16", "mtp2_b32_l4096_fp8")
+                  "b32_l4096_fp8", "long_b4_l131072_fp8", "mtp2_b32_l4096_bf16", "mtp2_b32_l4096_fp8",
+                  "gqa_b32_l4096_bf16", "mla_b32_l4096_bf16")
+
+
+def shape_args(w) -> dict:
+    """Accounting arguments of a workload's attention shape."""
+    return dict(H=w.num_q_heads, d=w.head_dim, row=w.head_dim * w.num_kv_heads, shared=w.kv_shared)
 SIDE_STEPS = 100
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
@@ -55,19 +62,22 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # ------------------------------------------------------------------ accounting
 
-def kv_bytes_per_token(kv_dtype: str) -> int:
-    """K and V rows of one token: 2*256 elements (+ two fp32 scales for e4m3)."""
-    return 2 * 256 * 2 if kv_dtype == "bf16" else 2 * 256 * 1 + 2 * 4
+def kv_bytes_per_token(kv_dtype: str, row: int = 256, shared: bool = False) -> int:
+    """Cached rows of one token: K and V rows of `row` elements (all key/value heads), or one
+    row when a latent serves as both, in bf16 or e4m3 (+ one fp32 scale per stored row)."""
+    rows = 1 if shared else 2
+    return rows * row * 2 if kv_dtype == "bf16" else rows * (row + 4)
 
 
-def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64, T: int = 1) -> dict:
+def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64, T: int = 1,
+                      row: int = 256, shared: bool = False) -> dict:
     """HBM bytes one decode step must move: every cached K/V row once (shared by a sequence's
     T new query tokens), q, out and lse once per query token, the used block-table entries
     and the lengths."""
     tokens = int(sum(lens))
     pages = int(sum((L + page - 1) // page for L in lens))
     B = len(lens)
-    kv = tokens * kv_bytes_per_token(kv_dtype)
+    kv = tokens * kv_bytes_per_token(kv_dtype, row, shared)
     other = B * T * (H * d * 2) * 2 + pages * 4 + B * 4 + B * T * H * 4
     return {"kv": kv, "total": kv + other}
 
@@ -227,7 +237,7 @@ def cpu_oracle_sample(case, target_s: float = 10.0, nthreads: int = 0):
     for _ in range(reps):
         oracle.decode(case, batch_slice=slice(0, k * T), nthreads=nthreads)
     dt = time.perf_counter() - t0
-    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"] * reps
+    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype, **shape_args(case.workload))["kv"] * reps
     return kv / dt / 1e9, dt, k, reps
 
 
@@ -251,7 +261,7 @@ def run_reference(args, case, rank: int, world: int):
         t0 = time.perf_counter()
         oracle.decode(case, batch_slice=slice(0, k * T))
         times.append(time.perf_counter() - t0)
-    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype)["kv"]
+    kv = algorithmic_bytes(lens[:k], case.workload.kv_dtype, **shape_args(case.workload))["kv"]
     total = sum(times)
     value = kv * args.steps / total / 1e9
     sample = f"{k} of {len(lens)} sequences per step ({sum(lens[:k])} tokens), fp64, all {cores} cores"
@@ -273,7 +283,8 @@ def workload_config(case, extra=None):
     lens = case.seq_lens.tolist()
     cfg = {"workload": w.name, "batch": len(lens), "total_tokens": int(sum(lens)),
            "min_len": int(min(lens)), "max_len": int(max(lens)), "num_q_heads": w.num_q_heads,
-           "head_dim": w.head_dim, "kv_heads": 1, "page_size": w.page_size, "kv_dtype": w.kv_dtype,
+           "head_dim": w.head_dim, "kv_heads": w.num_kv_heads, "kv_shared": w.kv_shared,
+           "page_size": w.page_size, "kv_dtype": w.kv_dtype,
            "softmax_scale": w.scale(), "parallelism": "replica per GPU",
            "new_tokens_per_seq": w.tokens_per_seq}
     if extra:
@@ -375,25 +386,29 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
     kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
     B = len(lens)
     T = w.tokens_per_seq
-    acct = algorithmic_bytes(lens, w.kv_dtype, T=T)
-    flops = algorithmic_flops(lens, T=T)
+    sa = shape_args(w)
+    acct = algorithmic_bytes(lens, w.kv_dtype, T=T, **sa)
+    flops = algorithmic_flops(lens, H=sa["H"], d=sa["d"], T=T)
+    H, dq = w.num_q_heads, w.head_dim
 
     # rotating input copies: consecutive steps never find their KV in L2
-    set_bytes = case.k_cache.numel() * case.k_cache.element_size() * 2
+    set_bytes = case.k_cache.numel() * case.k_cache.element_size() * (1 if w.kv_shared else 2)
     nsets = 1 + max(1, math.ceil(2 * L2_BYTES / max(set_bytes, 1)))
     sets = []
     for _ in range(nsets):
+        k_dev = case.k_cache.to(dev)
         sets.append(dict(
-            q=case.q.to(dev), k=case.k_cache.to(dev), v=case.v_cache.to(dev),
+            q=case.q.to(dev), k=k_dev, v=k_dev if w.kv_shared else case.v_cache.to(dev),
             ks=None if case.k_scale is None else case.k_scale.to(dev),
             vs=None if case.v_scale is None else case.v_scale.to(dev),
             table=case.block_table.to(dev), lens=case.seq_lens.to(dev)))
-    out = torch.empty(B * T, 64, 256, dtype=torch.bfloat16, device=dev)
-    lse = torch.empty(B * T, 64, dtype=torch.float32, device=dev)
+    out = torch.empty(B * T, H, dq, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B * T, H, dtype=torch.float32, device=dev)
 
     def decoder(flags):
         return mfa.Decoder(B, case.max_pages, case.num_blocks, kv_dtype=kv, softmax_scale=w.scale(),
-                           host_seq_lens=lens, flags=flags, device=dev, tokens_per_seq=T)
+                           host_seq_lens=lens, flags=flags, device=dev, tokens_per_seq=T,
+                           shape=(w.num_q_heads, w.head_dim, w.num_kv_heads, w.kv_shared))
 
     # the timed steps are back-to-back decode steps whose lengths and block table are
     # filled once, before the loop: each step's decode may therefore read them while the
@@ -432,8 +447,8 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
     lanes = []
     for _ in range(E2E_LANES):
         lanes.append((decoder(mfa.MFA_PLAN_EARLY_METADATA), torch.cuda.Stream(dev),
-                      torch.empty(B * T, 64, 256, dtype=torch.bfloat16).pin_memory(),
-                      torch.empty(B * T, 64, dtype=torch.float32).pin_memory()))
+                      torch.empty(B * T, H, dq, dtype=torch.bfloat16).pin_memory(),
+                      torch.empty(B * T, H, dtype=torch.float32).pin_memory()))
     h2d = sum(t.numel() * t.element_size() for t in (q_h, table_h, lens_h))
     d2h = sum(t.numel() * t.element_size() for t in lanes[0][2:])
 
@@ -507,6 +522,12 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
         lambda i: mfa.mfa_combine(dec_only.plan, dec_only.problem, dec_only.workspace, comb_lens, out, lse),
         max(min(steps, 400), 50))
 
+    if (w.num_q_heads, w.head_dim, w.num_kv_heads) != (64, 256, 1):
+        # the append writes MFA cache rows only
+        res["kernels_live"] = {"mean_launch_ms": {"mfa_decode_kernel": kern_mean_ms, "mfa_combine_kernel": comb_mean_ms}}
+        res["kv_append"] = None
+        return res
+
     # --- the KV append of the same batch (each sequence's T new rows at its last T positions),
     #     alone and chained in front of the decode step (append -> decode -> combine)
     k_new = inputs.new_token_rows(B * T, seed=w.seed + 101, kinds=("normal",)).to(dev)
@@ -574,7 +595,8 @@ def run_native(args, case, rank: int, world: int, side_names=()):
         side[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "tflops", "hbm_roofline_frac", "roofline",
                                         "e2e", "steps", "device_status")}
         side[name]["config"] = {k: r["config"][k] for k in ("batch", "total_tokens", "kv_dtype", "num_ctas",
-                                                             "new_tokens_per_seq")}
+                                                             "new_tokens_per_seq", "num_q_heads", "head_dim",
+                                                             "kv_heads", "kv_shared")}
         del c, r
         torch.cuda.empty_cache()
 

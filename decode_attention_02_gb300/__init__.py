@@ -59,7 +59,8 @@ class MfaProblem(ctypes.Structure):
                 ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_seq", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("softmax_scale", ctypes.c_float),
-                ("out_dtype", ctypes.c_int32), ("tokens_per_seq", ctypes.c_int32)]
+                ("out_dtype", ctypes.c_int32), ("tokens_per_seq", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("kv_shared", ctypes.c_int32)]
 
 
 class MfaPlan(ctypes.Structure):
@@ -159,12 +160,20 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
+# The attention shapes the library runs: (num_q_heads, head_dim, num_kv_heads, kv_shared).
+SHAPE_MFA = (64, 256, 1, False)     # Step-3's MFA: one shared K head and one shared V head
+SHAPE_GQA = (64, 128, 4, False)     # grouped-query attention: 4 key/value heads of 128
+SHAPE_MLA = (128, 512, 1, True)     # one 512-wide latent that is both key and value
+
+
 def make_problem(batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
-                 softmax_scale: float = HEAD_DIM ** -0.5, num_q_heads: int = NUM_Q_HEADS,
+                 softmax_scale: Optional[float] = None, num_q_heads: int = NUM_Q_HEADS,
                  head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE, out_dtype: int = MFA_OUT_BF16,
-                 tokens_per_seq: int = 1) -> MfaProblem:
+                 tokens_per_seq: int = 1, num_kv_heads: int = 1, kv_shared: bool = False) -> MfaProblem:
+    if softmax_scale is None:
+        softmax_scale = head_dim ** -0.5
     return MfaProblem(batch, num_q_heads, head_dim, page_size, max_pages_per_seq, num_blocks, kv_dtype,
-                      softmax_scale, out_dtype, tokens_per_seq)
+                      softmax_scale, out_dtype, tokens_per_seq, num_kv_heads, 1 if kv_shared else 0)
 
 
 def mfa_decode_plan(problem: MfaProblem, host_seq_lens: Optional[Sequence[int]] = None, max_seq_len: int = 0,
@@ -268,10 +277,10 @@ def mfa_read_device_status(workspace, clear: bool = True, stream=None) -> int:
     return int(word.value)
 
 
-def workspace_layout(plan: MfaPlan):
+def workspace_layout(plan: MfaPlan, head_dim: int = HEAD_DIM):
     """Byte offsets of (partial O, partial lse) inside the workspace (see include/mfa.h)."""
     o_off = 256
-    lse_off = (o_off + plan.num_partials * NUM_Q_HEADS * HEAD_DIM * 4 + 255) // 256 * 256
+    lse_off = (o_off + plan.num_partials * NUM_Q_HEADS * head_dim * 4 + 255) // 256 * 256
     return o_off, lse_off
 
 
@@ -283,12 +292,14 @@ class Decoder:
     """
 
     def __init__(self, batch: int, max_pages_per_seq: int, num_blocks: int, kv_dtype: int = MFA_KV_BF16,
-                 softmax_scale: float = HEAD_DIM ** -0.5, host_seq_lens=None, max_seq_len: int = 0,
+                 softmax_scale: Optional[float] = None, host_seq_lens=None, max_seq_len: int = 0,
                  force_ctas: int = 0, flags: int = 0, device=None, out_dtype: int = MFA_OUT_BF16,
-                 tokens_per_seq: int = 1):
+                 tokens_per_seq: int = 1, shape=SHAPE_MFA):
         import torch
+        H, d, G, shared = shape
         self.problem = make_problem(batch, max_pages_per_seq, num_blocks, kv_dtype, softmax_scale,
-                                    out_dtype=out_dtype, tokens_per_seq=tokens_per_seq)
+                                    num_q_heads=H, head_dim=d, out_dtype=out_dtype, tokens_per_seq=tokens_per_seq,
+                                    num_kv_heads=G, kv_shared=shared)
         if host_seq_lens is None and max_seq_len == 0:
             max_seq_len = max_pages_per_seq * PAGE_SIZE
         self.plan = mfa_decode_plan(self.problem, host_seq_lens, max_seq_len, 0, force_ctas, flags)
@@ -298,12 +309,13 @@ class Decoder:
     def __call__(self, q, k_cache, v_cache, block_table, seq_lens, k_scale=None, v_scale=None, out=None,
                  lse=None, stream=None):
         import torch
-        rows = self.problem.batch * self.problem.tokens_per_seq   # (sequence, new token) pairs
+        pr = self.problem
+        rows = pr.batch * pr.tokens_per_seq   # (sequence, new token) pairs
         if out is None:
-            dt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
-            out = torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=dt, device=q.device)
+            dt = torch.float32 if pr.out_dtype == MFA_OUT_FP32 else torch.bfloat16
+            out = torch.empty((rows, pr.num_q_heads, pr.head_dim), dtype=dt, device=q.device)
         if lse is None:
-            lse = torch.empty((rows, NUM_Q_HEADS), dtype=torch.float32, device=q.device)
+            lse = torch.empty((rows, pr.num_q_heads), dtype=torch.float32, device=q.device)
         mfa_decode_run(self.plan, self.problem, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                        out, lse, self.workspace, stream)
         return out, lse
@@ -315,15 +327,16 @@ class Decoder:
         import torch
         if not hasattr(self, "_staging"):
             dev = self.device
-            B = self.problem.batch
-            rows = B * self.problem.tokens_per_seq
-            odt = torch.float32 if self.problem.out_dtype == MFA_OUT_FP32 else torch.bfloat16
+            pr = self.problem
+            B = pr.batch
+            rows = B * pr.tokens_per_seq
+            odt = torch.float32 if pr.out_dtype == MFA_OUT_FP32 else torch.bfloat16
             self._staging = dict(
-                q=torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=torch.bfloat16, device=dev),
-                table=torch.empty((B, self.problem.max_pages_per_seq), dtype=torch.int32, device=dev),
+                q=torch.empty((rows, pr.num_q_heads, pr.head_dim), dtype=torch.bfloat16, device=dev),
+                table=torch.empty((B, pr.max_pages_per_seq), dtype=torch.int32, device=dev),
                 lens=torch.empty((B,), dtype=torch.int32, device=dev),
-                out=torch.empty((rows, NUM_Q_HEADS, HEAD_DIM), dtype=odt, device=dev),
-                lse=torch.empty((rows, NUM_Q_HEADS), dtype=torch.float32, device=dev))
+                out=torch.empty((rows, pr.num_q_heads, pr.head_dim), dtype=odt, device=dev),
+                lse=torch.empty((rows, pr.num_q_heads), dtype=torch.float32, device=dev))
         st = self._staging
         mfa_decode_run_host(self.plan, self.problem, q_host, block_table_host, seq_lens_host, out_host, lse_host,
                             st["q"], st["table"], st["lens"], st["out"], None if lse_host is None else st["lse"],

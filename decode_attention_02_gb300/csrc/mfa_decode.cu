@@ -67,8 +67,41 @@
 
 namespace mfa {
 
-constexpr int kH = 64;             // query heads
-constexpr int kD = 256;            // head width
+constexpr int kH = 64;             // query heads a CTA holds (one unit)
+constexpr int kD = 256;            // MFA head width
+
+// Attention shapes.  MFA (the path) and the two designs the Step-3 page sets it against
+// (section 5, "Attention Design"; section 7, attention ablation), run by the same kernel:
+//   kShapeMfa: 64 query heads of width 256 over one K head and one V head (rows of 256);
+//   kShapeGqa: 64 query heads of width 128 over 4 key/value heads (grouped-query attention:
+//              cache rows of 4 x 128, query head h reads head h / 16);
+//   kShapeMla: 128 query heads of width 512 over one 512-wide latent that is both the key
+//              and the value (MLA-style, V = K); a CTA holds one unit of 64 heads, so a
+//              sequence is two units.
+enum : int { kShapeMfa = 0, kShapeGqa = 1, kShapeMla = 2 };
+template <int kShp>
+struct ShapeOf;
+template <>
+struct ShapeOf<kShapeMfa> {
+  static constexpr int kRow = 256;      // elements of a cache row (all key/value heads of a token)
+  static constexpr int kDq = 256;       // width of q and out per query head
+  static constexpr int kGroups = 1;     // key/value heads per cache row
+  static constexpr int kUnits = 1;      // 64-head units per sequence (per query token)
+  static constexpr int kOBlocks = 2;    // O^T blocks of 128 d lanes x 64 columns per head set
+  static constexpr int kOBufs = 2;      // O^T buffers (sequence switches overlap)
+};
+template <>
+struct ShapeOf<kShapeGqa> {
+  static constexpr int kRow = 512, kDq = 128, kGroups = 4, kUnits = 1;
+  static constexpr int kOBlocks = 1;    // one 64-column block: group g's 16 heads at columns 16 g
+  static constexpr int kOBufs = 2;
+};
+template <>
+struct ShapeOf<kShapeMla> {
+  static constexpr int kRow = 512, kDq = 512, kGroups = 1, kUnits = 2;
+  static constexpr int kOBlocks = 4;    // 512 d = four blocks of 128 lanes: 256 columns
+  static constexpr int kOBufs = 1;      // no room for a second buffer in tensor memory
+};
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
@@ -111,45 +144,54 @@ constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s for drains after an a
 //   e4m3 : Q 32 KB (e4m3 hi and lo parts) | P 16 KB (e4m3 weights: hi part 8 KB, lo part 8 KB) |
 //          ring 20 x 8 KB (raw e4m3 boxes: both MMAs read K and V as TMA wrote them); the
 //          per-token scales are read from global memory by the threads that apply them
-constexpr int kOffQ = 0;                                     // 4 x [64 heads x 128 B]
-constexpr int kOffP = 32768;                                 // [128 tokens x 128 B]
+constexpr int kOffQ = 0;                                     // kDq / 64 x [64 heads x 128 B]
 constexpr int kOffBar = 212992;                              // mbarriers
-template <bool kFp8>
-struct KvLayout;
-template <>
-struct KvLayout<false> {
-  static constexpr int kOffRing = 49152;
-  static constexpr int kNumSlots = 10;
-  static constexpr int kSlotBytes = 16384;
+// Q (bf16: 64 heads x kDq; e4m3: hi and lo parts, 32 KB), then P (16 KB: bf16 weights
+// [128 tokens x 64 heads], or the e4m3 hi and lo parts), then the ring up to the barriers:
+//   bf16: slots of 16 KB (a 64-element chunk of both pages of a tile for K; a 128-element
+//         block of one page for V), kRow / 64 uses per tile for each of K and V;
+//   e4m3: slots of 8 KB (one page's 128-element half row block), four uses each.
+template <bool kFp8, int kShp>
+struct Layout {
+  using Sh = ShapeOf<kShp>;
+  static constexpr int kOffP = kFp8 ? 32768 : 64 * Sh::kDq * 2;
+  static constexpr int kOffRing = kOffP + 16384;
+  static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
+  static constexpr int kNumSlots = (kOffBar - kOffRing) / kSlotBytes;
+  static constexpr int kKU = kFp8 ? 4 : Sh::kRow / 64;   // ring uses per K group and per V group
   static constexpr int kExtraSmem = 0;
 };
-template <>
-struct KvLayout<true> {
-  static constexpr int kOffRing = 49152;
-  static constexpr int kNumSlots = 20;
-  static constexpr int kSlotBytes = 8192;
-  static constexpr int kExtraSmem = 0;
-};
-static_assert(KvLayout<false>::kOffRing + KvLayout<false>::kNumSlots * KvLayout<false>::kSlotBytes == kOffBar, "");
-static_assert(KvLayout<true>::kOffRing + KvLayout<true>::kNumSlots * KvLayout<true>::kSlotBytes == kOffBar, "");
+static_assert(Layout<false, kShapeMfa>::kNumSlots == 10 && Layout<true, kShapeMfa>::kNumSlots == 20 &&
+              Layout<false, kShapeGqa>::kNumSlots == 11 && Layout<false, kShapeMla>::kNumSlots == 8, "");
+static_assert(Layout<false, kShapeMla>::kNumSlots >= Layout<false, kShapeMla>::kKU, "a ring holds one group");
 // The e4m3 QK^T reads a d-half's two pages as one 128-row operand from two adjacent slots
 // (uses 2k and 2k + 1 of an aligned group of four): they stay adjacent only for an even count.
-static_assert(KvLayout<true>::kNumSlots % 2 == 0, "e4m3 ring: page pairs must not wrap");
+static_assert(Layout<true, kShapeMfa>::kNumSlots % 4 == 0, "e4m3 ring: groups must not wrap");
 constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nseg [3] ntiles [4..19] scan
                                          //      [20..21] CTA tile range [24..31] q maxima
 // Ring-order counts.  K and V uses share one ring, and a consumer may only wait on a slot's
 // Full barrier once the slot's previous use has landed: a waiter two phases behind would see
 // the parity it wants and read a slot still being written.  With the QK^T and PV streams in
 // different threads, some slots of tile n's K uses last held the V uses of an earlier tile
-// (bf16, 10 slots: V(n - 3); e4m3, 20 slots: V(n - 4)), with no barrier between the two
-// streams that orders them.  So the PV issuer publishes, after its Full waits, how many
-// tiles of V uses have landed (cnt[1], cnt[2]: page 0 and page 1, written together), and
-// the QK^T issuer waits for both counts >= n - kVLag + 1 before tile n's K uses.  The other
-// direction needs no count: tile n's V slots last held K uses of tile n - 1 or earlier, and
-// a PV of tile n follows tile n's K through the softmax's P.  cnt[0] counts the K tiles the
-// QK^T issuer has issued (diagnostic).
-template <bool kFp8>
-__host__ __device__ constexpr int v_lag() { return kFp8 ? 4 : 3; }
+// (MFA bf16, 10 slots: V(n - 3); e4m3, 20 slots: V(n - 4)), and with a small ring some slots
+// of tile m's V uses last held K uses of tile m + 1 (the 11- and 8-slot rings of the wider
+// shapes), with no barrier between the two streams that orders them.  So each stream
+// publishes how many tiles of its uses have landed -- cnt[0]: K tiles, by the QK^T issuer
+// after its Full waits; cnt[1], cnt[2]: V tiles (page 0 and page 1, written together), by
+// the PV issuer after its Full waits -- and waits on the other's count where the slot's
+// previous use is not already ordered before it (k_needs_v, v_needs_k: the counts follow from
+// the ring order; a PV of tile m follows K(m) through the softmax's P).
+template <int kKU, int kSlots>
+__device__ __forceinline__ int k_needs_v(int n) {
+  const int hi = (n == 0 ? 0 : 2 * kKU * n - kKU) + kKU - 1 - kSlots;   // last previous use
+  return hi >= 2 * kKU ? (hi - 2 * kKU) / (2 * kKU) + 1 : 0;
+}
+template <int kKU, int kSlots>
+__device__ __forceinline__ int v_needs_k(int m, int ntiles) {
+  const int base = (m + 1 < ntiles) ? 2 * kKU * m + 2 * kKU : 2 * kKU * m + kKU;
+  const int hi = base + kKU - 1 - kSlots;
+  return hi >= 0 ? (hi + kKU) / (2 * kKU) + 1 : 0;
+}
 constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1, spare
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
@@ -159,9 +201,8 @@ constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, e
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileInfo = kOffSegN0 + 4 * kMaxSeg;   // int4[kMaxTilesPerCta] {page 0, page 1, rows 0, rows 1}
 constexpr int kSmemUsed = kOffTileInfo + 16 * kMaxTilesPerCta;
-template <bool kFp8>
-constexpr int smem_bytes() { return kSmemUsed + KvLayout<kFp8>::kExtraSmem + 1024; }
-static_assert(smem_bytes<true>() <= 232448, "shared memory budget");
+constexpr int smem_bytes() { return kSmemUsed + 1024; }
+static_assert(smem_bytes() <= 232448, "shared memory budget");
 
 enum Bar : int {
   kBarFull = 0,
@@ -185,8 +226,10 @@ constexpr uint32_t kTmemS = 0;     // S^T buffers: bf16 [0,64) and [64,128); e4m
                                    // [128,256) (64 columns of hi-part scores, then 64 of lo)
 template <bool kFp8>
 __host__ __device__ constexpr uint32_t s_cols() { return kFp8 ? 128u : 64u; }
+// O^T buffer k, block j: + 64 kOBlocks k + 64 j (MFA: d-halves; MLA: four 128-d blocks; GQA:
+// one block whose columns 16 g .. 16 g + 15 hold the heads of key/value head g)
 template <bool kFp8>
-__host__ __device__ constexpr uint32_t tmem_o() { return kFp8 ? 256u : 128u; }   // O^T buffer k, half hh: + 128k + 64hh
+__host__ __device__ constexpr uint32_t tmem_o() { return kFp8 ? 256u : 128u; }
 constexpr uint32_t kTmemL = 384;   // bf16: per-lane row sums of the bf16-rounded weights (normalise O)
 constexpr uint32_t kTmemLx = 448;  // bf16: per-lane row sums of the fp32 weights (lse)
 
@@ -209,7 +252,8 @@ struct DecodeParams {
   int out_f32;        // 1: fp32 output, 0: bf16 output
   int early_metadata; // 1: seq_lens/block_table may be read before the preceding grid completes
   float scale_log2;   // softmax_scale * log2(e)
-  int tokens;         // new query tokens per sequence T: batch counts the B * T (sequence, token) pairs
+  int tokens;         // new query tokens per sequence T
+  int units;          // 64-head units per query token U: batch counts the B * T * U units
 };
 
 struct CombineParams {
@@ -224,6 +268,7 @@ struct CombineParams {
   int out_f32;
   int heads_per_cta;  // 1, 4 or 16
   int tokens;         // as DecodeParams::tokens
+  int units;          // as DecodeParams::units
   int seq_cost;       // cost_seq of the KV format: the decode kernel's split
 };
 
@@ -267,14 +312,16 @@ __device__ __forceinline__ int clamp_len(int L, int cap, bool& bad) {
 
 __device__ __forceinline__ int tiles_of(int L) { return (L + kTile - 1) / kTile; }
 
-// Multi-token decode: with T new query tokens per sequence (the last T of its L cached tokens),
-// query token i of sequence b is the "sequence" x = b T + i of length L - T + 1 + i: it
-// attends to the cached tokens up to its own position, which is the causal mask among the new
-// tokens.  T = 1 is the ordinary decode step (x = b, length L).
-__device__ __forceinline__ int raw_len(const int32_t* lens, int T, int x) { return lens[T == 1 ? x : x / T]; }
-__device__ __forceinline__ int vlen_from(int L_raw, int T, int x, int cap, bool& bad) {
+// Units.  With T new query tokens per sequence (the last T of its L cached tokens) and U
+// 64-head units per query token, unit x = (b T + i) U + u is head set u of query token i of
+// sequence b: it reads b's block-table row and attends to the cached tokens 0 .. L - T + i
+// (length L - T + 1 + i), which is the causal mask among the new tokens.  T = U = 1 is the
+// ordinary MFA decode step (x = b, length L).
+__device__ __forceinline__ int seq_of(int x, int T, int U) { return (T == 1 && U == 1) ? x : x / (T * U); }
+__device__ __forceinline__ int raw_len(const int32_t* lens, int T, int U, int x) { return lens[seq_of(x, T, U)]; }
+__device__ __forceinline__ int vlen_from(int L_raw, int T, int U, int x, int cap, bool& bad) {
   const int L = clamp_len(L_raw, cap, bad);
-  return T == 1 ? L : max(0, L - (T - 1 - x % T));
+  return T == 1 ? L : max(0, L - (T - 1 - (x / U) % T));
 }
 
 // Bounded wait on an mbarrier phase.  Returns false after kWaitLimitNs, or at
@@ -495,24 +542,32 @@ __device__ __forceinline__ float token_scale(const float* __restrict__ sc, const
   return __ldg(sc + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
 }
 
-// e4m3 ring use index of the K (is_v = false) or V part (page pg, d-half dh) of tile t of a
-// CTA with `ntiles` tiles.  The producer issues K(0), then K(t) and V(t-1) for t = 1..N-1,
-// then V(N-1), four uses each: K(0) = 0..3, K(t) = 8t-4.., V(t) = 8t+8.. except the last
-// tile's V, which directly follows its K: V(N-1) = 8N-4...  Every group of four starts at
-// a multiple of 4 and the e4m3 ring has 20 slots, so a group never wraps: K's two pages of
-// one d-half sit in adjacent slots and form one 128-row MMA operand.
-__device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v, int pg, int dh) {
-  const uint32_t base = is_v ? (t + 1 < ntiles ? 8u * t + 8u : 8u * t + 4u) : (t == 0 ? 0u : 8u * t - 4u);
-  return base + (is_v ? 2u * pg + dh : 2u * dh + pg);
+// Ring use index of the first use of the K (is_v = false) or V group of tile t of a CTA with
+// `ntiles` tiles, kKU uses per group.  The producer issues K(0), then K(t) and V(t-1) for
+// t = 1..N-1, then V(N-1): K(0) = 0.., K(t) = 2 kKU t - kKU.., V(t) = 2 kKU t + 2 kKU.. except
+// the last tile's V, which directly follows its K: V(N-1) = 2 kKU N - kKU...  e4m3 (kKU = 4):
+// every group starts at a multiple of 4 and the ring has 20 slots, so a group never wraps and
+// K's two pages of one d-half sit in adjacent slots, one 128-row MMA operand.
+template <int kKU>
+__device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v) {
+  constexpr uint32_t U = kKU;
+  return is_v ? (t + 1 < ntiles ? 2u * U * t + 2u * U : 2u * U * t + U) : (t == 0 ? 0u : 2u * U * t - U);
 }
 
-template <bool kFp8>
+template <bool kFp8, int kShp>
 __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Lay = KvLayout<kFp8>;
+  static_assert(!kFp8 || kShp == kShapeMfa, "the e4m3 cache is built for the MFA shape");
+  using Lay = Layout<kFp8, kShp>;
+  using Sh = ShapeOf<kShp>;
   constexpr int kThreads = threads_of<kFp8>();
   constexpr int kNumSlots = Lay::kNumSlots;
   constexpr int kSlotBytes = Lay::kSlotBytes;
   constexpr int kOffRing = Lay::kOffRing;
+  constexpr int kOffP = Lay::kOffP;
+  constexpr int kKU = Lay::kKU;
+  constexpr int kQBoxes = Sh::kDq / 64;          // 64-wide q boxes of a unit (bf16)
+  constexpr int kVBlocks = Sh::kRow / 128;       // bf16 V uses of one page (128-element blocks)
+  constexpr int kNh = 64 / Sh::kGroups;          // query heads per key/value head in a unit
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -528,7 +583,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // With early metadata the lengths are read before anything else: the schedule below
   // waits on them and on nothing the set-up does.
   int L_first = 0;
-  if (p.early_metadata && tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, tid);
+  if (p.early_metadata && tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, tid);
 
   // ---------------- set-up: barriers (one per lane of warp 0), tensor memory
   if (warp == 0) {
@@ -566,7 +621,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   // kernel does not write them); q, K, V and every output wait.
   if (!p.early_metadata) {
     grid_dep_wait();
-    if (tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, tid);
+    if (tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, tid);
   }
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
@@ -585,9 +640,9 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     auto packed = [](int T) { return static_cast<long long>(T) | (static_cast<long long>(T > 0) << 32); };
     long long loc = 0;
     // L_first (read above) is reused by the segment scan below
-    loc += packed(tiles_of(tid < p.batch ? vlen_from(L_first, p.tokens, tid, cap, bad) : 0));
+    loc += packed(tiles_of(tid < p.batch ? vlen_from(L_first, p.tokens, p.units, tid, cap, bad) : 0));
     for (int b = tid + kThreads; b < p.batch; b += kThreads)
-      loc += packed(tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, bad)));
+      loc += packed(tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, bad)));
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     long long tot0 = 0;
     const long long incl0 = block_incl_scan<kThreads, long long>(loc, scratch, tot0);
@@ -621,7 +676,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       // one sequence per thread: its tiles are [S, S + T) of the first scan; the sequences
       // overlapping the CTA are numbered by a ballot count
       bool dummy = false;
-      const int L = (tid < p.batch) ? vlen_from(L_first, p.tokens, tid, cap, dummy) : 0;
+      const int L = (tid < p.batch) ? vlen_from(L_first, p.tokens, p.units, tid, cap, dummy) : 0;
       const int T = tiles_of(L);
       const long long ex = incl0 - packed(T);
       const int S = static_cast<int>(ex & 0xFFFFFFFFll), Nb = static_cast<int>(ex >> 32);
@@ -656,7 +711,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       for (int c0 = 0; c0 < p.batch && cost_of(carry) <= X1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
-        const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) : 0;
+        const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy) : 0;
         const int T = tiles_of(L);
         long long tot = 0;
         const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -674,7 +729,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         for (int c0 = 0; c0 < p.batch && (carry & 0xFFFFFFFFll) < t1; c0 += kThreads) {
           const int b = c0 + tid;
           bool dummy = false;
-          const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) : 0;
+          const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy) : 0;
           const int T = tiles_of(L);
           long long tot = 0;
           const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -714,7 +769,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       const int4 sg = seg[s];
       const int j = sg.y + (n - seg_n0[s]);
       const int r0 = min(kPage, sg.w - kTile * j), r1 = min(kPage, sg.w - kTile * j - kPage);
-      const int32_t* row = p.block_table + static_cast<size_t>(sg.x / p.tokens) * p.max_pages;
+      const int32_t* row = p.block_table + static_cast<size_t>(seq_of(sg.x, p.tokens, p.units)) * p.max_pages;
       int b0 = row[2 * j];
       int b1 = (r1 > 0) ? row[2 * j + 1] : 0;
       // an id outside the pool is reported and replaced by -1: the TMA box then lies wholly
@@ -739,22 +794,24 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       // the lines (evict last) for the next one.
       const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_last();
       int seg_k = 0, seg_v = 0;   // segment of the producer's current K and V tiles
-      const bool act = lane < 4;
-      const int c = lane & 3;
+      const bool act = lane < kKU;
+      const int c = lane;
       bool ok = true;
       int sq = 0, nq = 0;                 // next segment whose q is loaded; q loads issued
       uint32_t mine[3] = {0u, 0u, 0u};    // this lane's last three uses (drain after an abort)
       int nmine = 0;
-      // lane c: use c of the group (bf16 K: 64-d chunk c of both pages; e4m3 K: page c & 1,
-      // d-half c >> 1; V: page c >> 1, d-half c & 1)
+      // lane c: use c of the group (bf16 K: 64-element chunk c of both pages; bf16 V: page
+      // c / kVBlocks, 128-element block c % kVBlocks; e4m3 K: page c & 1, d-half c >> 1; e4m3
+      // V: page c >> 1, d-half c & 1)
+      const int reads = p.tokens * p.units;   // units that read one sequence's pages
       auto group = [&](bool is_v, int t) -> bool {
         bool okl = true;
         int& sc_ = is_v ? seg_v : seg_k;
         while (sc_ + 1 < nseg && seg_n0[sc_ + 1] <= t) ++sc_;
-        const uint64_t pol = (p.tokens > 1 && seg[sc_].x % p.tokens != p.tokens - 1) ? pol_again : pol_once;
+        const uint64_t pol = (reads > 1 && seg[sc_].x % reads != reads - 1) ? pol_again : pol_once;
         if (act) {
           const int4 ti = tile_info[t];
-          const uint32_t u = ring_use(t, ntiles, is_v, 0, 0) + c;
+          const uint32_t u = ring_use<kKU>(t, ntiles, is_v) + c;
           const uint32_t slot = u % kNumSlots;
           okl = wait_bar(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag);
           if (okl) {
@@ -766,8 +823,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               tma_load_3d_hint(dst, map, fb, 64 * c, ti.z - kPage, ti.x, pol);
               if (ti.w > 0) tma_load_3d_hint(dst + 8192, map, fb, 64 * c, ti.w - kPage, ti.y, pol);
             } else {
-              const int pg = (kFp8 && !is_v) ? (c & 1) : (c >> 1);
-              const int dh = (kFp8 && !is_v) ? (c >> 1) : (c & 1);
+              const int pg = kFp8 ? ((!is_v) ? (c & 1) : (c >> 1)) : c / kVBlocks;
+              const int dh = kFp8 ? ((!is_v) ? (c >> 1) : (c & 1)) : c % kVBlocks;
               const int r = pg ? ti.w : ti.z;
               const int blk = pg ? ti.y : ti.x;
               if (r <= 0) {
@@ -795,14 +852,15 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
             if (lane == 0) {
               if (sq > 0) okq = wait_bar(bar(kBarQEmpty), (sq - 1) & 1, abort_flag);
               if (okq) {
-                mbar_arrive_expect_tx(bar(kBarQFull), kH * kD * 2);
-                for (int q = 0; q < 4; ++q)
+                constexpr int kQB = kFp8 ? 4 : kQBoxes;
+                mbar_arrive_expect_tx(bar(kBarQFull), kQB * 8192);
+                for (int q = 0; q < kQB; ++q)
                   tma_load_2d(sbase + kOffQ + q * 8192, &p.tm_q, bar(kBarQFull), 64 * q, kH * seg[sq].x);
                 ++nq;
                 // the next segment's q waits for this segment's last QK^T; bring it into L2
                 // now so that its load then comes from L2
                 if (sq + 1 < nseg)
-                  for (int q = 0; q < 4; ++q) tma_prefetch_2d(&p.tm_q, 64 * q, kH * seg[sq + 1].x);
+                  for (int q = 0; q < kQB; ++q) tma_prefetch_2d(&p.tm_q, 64 * q, kH * seg[sq + 1].x);
               }
             }
             ok = __all_sync(0xffffffffu, okq);
@@ -828,38 +886,44 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     // waits behind the issue of the next QK^T; both commit to the drain barrier before
     // tensor memory is released.
     if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, 64);
+      // N = the query heads that share one key/value head (64; GQA: 16, one MMA per group)
+      constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, kNh);
       constexpr uint32_t kIdescQK8 = idesc_e4m3(false, false, 128, 128);
-      constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, 64);
+      constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, kNh);
       constexpr uint32_t kIdescPV8 = idesc_e4m3(true, true, 128, 64);
+      constexpr int kChunksPerHead = Sh::kDq / 64;   // 64-element K chunks of one key head
       int sk = 0, jk = seg[0].y, sv = 0, jv = seg[0].y;
       bool ok = true;
       for (int n = 0; n <= ntiles && ok; ++n) {
         if (n < ntiles && warp == 1) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
-          const uint32_t u0 = ring_use(n, ntiles, false, 0, 0);
-          // some slots of tile n's K last held V(n - v_lag): it must have landed (ring-order counts)
-          constexpr int kLag = v_lag<kFp8>();
-          if (n >= kLag)
-            ok = wait_count(cnt + 1, n - kLag + 1, abort_flag) && wait_count(cnt + 2, n - kLag + 1, abort_flag);
+          const uint32_t u0 = ring_use<kKU>(n, ntiles, false);
+          // some slots of tile n's K last held an earlier tile's V: it must have landed
+          const int nv = k_needs_v<kKU, kNumSlots>(n);
+          if (nv > 0) ok = wait_count(cnt + 1, nv, abort_flag) && wait_count(cnt + 2, nv, abort_flag);
           if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
           if (!ok) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem + kTmemS + s_cols<kFp8>() * (n & 1);
           if constexpr (!kFp8) {
-            for (int c = 0; c < 4; ++c) {
+            // chunk c = 64 elements of the cache row; with grouped heads it belongs to key
+            // head g = c / kChunksPerHead, whose query heads are rows 16 g .. 16 g + 15 of q
+            // box c % kChunksPerHead and columns 16 g .. of S^T
+            for (int c = 0; c < kKU; ++c) {
               const uint32_t slot = (u0 + c) % kNumSlots;
               ok = wait_bar(bar(kBarFull + slot), ((u0 + c) / kNumSlots) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
+              const int g = c / kChunksPerHead, cq = c % kChunksPerHead;
               const uint32_t a0 = sbase + kOffRing + slot * kSlotBytes;
-              const uint32_t b0 = sbase + kOffQ + c * 8192;
+              const uint32_t b0 = sbase + kOffQ + cq * 8192 + 128 * kNh * (Sh::kGroups > 1 ? g : 0);
+              const uint32_t dq = d_tmem + (Sh::kGroups > 1 ? kNh * g : 0);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_f16_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
-                            kIdescQK, (c | kk) != 0);
+                umma_f16_ss(dq, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
+                            kIdescQK, ((Sh::kGroups > 1 ? cq : c) | kk) != 0);
               umma_commit(bar(kBarEmpty + slot));
             }
             if (!ok) break;
@@ -893,25 +957,34 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           const int m = n - 1;
           const int4 sg = seg[sv];
           const bool first = (jv == sg.y), last = (jv == sg.z - 1);
-          const int kb = sv & 1;
+          constexpr int kOBufs = kFp8 ? 2 : Sh::kOBufs;
+          constexpr int kBlocksPerPage = kFp8 ? 2 : kVBlocks;
+          const int kb = sv % kOBufs;
           const int4 ti = tile_info[m];
-          const uint32_t uv = ring_use(m, ntiles, true, 0, 0);
+          const uint32_t uv = ring_use<kKU>(m, ntiles, true);
           ok = wait_bar(bar(kBarPFull), m & 1, abort_flag);
-          if (ok && first && sv >= 2) ok = wait_bar(bar(kBarOEmpty + kb), ((sv >> 1) - 1) & 1, abort_flag);
+          if (ok && first && sv >= kOBufs)
+            ok = wait_bar(bar(kBarOEmpty + kb), ((sv / kOBufs) - 1) & 1, abort_flag);
+          // some slots of tile m's V last held a later tile's K (small rings): it must have landed
+          const int nk = v_needs_k<kKU, kNumSlots>(m, ntiles);
+          if (ok && nk > m + 1) ok = wait_count(cnt, nk, abort_flag);
           if (!ok) break;
           tc_fence_after();
           for (int pg = 0; pg < 2 && ok; ++pg) {
             const int r = pg ? ti.w : ti.z;
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t u = uv + 2 * pg + hh;
+            for (int hh = 0; hh < kBlocksPerPage; ++hh) {
+              const uint32_t u = uv + kBlocksPerPage * pg + hh;
               ok = wait_bar(bar(kBarFull + u % kNumSlots), (u / kNumSlots) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
               const uint32_t a0 = sbase + kOffRing + (u % kNumSlots) * kSlotBytes;
-              const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 128u * kb + 64u * hh;
+              // block hh: O^T lanes d of 128-element block hh; with grouped heads it is key
+              // head hh's value, for its 16 query heads only (columns 16 hh .., P columns 16 hh ..)
+              const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 64u * (kFp8 ? 2 : Sh::kOBlocks) * kb +
+                                      (Sh::kGroups > 1 ? static_cast<uint32_t>(kNh) : 64u) * hh;
               if (r > 0) {
                 if constexpr (!kFp8) {
-                  const uint32_t b0 = sbase + kOffP + pg * 8192;
+                  const uint32_t b0 = sbase + kOffP + pg * 8192 + (Sh::kGroups > 1 ? 2 * kNh * hh : 0);
 #pragma unroll
                   for (int kk = 0; kk < 4; ++kk)
                     umma_f16_ss(d_tmem, smem_desc(a0 + 2048 * kk, 8192, 1024),
@@ -965,16 +1038,19 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     float* linv = reinterpret_cast<float*>(smem + kOffLinv);
     const float c = p.scale_log2;
     const bool issuer = (lane == 0) && ((sw & 3) == 0);   // one bulk-store thread per head half
+    constexpr int kOBufs = kFp8 ? 2 : Sh::kOBufs;
+    constexpr int kOBlocks = kFp8 ? 2 : Sh::kOBlocks;
+    constexpr int kDq = Sh::kDq;
     float qinv = 1.f, qinv_next = 1.f;              // e4m3: 2^-sigma of the segment's q split
 
     if (p.early_metadata) grid_dep_wait();
     // sequences with no tokens: out = 0, lse = -inf (one CTA each, round robin)
     for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
       bool dummy = false;
-      if (vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy) != 0) continue;
+      if (vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy) != 0) continue;
       const int esz = p.out_f32 ? 4 : 2;
-      uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * kH * kD * esz);
-      for (int i = ts; i < kH * kD * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
+      uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + static_cast<size_t>(b) * kH * kDq * esz);
+      for (int i = ts; i < kH * kDq * esz / 16; i += kSoftmaxThreads) o[i] = make_uint4(0, 0, 0, 0);
       if (p.lse != nullptr && ts < kH) p.lse[b * kH + ts] = -INFINITY;
     }
 
@@ -990,19 +1066,45 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     // valid rows of a tile's page pg: the last page's rows sit at the end of the box
     auto page_rows = [&](int L, int j, int pg) { return min(kPage, L - kTile * j - kPage * pg); };
 
-    // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx & 1),
+    // Write the finished accumulator of this CTA's segment `sidx` (O buffer sidx % kOBufs),
     // normalised by 1/l from linv, as [head][d] rows.  `direct`: plain stores from
     // registers (the CTA's last two segments, after its last MMA); otherwise the rows are
     // staged in this half's 8 KB of the P buffer and sent by bulk async copies in
-    // double-buffered 4 KB rounds, off the threads' critical path.  Returns false if the
-    // CTA is aborting.
+    // double-buffered 4 KB rounds, off the threads' critical path (MFA; the other shapes
+    // always store directly, one 128-d block at a time).  Returns false if the CTA is aborting.
     auto write_segment = [&](int sidx, int b, int slot_p, bool whole, bool direct) -> bool {
-      const int kb = sidx & 1;
-      const bool okO = wait_warp(bar(kBarOFull + kb), (sidx >> 1) & 1, abort_flag);
+      const int kb = sidx % kOBufs;
+      const bool okO = wait_warp(bar(kBarOFull + kb), (sidx / kOBufs) & 1, abort_flag);
       aborted = aborted || !okO;
       if (named_bar_or(1, kSoftmaxThreads, aborted || *abort_flag)) return false;
       tc_fence_after();
-      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 128u * kb + h0 + lane_base;
+      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 64u * kOBlocks * kb + h0 + lane_base;
+      if constexpr (kShp != kShapeMfa) {
+        const bool bf16_out = whole && !p.out_f32;
+        const int esz = bf16_out ? 2 : 4;
+        uint8_t* gdst = whole ? static_cast<uint8_t*>(p.out) + (static_cast<size_t>(b) * kH + h0) * kDq * esz
+                              : reinterpret_cast<uint8_t*>(p.part_o) + (static_cast<size_t>(slot_p) * kH + h0) * kDq * 4;
+#pragma unroll 1
+        for (int blk = 0; blk < kOBlocks; ++blk) {
+          uint32_t oa[32];
+          tmem_ld32(o_tmem + 64u * blk, oa);
+          tmem_ld_wait(oa);
+          if (blk == kOBlocks - 1) {
+            tc_fence_before();
+            mbar_arrive(bar(kBarOEmpty + kb));   // the accumulator is free
+          }
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const float v = __uint_as_float(oa[h]) * linv[kb * kH + h0 + h];
+            const size_t e = static_cast<size_t>(h) * kDq + 128 * blk + row;
+            if (bf16_out)
+              reinterpret_cast<__nv_bfloat16*>(gdst)[e] = __float2bfloat16_rn(v);
+            else
+              reinterpret_cast<float*>(gdst)[e] = v;
+          }
+        }
+        return true;
+      }
       uint32_t oa[32], ob[32];
       tmem_ld32(o_tmem, oa);
       tmem_ld32(o_tmem + 64, ob);
@@ -1156,10 +1258,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
 
     for (int s = 0; s < nseg && !aborted; ++s) {
       const int4 sg = seg[s];
-      const int b = sg.x, L = sg.w, kb = s & 1;
+      const int b = sg.x, L = sg.w, kb = s % kOBufs;
       const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
       const int slot_p = b + static_cast<int>(blockIdx.x);
-      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 128u * kb + h0 + lane_base;   // + 64 for d in [128, 256)
+      const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 64u * kOBlocks * kb + h0 + lane_base;   // + 64 per block
       if (ts < kH) m_ref[ts] = -INFINITY;
       if constexpr (kFp8) {
         qinv = qinv_next;
@@ -1266,10 +1368,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
               for (int h = 0; h < 32; ++h) lreg[h] *= alpha_s[h0 + h];
             }
 #pragma unroll 1
-            for (int k3 = 0; k3 < (kFp8 ? 2 : 4); ++k3) {
+            for (int k3 = 0; k3 < kOBlocks + (kFp8 ? 0 : 2); ++k3) {
               uint32_t ov[32];
-              const uint32_t ta = (k3 == 2) ? l_tmem : (k3 == 3) ? lx_tmem : o_tmem + 64u * k3;
-              const float ox = (k3 < 2) ? o_extra : 1.f;
+              const uint32_t ta = (k3 == kOBlocks) ? l_tmem : (k3 == kOBlocks + 1) ? lx_tmem : o_tmem + 64u * k3;
+              const float ox = (k3 < kOBlocks) ? o_extra : 1.f;
               tmem_ld32(ta, ov);
               tmem_ld_wait(ov);
 #pragma unroll
@@ -1378,7 +1480,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         // its last PV completed before that P could be written, so the stores overlap the
         // remaining tiles instead of adding to the CTA's tail (the e4m3 softmax, which bounds
         // its tile period, keeps both writes for the end)
-        if (!kFp8 && first && s >= 1 && s == nseg - 1) {
+        if (!kFp8 && kOBufs == 2 && first && s >= 1 && s == nseg - 1) {
           const int ps = s - 1, pkb = ps & 1;
           if (!write_segment(ps, defer_b[pkb], defer_slot[pkb], defer_whole[pkb], true)) { stop = true; break; }
           prev_written = true;
@@ -1417,8 +1519,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         }
       }
       named_bar_sync(1, kSoftmaxThreads);
-      if (s + 2 < nseg) {
-        // the accumulator is needed again by segment s + 2: write it out now
+      if (s + kOBufs < nseg) {
+        // the accumulator is needed again by segment s + kOBufs: write it out now
         if (!write_segment(s, b, slot_p, whole, false)) break;
       } else {
         // one of the CTA's last two segments: its accumulator stays in tensor memory and is
@@ -1432,9 +1534,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     if (!aborted && !*abort_flag) {
       // deferred accumulators, newest first, stored straight from registers (uniform:
       // every thread reads the same values)
-      const int first_def = (nseg >= 2 && !prev_written) ? nseg - 2 : nseg - 1;
-      for (int s = nseg - 1; s >= first_def; --s) {
-        const int kb = s & 1;
+      // (a CTA whose cost range holds no tile has no segment, and nothing to write)
+      const int first_def = (kOBufs == 2 && nseg >= 2 && !prev_written) ? nseg - 2 : nseg - 1;
+      for (int s = nseg - 1; s >= 0 && s >= first_def; --s) {
+        const int kb = s % kOBufs;
         if (!write_segment(s, defer_b[kb], defer_slot[kb], defer_whole[kb], true)) break;
       }
     }
@@ -1464,20 +1567,23 @@ __device__ __forceinline__ int cta_of_cost(long long c, long long C, long long G
 constexpr int kCombineThreads = 256;
 constexpr int kCombineMaxParts = 256;        // partials staged per pass
 
-// One CTA per (sequence, group of `heads_per_cta` heads).  The 256 threads form
-// four quads of 64 (each thread owns 4 consecutive d, a float4).  With one head
-// per CTA the quads split the partials four ways; with four or more heads each
-// quad owns a head and the CTA walks its heads in rounds of four.  Partial lse
-// values are staged in shared memory; partial O rows stream in with batched
-// independent float4 loads.
+// One CTA per (unit, group of `heads_per_cta` heads).  The 256 threads form four quads of
+// 64; a thread owns 4 consecutive d (a float4) of each 256-d span of the kDq-wide row (for
+// kDq = 128 the quad's upper 32 threads hold nothing).  With one head per CTA the quads split
+// the partials four ways; with four or more heads each quad owns a head and the CTA walks its
+// heads in rounds of four.  Partial lse values are staged in shared memory; partial O rows
+// stream in with batched independent float4 loads.
+template <int kDq>
 __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
+  constexpr int kF = (kDq + 255) / 256;          // float4s per thread and row
+  constexpr int kRowF4 = kDq / 4;
   grid_dep_wait();
   grid_dep_launch();   // the next kernel may start its own set-up
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
   __shared__ int red_nb[kCombineThreads / 32], red_nt[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
   __shared__ float wts[4][kCombineMaxParts];
-  __shared__ float4 part_acc[3][64];
+  __shared__ float4 part_acc[3][64 * kF];
   __shared__ float pass_max[4], pass_sum[4];
   __shared__ int nparts_s;
   const int b = blockIdx.x;
@@ -1490,7 +1596,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   int before = 0, total = 0, nb = 0, nt = 0;
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
     bool dummy = false;
-    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, i), p.tokens, i, cap, dummy));
+    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, i), p.tokens, p.units, i, cap, dummy));
     total += T;
     nt += (T > 0);
     before += (i < b) ? T : 0;
@@ -1518,7 +1624,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
     nt += red_nt[w];
   }
   bool dummy = false;
-  const int Tb = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, b), p.tokens, b, cap, dummy));
+  const int Tb = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy));
   if (Tb == 0) return;
   const long long sw = p.seq_cost;
   const long long C = kCostTile * static_cast<long long>(total) + sw * max(nt - 1, 0);
@@ -1530,10 +1636,13 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int quad = threadIdx.x >> 6;
   const int hr = quad / groups;               // head of the round owned by this quad
   const int grp = quad % groups;              // partial group within that head
-  const int d4 = threadIdx.x & 63;            // float4 column: d = 4*d4 .. 4*d4+3
+  const int d4 = threadIdx.x & 63;            // float4 columns d4 + 64 f: d = 4 (d4 + 64 f) .. + 3
+  const bool live_d = d4 < kRowF4;
   for (int r = 0; r < rounds; ++r) {
     const int h = blockIdx.y * hpc + r * hpr + hr;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[kF];
+#pragma unroll
+    for (int f = 0; f < kF; ++f) acc[f] = make_float4(0.f, 0.f, 0.f, 0.f);
     float run_max = -INFINITY, run_sum = 0.f;
     // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
     for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
@@ -1591,53 +1700,76 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
       const float m_new = fmaxf(run_max, pass_max[hr]);
       const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
       const float a_new = expf(pass_max[hr] - m_new);
-      acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
+#pragma unroll
+      for (int f = 0; f < kF; ++f) {
+        acc[f].x *= a_old; acc[f].y *= a_old; acc[f].z *= a_old; acc[f].w *= a_old;
+      }
       run_sum = run_sum * a_old + pass_sum[hr] * a_new;
       run_max = m_new;
       const float* wrow = wts[hr];
-      int k = grp;
-      for (; k + 3 * groups < n; k += 4 * groups) {
-        float4 v[4];
+      if (live_d) {
+        int k = grp;
+        for (; k + 3 * groups < n; k += 4 * groups) {
+          float4 v[4][kF];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          v[u] = reinterpret_cast<const float4*>(
-              p.part_o + (static_cast<size_t>(slots[k + u * groups]) * kH + h) * kD)[d4];
+          for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float w = wrow[k + u * groups] * a_new;
-          acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
-          acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+            for (int f = 0; f < kF; ++f)
+              v[u][f] = reinterpret_cast<const float4*>(
+                  p.part_o + (static_cast<size_t>(slots[k + u * groups]) * kH + h) * kDq)[d4 + 64 * f];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float w = wrow[k + u * groups] * a_new;
+#pragma unroll
+            for (int f = 0; f < kF; ++f) {
+              acc[f].x = fmaf(w, v[u][f].x, acc[f].x); acc[f].y = fmaf(w, v[u][f].y, acc[f].y);
+              acc[f].z = fmaf(w, v[u][f].z, acc[f].z); acc[f].w = fmaf(w, v[u][f].w, acc[f].w);
+            }
+          }
         }
-      }
-      for (; k < n; k += groups) {
-        const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
-        const float w = wrow[k] * a_new;
-        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+        for (; k < n; k += groups) {
+          const float w = wrow[k] * a_new;
+#pragma unroll
+          for (int f = 0; f < kF; ++f) {
+            const float4 v =
+                reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kDq)[d4 + 64 * f];
+            acc[f].x = fmaf(w, v.x, acc[f].x); acc[f].y = fmaf(w, v.y, acc[f].y);
+            acc[f].z = fmaf(w, v.z, acc[f].z); acc[f].w = fmaf(w, v.w, acc[f].w);
+          }
+        }
       }
     }
     if (groups > 1) {
       __syncthreads();
-      if (grp > 0) part_acc[grp - 1][d4] = acc;
+      if (grp > 0)
+#pragma unroll
+        for (int f = 0; f < kF; ++f) part_acc[grp - 1][d4 + 64 * f] = acc[f];
       __syncthreads();
       if (grp != 0) continue;
-      for (int k = 0; k < groups - 1; ++k) {
-        const float4 o = part_acc[k][d4];
-        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
-      }
+      for (int k = 0; k < groups - 1; ++k)
+#pragma unroll
+        for (int f = 0; f < kF; ++f) {
+          const float4 o = part_acc[k][d4 + 64 * f];
+          acc[f].x += o.x; acc[f].y += o.y; acc[f].z += o.z; acc[f].w += o.w;
+        }
     }
     const float inv = 1.f / run_sum;
-    const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
-    if (p.out_f32) {
-      reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
-          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    } else {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
+    if (live_d) {
+#pragma unroll
+      for (int f = 0; f < kF; ++f) {
+        const size_t oi = (static_cast<size_t>(b) * kH + h) * kDq + 4 * (d4 + 64 * f);
+        if (p.out_f32) {
+          reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
+              make_float4(acc[f].x * inv, acc[f].y * inv, acc[f].z * inv, acc[f].w * inv);
+        } else {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(acc[f].x * inv, acc[f].y * inv);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(acc[f].z * inv, acc[f].w * inv);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&lo);
+          pk.y = *reinterpret_cast<uint32_t*>(&hi);
+          reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
+        }
+      }
     }
     if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h] = run_max + logf(run_sum);
   }
@@ -1663,11 +1795,11 @@ static mfa_status cuda_fail_msg(const char* msg) {
 static uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 static uint64_t partial_o_offset() { return kWsHeader; }
-static uint64_t partial_lse_offset(int num_partials) {
-  return align_up(kWsHeader + static_cast<uint64_t>(num_partials) * kH * kD * 4, 256);
+static uint64_t partial_lse_offset(int num_partials, int dq) {
+  return align_up(kWsHeader + static_cast<uint64_t>(num_partials) * kH * dq * 4, 256);
 }
-static uint64_t workspace_bytes_for(int num_partials) {
-  return align_up(partial_lse_offset(num_partials) + static_cast<uint64_t>(num_partials) * kH * 4, 256);
+static uint64_t workspace_bytes_for(int num_partials, int dq) {
+  return align_up(partial_lse_offset(num_partials, dq) + static_cast<uint64_t>(num_partials) * kH * 4, 256);
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1715,9 +1847,21 @@ static long long max_cta_tiles(const std::vector<long long>& Tall, long long G, 
   return most;
 }
 
-// The (sequence, new query token) pairs the kernels treat as sequences: B * T.
+// The attention shape of a problem (kShapeMfa / kShapeGqa / kShapeMla), or -1.
+int problem_shape(const mfa_problem* pr) {
+  if (pr->page_size != kPage) return -1;
+  if (pr->num_q_heads == 64 && pr->head_dim == 256 && pr->num_kv_heads == 1 && !pr->kv_shared) return kShapeMfa;
+  if (pr->num_q_heads == 64 && pr->head_dim == 128 && pr->num_kv_heads == 4 && !pr->kv_shared) return kShapeGqa;
+  if (pr->num_q_heads == 128 && pr->head_dim == 512 && pr->num_kv_heads == 1 && pr->kv_shared) return kShapeMla;
+  return -1;
+}
+static int units_of(const mfa_problem* pr) { return problem_shape(pr) == kShapeMla ? 2 : 1; }
+static int dq_of(const mfa_problem* pr) { return pr->head_dim; }
+static int row_of(const mfa_problem* pr) { return pr->head_dim * pr->num_kv_heads; }
+
+// The units the kernels treat as sequences: (sequence, new query token, 64-head set), B * T * U.
 static long long vbatch(const mfa_problem* pr) {
-  return static_cast<long long>(pr->batch) * pr->tokens_per_seq;
+  return static_cast<long long>(pr->batch) * pr->tokens_per_seq * units_of(pr);
 }
 
 mfa_status check_problem(const mfa_problem* pr) {
@@ -1727,7 +1871,11 @@ mfa_status check_problem(const mfa_problem* pr) {
   if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;
   if (pr->out_dtype != MFA_OUT_BF16 && pr->out_dtype != MFA_OUT_FP32) return MFA_ERR_INVALID_ARG;
   if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
-  if (pr->num_q_heads != kH || pr->head_dim != kD || pr->page_size != kPage) return MFA_ERR_UNSUPPORTED;
+  if (pr->num_kv_heads < 1 || (pr->kv_shared != 0 && pr->kv_shared != 1)) return MFA_ERR_INVALID_ARG;
+  const int shp = problem_shape(pr);
+  if (shp < 0) return MFA_ERR_UNSUPPORTED;
+  // the grouped-head and shared-latent shapes are built for a bf16 cache and one query token
+  if (shp != kShapeMfa && (pr->kv_dtype != MFA_KV_BF16 || pr->tokens_per_seq != 1)) return MFA_ERR_UNSUPPORTED;
   if (static_cast<long long>(pr->max_pages_per_seq) * kPage > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   if (vbatch(pr) * kH > INT_MAX / 2) return MFA_ERR_INVALID_ARG;
   return MFA_OK;
@@ -1738,7 +1886,7 @@ static mfa_status check_plan(const mfa_plan* pl, const mfa_problem* pr) {
   if (pl->batch != pr->batch || pl->kv_dtype != pr->kv_dtype || pl->tokens_per_seq != pr->tokens_per_seq)
     return MFA_ERR_INVALID_ARG;
   if (pl->num_ctas < 1 || pl->num_partials != vbatch(pr) + pl->num_ctas - 1) return MFA_ERR_INVALID_ARG;
-  if (pl->workspace_bytes != workspace_bytes_for(pl->num_partials)) return MFA_ERR_INVALID_ARG;
+  if (pl->workspace_bytes != workspace_bytes_for(pl->num_partials, dq_of(pr))) return MFA_ERR_INVALID_ARG;
   return MFA_OK;
 }
 
@@ -1746,9 +1894,10 @@ static mfa_status encode_maps_uncached(DecodeParams& prm, const mfa_problem* pr,
                                        const void* v) {
   auto enc = encode_fn();
   if (enc == nullptr) return cuda_fail_msg("cuTensorMapEncodeTiled is not available from the driver");
+  const int dq = dq_of(pr), rowlen = row_of(pr);
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(vbatch(pr)) * kH};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(dq), static_cast<cuuint64_t>(vbatch(pr)) * kH};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(dq) * 2};
     cuuint32_t box[2] = {64, 64};
     cuuint32_t es[2] = {1, 1};
     if (enc(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(q), dims, strides, box, es,
@@ -1756,14 +1905,14 @@ static mfa_status encode_maps_uncached(DecodeParams& prm, const mfa_problem* pr,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cuda_fail_msg("cuTensorMapEncodeTiled rejected a tensor map");
   }
-  const void* pools[2] = {k, v};
+  const void* pools[2] = {k, pr->kv_shared ? k : v};   // one latent: the V map reads the K pool
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
   const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
   const cuuint64_t esz = fp8 ? 1 : 2;
   for (int i = 0; i < 2; ++i) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(rowlen), static_cast<cuuint64_t>(kPage),
                           static_cast<cuuint64_t>(pr->num_blocks)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * esz, static_cast<cuuint64_t>(kD) * esz * kPage};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(rowlen) * esz, static_cast<cuuint64_t>(rowlen) * esz * kPage};
     // one 128-byte swizzle row per box row: 64 bf16 or 128 e4m3 codes
     cuuint32_t box[3] = {fp8 ? 128u : 64u, 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
@@ -1786,7 +1935,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
     const void* k;
     const void* v;
     long long rows;
-    int num_blocks, kv_dtype;
+    int num_blocks, kv_dtype, shape;
     CUtensorMap tq, tk, tv;
   };
   constexpr int kEntries = 8;
@@ -1796,7 +1945,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   for (int i = 0; i < used; ++i) {
     const Entry& e = cache[i];
     if (e.q == q && e.k == k && e.v == v && e.rows == rows && e.num_blocks == pr->num_blocks &&
-        e.kv_dtype == pr->kv_dtype) {
+        e.kv_dtype == pr->kv_dtype && e.shape == problem_shape(pr)) {
       prm.tm_q = e.tq;
       prm.tm_k = e.tk;
       prm.tm_v = e.tv;
@@ -1812,6 +1961,7 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   e.rows = rows;
   e.num_blocks = pr->num_blocks;
   e.kv_dtype = pr->kv_dtype;
+  e.shape = problem_shape(pr);
   e.tq = prm.tm_q;
   e.tk = prm.tm_k;
   e.tv = prm.tm_v;
@@ -1820,20 +1970,33 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
   return MFA_OK;
 }
 
+// The decode kernel instance of a problem: bf16 MFA, e4m3 MFA, bf16 GQA, bf16 MLA.
+using DecodeKernelFn = void (*)(DecodeParams);
+static int kernel_index(const mfa_problem* pr) {
+  const int shp = problem_shape(pr);
+  return shp == kShapeMfa ? (pr->kv_dtype == MFA_KV_FP8_E4M3 ? 1 : 0) : (shp == kShapeGqa ? 2 : 3);
+}
+static DecodeKernelFn decode_kernel_of(int idx) {
+  switch (idx) {
+    case 1: return mfa_decode_kernel<true, kShapeMfa>;
+    case 2: return mfa_decode_kernel<false, kShapeGqa>;
+    case 3: return mfa_decode_kernel<false, kShapeMla>;
+    default: return mfa_decode_kernel<false, kShapeMfa>;
+  }
+}
+
 // cudaFuncSetAttribute for a kernel's dynamic shared memory, once per device and kernel.
-static mfa_status ensure_smem_attribute(bool fp8) {
+static mfa_status ensure_smem_attribute(int idx) {
   constexpr int kMaxDevices = 64;
-  static std::atomic<bool> done[2][kMaxDevices];
+  static std::atomic<bool> done[4][kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   const bool cacheable = dev >= 0 && dev < kMaxDevices;
-  if (cacheable && done[fp8][dev].load(std::memory_order_acquire)) return MFA_OK;
-  auto kernel = fp8 ? mfa_decode_kernel<true> : mfa_decode_kernel<false>;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           fp8 ? smem_bytes<true>() : smem_bytes<false>());
+  if (cacheable && done[idx][dev].load(std::memory_order_acquire)) return MFA_OK;
+  e = cudaFuncSetAttribute(decode_kernel_of(idx), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
-  if (cacheable) done[fp8][dev].store(true, std::memory_order_release);
+  if (cacheable) done[idx][dev].store(true, std::memory_order_release);
   return MFA_OK;
 }
 
@@ -1843,13 +2006,14 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   CombineParams cp;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   cp.part_o = reinterpret_cast<const float*>(ws + partial_o_offset());
-  cp.part_lse = reinterpret_cast<const float*>(ws + partial_lse_offset(pl->num_partials));
+  cp.part_lse = reinterpret_cast<const float*>(ws + partial_lse_offset(pl->num_partials, dq_of(pr)));
   cp.seq_lens = seq_lens;
   cp.out = out;
   cp.out_f32 = pr->out_dtype == MFA_OUT_FP32 ? 1 : 0;
   cp.lse = lse;
   cp.batch = static_cast<int>(vbatch(pr));
   cp.tokens = pr->tokens_per_seq;
+  cp.units = units_of(pr);
   cp.seq_cost = cost_seq(pr->kv_dtype == MFA_KV_FP8_E4M3);
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
@@ -1866,7 +2030,10 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, mfa_combine_kernel, cp);
+  const int dq = dq_of(pr);
+  const cudaError_t e = dq == 128   ? cudaLaunchKernelEx(&cfg, mfa_combine_kernel<128>, cp)
+                        : dq == 512 ? cudaLaunchKernelEx(&cfg, mfa_combine_kernel<512>, cp)
+                                    : cudaLaunchKernelEx(&cfg, mfa_combine_kernel<256>, cp);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return MFA_OK;
 }
@@ -1899,10 +2066,10 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   if (st != MFA_OK) return st;
   if (plan == nullptr || force_ctas < 0) return MFA_ERR_INVALID_ARG;
   const long long cap = static_cast<long long>(pr->max_pages_per_seq) * kPage;
-  const int nt = pr->tokens_per_seq;
+  const int nt = pr->tokens_per_seq, nu = units_of(pr);
   const long long Bv = vbatch(pr);
-  // tiles of each (sequence, new token) pair: query token i of a sequence of L tokens attends
-  // to its first L - T + 1 + i
+  // tiles of each unit (sequence, new token, head set): query token i of a sequence of L
+  // tokens attends to its first L - T + 1 + i
   std::vector<long long> T(static_cast<size_t>(Bv));
   long long W = 0;
   if (host_seq_lens != nullptr) {
@@ -1910,8 +2077,11 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
       if (host_seq_lens[b] < 0 || host_seq_lens[b] > cap) return MFA_ERR_INVALID_ARG;
       for (int i = 0; i < nt; ++i) {
         const long long L = std::max(0ll, static_cast<long long>(host_seq_lens[b]) - (nt - 1 - i));
-        T[static_cast<size_t>(b) * nt + i] = (L + kTile - 1) / kTile;
-        W += T[static_cast<size_t>(b) * nt + i];
+        for (int u = 0; u < nu; ++u) {
+          const size_t x = (static_cast<size_t>(b) * nt + i) * nu + u;
+          T[x] = (L + kTile - 1) / kTile;
+          W += T[x];
+        }
       }
     }
   } else {
@@ -1961,7 +2131,7 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   plan->flags = flags;
   plan->num_sms = num_sms;
   plan->total_tiles = static_cast<uint64_t>(W);
-  plan->workspace_bytes = workspace_bytes_for(plan->num_partials);
+  plan->workspace_bytes = workspace_bytes_for(plan->num_partials, dq_of(pr));
   return MFA_OK;
 }
 
@@ -1975,6 +2145,8 @@ static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const v
   st = check_plan(plan, pr);
   if (st != MFA_OK) return st;
   if (pr->batch == 0) return MFA_OK;
+  // a shared latent has no V pool: v_cache is ignored (NULL or the K pool)
+  if (pr->kv_shared) v_cache = k_cache;
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       seq_lens == nullptr || out == nullptr || workspace == nullptr)
     return MFA_ERR_INVALID_ARG;
@@ -2011,10 +2183,11 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.out_f32 = pr->out_dtype == MFA_OUT_FP32 ? 1 : 0;
   prm.lse = lse;
   prm.part_o = reinterpret_cast<float*>(ws + partial_o_offset());
-  prm.part_lse = reinterpret_cast<float*>(ws + partial_lse_offset(plan->num_partials));
+  prm.part_lse = reinterpret_cast<float*>(ws + partial_lse_offset(plan->num_partials, dq_of(pr)));
   prm.status = reinterpret_cast<unsigned int*>(ws);
   prm.batch = static_cast<int>(vbatch(pr));
   prm.tokens = pr->tokens_per_seq;
+  prm.units = units_of(pr);
   prm.max_pages = pr->max_pages_per_seq;
   prm.num_blocks = pr->num_blocks;
   prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
@@ -2023,22 +2196,20 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
   cudaError_t e = cudaSuccess;
   if (check && (e = cudaMemsetAsync(ws, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
-  const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
-  auto kernel = fp8 ? mfa_decode_kernel<true> : mfa_decode_kernel<false>;
-  const int smem = fp8 ? smem_bytes<true>() : smem_bytes<false>();
-  st = ensure_smem_attribute(fp8);
+  const int kidx = kernel_index(pr);
+  st = ensure_smem_attribute(kidx);
   if (st != MFA_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
-  cfg.blockDim = dim3(fp8 ? threads_of<true>() : threads_of<false>(), 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.blockDim = dim3(threads_of<false>(), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  e = cudaLaunchKernelEx(&cfg, decode_kernel_of(kidx), prm);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (plan->num_ctas > 1 && (plan->flags & MFA_PLAN_NO_COMBINE) == 0) {
     st = launch_combine(plan, pr, workspace, seq_lens, out, lse, stream, true);
@@ -2066,8 +2237,9 @@ mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* pr, cons
   if (!q_host || !block_table_host || !seq_lens_host || !out_host) return MFA_ERR_INVALID_ARG;
   if ((lse_host == nullptr) != (lse_dev == nullptr)) return MFA_ERR_INVALID_ARG;
   const size_t B = static_cast<size_t>(pr->batch), Bv = static_cast<size_t>(vbatch(pr));
-  const size_t q_bytes = Bv * kH * kD * 2, table_bytes = B * pr->max_pages_per_seq * 4, lens_bytes = B * 4;
-  const size_t out_bytes = Bv * kH * kD * (pr->out_dtype == MFA_OUT_FP32 ? 4 : 2), lse_bytes = Bv * kH * 4;
+  const size_t dq = static_cast<size_t>(dq_of(pr));
+  const size_t q_bytes = Bv * kH * dq * 2, table_bytes = B * pr->max_pages_per_seq * 4, lens_bytes = B * 4;
+  const size_t out_bytes = Bv * kH * dq * (pr->out_dtype == MFA_OUT_FP32 ? 4 : 2), lse_bytes = Bv * kH * 4;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e;
   if ((e = cudaMemcpyAsync(q_dev, q_host, q_bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||

@@ -112,6 +112,7 @@ extern "C" mfa_status mfa_kv_append(const mfa_problem* pr, const void* k_new, co
                                     void* stream_ptr) {
   const mfa_status st = check_problem(pr);
   if (st != MFA_OK) return st;
+  if (problem_shape(pr) != 0) return MFA_ERR_UNSUPPORTED;   // rows of the MFA cache (256 wide)
   if (pr->batch == 0) return MFA_OK;
   const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
   if (!k_new || !v_new || !positions || !block_table || !k_cache || !v_cache) return MFA_ERR_INVALID_ARG;

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MFA_ABI_VERSION 2
+#define MFA_ABI_VERSION 3
 
 typedef enum mfa_status {
     MFA_OK = 0,
@@ -101,6 +101,8 @@ typedef struct mfa_problem {
     float softmax_scale;       /* finite, > 0; 1/sqrt(256) = 0.0625 for MFA */
     int32_t out_dtype;         /* mfa_out_dtype */
     int32_t tokens_per_seq;    /* T new query tokens per sequence, 1..4 (see below) */
+    int32_t num_kv_heads;      /* G key/value heads per cache row: 1 (MFA, shared latent) or 4 */
+    int32_t kv_shared;         /* 1: one latent serves as keys and values (no V pool), else 0 */
 } mfa_problem;
 
 /*

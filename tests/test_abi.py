@@ -28,7 +28,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(mfa.EXPORTED_SYMBOLS)
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
-    assert lib.mfa_abi_version() == 2
+    assert lib.mfa_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -137,10 +137,36 @@ def test_plan_rejects_bad_input(lib):
                       (dict(kv_dtype=7), mfa.MFA_ERR_INVALID_ARG),
                       (dict(out_dtype=2), mfa.MFA_ERR_INVALID_ARG),
                       (dict(batch=-1), mfa.MFA_ERR_INVALID_ARG),
-                      (dict(num_blocks=0), mfa.MFA_ERR_INVALID_ARG)]:
+                      (dict(num_blocks=0), mfa.MFA_ERR_INVALID_ARG),
+                      # shapes: only MFA, the grouped-head shape and the shared latent are built,
+                      # the last two for a bf16 cache and one query token
+                      (dict(num_kv_heads=2), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(num_kv_heads=0), mfa.MFA_ERR_INVALID_ARG),
+                      (dict(kv_shared=True), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(head_dim=128, num_kv_heads=4, kv_dtype=mfa.MFA_KV_FP8_E4M3), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(head_dim=128, num_kv_heads=4, tokens_per_seq=2), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(num_q_heads=128, head_dim=512), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(num_q_heads=128, head_dim=512, kv_shared=True, kv_dtype=mfa.MFA_KV_FP8_E4M3),
+                       mfa.MFA_ERR_UNSUPPORTED)]:
         with pytest.raises(mfa.MfaError) as e:
             mfa.mfa_decode_plan(problem(**bad), None, max_seq_len=64, num_sms=8)
         assert e.value.status == code, bad
+
+
+def test_plan_for_the_comparison_shapes(lib):
+    """Grouped heads: one 64-head unit per sequence, 128-wide partials; shared latent: two
+    64-head units per sequence (128 query heads), 512-wide partials."""
+    lens = [4096, 100, 0]
+    g = mfa.mfa_decode_plan(problem(batch=3, head_dim=128, num_kv_heads=4, max_pages_per_seq=64), lens, num_sms=8)
+    assert g.total_tiles == 32 + 1 and g.num_partials == 3 + g.num_ctas - 1
+    o, l = mfa.workspace_layout(g, head_dim=128)
+    assert l == (256 + g.num_partials * 64 * 128 * 4 + 255) // 256 * 256
+    assert g.workspace_bytes == (l + g.num_partials * 64 * 4 + 255) // 256 * 256
+    m = mfa.mfa_decode_plan(problem(batch=3, num_q_heads=128, head_dim=512, kv_shared=True, max_pages_per_seq=64),
+                            lens, num_sms=8)
+    assert m.total_tiles == 2 * (32 + 1) and m.num_partials == 6 + m.num_ctas - 1
+    o, l = mfa.workspace_layout(m, head_dim=512)
+    assert m.workspace_bytes == (l + m.num_partials * 64 * 4 + 255) // 256 * 256
 
 
 def _run_raw(lib, plan, prob, ptrs, ws_bytes):
@@ -185,6 +211,8 @@ def test_kv_append_validates_before_touching_the_device(lib):
     odd_status = list(good); odd_status[8] = 0x9002
     assert _append_raw(lib, f8, odd_status) == mfa.MFA_ERR_INVALID_ARG
     assert _append_raw(lib, problem(head_dim=128), good) == mfa.MFA_ERR_UNSUPPORTED
+    assert _append_raw(lib, problem(head_dim=128, num_kv_heads=4), good) == mfa.MFA_ERR_UNSUPPORTED
+    assert _append_raw(lib, problem(num_q_heads=128, head_dim=512, kv_shared=True), good) == mfa.MFA_ERR_UNSUPPORTED
     assert _append_raw(lib, problem(batch=-1), good) == mfa.MFA_ERR_INVALID_ARG
 
 

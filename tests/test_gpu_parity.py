@@ -29,12 +29,20 @@ def to_dev(case, dev="cuda"):
                 v_scale=None if case.v_scale is None else case.v_scale.to(dev))
 
 
+def shape_of(w):
+    """The library shape tuple of a workload (query heads, head width, key/value heads, shared)."""
+    return (w.num_q_heads, w.head_dim, w.num_kv_heads, w.kv_shared)
+
+
 def gpu_decode(case, force_ctas=0, flags=mfa.MFA_PLAN_CHECK, stream=None, out_dtype=mfa.MFA_OUT_FP32):
     t = to_dev(case)
-    kv = mfa.MFA_KV_FP8_E4M3 if case.workload.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
-    dec = mfa.Decoder(case.q.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv,
-                      softmax_scale=case.workload.scale(), host_seq_lens=case.seq_lens.tolist(),
-                      force_ctas=force_ctas, flags=flags, out_dtype=out_dtype)
+    w = case.workload
+    kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    dec = mfa.Decoder(case.seq_lens.shape[0],
+                      case.max_pages, case.num_blocks, kv_dtype=kv,
+                      softmax_scale=w.scale(), host_seq_lens=case.seq_lens.tolist(),
+                      force_ctas=force_ctas, flags=flags, out_dtype=out_dtype, tokens_per_seq=w.tokens_per_seq,
+                      shape=shape_of(w))
     out, lse = dec(t["q"], t["k_cache"], t["v_cache"], t["block_table"], t["seq_lens"],
                    k_scale=t["k_scale"], v_scale=t["v_scale"], stream=stream)
     torch.cuda.synchronize()
@@ -435,3 +443,17 @@ def test_multi_token_decode_beyond_one_thread_per_pair(kv_dtype):
         check_parity(case, out, lse)
     else:
         check_parity(case, out, lse, max_abs=3e-2, rel_l2=1.5e-2)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+def test_ctas_without_tiles_leave_the_partials_alone(kv):
+    """With 16 CTAs over these lengths, CTA 11's cost range holds no tile while sequence 0 is
+    split over CTAs 0..3 (its partial from CTA 0 sits in slot 0).  A CTA without a segment
+    writes nothing; repeated steps stay exact against the oracle and set no status bit."""
+    lens = [700, 1, 1, 1, 1, 1, 1, 1, 1, 1, 300]
+    case = inputs.small("empty_cta", len(lens), lens, kv_dtype=kv, seed=70)
+    ref = oracle.decode(case)
+    lim = (3e-2, 1.5e-2) if kv == "fp8_e4m3" else (BF16_MAX_ABS, BF16_REL_L2)
+    for _ in range(5):
+        out, lse, _ = gpu_decode(case, force_ctas=16)
+        check_parity(case, out, lse, *lim, ref=ref)
