@@ -1567,6 +1567,186 @@ __device__ __forceinline__ int cta_of_cost(long long c, long long C, long long G
 constexpr int kCombineThreads = 256;
 constexpr int kCombineMaxParts = 256;        // partials staged per pass
 
+// One CTA per (sequence, group of `heads_per_cta` heads), for MFA's 256-wide rows.  The 256
+// threads form four quads of 64 (each thread owns 4 consecutive d, a float4).  With one head
+// per CTA the quads split the partials four ways; with four or more heads each
+// quad owns a head and the CTA walks its heads in rounds of four.  Partial lse
+// values are staged in shared memory; partial O rows stream in with batched
+// independent float4 loads.
+__global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
+  grid_dep_wait();
+  grid_dep_launch();   // the next kernel may start its own set-up
+  __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
+  __shared__ int red_nb[kCombineThreads / 32], red_nt[kCombineThreads / 32];
+  __shared__ int slots[kCombineMaxParts];
+  __shared__ float wts[4][kCombineMaxParts];
+  __shared__ float4 part_acc[3][64];
+  __shared__ float pass_max[4], pass_sum[4];
+  __shared__ int nparts_s;
+  const int b = blockIdx.x;
+  const int hpc = p.heads_per_cta;
+  const int hpr = hpc < 4 ? hpc : 4;          // heads per round
+  const int groups = 4 / hpr;                 // quads sharing one head
+  const int rounds = hpc / hpr;
+  const int cap = p.max_pages * kPage;
+  // tiles (and non-empty sequences) before b and in all: the decode kernel's cost positions
+  int before = 0, total = 0, nb = 0, nt = 0;
+  for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
+    bool dummy = false;
+    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, i), p.tokens, p.units, i, cap, dummy));
+    total += T;
+    nt += (T > 0);
+    before += (i < b) ? T : 0;
+    nb += (i < b && T > 0);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    nb += __shfl_xor_sync(0xffffffffu, nb, o);
+    nt += __shfl_xor_sync(0xffffffffu, nt, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red_b[threadIdx.x >> 5] = before;
+    red_t[threadIdx.x >> 5] = total;
+    red_nb[threadIdx.x >> 5] = nb;
+    red_nt[threadIdx.x >> 5] = nt;
+  }
+  __syncthreads();
+  before = total = nb = nt = 0;
+  for (int w = 0; w < kCombineThreads / 32; ++w) {
+    before += red_b[w];
+    total += red_t[w];
+    nb += red_nb[w];
+    nt += red_nt[w];
+  }
+  bool dummy = false;
+  const int Tb = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy));
+  if (Tb == 0) return;
+  const long long sw = p.seq_cost;
+  const long long C = kCostTile * static_cast<long long>(total) + sw * max(nt - 1, 0);
+  const long long base = kCostTile * static_cast<long long>(before) + sw * nb;   // cost of sequence b's first tile
+  const int g0 = cta_of_cost(base, C, p.num_ctas);
+  const int g1 = cta_of_cost(base + kCostTile * static_cast<long long>(Tb - 1), C, p.num_ctas);
+  if (g0 == g1) return;  // written whole by the decode kernel
+
+  const int quad = threadIdx.x >> 6;
+  const int hr = quad / groups;               // head of the round owned by this quad
+  const int grp = quad % groups;              // partial group within that head
+  const int d4 = threadIdx.x & 63;            // float4 column: d = 4*d4 .. 4*d4+3
+  for (int r = 0; r < rounds; ++r) {
+    const int h = blockIdx.y * hpc + r * hpr + hr;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float run_max = -INFINITY, run_sum = 0.f;
+    // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
+    for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
+      const int ge = min(g1 + 1, gs + kCombineMaxParts);
+      __syncthreads();
+      if (threadIdx.x < 32) {
+        int n = 0;
+        for (int g = gs + threadIdx.x; g - static_cast<int>(threadIdx.x) < ge; g += 32) {
+          // CTA g holds a tile of b if a tile cost of b lies in its cost range
+          bool live = false;
+          if (g < ge) {
+            const long long x0 = (static_cast<long long>(g) * C) / p.num_ctas;
+            const long long x1 = (static_cast<long long>(g + 1) * C) / p.num_ctas;
+            const long long k_lo = x0 <= base ? 0 : (x0 - base + kCostTile - 1) / kCostTile;
+            const long long k_hi = x1 <= base ? 0 : (x1 - base + kCostTile - 1) / kCostTile;
+            live = k_lo < min(k_hi, static_cast<long long>(Tb));
+          }
+          const unsigned m = __ballot_sync(0xffffffffu, live);
+          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
+          n += __popc(m);
+        }
+        if (threadIdx.x == 0) nparts_s = n;
+      }
+      __syncthreads();
+      const int n = nparts_s;
+      for (int k = threadIdx.x; k < n * hpr; k += kCombineThreads) {
+        const int kk = k / hpr, hh = k % hpr;
+        wts[hh][kk] = p.part_lse[static_cast<size_t>(slots[kk]) * kH + blockIdx.y * hpc + r * hpr + hh];
+      }
+      __syncthreads();
+      {
+        // warp w < hpr turns head w's lse values into weights relative to their max
+        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+        if (w < hpr) {
+          float m = -INFINITY;
+          for (int k = l; k < n; k += 32) m = fmaxf(m, wts[w][k]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          float sum = 0.f;
+          for (int k = l; k < n; k += 32) {
+            const float e = expf(wts[w][k] - m);
+            wts[w][k] = e;
+            sum += e;
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          if (l == 0) {
+            pass_max[w] = m;
+            pass_sum[w] = sum;
+          }
+        }
+      }
+      __syncthreads();
+      // rescale what earlier passes accumulated to this pass's reference
+      const float m_new = fmaxf(run_max, pass_max[hr]);
+      const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
+      const float a_new = expf(pass_max[hr] - m_new);
+      acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
+      run_sum = run_sum * a_old + pass_sum[hr] * a_new;
+      run_max = m_new;
+      const float* wrow = wts[hr];
+      int k = grp;
+      for (; k + 3 * groups < n; k += 4 * groups) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          v[u] = reinterpret_cast<const float4*>(
+              p.part_o + (static_cast<size_t>(slots[k + u * groups]) * kH + h) * kD)[d4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = wrow[k + u * groups] * a_new;
+          acc.x = fmaf(w, v[u].x, acc.x); acc.y = fmaf(w, v[u].y, acc.y);
+          acc.z = fmaf(w, v[u].z, acc.z); acc.w = fmaf(w, v[u].w, acc.w);
+        }
+      }
+      for (; k < n; k += groups) {
+        const float4 v = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slots[k]) * kH + h) * kD)[d4];
+        const float w = wrow[k] * a_new;
+        acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+      }
+    }
+    if (groups > 1) {
+      __syncthreads();
+      if (grp > 0) part_acc[grp - 1][d4] = acc;
+      __syncthreads();
+      if (grp != 0) continue;
+      for (int k = 0; k < groups - 1; ++k) {
+        const float4 o = part_acc[k][d4];
+        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+      }
+    }
+    const float inv = 1.f / run_sum;
+    const size_t oi = (static_cast<size_t>(b) * kH + h) * kD + 4 * d4;
+    if (p.out_f32) {
+      reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
+    }
+    if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h] = run_max + logf(run_sum);
+  }
+}
+
+// The same merge for the comparison shapes' rows (kDq = 128 or 512).
 // One CTA per (unit, group of `heads_per_cta` heads).  The 256 threads form four quads of
 // 64; a thread owns 4 consecutive d (a float4) of each 256-d span of the kDq-wide row (for
 // kDq = 128 the quad's upper 32 threads hold nothing).  With one head per CTA the quads split
@@ -1574,7 +1754,7 @@ constexpr int kCombineMaxParts = 256;        // partials staged per pass
 // heads in rounds of four.  Partial lse values are staged in shared memory; partial O rows
 // stream in with batched independent float4 loads.
 template <int kDq>
-__global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __grid_constant__ CombineParams p) {
+__global__ void __launch_bounds__(kCombineThreads) mfa_combine_wide_kernel(const __grid_constant__ CombineParams p) {
   constexpr int kF = (kDq + 255) / 256;          // float4s per thread and row
   constexpr int kRowF4 = kDq / 4;
   grid_dep_wait();
@@ -2031,9 +2211,9 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
   const int dq = dq_of(pr);
-  const cudaError_t e = dq == 128   ? cudaLaunchKernelEx(&cfg, mfa_combine_kernel<128>, cp)
-                        : dq == 512 ? cudaLaunchKernelEx(&cfg, mfa_combine_kernel<512>, cp)
-                                    : cudaLaunchKernelEx(&cfg, mfa_combine_kernel<256>, cp);
+  const cudaError_t e = dq == 128   ? cudaLaunchKernelEx(&cfg, mfa_combine_wide_kernel<128>, cp)
+                        : dq == 512 ? cudaLaunchKernelEx(&cfg, mfa_combine_wide_kernel<512>, cp)
+                                    : cudaLaunchKernelEx(&cfg, mfa_combine_kernel, cp);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return MFA_OK;
 }
