@@ -52,7 +52,7 @@ class Workload:
     batch: int
     lens: Optional[Sequence[int]] = None        # explicit lengths, or None to draw
     len_range: Optional[tuple] = None           # (lo, hi) inclusive when drawn
-    kv_dtype: str = "bf16"                      # "bf16" | "fp8_e4m3"
+    kv_dtype: str = "bf16"                      # "bf16" | "fp8_e4m3" | "mxfp4"
     layout: str = "shuffled"                    # "shuffled" | "contiguous"
     seed: int = 0
     k_spike_frac: float = 0.0
@@ -100,6 +100,11 @@ WORKLOADS = {
     # section 7, attention ablation), at the 4K shape: grouped-query attention with 64 query
     # heads over 4 key/value heads of width 128 (effective rank 8,192), and a 512-wide latent
     # shared by keys and values under 128 query heads (intensity 512 with 8-bit KV)
+    # 4-bit KV (MXFP4: E2M1 codes, one E8M0 scale per 32 elements of a row), the 4K shapes
+    "b128_l4096_mxfp4": Workload(
+        "b128_l4096_mxfp4", batch=128, lens=(4096,) * 128, kv_dtype="mxfp4", seed=11),
+    "b32_l4096_mxfp4": Workload(
+        "b32_l4096_mxfp4", batch=32, lens=(4096,) * 32, kv_dtype="mxfp4", seed=12),
     "gqa_b32_l4096_bf16": Workload(
         "gqa_b32_l4096_bf16", batch=32, lens=(4096,) * 32, seed=9, head_dim=128, num_kv_heads=4),
     "mla_b32_l4096_bf16": Workload(
@@ -147,6 +152,32 @@ def _draw_pool(rng, nb, page, d, spike_frac, spike_mult):
 
 def _to_bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(x).to(torch.bfloat16)
+
+
+# E2M1 magnitudes by code (OCP Microscaling FP4) and the midpoints between neighbours.
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+_E2M1_MID = (_E2M1[1:] + _E2M1[:-1]) / 2
+
+
+def _to_mxfp4(x: np.ndarray):
+    """MXFP4 storage of rows of fp32 x [..., d]: codes uint8 [..., d/2] (element 2i in the low
+    nibble of byte i) and E8M0 scales uint8 [..., d/32].  Per block of 32 elements the scale
+    is 2^e, e = floor(log2(amax)) - 2 clamped to [-127, 127] (-127 for an all-zero block), and
+    each element is rounded to the nearest E2M1 value of x / 2^e, ties to the even code,
+    saturating at 6, sign kept."""
+    *lead, d = x.shape
+    blocks = x.reshape(*lead, d // 32, 32).astype(np.float32)
+    amax = np.abs(blocks).max(axis=-1)
+    _, E = np.frexp(amax)
+    e = np.where(amax > 0, E - 3, -127).clip(-127, 127)
+    y = np.ldexp(blocks.astype(np.float64), -e[..., None])
+    a = np.abs(y)
+    lo = np.searchsorted(_E2M1_MID, a, side="left")
+    hi = np.searchsorted(_E2M1_MID, a, side="right")
+    idx = np.minimum(np.where(lo != hi, lo + (lo % 2), lo), 7)
+    code = (idx | np.where(np.signbit(y), 8, 0)).reshape(*lead, d).astype(np.uint8)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    return torch.from_numpy(np.ascontiguousarray(packed)), torch.from_numpy((e + 127).astype(np.uint8))
 
 
 def _to_e4m3(x: np.ndarray):
@@ -233,6 +264,22 @@ def generate(w: Workload, lens_override: Optional[Sequence[int]] = None) -> Case
                 v_cache[unused] = E4M3_NAN_CODE
                 k_scale[unused] = float("nan")
                 v_scale[unused] = float("nan")
+    elif w.kv_dtype == "mxfp4":
+        k_cache, k_scale = _to_mxfp4(kf)
+        if w.kv_shared:
+            v_cache, v_scale = k_cache, k_scale
+        else:
+            v_cache, v_scale = _to_mxfp4(vf)
+        if w.poison:
+            # unused slots: code 6.0 everywhere and NaN scales (E8M0 255)
+            for cache, sc in ((k_cache, k_scale), (v_cache, v_scale)):
+                for blk, rem in tails:
+                    cache[blk, rem:] = 0x77
+                    sc[blk, rem:] = 255
+                unused = torch.from_numpy(np.nonzero(~used)[0])
+                if unused.numel():
+                    cache[unused] = 0x77
+                    sc[unused] = 255
     else:
         raise ValueError(f"unknown kv_dtype {w.kv_dtype!r}")
 

@@ -65,7 +65,37 @@ def load_library(path: str):
     lib.mfa_oracle_e4m3_from_float_array.restype = None
     lib.mfa_oracle_kv_append.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
     lib.mfa_oracle_kv_append.restype = I
+    lib.mfa_oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+    lib.mfa_oracle_e2m1_to_double.restype = ctypes.c_double
+    lib.mfa_oracle_e8m0_to_double.argtypes = [ctypes.c_uint8]
+    lib.mfa_oracle_e8m0_to_double.restype = ctypes.c_double
+    lib.mfa_oracle_e2m1_from_double.argtypes = [ctypes.c_double]
+    lib.mfa_oracle_e2m1_from_double.restype = ctypes.c_uint8
+    lib.mfa_oracle_mx_block_exponent.argtypes = [P, I]
+    lib.mfa_oracle_mx_block_exponent.restype = I
     return lib
+
+
+KV_FORMATS = {"bf16": 0, "fp8_e4m3": 1, "mxfp4": 2}
+
+
+def e2m1_to_double(code: int, lib=None) -> float:
+    return float((lib or _load()).mfa_oracle_e2m1_to_double(int(code) & 0xF))
+
+
+def e8m0_to_double(code: int, lib=None) -> float:
+    return float((lib or _load()).mfa_oracle_e8m0_to_double(int(code) & 0xFF))
+
+
+def e2m1_from_double(y: float, lib=None) -> int:
+    """Nearest E2M1 code to y (ties to the even code, |y| >= 6 -> 6, sign kept)."""
+    return int((lib or _load()).mfa_oracle_e2m1_from_double(float(y)))
+
+
+def mx_block_exponent(x, lib=None) -> int:
+    """OCP MX shared exponent of a block of fp32 values (floor(log2 amax) - 2, in [-127, 127])."""
+    a = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    return int((lib or _load()).mfa_oracle_mx_block_exponent(_ptr(a), a.size))
 
 
 def _load():
@@ -119,13 +149,17 @@ def kv_append(k_new, v_new, positions, block_table, k_cache, v_cache, k_scale=No
     table = np.ascontiguousarray(_np(block_table).astype(np.int32))
     kc = np.array(_np(k_cache), copy=True)
     vc = np.array(_np(v_cache), copy=True)
-    fp8 = kc.dtype == np.uint8
+    # the cache format from its layout: bf16 rows, e4m3 rows of d codes, or MXFP4 rows of d/2 bytes
+    fmt = 0 if kc.dtype != np.uint8 else (2 if kc.shape[-1] * 2 == d else 1)
     ks = vs = None
-    if fp8:
+    if fmt == 1:
         ks = np.array(_np(k_scale), dtype=np.float32, copy=True)
         vs = np.array(_np(v_scale), dtype=np.float32, copy=True)
+    elif fmt == 2:
+        ks = np.array(_np(k_scale), dtype=np.uint8, copy=True)
+        vs = np.array(_np(v_scale), dtype=np.uint8, copy=True)
     mask = (lib or _load()).mfa_oracle_kv_append(
-        B, T, d, page_size, table.shape[1], kc.shape[0], 1 if fp8 else 0, _ptr(kn), _ptr(vn), _ptr(pos),
+        B, T, d, page_size, table.shape[1], kc.shape[0], fmt, _ptr(kn), _ptr(vn), _ptr(pos),
         _ptr(table), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs))
     if mask < 0:
         raise ValueError("mfa_oracle_kv_append: bad argument")
@@ -187,17 +221,19 @@ def decode(case, t_begin=None, t_end=None, nthreads: int = 0,
     vc = None if shared else _np(case.v_cache)
     ks = _np(case.k_scale)
     vs = None if shared else _np(case.v_scale)
+    fmt = KV_FORMATS[w.kv_dtype]
+    sdt = np.uint8 if fmt == 2 else np.float32
     if ks is not None:
-        ks = ks.astype(np.float32)
+        ks = np.ascontiguousarray(ks.astype(sdt))
     if vs is not None:
-        vs = vs.astype(np.float32)
+        vs = np.ascontiguousarray(vs.astype(sdt))
     tb = None if t_begin is None else np.ascontiguousarray(np.asarray(t_begin, dtype=np.int32))
     te = None if t_end is None else np.ascontiguousarray(np.asarray(t_end, dtype=np.int32))
     out = np.zeros((B, H, d), dtype=np.float64)
     lse = np.zeros((B, H), dtype=np.float64)
     scale = w.scale() if softmax_scale is None else float(softmax_scale)
     rc = (lib or _load()).mfa_oracle_decode(
-        B, H, G, d, w.page_size, table.shape[1], 1 if w.kv_dtype == "fp8_e4m3" else 0,
+        B, H, G, d, w.page_size, table.shape[1], fmt,
         _ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(table), _ptr(lens),
         _ptr(tb), _ptr(te), scale, _ptr(out), _ptr(lse), int(nthreads))
     if rc != 0:

@@ -45,8 +45,12 @@
  *     is the key row itself.
  * MFA is G = 1 with separate pools.
  *
+ * 4-bit caches (MXFP4, the OCP Microscaling format): two E2M1 codes a byte and one E8M0
+ * power-of-two scale per 32 consecutive elements of a row; decoded exactly, code value times
+ * scale.
+ *
  * mfa_oracle_kv_append() (end of file) writes a decode step's new key and value rows into
- * the paged cache, quantising them to e4m3 with per-row scales for an FP8 cache.
+ * the paged cache, quantising them to e4m3 with per-row scales for an FP8 cache, or to MXFP4.
  */
 #include <math.h>
 #include <pthread.h>
@@ -64,6 +68,23 @@ static double bf16_to_double(uint16_t bits) {
 
 /* OCP FP8 E4M3 ("fn" variant): value = (-1)^s * 2^(e-7) * (1 + m/8) for e > 0,
  * (-1)^s * 2^(-6) * (m/8) for e == 0; e == 15 && m == 7 is NaN. */
+/* OCP MX FP4 E2M1 (low nibble of code): value = (-1)^s * 2^(e-1) * (1 + m/2) for e > 0,
+ * (-1)^s * m/2 for e == 0 (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; no
+ * infinities or NaN): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double mfa_oracle_e2m1_to_double(uint8_t code) {
+    int s = (code >> 3) & 1;
+    int e = (code >> 1) & 3;
+    int m = code & 1;
+    double v = (e == 0) ? (double)m / 2.0 : ldexp(1.0 + (double)m / 2.0, e - 1);
+    return s ? -v : v;
+}
+
+/* OCP MX E8M0 scale: 2^(e - 127), e = 255 is NaN. */
+double mfa_oracle_e8m0_to_double(uint8_t e) {
+    if (e == 255) return NAN;
+    return ldexp(1.0, (int)e - 127);
+}
+
 double mfa_oracle_e4m3_to_double(uint8_t code) {
     int s = (code >> 7) & 1;
     int e = (code >> 3) & 15;
@@ -78,10 +99,10 @@ double mfa_oracle_e4m3_to_double(uint8_t code) {
 }
 
 typedef struct {
-    int B, H, G, d, page, max_pages, kv_fp8;
+    int B, H, G, d, page, max_pages, kv_fmt;   /* kv_fmt: 0 bf16, 1 e4m3, 2 MXFP4 */
     const uint16_t *q;
     const void *k_cache, *v_cache;
-    const float *k_scale, *v_scale;
+    const void *k_scale, *v_scale;
     const int32_t *block_table, *seq_lens, *t_begin, *t_end;
     double scale;
     double *out, *lse;
@@ -105,11 +126,23 @@ static void kv_row(const job_t *J, int which_v, int b, int t, int g, double *dst
     size_t row = (size_t)blk * J->page + (size_t)(t % J->page);
     size_t base = row * (size_t)J->G * (size_t)J->d + (size_t)g * (size_t)J->d;
     const void *vpool = J->v_cache ? J->v_cache : J->k_cache;
-    if (J->kv_fp8) {
+    if (J->kv_fmt == 1) {
         const uint8_t *pool = (const uint8_t *)(which_v ? vpool : J->k_cache);
-        const float *sc = which_v && J->v_cache ? J->v_scale : J->k_scale;
+        const float *sc = (const float *)(which_v && J->v_cache ? J->v_scale : J->k_scale);
         for (int i = 0; i < J->d; ++i)
             dst[i] = mfa_oracle_e4m3_to_double(pool[base + i]) * (double)sc[row];
+    } else if (J->kv_fmt == 2) {
+        /* MXFP4: element e of the row is E2M1 code (byte e / 2, low nibble for even e) times
+         * the E8M0 scale of its block of 32, scale byte e / 32 of the row */
+        const uint8_t *pool = (const uint8_t *)(which_v ? vpool : J->k_cache);
+        const uint8_t *sc = (const uint8_t *)(which_v && J->v_cache ? J->v_scale : J->k_scale);
+        const size_t rowlen = (size_t)J->G * (size_t)J->d;
+        for (int i = 0; i < J->d; ++i) {
+            const size_t e = (size_t)g * (size_t)J->d + (size_t)i;
+            const uint8_t byte = pool[row * (rowlen / 2) + e / 2];
+            const uint8_t code = (e & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            dst[i] = mfa_oracle_e2m1_to_double(code) * mfa_oracle_e8m0_to_double(sc[row * (rowlen / 32) + e / 32]);
+        }
     } else {
         const uint16_t *pool = (const uint16_t *)(which_v ? vpool : J->k_cache);
         for (int i = 0; i < J->d; ++i) dst[i] = bf16_to_double(pool[base + i]);
@@ -213,30 +246,33 @@ int mfa_oracle_num_cpus(void) {
 
 /*
  * Returns 0 on success, -1 on a bad argument, -2 on allocation failure.
- * q: bf16 bits [B,H,d]; k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,G*d]
- * (v_cache NULL: values are the key rows); k_scale/v_scale: fp32 [num_blocks,page] (FP8
- * only; v_scale unused when v_cache is NULL); G divides H, and H / G is at most HEAD_GROUP
+ * q: bf16 bits [B,H,d]; k_cache/v_cache by kv_fmt: 0 bf16 bits [num_blocks,page,G*d],
+ * 1 e4m3 codes [num_blocks,page,G*d] with fp32 scales k_scale/v_scale [num_blocks,page],
+ * 2 MXFP4 codes [num_blocks,page,G*d/2] (two a byte) with E8M0 scales [num_blocks,page,
+ * G*d/32] (v_cache NULL: values are the key rows, v_scale unused); G divides H, and H / G is at most HEAD_GROUP
  * or a multiple of it; block_table: int32 [B,max_pages]; seq_lens: int32 [B];
  * t_begin/t_end: int32 [B] or NULL; out: double [B,H,d]; lse: double [B,H].
  * nthreads <= 0 uses every online CPU.
  */
-int mfa_oracle_decode(int B, int H, int G, int d, int page, int max_pages, int kv_fp8,
+int mfa_oracle_decode(int B, int H, int G, int d, int page, int max_pages, int kv_fmt,
                       const uint16_t *q, const void *k_cache, const void *v_cache,
-                      const float *k_scale, const float *v_scale,
+                      const void *k_scale, const void *v_scale,
                       const int32_t *block_table, const int32_t *seq_lens,
                       const int32_t *t_begin, const int32_t *t_end,
                       double scale, double *out, double *lse, int nthreads) {
     if (B < 0 || H <= 0 || G <= 0 || H % G != 0 || d <= 0 || page <= 0 || max_pages <= 0) return -1;
     if (H / G > HEAD_GROUP && (H / G) % HEAD_GROUP != 0) return -1;
     if (!q || !k_cache || !block_table || !seq_lens || !out || !lse) return -1;
-    if (kv_fp8 && (!k_scale || (v_cache && !v_scale))) return -1;
+    if (kv_fmt < 0 || kv_fmt > 2) return -1;
+    if (kv_fmt == 2 && (G * d) % 32 != 0) return -1;
+    if (kv_fmt != 0 && (!k_scale || (v_cache && !v_scale))) return -1;
     for (int b = 0; b < B; ++b) {
         int L = seq_lens[b];
         int t0 = t_begin ? t_begin[b] : 0;
         int t1 = t_end ? t_end[b] : L;
         if (L < 0 || L > max_pages * page || t0 < 0 || t1 > L) return -1;
     }
-    job_t J = {B, H, G, d, page, max_pages, kv_fp8, q, k_cache, v_cache, k_scale, v_scale,
+    job_t J = {B, H, G, d, page, max_pages, kv_fmt, q, k_cache, v_cache, k_scale, v_scale,
                block_table, seq_lens, t_begin, t_end, scale, out, lse, 0};
     if (nthreads <= 0) nthreads = mfa_oracle_num_cpus();
     int hg = H / G < HEAD_GROUP ? H / G : HEAD_GROUP;
@@ -363,20 +399,77 @@ static void quantise_row(const uint16_t *x, int d, uint8_t *codes, float *scale)
     *scale = s;
 }
 
+/* Nearest E2M1 value to y (codes 0..7 increase in value); of two equally near codes the one
+ * with an even code wins; |y| >= 6 gives 6.  The sign bit of y is kept (a negative y that
+ * rounds to zero gives code 8).  y must not be NaN. */
+uint8_t mfa_oracle_e2m1_from_double(double y) {
+    const int neg = signbit(y) != 0;
+    const double a = fabs(y);
+    int best = 7;
+    if (a < 6.0) {
+        double bd = a;
+        best = 0;
+        for (int c = 1; c <= 7; ++c) {
+            const double dist = fabs(mfa_oracle_e2m1_to_double((uint8_t)c) - a);
+            if (dist < bd || (dist == bd && (c & 1) == 0)) {
+                best = c;
+                bd = dist;
+            }
+        }
+    }
+    return (uint8_t)(neg ? (8 | best) : best);
+}
+
+/* The OCP MX shared exponent of a block: floor(log2(amax)) minus E2M1's largest exponent
+ * (2), clamped to E8M0's [-127, 127]; an all-zero block takes -127. */
+int mfa_oracle_mx_block_exponent(const float *x, int n) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i)
+        if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
+    if (amax == 0.0f) return -127;
+    int E = 0;
+    frexpf(amax, &E);               /* amax = f 2^E, f in [0.5, 1): floor(log2 amax) = E - 1 */
+    int e = (E - 1) - 2;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* MXFP4 row: per block of 32, scale 2^e with e the shared exponent, codes E2M1(x / 2^e)
+ * (an exact power-of-two scaling, then rounding to nearest even, saturating at 6). */
+static void quantise_row_mx(const uint16_t *x, int d, uint8_t *codes, uint8_t *scales) {
+    float blk[32];
+    for (int b = 0; b < d / 32; ++b) {
+        for (int i = 0; i < 32; ++i) blk[i] = bf16_to_float(x[32 * b + i]);
+        const int e = mfa_oracle_mx_block_exponent(blk, 32);
+        scales[b] = (uint8_t)(e + 127);
+        for (int i = 0; i < 32; ++i) {
+            const int j = 32 * b + i;
+            const uint8_t c = mfa_oracle_e2m1_from_double(ldexp((double)blk[i], -e));
+            if (j & 1)
+                codes[j / 2] = (uint8_t)((codes[j / 2] & 0x0F) | (c << 4));
+            else
+                codes[j / 2] = (uint8_t)((codes[j / 2] & 0xF0) | c);
+        }
+    }
+}
+
 /*
  * k_new/v_new: bf16 bits [B*T,d]; positions: int32 [B]; block_table: int32 [B,max_pages];
- * k_cache/v_cache: bf16 bits or e4m3 codes [num_blocks,page,d], updated in place;
- * k_scale/v_scale: fp32 [num_blocks,page] (FP8 only), updated in place.
+ * k_cache/v_cache by kv_fmt (0 bf16, 1 e4m3, 2 MXFP4, layouts as mfa_oracle_decode's with
+ * G = 1), updated in place; k_scale/v_scale: fp32 [num_blocks,page] (e4m3) or E8M0 bytes
+ * [num_blocks,page,d/32] (MXFP4), updated in place.
  * Returns the error mask described above (0 = every row written or skipped by choice),
  * or -1 on a bad argument.
  */
-int mfa_oracle_kv_append(int B, int T, int d, int page, int max_pages, int num_blocks, int kv_fp8,
+int mfa_oracle_kv_append(int B, int T, int d, int page, int max_pages, int num_blocks, int kv_fmt,
                          const uint16_t *k_new, const uint16_t *v_new, const int32_t *positions,
                          const int32_t *block_table, void *k_cache, void *v_cache,
-                         float *k_scale, float *v_scale) {
+                         void *k_scale, void *v_scale) {
     if (B < 0 || T < 1 || d <= 0 || page <= 0 || max_pages <= 0 || num_blocks <= 0) return -1;
     if (!k_new || !v_new || !positions || !block_table || !k_cache || !v_cache) return -1;
-    if (kv_fp8 && (!k_scale || !v_scale)) return -1;
+    if (kv_fmt < 0 || kv_fmt > 2 || (kv_fmt == 2 && d % 32 != 0)) return -1;
+    if (kv_fmt != 0 && (!k_scale || !v_scale)) return -1;
     int mask = 0;
     for (int x = 0; x < B * T; ++x) {
         const int b = x / T;
@@ -392,9 +485,14 @@ int mfa_oracle_kv_append(int B, int T, int d, int page, int max_pages, int num_b
             continue;
         }
         const size_t row = (size_t)blk * page + (size_t)(t % page);
-        if (kv_fp8) {
-            quantise_row(k_new + (size_t)x * d, d, (uint8_t *)k_cache + row * d, k_scale + row);
-            quantise_row(v_new + (size_t)x * d, d, (uint8_t *)v_cache + row * d, v_scale + row);
+        if (kv_fmt == 1) {
+            quantise_row(k_new + (size_t)x * d, d, (uint8_t *)k_cache + row * d, (float *)k_scale + row);
+            quantise_row(v_new + (size_t)x * d, d, (uint8_t *)v_cache + row * d, (float *)v_scale + row);
+        } else if (kv_fmt == 2) {
+            quantise_row_mx(k_new + (size_t)x * d, d, (uint8_t *)k_cache + row * (d / 2),
+                            (uint8_t *)k_scale + row * (d / 32));
+            quantise_row_mx(v_new + (size_t)x * d, d, (uint8_t *)v_cache + row * (d / 2),
+                            (uint8_t *)v_scale + row * (d / 32));
         } else {
             memcpy((uint16_t *)k_cache + row * d, k_new + (size_t)x * d, (size_t)d * sizeof(uint16_t));
             memcpy((uint16_t *)v_cache + row * d, v_new + (size_t)x * d, (size_t)d * sizeof(uint16_t));

@@ -35,6 +35,9 @@ def dense_kv(case, b):
     if w.kv_dtype == "bf16":
         K = case.k_cache[blk, slot].to(torch.float64)
         V = case.v_cache[blk, slot].to(torch.float64)
+    elif w.kv_dtype == "mxfp4":
+        K = mx_dense(case.k_cache[blk, slot], case.k_scale[blk, slot])
+        V = mx_dense(case.v_cache[blk, slot], case.v_scale[blk, slot])
     else:
         K = case.k_cache[blk, slot].view(torch.float8_e4m3fn).to(torch.float64) * \
             case.k_scale[blk, slot].to(torch.float64)[:, None]
@@ -43,6 +46,21 @@ def dense_kv(case, b):
     if getattr(w, "kv_shared", False):
         V = K.clone()
     return K, V
+
+
+# OCP MX FP4 (E2M1) magnitudes by code 0..7; codes 8..15 are their negatives
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def mx_dense(codes, scales):
+    """MXFP4 rows (uint8 [..., n/2] nibble pairs, element 2i in the low nibble; E8M0 uint8
+    [..., n/32]) -> float64 [..., n]: the E2M1 value times its block's scale, the scale
+    decoded by torch's float8_e8m0fnu."""
+    c = codes.numpy()
+    full = np.empty(c.shape[:-1] + (2 * c.shape[-1],), dtype=np.uint8)
+    full[..., 0::2], full[..., 1::2] = c & 15, c >> 4
+    s = scales.contiguous().view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    return torch.from_numpy(E2M1_VALUES[full] * np.repeat(s, 32, axis=-1))
 
 
 def sdpa_reference(case, scale=None):
