@@ -45,10 +45,12 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "ragged_b128_l1024_8192_bf16"
 # The other target workloads, measured on the same run and reported under "workloads" (the
-# last two are the comparison attention shapes).
+# comparison attention shapes and the 4-bit cache last).
 SIDE_WORKLOADS = ("tiny_b1_l512_bf16", "b32_l4096_bf16", "b128_l4096_fp8", "long_b4_l131072_bf16",
                   "b32_l4096_fp8", "long_b4_l131072_fp8", "mtp2_b32_l4096_bf16", "mtp2_b32_l4096_fp8",
-                  "gqa_b32_l4096_bf16", "mla_b32_l4096_bf16")
+                  "gqa_b32_l4096_bf16", "mla_b32_l4096_bf16", "b128_l4096_mxfp4", "b32_l4096_mxfp4")
+# the arithmetic each cache format's path computes in
+PATH_DTYPE = {"bf16": "bf16", "fp8_e4m3": "e4m3", "mxfp4": "mxfp4 KV, e4m3 MMA"}
 
 
 def shape_args(w) -> dict:
@@ -62,11 +64,20 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # ------------------------------------------------------------------ accounting
 
+def row_bytes(kv_dtype: str, row: int = 256) -> int:
+    """Bytes of one stored row of `row` elements: bf16; e4m3 codes + one fp32 scale; or MXFP4
+    code pairs + one E8M0 byte per 32 elements."""
+    if kv_dtype == "bf16":
+        return 2 * row
+    if kv_dtype == "mxfp4":
+        return row // 2 + row // 32
+    return row + 4
+
+
 def kv_bytes_per_token(kv_dtype: str, row: int = 256, shared: bool = False) -> int:
     """Cached rows of one token: K and V rows of `row` elements (all key/value heads), or one
-    row when a latent serves as both, in bf16 or e4m3 (+ one fp32 scale per stored row)."""
-    rows = 1 if shared else 2
-    return rows * row * 2 if kv_dtype == "bf16" else rows * (row + 4)
+    row when a latent serves as both."""
+    return (1 if shared else 2) * row_bytes(kv_dtype, row)
 
 
 def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int = 64, T: int = 1,
@@ -84,9 +95,8 @@ def algorithmic_bytes(lens, kv_dtype: str, H: int = 64, d: int = 256, page: int 
 
 def append_bytes(batch: int, kv_dtype: str, d: int = 256, T: int = 1) -> int:
     """Algorithmic bytes of one KV append: per sequence its position in, and per new token
-    (T of them) the bf16 K and V rows and the page id in, and the stored rows out (bf16, or
-    e4m3 codes + fp32 scale)."""
-    out_row = 2 * d if kv_dtype == "bf16" else d + 4
+    (T of them) the bf16 K and V rows and the page id in, and the stored rows out."""
+    out_row = row_bytes(kv_dtype, d)
     return batch * (4 + T * (2 * 2 * d + 4 + 2 * out_row))
 
 
@@ -383,7 +393,7 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
     dev = tm.dev
     w = case.workload
     lens = case.seq_lens.tolist()
-    kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    kv = mfa.KV_DTYPES[w.kv_dtype]
     B = len(lens)
     T = w.tokens_per_seq
     sa = shape_args(w)
@@ -617,7 +627,7 @@ def run_native(args, case, rank: int, world: int, side_names=()):
     result = {
         "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 KV, f16 MMA",
+        "vs_baseline": None, "dtype": PATH_DTYPE[w.kv_dtype],
         "data": "synthetic", "config": head["config"],
     }
     for k in ("tflops", "ms_per_step_without_early_metadata", "hbm_roofline_frac", "tensor_roofline_frac",

@@ -27,6 +27,9 @@ MFA_ERR_DEVICE_CHECK = 5
 
 MFA_KV_BF16 = 0
 MFA_KV_FP8_E4M3 = 1
+MFA_KV_MXFP4 = 2
+# the cache formats by the names the input generator uses
+KV_DTYPES = {"bf16": MFA_KV_BF16, "fp8_e4m3": MFA_KV_FP8_E4M3, "mxfp4": MFA_KV_MXFP4}
 
 MFA_OUT_BF16 = 0
 MFA_OUT_FP32 = 1

@@ -105,14 +105,23 @@ struct ShapeOf<kShapeMla> {
 constexpr int kPage = 64;          // tokens per KV page
 constexpr int kTile = 128;         // tokens per pipeline tile (MMA M)
 constexpr int kSoftmaxThreads = 256;  // two warps per TMEM lane quarter, 32 heads each
-// Both KV formats: warp 0 TMA, warp 1 QK^T MMAs, warps 2..9 softmax, warp 10 PV MMAs (352
-// threads, 168 registers each).
-template <bool kFp8>
-__host__ __device__ constexpr int threads_of() { return 352; }
-template <bool kFp8>
-__host__ __device__ constexpr int pv_warp() { return 10; }   // issues the PV MMAs
-template <bool kFp8>
-__host__ __device__ constexpr int softmax_warp0() { return 2; }
+// bf16 and e4m3 caches: warp 0 TMA, warp 1 QK^T MMAs, warps 2..9 softmax, warp 10 PV MMAs
+// (352 threads, 168 registers each).
+// MXFP4 cache: warpgroup 0 = warp 0 TMA, warp 1 QK^T MMAs, warp 2 PV MMAs (warp 3 idle);
+// warpgroups 1-2 = warps 4..11 softmax; warpgroup 3 = warps 12..15 convert the 4-bit pages
+// into the e4m3 operand ring.  Launched with 128 registers per thread and rebalanced to
+// 80 / 168 / 168 / 96 (the sum of the four is the launch's 4 x 128).
+template <bool kMx>
+__host__ __device__ constexpr int threads_of() { return kMx ? 512 : 352; }
+template <bool kMx>
+__host__ __device__ constexpr int pv_warp() { return kMx ? 2 : 10; }   // issues the PV MMAs
+template <bool kMx>
+__host__ __device__ constexpr int softmax_warp0() { return kMx ? 4 : 2; }
+constexpr int kConvWarp0 = 12;       // MXFP4: first converter warp
+constexpr int kConvThreads = 128;
+constexpr uint32_t kRegsCtl = 80, kRegsSoftmax = 168, kRegsConv = 96;
+static_assert(kRegsCtl + 2 * kRegsSoftmax + kRegsConv == 4 * (65536 / 512),
+              "MXFP4 register split must add up to the launch budget (4 warpgroups x 128)");
 constexpr int kMaxTilesPerCta = 128;
 // Schedule cost units: a 128-token tile weighs kCostTile, a sequence boundary inside a CTA's
 // range cost_seq (the next sequence's q and one more epilogue).  Measured per sequence switch:
@@ -151,16 +160,24 @@ constexpr int kOffBar = 212992;                              // mbarriers
 //   bf16: slots of 16 KB (a 64-element chunk of both pages of a tile for K; a 128-element
 //         block of one page for V), kRow / 64 uses per tile for each of K and V;
 //   e4m3: slots of 8 KB (one page's 128-element half row block), four uses each.
-template <bool kFp8, int kShp>
+//   MXFP4: the e4m3 ring shrinks to 12 slots, filled by the converter warps; after it, 8
+//          staging slots of 8 KB hold 4-bit pages as TMA writes them ([64 tokens][128 B] of
+//          E2M1 pairs, 128-byte swizzle), and their E8M0 scale bytes (512 B a page) sit past
+//          the metadata (kOffStageScale).
+template <bool kFp8, int kShp, bool kMx = false>
 struct Layout {
   using Sh = ShapeOf<kShp>;
   static constexpr int kOffP = kFp8 ? 32768 : 64 * Sh::kDq * 2;
   static constexpr int kOffRing = kOffP + 16384;
   static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
-  static constexpr int kNumSlots = (kOffBar - kOffRing) / kSlotBytes;
+  static constexpr int kNumSlots = kMx ? 12 : (kOffBar - kOffRing) / kSlotBytes;
   static constexpr int kKU = kFp8 ? 4 : Sh::kRow / 64;   // ring uses per K group and per V group
-  static constexpr int kExtraSmem = 0;
+  static constexpr int kOffStage = kOffRing + kNumSlots * kSlotBytes;   // MXFP4 staging slots
+  static constexpr int kStageSlots = 8;
+  static constexpr int kStageBytes = 8192;
 };
+static_assert(Layout<true, kShapeMfa, true>::kOffStage + 8 * 8192 == kOffBar, "MXFP4 staging fills the ring area");
+static_assert(Layout<true, kShapeMfa, true>::kNumSlots % 4 == 0, "MXFP4 e4m3 ring: groups must not wrap");
 static_assert(Layout<false, kShapeMfa>::kNumSlots == 10 && Layout<true, kShapeMfa>::kNumSlots == 20 &&
               Layout<false, kShapeGqa>::kNumSlots == 11 && Layout<false, kShapeMla>::kNumSlots == 8, "");
 static_assert(Layout<false, kShapeMla>::kNumSlots >= Layout<false, kShapeMla>::kKU, "a ring holds one group");
@@ -201,9 +218,11 @@ constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, e
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileInfo = kOffSegN0 + 4 * kMaxSeg;   // int4[kMaxTilesPerCta] {page 0, page 1, rows 0, rows 1}
 constexpr int kSmemUsed = kOffTileInfo + 16 * kMaxTilesPerCta;
-constexpr int smem_bytes() { return kSmemUsed + 1024; }
-static_assert(smem_bytes() <= 232448, "shared memory budget");
+constexpr int kOffStageScale = kSmemUsed;   // MXFP4: E8M0 bytes of the 8 staged pages, 512 B each
+constexpr int smem_bytes(bool mx) { return kSmemUsed + (mx ? 8 * 512 : 0) + 1024; }
+static_assert(smem_bytes(true) <= 232448, "shared memory budget");
 
+// MXFP4 uses Full/Empty 0..11 for its e4m3 ring and 12..19 for the staging slots.
 enum Bar : int {
   kBarFull = 0,
   kBarEmpty = kBarFull + 20,   // room for the larger ring
@@ -235,10 +254,11 @@ constexpr uint32_t kTmemLx = 448;  // bf16: per-lane row sums of the fp32 weight
 
 struct DecodeParams {
   CUtensorMap tm_q;   // 2-D [B*64 rows, 256] bf16, box 64x64, 128B swizzle
-  CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256]: bf16 box {64, 64, 1}, e4m3 box {128, 64, 1}; 128B swizzle
+  CUtensorMap tm_k;   // 3-D [num_blocks, 64, 256]: bf16 box {64, 64, 1}, e4m3 box {128, 64, 1};
+                      // MXFP4 [num_blocks, 64, 128 B of E2M1 pairs], box {128, 64, 1}; 128B swizzle
   CUtensorMap tm_v;
-  const float* k_scale;
-  const float* v_scale;
+  const void* k_scale;   // e4m3: fp32 [num_blocks, 64]; MXFP4: E8M0 bytes [num_blocks, 64, 8]
+  const void* v_scale;
   const int32_t* block_table;
   const int32_t* seq_lens;
   void* out;          // bf16 or fp32 [B, 64, 256]
@@ -542,6 +562,76 @@ __device__ __forceinline__ float token_scale(const float* __restrict__ sc, const
   return __ldg(sc + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
 }
 
+// MXFP4 (OCP MX FP4: E2M1 elements, one E8M0 scale byte 2^(e - 127) per 32 elements of a
+// row).  A token row's reference exponent is its largest scale byte minus 6, at least 1
+// (biased).  The converter stores each element as the e4m3 code of its value over
+// 2^(ref - 127): an E2M1 value is at most 6 times its block's scale, so the row's codes stay
+// at or under 6 x 2^6 = 384, inside e4m3's 448, and the token's scale 2^(ref - 127) is a
+// normal fp32 power of two that the softmax applies as it does an e4m3 row scale.
+__device__ __forceinline__ int mx_ref_exp(uint2 s8) {
+  const uint32_t m = __vmaxu4(s8.x, s8.y);
+  const uint32_t m2 = max(max(m & 0xFFu, (m >> 8) & 0xFFu), max((m >> 16) & 0xFFu, m >> 24));
+  return max(static_cast<int>(m2) - 6, 1);
+}
+__device__ __forceinline__ float mx_token_scale(const uint8_t* __restrict__ sc, const int4 ti, int pg, int ri) {
+  const int r = pg ? ti.w : ti.z;
+  const int blk = pg ? ti.y : ti.x;
+  if (r <= 0 || ri < kPage - r || blk < 0) return 0.f;
+  const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sc) + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
+  return __uint_as_float(static_cast<uint32_t>(mx_ref_exp(s8)) << 23);
+}
+template <bool kMx>
+__device__ __forceinline__ float kv_token_scale(const void* sc, const int4 ti, int pg, int ri) {
+  if constexpr (kMx)
+    return mx_token_scale(static_cast<const uint8_t*>(sc), ti, pg, ri);
+  else
+    return token_scale(static_cast<const float*>(sc), ti, pg, ri);
+}
+
+// MXFP4 -> e4m3 for one 32-element block: w holds the block's 32 E2M1 codes (element 2i in
+// the low nibble of byte i), D = the block's scale byte minus the row's reference exponent
+// (at most 6).  Output: 32 e4m3 codes of E2M1(x) * 2^D, element i in byte i.  The magnitude
+// of each nibble is looked up by prmt in an 8-byte table (e4m3 codes of 0, 0.5, ..., 6 times
+// 2^D) and its sign bit copied to bit 7.  For D >= -5 every nonzero table entry is a normal
+// e4m3 number, the code of m 2^D being the code of m plus 8 D; below that the table is built
+// by rounding each value to e4m3 (exact down to D = -8; smaller blocks round to e4m3's
+// subnormal grid of 2^-9, relative to the row's largest block at most 2^-16 of its scale).
+__device__ __forceinline__ void mx_block_to_e4m3(const uint4 w, int D, uint4& out0, uint4& out1) {
+  uint32_t l0, l1;
+  if (D >= -5) {
+    // e4m3 codes of 0, 0.5, 1, 1.5 and of 2, 3, 4, 6, every nonzero byte's exponent moved by D
+    l0 = 0x3C383000u + static_cast<uint32_t>(D) * 0x08080800u;
+    l1 = 0x4C484440u + static_cast<uint32_t>(D) * 0x08080808u;
+  } else {
+    const float f = D >= -126 ? __uint_as_float(static_cast<uint32_t>(D + 127) << 23) : 0.f;
+    uint16_t a, b, c, d;
+    // (the first source goes to the high byte of each pair)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(a) : "f"(0.5f * f), "f"(0.0f));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(1.5f * f), "f"(1.0f * f));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(3.0f * f), "f"(2.0f * f));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(6.0f * f), "f"(4.0f * f));
+    l0 = static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 16);   // bytes: 0, 0.5, 1, 1.5
+    l1 = static_cast<uint32_t>(c) | (static_cast<uint32_t>(d) << 16);   // bytes: 2, 3, 4, 6
+  }
+  auto eight = [&](uint32_t x, uint32_t& lo, uint32_t& hi) {
+    // lo: elements 0..3 of x (nibbles 0..3), hi: elements 4..7; the sign of nibble k is bit
+    // 4k + 3 of x: the msb of byte k/2 of (x << 4) for even k, of x for odd k, which prmt's
+    // sign-replicate selectors (bit 3 set) spread over an output byte
+    const uint32_t xs = x << 4;
+    uint32_t m0, m1, s0, s1;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(m0) : "r"(l0), "r"(l1), "r"(x & 0x7777u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(m1) : "r"(l0), "r"(l1), "r"((x >> 16) & 0x7777u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s0) : "r"(xs), "r"(x), "r"(0xD9C8u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(s1) : "r"(xs), "r"(x), "r"(0xFBEAu));
+    lo = m0 | (s0 & 0x80808080u);
+    hi = m1 | (s1 & 0x80808080u);
+  };
+  eight(w.x, out0.x, out0.y);
+  eight(w.y, out0.z, out0.w);
+  eight(w.z, out1.x, out1.y);
+  eight(w.w, out1.z, out1.w);
+}
+
 // Ring use index of the first use of the K (is_v = false) or V group of tile t of a CTA with
 // `ntiles` tiles, kKU uses per group.  The producer issues K(0), then K(t) and V(t-1) for
 // t = 1..N-1, then V(N-1): K(0) = 0.., K(t) = 2 kKU t - kKU.., V(t) = 2 kKU t + 2 kKU.. except
@@ -554,12 +644,15 @@ __device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v) {
   return is_v ? (t + 1 < ntiles ? 2u * U * t + 2u * U : 2u * U * t + U) : (t == 0 ? 0u : 2u * U * t - U);
 }
 
-template <bool kFp8, int kShp>
-__global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
+// kFp8: both contractions on e4m3 operands (an e4m3 cache, or an MXFP4 cache converted to
+// e4m3 on chip: kMx).
+template <bool kFp8, int kShp, bool kMx = false>
+__global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(!kFp8 || kShp == kShapeMfa, "the e4m3 cache is built for the MFA shape");
-  using Lay = Layout<kFp8, kShp>;
+  static_assert(!kMx || kFp8, "the MXFP4 path runs on the e4m3 MMAs");
+  using Lay = Layout<kFp8, kShp, kMx>;
   using Sh = ShapeOf<kShp>;
-  constexpr int kThreads = threads_of<kFp8>();
+  constexpr int kThreads = threads_of<kMx>();
   constexpr int kNumSlots = Lay::kNumSlots;
   constexpr int kSlotBytes = Lay::kSlotBytes;
   constexpr int kOffRing = Lay::kOffRing;
@@ -597,6 +690,10 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         count = kSoftmaxThreads;
       else if (i == kBarDrain)
         count = 2;
+      else if (kMx && i >= kBarFull && i < kBarFull + kNumSlots)
+        count = 2;   // MXFP4 e4m3 ring: the two converter warps that write a slot's rows
+      else if (kMx && i >= kBarEmpty + kNumSlots && i < kBarEmpty + kNumSlots + Lay::kStageSlots)
+        count = kConvThreads / 32;   // MXFP4 staging: every converter warp reads every slot
       mbar_init(bar(i), count);
     }
     if (lane == 0) {
@@ -783,10 +880,16 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
   }
   __syncthreads();
 
+  // MXFP4 warpgroup register split (see threads_of), at the top of each role so that the
+  // role's budget covers all of its code: the control warps and the converters give
+  // registers up, the softmax warpgroups take them
   if (warp == 0) {
+    if constexpr (kMx) reg_dealloc<kRegsCtl>();
     // ---------------- producer: TMA loads of Q, K and V in ring order.  Each group of four
     // ring uses (a tile's K, or a tile's V) is issued by lanes 0..3 together, one use per
     // lane; groups go out strictly in ring order, so every slot's phases stay in step.
+    // MXFP4: the groups go to the staging ring instead, two uses (one per page) each, by
+    // lanes 0..1: a page's 8 KB of E2M1 pairs by TMA and its 512 scale bytes by a bulk copy.
     if (ntiles > 0) {
       if (p.early_metadata) grid_dep_wait();
       // KV is streamed once: evict first.  Multi-token decode reads a sequence's pages once
@@ -794,7 +897,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       // the lines (evict last) for the next one.
       const uint64_t pol_once = l2_policy_evict_first(), pol_again = l2_policy_evict_last();
       int seg_k = 0, seg_v = 0;   // segment of the producer's current K and V tiles
-      const bool act = lane < kKU;
+      const bool act = lane < (kMx ? 2 : kKU);
       const int c = lane;
       bool ok = true;
       int sq = 0, nq = 0;                 // next segment whose q is loaded; q loads issued
@@ -809,6 +912,33 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
         int& sc_ = is_v ? seg_v : seg_k;
         while (sc_ + 1 < nseg && seg_n0[sc_ + 1] <= t) ++sc_;
         const uint64_t pol = (reads > 1 && seg[sc_].x % reads != reads - 1) ? pol_again : pol_once;
+        if constexpr (kMx) {
+          if (act) {
+            const int4 ti = tile_info[t];
+            const uint32_t u = ring_use<2>(t, ntiles, is_v) + c;
+            const uint32_t slot = u % Lay::kStageSlots;
+            okl = wait_bar(bar(kBarEmpty + kNumSlots + slot), ((u / Lay::kStageSlots) & 1) ^ 1, abort_flag);
+            if (okl) {
+              const uint32_t fb = bar(kBarFull + kNumSlots + slot);
+              const int r = c ? ti.w : ti.z;
+              const int blk = c ? ti.y : ti.x;   // -1: outside the pool (codes read as zeros, no scales)
+              if (r <= 0) {
+                mbar_arrive(fb);
+              } else {
+                mbar_arrive_expect_tx(fb, Lay::kStageBytes + (blk >= 0 ? 512u : 0u));
+                tma_load_3d_hint(sbase + Lay::kOffStage + slot * Lay::kStageBytes, is_v ? &p.tm_v : &p.tm_k, fb, 0,
+                                 r - kPage, blk, pol);
+                if (blk >= 0)
+                  bulk_load_g2s(sbase + kOffStageScale + slot * 512,
+                                static_cast<const uint8_t*>(is_v ? p.v_scale : p.k_scale) + static_cast<size_t>(blk) * 512,
+                                512, fb);
+              }
+              mine[nmine % 3] = u;
+              ++nmine;
+            }
+          }
+          return __all_sync(0xffffffffu, okl);
+        }
         if (act) {
           const int4 ti = tile_info[t];
           const uint32_t u = ring_use<kKU>(t, ntiles, is_v) + c;
@@ -872,13 +1002,16 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       if (!ok) {
         if (lane == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
         // let every copy already issued land before the CTA can exit
+        constexpr uint32_t kDrainSlots = kMx ? Lay::kStageSlots : kNumSlots;
+        constexpr int kDrainBar0 = kMx ? kBarFull + kNumSlots : kBarFull;
         if (act)
           for (int i = 0; i < (nmine < 3 ? nmine : 3); ++i)
-            wait_slow(bar(kBarFull + mine[i] % kNumSlots), (mine[i] / kNumSlots) & 1, nullptr, kDrainLimitNs);
+            wait_slow(bar(kDrainBar0 + mine[i] % kDrainSlots), (mine[i] / kDrainSlots) & 1, nullptr, kDrainLimitNs);
         if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
       }
     }
-  } else if (warp == 1 || warp == pv_warp<kFp8>()) {
+  } else if (warp == 1 || warp == pv_warp<kMx>()) {
+    if constexpr (kMx) reg_dealloc<kRegsCtl>();
     // ---------------- MMA issuers: QK^T of tile n, then PV of tile n - 1, so the next tile's
     // scores are computed while the softmax works on the current one.  Warp 1 issues the
     // QK^T stream and warp pv_warp the PV stream (they share no operand, accumulator or
@@ -953,7 +1086,7 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           if (last) umma_commit(bar(kBarQEmpty));
           if (++jk == sg.z && ++sk < nseg) jk = seg[sk].y;
         }
-        if (n >= 1 && warp == pv_warp<kFp8>()) {
+        if (n >= 1 && warp == pv_warp<kMx>()) {
           const int m = n - 1;
           const int4 sg = seg[sv];
           const bool first = (jv == sg.y), last = (jv == sg.z - 1);
@@ -1022,10 +1155,74 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
       umma_commit(bar(kBarDrain));
       wait_slow(bar(kBarDrain), 0, nullptr, kDrainLimitNs);
     }
+  } else if (kMx && warp < softmax_warp0<kMx>()) {
+    // MXFP4: warp 3 completes warpgroup 0 and has no role
+    if constexpr (kMx) reg_dealloc<kRegsCtl>();
+  } else if (kMx && warp >= kConvWarp0) {
+    if constexpr (kMx) {
+      reg_dealloc<kRegsConv>();
+      // ---------------- MXFP4 pages -> e4m3 operand ring (warps 12..15).  Each staging use
+      // holds one page (K or V) of a tile; thread dt converts box row ri = dt & 63 of d-half
+      // dh = dt >> 6 (warps 12-13: d 0..127, warps 14-15: d 128..255), four 32-element blocks,
+      // into the e4m3 slot of that page and d-half, laid out as TMA lays out an e4m3 box
+      // ([64 tokens][128 d], 128-byte swizzle), so that the MMAs read both caches alike.  Pages
+      // go in the producer's order; each warp releases the staging slot, and the two warps of
+      // a d-half together fill an e4m3 slot.
+      const int dt = tid - 32 * kConvWarp0;
+      const int ri = dt & 63, dh = dt >> 6;
+      auto page = [&](bool is_v, int t, int pg) -> bool {
+        const uint32_t su = ring_use<2>(t, ntiles, is_v) + pg;
+        const uint32_t ss = su % Lay::kStageSlots;
+        // the e4m3 use: K group use c = 2 dh + pg (page c & 1, d-half c >> 1), V c = 2 pg + dh
+        const uint32_t u = ring_use<kKU>(t, ntiles, is_v) + (is_v ? 2 * pg + dh : 2 * dh + pg);
+        const uint32_t slot = u % kNumSlots;
+        if (!wait_warp(bar(kBarFull + kNumSlots + ss), (su / Lay::kStageSlots) & 1, abort_flag)) return false;
+        if (!wait_warp(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag)) return false;
+        const int4 ti = tile_info[t];
+        const int r = pg ? ti.w : ti.z;
+        const int blk = pg ? ti.y : ti.x;
+        if (r > 0) {   // (an absent page is skipped by the MMAs' masks and the PV)
+          uint8_t* dst = smem + kOffRing + slot * kSlotBytes + ri * 128;
+          const int pr = ri - (kPage - r);   // page row of box row ri; rows above it read zeros
+          if (pr < 0 || blk < 0) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(dst + (q << 4)) = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            const uint8_t* src = smem + Lay::kOffStage + ss * Lay::kStageBytes + ri * 128;
+            const uint2 s8 = *reinterpret_cast<const uint2*>(smem + kOffStageScale + ss * 512 + pr * 8);
+            const int ref = mx_ref_exp(s8);
+            const uint32_t sh = dh ? s8.y : s8.x;   // scale bytes of blocks 4 dh .. 4 dh + 3
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int j = 4 * dh + k;            // block j: d 32 j .. 32 j + 31, 16-byte chunk j
+              const uint4 w = *reinterpret_cast<const uint4*>(src + ((j ^ (ri & 7)) << 4));
+              uint4 o0, o1;
+              mx_block_to_e4m3(w, static_cast<int>((sh >> (8 * k)) & 0xFFu) - ref, o0, o1);
+              *reinterpret_cast<uint4*>(dst + (((2 * k) ^ (ri & 7)) << 4)) = o0;
+              *reinterpret_cast<uint4*>(dst + (((2 * k + 1) ^ (ri & 7)) << 4)) = o1;
+            }
+          }
+        }
+        fence_proxy_async_smem();   // the rows are read by the tensor cores (async proxy)
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(kBarFull + slot));
+          mbar_arrive(bar(kBarEmpty + kNumSlots + ss));
+        }
+        return true;
+      };
+      bool ok = true;
+      for (int n = 0; n <= ntiles && ok; ++n) {
+        if (n < ntiles) ok = page(false, n, 0) && page(false, n, 1);
+        if (ok && n >= 1) ok = page(true, n - 1, 0) && page(true, n - 1, 1);
+      }
+      if (!ok && lane == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
+    }
   } else {
+    if constexpr (kMx) reg_alloc<kRegsSoftmax>();
     // ---------------- softmax + epilogue (256 threads: two warps per TMEM lane quarter)
-    const int ts = tid - 32 * softmax_warp0<kFp8>();   // 0..255
-    const int sw = warp - softmax_warp0<kFp8>();       // 0..7
+    const int ts = tid - 32 * softmax_warp0<kMx>();   // 0..255
+    const int sw = warp - softmax_warp0<kMx>();       // 0..7
     const int grp = sw >> 2;                       // head half [32*grp, +32)
     const int h0 = 32 * grp;
     const int wq = warp & 3;                       // TMEM lane quarter of this warp
@@ -1250,8 +1447,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
     int e_ref = kEMin;                              // e4m3: the segment's reference exponent of V scales
     if constexpr (kFp8) {
       if (ntiles > 0) {
-        sk_next = token_scale(p.k_scale, tile_info[0], rpg, ri);
-        sv_next = token_scale(p.v_scale, tile_info[0], rpg, ri);
+        sk_next = kv_token_scale<kMx>(p.k_scale, tile_info[0], rpg, ri);
+        sv_next = kv_token_scale<kMx>(p.v_scale, tile_info[0], rpg, ri);
         convert_q(0);
       }
     }
@@ -1287,8 +1484,8 @@ __global__ void __launch_bounds__(threads_of<kFp8>(), 1) mfa_decode_kernel(const
           ck = c * qinv * sk_next;                 // loaded one tile ahead
           svt = sv_next;
           if (n + 1 < ntiles) {
-            sk_next = token_scale(p.k_scale, tile_info[n + 1], rpg, ri);
-            sv_next = token_scale(p.v_scale, tile_info[n + 1], rpg, ri);
+            sk_next = kv_token_scale<kMx>(p.k_scale, tile_info[n + 1], rpg, ri);
+            sv_next = kv_token_scale<kMx>(p.v_scale, tile_info[n + 1], rpg, ri);
           }
           sv_e = static_cast<int>((__float_as_uint(svt) >> 23) & 0xFFu) - 127;
         }
@@ -2048,7 +2245,8 @@ mfa_status check_problem(const mfa_problem* pr) {
   if (pr == nullptr) return MFA_ERR_INVALID_ARG;
   if (pr->tokens_per_seq < 1 || pr->tokens_per_seq > kMaxTokensPerSeq) return MFA_ERR_INVALID_ARG;
   if (pr->batch < 0 || pr->max_pages_per_seq < 1 || pr->num_blocks < 1) return MFA_ERR_INVALID_ARG;
-  if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3) return MFA_ERR_INVALID_ARG;
+  if (pr->kv_dtype != MFA_KV_BF16 && pr->kv_dtype != MFA_KV_FP8_E4M3 && pr->kv_dtype != MFA_KV_MXFP4)
+    return MFA_ERR_INVALID_ARG;
   if (pr->out_dtype != MFA_OUT_BF16 && pr->out_dtype != MFA_OUT_FP32) return MFA_ERR_INVALID_ARG;
   if (!(std::isfinite(pr->softmax_scale) && pr->softmax_scale > 0.f)) return MFA_ERR_INVALID_ARG;
   if (pr->num_kv_heads < 1 || (pr->kv_shared != 0 && pr->kv_shared != 1)) return MFA_ERR_INVALID_ARG;
@@ -2087,13 +2285,14 @@ static mfa_status encode_maps_uncached(DecodeParams& prm, const mfa_problem* pr,
   }
   const void* pools[2] = {k, pr->kv_shared ? k : v};   // one latent: the V map reads the K pool
   CUtensorMap* maps[2] = {&prm.tm_k, &prm.tm_v};
-  const bool fp8 = pr->kv_dtype == MFA_KV_FP8_E4M3;
+  const bool fp8 = pr->kv_dtype != MFA_KV_BF16;   // byte elements: e4m3 codes or MXFP4 code pairs
   const cuuint64_t esz = fp8 ? 1 : 2;
+  // an MXFP4 row is rowlen / 2 bytes (two E2M1 codes a byte)
+  const cuuint64_t row_elems = pr->kv_dtype == MFA_KV_MXFP4 ? rowlen / 2 : rowlen;
   for (int i = 0; i < 2; ++i) {
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(rowlen), static_cast<cuuint64_t>(kPage),
-                          static_cast<cuuint64_t>(pr->num_blocks)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(rowlen) * esz, static_cast<cuuint64_t>(rowlen) * esz * kPage};
-    // one 128-byte swizzle row per box row: 64 bf16 or 128 e4m3 codes
+    cuuint64_t dims[3] = {row_elems, static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(pr->num_blocks)};
+    cuuint64_t strides[2] = {row_elems * esz, row_elems * esz * kPage};
+    // one 128-byte swizzle row per box row: 64 bf16, 128 e4m3 codes or 256 E2M1 codes
     cuuint32_t box[3] = {fp8 ? 128u : 64u, 64, 1};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(maps[i], fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -2154,13 +2353,16 @@ static mfa_status encode_maps(DecodeParams& prm, const mfa_problem* pr, const vo
 using DecodeKernelFn = void (*)(DecodeParams);
 static int kernel_index(const mfa_problem* pr) {
   const int shp = problem_shape(pr);
-  return shp == kShapeMfa ? (pr->kv_dtype == MFA_KV_FP8_E4M3 ? 1 : 0) : (shp == kShapeGqa ? 2 : 3);
+  if (shp != kShapeMfa) return shp == kShapeGqa ? 2 : 3;
+  return pr->kv_dtype == MFA_KV_FP8_E4M3 ? 1 : (pr->kv_dtype == MFA_KV_MXFP4 ? 4 : 0);
 }
+static int threads_of_kernel(int idx) { return idx == 4 ? threads_of<true>() : threads_of<false>(); }
 static DecodeKernelFn decode_kernel_of(int idx) {
   switch (idx) {
     case 1: return mfa_decode_kernel<true, kShapeMfa>;
     case 2: return mfa_decode_kernel<false, kShapeGqa>;
     case 3: return mfa_decode_kernel<false, kShapeMla>;
+    case 4: return mfa_decode_kernel<true, kShapeMfa, true>;
     default: return mfa_decode_kernel<false, kShapeMfa>;
   }
 }
@@ -2168,13 +2370,13 @@ static DecodeKernelFn decode_kernel_of(int idx) {
 // cudaFuncSetAttribute for a kernel's dynamic shared memory, once per device and kernel.
 static mfa_status ensure_smem_attribute(int idx) {
   constexpr int kMaxDevices = 64;
-  static std::atomic<bool> done[4][kMaxDevices];
+  static std::atomic<bool> done[5][kMaxDevices];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   const bool cacheable = dev >= 0 && dev < kMaxDevices;
   if (cacheable && done[idx][dev].load(std::memory_order_acquire)) return MFA_OK;
-  e = cudaFuncSetAttribute(decode_kernel_of(idx), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+  e = cudaFuncSetAttribute(decode_kernel_of(idx), cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(idx == 4));
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
   if (cacheable) done[idx][dev].store(true, std::memory_order_release);
   return MFA_OK;
@@ -2194,7 +2396,7 @@ static mfa_status launch_combine(const mfa_plan* pl, const mfa_problem* pr, cons
   cp.batch = static_cast<int>(vbatch(pr));
   cp.tokens = pr->tokens_per_seq;
   cp.units = units_of(pr);
-  cp.seq_cost = cost_seq(pr->kv_dtype == MFA_KV_FP8_E4M3);
+  cp.seq_cost = cost_seq(pr->kv_dtype != MFA_KV_BF16);
   cp.max_pages = pr->max_pages_per_seq;
   cp.num_ctas = pl->num_ctas;
   cudaLaunchConfig_t cfg = {};
@@ -2286,7 +2488,7 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   }
   // planned from a bound, any shorter mix must fit too: a CTA's cost range of at most
   // ceil(C / G) units holds at most ceil(ceil(C / G) / 4) tiles
-  const long long cs = cost_seq(pr->kv_dtype == MFA_KV_FP8_E4M3);
+  const long long cs = cost_seq(pr->kv_dtype != MFA_KV_BF16);
   const long long Cb = kCostTile * W + cs * std::max(Bv - 1, 0ll);
   auto worst = [&](long long g) {
     const long long exact = max_cta_tiles(T, g, cs);
@@ -2317,7 +2519,7 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
 
 // Host-side checks of one decode step's arguments (everything mfa_decode_run validates).
 static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
-                            const void* v_cache, const float* k_scale, const float* v_scale,
+                            const void* v_cache, const void* k_scale, const void* v_scale,
                             const int32_t* block_table, const int32_t* seq_lens, const void* out,
                             const float* lse, const void* workspace, uint64_t workspace_bytes) {
   mfa_status st = check_problem(pr);
@@ -2330,7 +2532,7 @@ static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const v
   if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
       seq_lens == nullptr || out == nullptr || workspace == nullptr)
     return MFA_ERR_INVALID_ARG;
-  if (pr->kv_dtype == MFA_KV_FP8_E4M3 &&
+  if (pr->kv_dtype != MFA_KV_BF16 &&
       (k_scale == nullptr || v_scale == nullptr || !aligned(k_scale, 16) || !aligned(v_scale, 16)))
     return MFA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
@@ -2342,7 +2544,7 @@ static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const v
 }
 
 mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
-                          const void* v_cache, const float* k_scale, const float* v_scale,
+                          const void* v_cache, const void* k_scale, const void* v_scale,
                           const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
                           void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
   mfa_status st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse,
@@ -2381,8 +2583,8 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   if (st != MFA_OK) return st;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(plan->num_ctas), 1, 1);
-  cfg.blockDim = dim3(threads_of<false>(), 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes();
+  cfg.blockDim = dim3(threads_of_kernel(kidx), 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes(kidx == 4);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -2408,7 +2610,7 @@ mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* pr, cons
                                const int32_t* block_table_host, const int32_t* seq_lens_host, void* out_host,
                                float* lse_host, void* q_dev, int32_t* block_table_dev, int32_t* seq_lens_dev,
                                void* out_dev, float* lse_dev, const void* k_cache, const void* v_cache,
-                               const float* k_scale, const float* v_scale, void* workspace,
+                               const void* k_scale, const void* v_scale, void* workspace,
                                uint64_t workspace_bytes, void* stream_ptr) {
   // the whole step is validated before anything is enqueued
   mfa_status st = check_run(plan, pr, q_dev, k_cache, v_cache, k_scale, v_scale, block_table_dev, seq_lens_dev,
@@ -2482,7 +2684,7 @@ void* g_static_ptr[kMaxDevices] = {};
 
 extern "C" mfa_status mfa_decode_run_static_workspace(
     const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache, const void* v_cache,
-    const float* k_scale, const float* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out,
+    const void* k_scale, const void* v_scale, const int32_t* block_table, const int32_t* seq_lens, void* out,
     float* lse, void* stream_ptr) {
   mfa_status st = check_problem(pr);
   if (st != MFA_OK) return st;

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MFA_ABI_VERSION 3
+#define MFA_ABI_VERSION 4
 
 typedef enum mfa_status {
     MFA_OK = 0,
@@ -65,7 +65,12 @@ typedef enum mfa_status {
 
 typedef enum mfa_kv_dtype {
     MFA_KV_BF16 = 0,           /* K/V cache in bf16 */
-    MFA_KV_FP8_E4M3 = 1        /* K/V cache as OCP e4m3 codes, one fp32 scale per token row */
+    MFA_KV_FP8_E4M3 = 1,       /* K/V cache as OCP e4m3 codes, one fp32 scale per token row */
+    MFA_KV_MXFP4 = 2           /* K/V cache in the OCP MX FP4 format: E2M1 codes, two a byte
+                                  (element 2i in the low nibble of byte i), and one E8M0
+                                  scale byte, 2^(e - 127), per 32 elements of a row
+                                  (Step-3 page section 5, "Quantization and MTP", names further
+                                  KV quantisation; this format is the reading taken) */
 } mfa_kv_dtype;
 
 typedef enum mfa_out_dtype {
@@ -151,7 +156,7 @@ typedef struct mfa_plan {
  * [floor(g*C/G), floor((g+1)*C/G)), C = 4 W + c (N - 1) for W tiles in N non-empty
  * sequences: every CTA gets the same share whatever the length mix, a sequence boundary
  * inside a CTA's range (the next sequence's q and one more epilogue) counting as c/4 of a
- * tile, c = 3 for bf16 KV and c = 10 for e4m3 KV.  A sequence is split once per CTA
+ * tile, c = 3 for bf16 KV and c = 10 for e4m3 and MXFP4 KV.  A sequence is split once per CTA
  * boundary that falls inside it.  Planned
  * from a length bound (host_seq_lens NULL), the grid keeps every CTA within 128 tiles
  * for any lengths up to the bound.
@@ -164,9 +169,18 @@ mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_l
  * Enqueue one decode step (decode kernel, then the combine kernel when the plan
  * has more than one CTA and MFA_PLAN_NO_COMBINE is not set).
  *   q            : device bf16 [B, 64, 256], 16-byte aligned.
- *   k_cache      : device [num_blocks, 64, 256], bf16 or e4m3 codes (uint8), 16-byte aligned.
+ *   k_cache      : device [num_blocks, 64, 256], bf16 or e4m3 codes (uint8); MXFP4: uint8
+ *                  [num_blocks, 64, 128] code pairs; 16-byte aligned.
  *   v_cache      : same layout as k_cache.
- *   k_scale      : device fp32 [num_blocks, 64], 16-byte aligned (e4m3 only; NULL for bf16):
+ *   k_scale      : MXFP4: device uint8 [num_blocks, 64, 8], the E8M0 byte of each 32-element
+ *                  block of a row (byte 255, NaN, gives unspecified results), 16-byte
+ *                  aligned.  Each row is converted on chip to e4m3 codes under one
+ *                  power-of-two scale per row, 2^(m - 6 - 127) for the row's largest scale
+ *                  byte m (at least 2^-126): exact for every block whose scale is at least
+ *                  2^-14 of the row's largest; smaller blocks round to e4m3's subnormal grid,
+ *                  an absolute error below 2^-16 of the row's largest block scale.  From
+ *                  there the path is the e4m3 one.
+ *                  e4m3: device fp32 [num_blocks, 64], 16-byte aligned (NULL for bf16):
  *                  value = code * scale, any positive finite scale.  The e4m3 path runs
  *                  both contractions on the e4m3 codes as stored: q.K^T against q split
  *                  exactly into two e4m3 parts under one power-of-two scale per sequence,
@@ -190,7 +204,7 @@ mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_l
  */
 mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* problem,
                           const void* q, const void* k_cache, const void* v_cache,
-                          const float* k_scale, const float* v_scale,
+                          const void* k_scale, const void* v_scale,
                           const int32_t* block_table, const int32_t* seq_lens,
                           void* out, float* lse, void* workspace, uint64_t workspace_bytes,
                           void* stream);
@@ -219,7 +233,7 @@ mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* problem,
                                void* q_dev, int32_t* block_table_dev, int32_t* seq_lens_dev,
                                void* out_dev, float* lse_dev,
                                const void* k_cache, const void* v_cache,
-                               const float* k_scale, const float* v_scale,
+                               const void* k_scale, const void* v_scale,
                                void* workspace, uint64_t workspace_bytes, void* stream);
 
 /*
@@ -278,7 +292,7 @@ const char* mfa_status_string(mfa_status status);
 #define MFA_STATIC_WORKSPACE_BYTES (24u * 1024u * 1024u)
 mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_problem* problem,
                                            const void* q, const void* k_cache, const void* v_cache,
-                                           const float* k_scale, const float* v_scale,
+                                           const void* k_scale, const void* v_scale,
                                            const int32_t* block_table, const int32_t* seq_lens,
                                            void* out, float* lse, void* stream);
 
@@ -296,7 +310,13 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  *     k_scale/v_scale[page][slot], and each value x to the e4m3 code of x / s
  *     (both divisions fp32, rounded to nearest; the code rounded to nearest even,
  *     magnitudes above 448 saturated to 448; a negative x that rounds to zero gives
- *     the code 0x80).  The row maximum always lands on code +-448.
+ *     the code 0x80).  The row maximum always lands on code +-448;
+ *   - MXFP4 cache (quantisation fused in the same pass): per block of 32 elements the
+ *     scale byte max(E - 2, 0), E the biased fp32 exponent of the block's largest |x|
+ *     (the OCP MX rule: 2^(floor(log2 amax) - 2), clamped to [2^-127, 2^127]; an all-zero
+ *     or subnormal block takes byte 0), and each x to the E2M1 code of x / 2^(byte - 127),
+ *     rounded to nearest even, saturated to 6, sign kept (a negative x that rounds to zero
+ *     gives the code 8).
  *   problem      : the decode's problem description (kv_dtype, batch, table width and
  *                  pool size are used); validated as for mfa_decode_plan.
  *   k_new, v_new : device bf16 [B, T, 256], 16-byte aligned, finite values (non-finite
@@ -307,7 +327,8 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  *   block_table  : device int32 [B, max_pages_per_seq]: must already hold the page of
  *                  position t (allocate it before the step).
  *   k_cache, v_cache, k_scale, v_scale : the pools of mfa_decode_run, written in place;
- *                  only the target slots change.  Scales NULL for a bf16 cache.
+ *                  only the target slots change.  Scales NULL for a bf16 cache; fp32 for
+ *                  e4m3, E8M0 bytes for MXFP4.
  *   device_status: device uint32, or NULL.  A position >= max_pages_per_seq * 64 sets
  *                  MFA_DEV_BAD_LENGTH, a page id outside [0, num_blocks) sets
  *                  MFA_DEV_BAD_BLOCK; that token's rows are then not written.  The
@@ -320,7 +341,7 @@ mfa_status mfa_decode_run_static_workspace(const mfa_plan* plan, const mfa_probl
  */
 mfa_status mfa_kv_append(const mfa_problem* problem, const void* k_new, const void* v_new,
                          const int32_t* positions, const int32_t* block_table,
-                         void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                         void* k_cache, void* v_cache, void* k_scale, void* v_scale,
                          uint32_t* device_status, void* stream);
 
 /* MFA_ABI_VERSION of the loaded library. */

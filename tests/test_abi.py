@@ -28,7 +28,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(mfa.EXPORTED_SYMBOLS)
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
-    assert lib.mfa_abi_version() == 3
+    assert lib.mfa_abi_version() == 4
 
 
 def test_status_strings(lib):
@@ -72,7 +72,7 @@ def split_tiles_brute_force(lens, G, c):
     return per
 
 
-@pytest.mark.parametrize("kv, c", [(mfa.MFA_KV_BF16, 3), (mfa.MFA_KV_FP8_E4M3, 10)])
+@pytest.mark.parametrize("kv, c", [(mfa.MFA_KV_BF16, 3), (mfa.MFA_KV_FP8_E4M3, 10), (mfa.MFA_KV_MXFP4, 10)])
 def test_plan_tile_counts_follow_the_documented_split(lib, kv, c):
     import random
     rng = random.Random(5)
@@ -147,7 +147,9 @@ def test_plan_rejects_bad_input(lib):
                       (dict(head_dim=128, num_kv_heads=4, tokens_per_seq=2), mfa.MFA_ERR_UNSUPPORTED),
                       (dict(num_q_heads=128, head_dim=512), mfa.MFA_ERR_UNSUPPORTED),
                       (dict(num_q_heads=128, head_dim=512, kv_shared=True, kv_dtype=mfa.MFA_KV_FP8_E4M3),
-                       mfa.MFA_ERR_UNSUPPORTED)]:
+                       mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(head_dim=128, num_kv_heads=4, kv_dtype=mfa.MFA_KV_MXFP4), mfa.MFA_ERR_UNSUPPORTED),
+                      (dict(kv_dtype=3), mfa.MFA_ERR_INVALID_ARG)]:
         with pytest.raises(mfa.MfaError) as e:
             mfa.mfa_decode_plan(problem(**bad), None, max_seq_len=64, num_sms=8)
         assert e.value.status == code, bad
@@ -189,6 +191,13 @@ def test_run_validates_before_touching_the_device(lib):
     assert _run_raw(lib, plan, prob, good, plan.workspace_bytes - 1) == mfa.MFA_ERR_WORKSPACE
     other = problem(batch=5)
     assert _run_raw(lib, plan, other, good, plan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+    # an MXFP4 cache needs both scale arrays, 16-byte aligned (their pages are bulk copies)
+    mxp = problem(kv_dtype=mfa.MFA_KV_MXFP4)
+    mplan = mfa.mfa_decode_plan(mxp, [10, 20, 30, 40], num_sms=8)
+    assert _run_raw(lib, mplan, mxp, good, mplan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
+    mgood = list(good); mgood[3], mgood[4] = 0x8000, 0x9000
+    mbad = list(mgood); mbad[4] = 0x9008
+    assert _run_raw(lib, mplan, mxp, mbad, mplan.workspace_bytes) == mfa.MFA_ERR_INVALID_ARG
 
 
 def _append_raw(lib, prob, ptrs):
@@ -208,6 +217,10 @@ def test_kv_append_validates_before_touching_the_device(lib):
         assert _append_raw(lib, bf, bad) == mfa.MFA_ERR_INVALID_ARG
     no_scale = list(good); no_scale[6] = None
     assert _append_raw(lib, f8, no_scale) == mfa.MFA_ERR_INVALID_ARG
+    mx = problem(kv_dtype=mfa.MFA_KV_MXFP4)
+    assert _append_raw(lib, mx, no_scale) == mfa.MFA_ERR_INVALID_ARG
+    odd_scale = list(good); odd_scale[7] += 4   # MXFP4 writes the 8 scale bytes of a row at once
+    assert _append_raw(lib, mx, odd_scale) == mfa.MFA_ERR_INVALID_ARG
     odd_status = list(good); odd_status[8] = 0x9002
     assert _append_raw(lib, f8, odd_status) == mfa.MFA_ERR_INVALID_ARG
     assert _append_raw(lib, problem(head_dim=128), good) == mfa.MFA_ERR_UNSUPPORTED

@@ -1,8 +1,8 @@
 """Parity of the KV-cache append kernel (through the C ABI) with the oracle's append.
 
-The bar is bit-exact: the same bf16 bits, e4m3 codes and fp32 scales in every byte of both
-pools (a quantised code is an integer decided by fp32 divisions that both sides round to
-nearest).  Every other slot keeps its bytes.  An append followed by a decode on the same
+The bar is bit-exact: the same bf16 bits, e4m3 codes and fp32 scales, or E2M1 codes and E8M0
+scale bytes, in every byte of both pools (a quantised code is an integer decided by fp32
+divisions, or exact power-of-two scalings, that both sides round to nearest).  Every other slot keeps its bytes.  An append followed by a decode on the same
 stream must give the oracle's attention over the oracle-appended cache.
 """
 import numpy as np
@@ -19,7 +19,7 @@ RAGGED = [1, 64, 65, 127, 128, 129, 200, 7, 300, 63, 2, 192, 256, 5, 66, 190, 33
 
 
 def kv_of(case):
-    return mfa.MFA_KV_FP8_E4M3 if case.workload.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    return mfa.KV_DTYPES[case.workload.kv_dtype]
 
 
 def gpu_append(case, step, positions=None, block_table=None, status=None, tokens_per_seq=1):
@@ -61,11 +61,12 @@ def assert_pools_equal(got, want):
     assert np.array_equal(kc, okc.view(view)), "K pool differs"
     assert np.array_equal(vc, ovc.view(view)), "V pool differs"
     if oks is not None:
-        assert np.array_equal(ks, oks.view(np.int32)), "K scales differ"
-        assert np.array_equal(vs, ovs.view(np.int32)), "V scales differ"
+        sv = np.uint8 if oks.dtype == np.uint8 else np.int32   # E8M0 bytes or fp32 bits
+        assert np.array_equal(ks, oks.view(sv)), "K scales differ"
+        assert np.array_equal(vs, ovs.view(sv)), "V scales differ"
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
 def test_append_matches_oracle_bit_exactly(kv_dtype):
     case = inputs.small("append", len(RAGGED), RAGGED, kv_dtype=kv_dtype, seed=61)
     step = inputs.append_step(case, seed=62, inactive_every=5)
@@ -74,7 +75,7 @@ def test_append_matches_oracle_bit_exactly(kv_dtype):
     assert_pools_equal(gpu_append(case, step), want)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
 def test_append_every_row_kind_many_times(kv_dtype):
     # 8 row kinds x 40 sequences each, every slot position of a page
     lens = [1 + (7 * b) % 256 for b in range(320)]
@@ -87,6 +88,12 @@ def test_append_full_size_fp8_batch():
     w = inputs.WORKLOADS["b128_l4096_fp8"]
     case = inputs.generate(w)                      # 4096 tokens: the new one at 4095
     step = inputs.append_step(case, seed=65)
+    assert_pools_equal(gpu_append(case, step), oracle_append(case, step))
+
+
+def test_append_full_size_mxfp4_batch():
+    case = inputs.generate(inputs.WORKLOADS["b128_l4096_mxfp4"])
+    step = inputs.append_step(case, seed=75)
     assert_pools_equal(gpu_append(case, step), oracle_append(case, step))
 
 
@@ -115,7 +122,7 @@ def test_append_without_new_tokens_changes_nothing():
                              case.k_scale.numpy(), case.v_scale.numpy()))
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
 @pytest.mark.parametrize("flags", [0, mfa.MFA_PLAN_EARLY_METADATA])
 def test_append_then_decode_sees_the_new_token(kv_dtype, flags):
     """One decode step: append (a programmatic dependent launch) then decode, one stream."""
@@ -152,7 +159,7 @@ def test_append_then_decode_sees_the_new_token(kv_dtype, flags):
 
 
 @pytest.mark.parametrize("T", [2, 3])
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
 def test_append_of_several_tokens_matches_oracle(T, kv_dtype):
     """Multi-token step: T new rows per sequence at positions[b] .. positions[b] + T - 1, some
     across a page boundary, some sequences too short to hold T (skipped)."""
@@ -164,7 +171,7 @@ def test_append_of_several_tokens_matches_oracle(T, kv_dtype):
     assert_pools_equal(gpu_append(case, step, tokens_per_seq=T), want)
 
 
-@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
 def test_multi_token_append_then_decode(kv_dtype):
     """A multi-token step on one stream: append the T new rows, then decode the T query tokens
     (causal among them), against the oracle's decode over the oracle-appended cache."""

@@ -37,7 +37,7 @@ def shape_of(w):
 def gpu_decode(case, force_ctas=0, flags=mfa.MFA_PLAN_CHECK, stream=None, out_dtype=mfa.MFA_OUT_FP32):
     t = to_dev(case)
     w = case.workload
-    kv = mfa.MFA_KV_FP8_E4M3 if w.kv_dtype == "fp8_e4m3" else mfa.MFA_KV_BF16
+    kv = mfa.KV_DTYPES[w.kv_dtype]
     dec = mfa.Decoder(case.seq_lens.shape[0],
                       case.max_pages, case.num_blocks, kv_dtype=kv,
                       softmax_scale=w.scale(), host_seq_lens=case.seq_lens.tolist(),
@@ -211,7 +211,7 @@ def test_bad_block_id_is_reported_not_faulted():
     assert e.value.status == mfa.MFA_ERR_DEVICE_CHECK
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3", "mxfp4"])
 @pytest.mark.parametrize("bad_id", [-3, 10 ** 6])
 def test_bad_block_id_reads_as_a_page_of_zeros(kv, bad_id):
     """A block id outside the pool is reported, and its page contributes zero keys and zero
@@ -224,14 +224,18 @@ def test_bad_block_id_reads_as_a_page_of_zeros(kv, bad_id):
     zero_k = torch.zeros((1,) + tuple(ref_case.k_cache.shape[1:]), dtype=ref_case.k_cache.dtype)
     ref_case.k_cache = torch.cat([ref_case.k_cache, zero_k]).contiguous()
     ref_case.v_cache = torch.cat([ref_case.v_cache, zero_k.clone()]).contiguous()
-    if ref_case.k_scale is not None:
+    if ref_case.k_scale is not None and kv == "mxfp4":
+        one = torch.full((1,) + tuple(ref_case.k_scale.shape[1:]), 127, dtype=torch.uint8)   # E8M0 1.0
+        ref_case.k_scale = torch.cat([ref_case.k_scale, one]).contiguous()
+        ref_case.v_scale = torch.cat([ref_case.v_scale, one.clone()]).contiguous()
+    elif ref_case.k_scale is not None:
         one = torch.ones((1, ref_case.k_scale.shape[1]), dtype=torch.float32)
         ref_case.k_scale = torch.cat([ref_case.k_scale, one]).contiguous()
         ref_case.v_scale = torch.cat([ref_case.v_scale, one.clone()]).contiguous()
     ref_case.block_table[1, 2] = nb
     out, lse, dec = gpu_decode(case, flags=0)
     assert mfa.mfa_read_device_status(dec.workspace) == mfa.MFA_DEV_BAD_BLOCK
-    lim = (3e-2, 1.5e-2) if kv == "fp8_e4m3" else (BF16_MAX_ABS, BF16_REL_L2)
+    lim = (BF16_MAX_ABS, BF16_REL_L2) if kv == "bf16" else (3e-2, 1.5e-2)
     check_parity(case, out, lse, *lim, ref=oracle.decode(ref_case))
 
 
