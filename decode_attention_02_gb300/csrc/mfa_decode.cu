@@ -647,6 +647,25 @@ __device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v) {
   return is_v ? (t + 1 < ntiles ? 2u * U * t + 2u * U : 2u * U * t + U) : (t == 0 ? 0u : 2u * U * t - U);
 }
 
+// The e4m3 operand slots (e4m3 and MXFP4 caches) form two sub-rings: K in slots 0..7 (two
+// tiles), V in slots 8..kSlots-1 (e4m3: three tiles, MXFP4: two).  Each stream's uses only
+// follow its own earlier uses, so V is issued as soon as PV has released V slots, not when
+// QK^T frees K's (V's late arrival bound the e4m3 tile period), and a stream's waiter can
+// never be a phase behind (no ring-order counts).  Use u = 4 t + c of tile t: K use c = page
+// c & 1, d-half c >> 1 (a d-half's two pages in adjacent slots, one 128-row MMA operand); V
+// use c = page c >> 1, d-half c & 1.
+constexpr uint32_t kKSub = 8;
+template <int kSlots>
+constexpr uint32_t kVSub = kSlots > static_cast<int>(kKSub) ? kSlots - kKSub : 1u;   // (only e4m3 rings use it)
+template <int kSlots>
+__device__ __forceinline__ uint32_t sub_slot(uint32_t u, bool is_v) {
+  return is_v ? kKSub + u % kVSub<kSlots> : u % kKSub;
+}
+template <int kSlots>
+__device__ __forceinline__ uint32_t sub_phase(uint32_t u, bool is_v) {
+  return (is_v ? u / kVSub<kSlots> : u / kKSub) & 1u;
+}
+
 // kFp8: both contractions on e4m3 operands (an e4m3 cache, or an MXFP4 cache converted to
 // e4m3 on chip: kMx).
 template <bool kFp8, int kShp, bool kMx = false>
@@ -906,9 +925,8 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       int sq = 0, nq = 0;                 // next segment whose q is loaded; q loads issued
       uint32_t mine[3] = {0u, 0u, 0u};    // this lane's last three uses (drain after an abort)
       int nmine = 0;
-      // lane c: use c of the group (bf16 K: 64-element chunk c of both pages; bf16 V: page
-      // c / kVBlocks, 128-element block c % kVBlocks; e4m3 K: page c & 1, d-half c >> 1; e4m3
-      // V: page c >> 1, d-half c & 1)
+      // (one ring, bf16) lane c: use c of the group (K: 64-element chunk c of both pages; V:
+      // page c / kVBlocks, 128-element block c % kVBlocks); the e4m3 path has its own loop below
       const int reads = p.tokens * p.units;   // units that read one sequence's pages
       auto group = [&](bool is_v, int t) -> bool {
         bool okl = true;
@@ -951,20 +969,16 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
             const uint32_t dst = sbase + kOffRing + slot * kSlotBytes;
             const uint32_t fb = bar(kBarFull + slot);
             const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-            if (!kFp8 && !is_v) {
+            if (!is_v) {
               mbar_arrive_expect_tx(fb, ti.w > 0 ? 16384 : 8192);
               tma_load_3d_hint(dst, map, fb, 64 * c, ti.z - kPage, ti.x, pol);
               if (ti.w > 0) tma_load_3d_hint(dst + 8192, map, fb, 64 * c, ti.w - kPage, ti.y, pol);
             } else {
-              const int pg = kFp8 ? ((!is_v) ? (c & 1) : (c >> 1)) : c / kVBlocks;
-              const int dh = kFp8 ? ((!is_v) ? (c >> 1) : (c & 1)) : c % kVBlocks;
+              const int pg = c / kVBlocks, dh = c % kVBlocks;
               const int r = pg ? ti.w : ti.z;
               const int blk = pg ? ti.y : ti.x;
               if (r <= 0) {
                 mbar_arrive(fb);
-              } else if constexpr (kFp8) {
-                mbar_arrive_expect_tx(fb, 8192);
-                tma_load_3d_hint(dst, map, fb, 128 * dh, r - kPage, blk, pol);
               } else {
                 mbar_arrive_expect_tx(fb, 16384);
                 tma_load_3d_hint(dst, map, fb, 128 * dh, r - kPage, blk, pol);
@@ -977,6 +991,62 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         }
         return __all_sync(0xffffffffu, okl);
       };
+      if constexpr (kFp8 && !kMx) {
+        // e4m3: the K sub-ring by lanes 0..3 and the V sub-ring by lanes 4..7, each stream
+        // issued on its own as its slots free (one use a lane per tile: K use c = page c & 1,
+        // d-half c >> 1; V use c = page c >> 1, d-half c & 1).  Lane 0 also loads each
+        // segment's q, after its K use of the segment's first tile.
+        uint32_t mine_bar[3] = {0u, 0u, 0u}, mine_par[3] = {0u, 0u, 0u};
+        bool okl = true;
+        if (lane < 8) {
+          const bool is_v = lane >= 4;
+          const int cc = lane & 3;
+          const int pg = is_v ? (cc >> 1) : (cc & 1);
+          const int dh = is_v ? (cc & 1) : (cc >> 1);
+          int segl = 0;
+          for (int t = 0; t < ntiles && okl; ++t) {
+            while (segl + 1 < nseg && seg_n0[segl + 1] <= t) ++segl;
+            const uint64_t pol = (reads > 1 && seg[segl].x % reads != reads - 1) ? pol_again : pol_once;
+            const uint32_t u = 4u * t + cc;
+            const uint32_t slot = sub_slot<kNumSlots>(u, is_v);
+            okl = wait_bar(bar(kBarEmpty + slot), sub_phase<kNumSlots>(u, is_v) ^ 1, abort_flag);
+            if (!okl) break;
+            const int4 ti = tile_info[t];
+            const int r = pg ? ti.w : ti.z;
+            const int blk = pg ? ti.y : ti.x;
+            const uint32_t fb = bar(kBarFull + slot);
+            if (r <= 0) {
+              mbar_arrive(fb);
+            } else {
+              mbar_arrive_expect_tx(fb, 8192);
+              tma_load_3d_hint(sbase + kOffRing + slot * kSlotBytes, is_v ? &p.tm_v : &p.tm_k, fb, 128 * dh, r - kPage,
+                               blk, pol);
+            }
+            mine_bar[nmine % 3] = kBarFull + slot;
+            mine_par[nmine % 3] = sub_phase<kNumSlots>(u, is_v);
+            ++nmine;
+            if (lane == 0 && sq < nseg && t == seg_n0[sq]) {
+              if (sq > 0) okl = wait_bar(bar(kBarQEmpty), (sq - 1) & 1, abort_flag);
+              if (okl) {
+                mbar_arrive_expect_tx(bar(kBarQFull), 4 * 8192);
+                for (int q = 0; q < 4; ++q)
+                  tma_load_2d(sbase + kOffQ + q * 8192, &p.tm_q, bar(kBarQFull), 64 * q, kH * seg[sq].x);
+                ++nq;
+                if (sq + 1 < nseg)
+                  for (int q = 0; q < 4; ++q) tma_prefetch_2d(&p.tm_q, 64 * q, kH * seg[sq + 1].x);
+              }
+              ++sq;
+            }
+          }
+        }
+        ok = __all_sync(0xffffffffu, okl);
+        if (!ok) {
+          if (lane == 0) atomicOr(p.status, MFA_DEV_TIMEOUT);
+          // let every copy already issued land before the CTA can exit
+          for (int i = 0; i < (nmine < 3 ? nmine : 3); ++i) wait_slow(bar(mine_bar[i]), mine_par[i], nullptr, kDrainLimitNs);
+          if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
+        }
+      } else {
       for (int n = 0; n <= ntiles && ok; ++n) {
         if (n < ntiles) {
           if (ok) ok = group(false, n);
@@ -1012,6 +1082,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
             wait_slow(bar(kDrainBar0 + mine[i] % kDrainSlots), (mine[i] / kDrainSlots) & 1, nullptr, kDrainLimitNs);
         if (lane == 0 && nq > 0) wait_slow(bar(kBarQFull), (nq - 1) & 1, nullptr, kDrainLimitNs);
       }
+      }
     }
   } else if (warp == 1 || warp == pv_warp<kMx>()) {
     if constexpr (kMx) reg_dealloc<kRegsCtl>();
@@ -1034,9 +1105,9 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         if (n < ntiles && warp == 1) {
           const int4 sg = seg[sk];
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
-          const uint32_t u0 = ring_use<kKU>(n, ntiles, false);
-          // some slots of tile n's K last held an earlier tile's V: it must have landed
-          const int nv = k_needs_v<kKU, kNumSlots>(n);
+          const uint32_t u0 = kFp8 ? 4u * n : ring_use<kKU>(n, ntiles, false);
+          // (one ring) some slots of tile n's K last held an earlier tile's V: it must have landed
+          const int nv = kFp8 ? 0 : k_needs_v<kKU, kNumSlots>(n);
           if (nv > 0) ok = wait_count(cnt + 1, nv, abort_flag) && wait_count(cnt + 2, nv, abort_flag);
           if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
@@ -1070,17 +1141,18 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
 #pragma unroll
             for (int dh = 0; dh < 2; ++dh) {
               for (int c = 2 * dh; c < 2 * dh + 2 && ok; ++c)
-                ok = wait_bar(bar(kBarFull + (u0 + c) % kNumSlots), ((u0 + c) / kNumSlots) & 1, abort_flag);
+                ok = wait_bar(bar(kBarFull + sub_slot<kNumSlots>(u0 + c, false)), sub_phase<kNumSlots>(u0 + c, false),
+                              abort_flag);
               if (!ok) break;
               tc_fence_after();
-              const uint32_t a0 = sbase + kOffRing + ((u0 + 2 * dh) % kNumSlots) * kSlotBytes;
+              const uint32_t a0 = sbase + kOffRing + sub_slot<kNumSlots>(u0 + 2 * dh, false) * kSlotBytes;
               const uint32_t b0 = sbase + kOffQ + dh * 16384;
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
                 umma_f8_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
                            kIdescQK8, (dh | kk) != 0);
-              umma_commit(bar(kBarEmpty + (u0 + 2 * dh) % kNumSlots));
-              umma_commit(bar(kBarEmpty + (u0 + 2 * dh + 1) % kNumSlots));
+              umma_commit(bar(kBarEmpty + sub_slot<kNumSlots>(u0 + 2 * dh, false)));
+              umma_commit(bar(kBarEmpty + sub_slot<kNumSlots>(u0 + 2 * dh + 1, false)));
             }
             if (!ok) break;
           }
@@ -1097,12 +1169,12 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           constexpr int kBlocksPerPage = kFp8 ? 2 : kVBlocks;
           const int kb = sv % kOBufs;
           const int4 ti = tile_info[m];
-          const uint32_t uv = ring_use<kKU>(m, ntiles, true);
+          const uint32_t uv = kFp8 ? 4u * m : ring_use<kKU>(m, ntiles, true);
           ok = wait_bar(bar(kBarPFull), m & 1, abort_flag);
           if (ok && first && sv >= kOBufs)
             ok = wait_bar(bar(kBarOEmpty + kb), ((sv / kOBufs) - 1) & 1, abort_flag);
           // some slots of tile m's V last held a later tile's K (small rings): it must have landed
-          const int nk = v_needs_k<kKU, kNumSlots>(m, ntiles);
+          const int nk = kFp8 ? 0 : v_needs_k<kKU, kNumSlots>(m, ntiles);
           if (ok && nk > m + 1) ok = wait_count(cnt, nk, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -1110,10 +1182,11 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
             const int r = pg ? ti.w : ti.z;
             for (int hh = 0; hh < kBlocksPerPage; ++hh) {
               const uint32_t u = uv + kBlocksPerPage * pg + hh;
-              ok = wait_bar(bar(kBarFull + u % kNumSlots), (u / kNumSlots) & 1, abort_flag);
+              const uint32_t vslot = kFp8 ? sub_slot<kNumSlots>(u, true) : u % kNumSlots;
+              ok = wait_bar(bar(kBarFull + vslot), kFp8 ? sub_phase<kNumSlots>(u, true) : (u / kNumSlots) & 1, abort_flag);
               if (!ok) break;
               tc_fence_after();
-              const uint32_t a0 = sbase + kOffRing + (u % kNumSlots) * kSlotBytes;
+              const uint32_t a0 = sbase + kOffRing + vslot * kSlotBytes;
               // block hh: O^T lanes d of 128-element block hh; with grouped heads it is key
               // head hh's value, for its 16 query heads only (columns 16 hh .., P columns 16 hh ..)
               const uint32_t d_tmem = tmem + tmem_o<kFp8>() + 64u * (kFp8 ? 2 : Sh::kOBlocks) * kb +
@@ -1141,7 +1214,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
                   }
                 }
               }
-              umma_commit(bar(kBarEmpty + u % kNumSlots));
+              umma_commit(bar(kBarEmpty + vslot));
             }
           }
           if (!ok) break;
@@ -1176,11 +1249,11 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       auto page = [&](bool is_v, int t, int pg) -> bool {
         const uint32_t su = ring_use<2>(t, ntiles, is_v) + pg;
         const uint32_t ss = su % Lay::kStageSlots;
-        // the e4m3 use: K group use c = 2 dh + pg (page c & 1, d-half c >> 1), V c = 2 pg + dh
-        const uint32_t u = ring_use<kKU>(t, ntiles, is_v) + (is_v ? 2 * pg + dh : 2 * dh + pg);
-        const uint32_t slot = u % kNumSlots;
+        // the e4m3 use: K use c = 2 dh + pg (page c & 1, d-half c >> 1), V c = 2 pg + dh
+        const uint32_t u = 4u * t + (is_v ? 2 * pg + dh : 2 * dh + pg);
+        const uint32_t slot = sub_slot<kNumSlots>(u, is_v);
         if (!wait_warp(bar(kBarFull + kNumSlots + ss), (su / Lay::kStageSlots) & 1, abort_flag)) return false;
-        if (!wait_warp(bar(kBarEmpty + slot), ((u / kNumSlots) & 1) ^ 1, abort_flag)) return false;
+        if (!wait_warp(bar(kBarEmpty + slot), sub_phase<kNumSlots>(u, is_v) ^ 1, abort_flag)) return false;
         const int4 ti = tile_info[t];
         const int r = pg ? ti.w : ti.z;
         const int blk = pg ? ti.y : ti.x;
