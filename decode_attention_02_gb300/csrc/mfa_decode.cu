@@ -244,10 +244,10 @@ enum Bar : int {
 static_assert(kBarCount * 8 <= kOffCnt - kOffBar, "barrier area (the ring-order counts follow it)");
 
 // Tensor-memory columns.
-constexpr uint32_t kTmemS = 0;     // S^T buffers: bf16 [0,64) and [64,128); e4m3 [0,128) and
-                                   // [128,256) (64 columns of hi-part scores, then 64 of lo)
+constexpr uint32_t kTmemS = 0;     // S^T buffers [0,64) and [64,128) (e4m3: the hi-part and
+                                   // lo-part products of q summed by the tensor core)
 template <bool kFp8>
-__host__ __device__ constexpr uint32_t s_cols() { return kFp8 ? 128u : 64u; }
+__host__ __device__ constexpr uint32_t s_cols() { return 64u; }
 // O^T buffer k, block j: + 64 kOBlocks k + 64 j (MFA: d-halves; MLA: four 128-d blocks; GQA:
 // one block whose columns 16 g .. 16 g + 15 hold the heads of key/value head g)
 template <bool kFp8>
@@ -1095,7 +1095,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
     if (lane == 0 && ntiles > 0) {
       // N = the query heads that share one key/value head (64; GQA: 16, one MMA per group)
       constexpr uint32_t kIdescQK = idesc_f16(!kFp8, false, false, 128, kNh);
-      constexpr uint32_t kIdescQK8 = idesc_e4m3(false, false, 128, 128);
+      constexpr uint32_t kIdescQK8 = idesc_e4m3(false, false, 128, 64);
       constexpr uint32_t kIdescPV = idesc_f16(!kFp8, true, true, 128, kNh);
       constexpr uint32_t kIdescPV8 = idesc_e4m3(true, true, 128, 64);
       constexpr int kChunksPerHead = Sh::kDq / 64;   // 64-element K chunks of one key head
@@ -1136,8 +1136,9 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
             if (!ok) break;
           } else {
             // e4m3 K boxes as TMA wrote them: the two pages of d-half dh are adjacent slots,
-            // one 128-row A operand; B stacks q's e4m3 hi part (rows 0..63) over its lo part
-            // (rows 64..127), so each K step (32) reads K once for both
+            // one 128-row A operand; per K step (32) one N = 64 MMA against q's e4m3 hi part
+            // (rows 0..63 of the q tile) and one against its lo part (rows 64..127), into the
+            // same accumulator, so the scores arrive summed
 #pragma unroll
             for (int dh = 0; dh < 2; ++dh) {
               for (int c = 2 * dh; c < 2 * dh + 2 && ok; ++c)
@@ -1148,9 +1149,11 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
               const uint32_t a0 = sbase + kOffRing + sub_slot<kNumSlots>(u0 + 2 * dh, false) * kSlotBytes;
               const uint32_t b0 = sbase + kOffQ + dh * 16384;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                umma_f8_ss(d_tmem, smem_desc(a0 + 32 * kk, 16, 1024), smem_desc(b0 + 32 * kk, 16, 1024),
-                           kIdescQK8, (dh | kk) != 0);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = smem_desc(a0 + 32 * kk, 16, 1024);
+                umma_f8_ss(d_tmem, ad, smem_desc(b0 + 32 * kk, 16, 1024), kIdescQK8, (dh | kk) != 0);
+                umma_f8_ss(d_tmem, ad, smem_desc(b0 + 8192 + 32 * kk, 16, 1024), kIdescQK8, 1u);
+              }
               umma_commit(bar(kBarEmpty + sub_slot<kNumSlots>(u0 + 2 * dh, false)));
               umma_commit(bar(kBarEmpty + sub_slot<kNumSlots>(u0 + 2 * dh + 1, false)));
             }
@@ -1453,20 +1456,10 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       return true;
     };
 
-    // 32 scores of this thread's row (token) for its heads: e4m3 adds the hi-part and the
-    // lo-part columns of S^T (the two halves of the N = 128 QK^T result)
+    // 32 scores of this thread's row (token) for its heads
     auto ld_s32 = [&](uint32_t taddr, uint32_t (&sv)[32]) {
       tmem_ld32(taddr, sv);
-      if constexpr (kFp8) {
-        uint32_t sl[32];
-        tmem_ld32(taddr + 64, sl);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(sl);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) sv[h] = __float_as_uint(__uint_as_float(sv[h]) + __uint_as_float(sl[h]));
-      } else {
-        tmem_ld_wait(sv);
-      }
+      tmem_ld_wait(sv);
     };
 
     // e4m3: q of segment sidx arrives in bf16 and is split in place into two e4m3 parts,
@@ -1678,13 +1671,10 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           uint32_t lv[16], lx[16], sf[16];
           const uint32_t* sv = sc + 16 * half;
           if constexpr (kFp8) {
-            // hi-part and lo-part scores, summed
+            // (read again: the row sums of e4m3 live in registers, which leaves no room to keep
+            // the scores across the vote)
             tmem_ld16(s_tmem + 16 * half, sf);
-            tmem_ld16(s_tmem + 64 + 16 * half, lv);
             tmem_ld_wait(sf);
-            tmem_ld_wait(lv);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sf[e] = __float_as_uint(__uint_as_float(sf[e]) + __uint_as_float(lv[e]));
             sv = sf;
           }
           if (!kFp8 && !first) {
