@@ -576,19 +576,26 @@ __device__ __forceinline__ int mx_ref_exp(uint2 s8) {
   const uint32_t m2 = max(max(m & 0xFFu, (m >> 8) & 0xFFu), max((m >> 16) & 0xFFu, m >> 24));
   return max(static_cast<int>(m2) - 6, 1);
 }
-__device__ __forceinline__ float mx_token_scale(const uint8_t* __restrict__ sc, const int4 ti, int pg, int ri) {
-  const int r = pg ? ti.w : ti.z;
-  const int blk = pg ? ti.y : ti.x;
-  if (r <= 0 || ri < kPage - r || blk < 0) return 0.f;
-  const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sc) + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
-  return __uint_as_float(static_cast<uint32_t>(mx_ref_exp(s8)) << 23);
+// A row's scale is loaded one tile ahead as raw bits (e4m3: the fp32 scale; MXFP4: the 8 scale
+// bytes, zeros for a row past the sequence end or outside the pool, which the softmax masks)
+// and turned into the fp32 scale only where it is used, so that no thread waits on the load.
+template <bool kMx>
+__device__ __forceinline__ uint2 kv_scale_raw(const void* sc, const int4 ti, int pg, int ri) {
+  if constexpr (kMx) {
+    const int r = pg ? ti.w : ti.z;
+    const int blk = pg ? ti.y : ti.x;
+    if (r <= 0 || ri < kPage - r || blk < 0) return make_uint2(0u, 0u);
+    return __ldg(reinterpret_cast<const uint2*>(sc) + static_cast<size_t>(blk) * kPage + ri - (kPage - r));
+  } else {
+    return make_uint2(__float_as_uint(token_scale(static_cast<const float*>(sc), ti, pg, ri)), 0u);
+  }
 }
 template <bool kMx>
-__device__ __forceinline__ float kv_token_scale(const void* sc, const int4 ti, int pg, int ri) {
+__device__ __forceinline__ float kv_scale_of(uint2 raw) {
   if constexpr (kMx)
-    return mx_token_scale(static_cast<const uint8_t*>(sc), ti, pg, ri);
+    return __uint_as_float(static_cast<uint32_t>(mx_ref_exp(raw)) << 23);
   else
-    return token_scale(static_cast<const float*>(sc), ti, pg, ri);
+    return __uint_as_float(raw.x);
 }
 
 // MXFP4 -> e4m3 for one 32-element block: w holds the block's 32 E2M1 codes (element 2i in
@@ -1520,12 +1527,13 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       mbar_arrive(bar(kBarQReady));
     };
 
-    float sk_next = 0.f, sv_next = 0.f;            // e4m3: K and V scales of this row in the next tile
+    uint2 sk_next = make_uint2(0u, 0u), sv_next = make_uint2(0u, 0u);   // e4m3: the row's K and V
+                                                                        // scales in the next tile
     int e_ref = kEMin;                              // e4m3: the segment's reference exponent of V scales
     if constexpr (kFp8) {
       if (ntiles > 0) {
-        sk_next = kv_token_scale<kMx>(p.k_scale, tile_info[0], rpg, ri);
-        sv_next = kv_token_scale<kMx>(p.v_scale, tile_info[0], rpg, ri);
+        sk_next = kv_scale_raw<kMx>(p.k_scale, tile_info[0], rpg, ri);
+        sv_next = kv_scale_raw<kMx>(p.v_scale, tile_info[0], rpg, ri);
         convert_q(0);
       }
     }
@@ -1558,11 +1566,11 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         float ck = c, svt = 0.f;
         int sv_e = kEMin;   // e4m3: unbiased exponent of the token's V scale
         if constexpr (kFp8) {
-          ck = c * qinv * sk_next;                 // loaded one tile ahead
-          svt = sv_next;
+          ck = c * qinv * kv_scale_of<kMx>(sk_next);   // loaded one tile ahead
+          svt = kv_scale_of<kMx>(sv_next);
           if (n + 1 < ntiles) {
-            sk_next = kv_token_scale<kMx>(p.k_scale, tile_info[n + 1], rpg, ri);
-            sv_next = kv_token_scale<kMx>(p.v_scale, tile_info[n + 1], rpg, ri);
+            sk_next = kv_scale_raw<kMx>(p.k_scale, tile_info[n + 1], rpg, ri);
+            sv_next = kv_scale_raw<kMx>(p.v_scale, tile_info[n + 1], rpg, ri);
           }
           sv_e = static_cast<int>((__float_as_uint(svt) >> 23) & 0xFFu) - 127;
         }
