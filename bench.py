@@ -21,8 +21,10 @@ roofline   : the decode kernel alone, algorithmic bytes per launch / its mean
              CUDA-event duration, against the measured HBM copy bandwidth.
 cpu_baseline: the fp64 CPU oracle on a bounded sample of the same workload.
 kv_append  : the KV-cache append kernel for the same batch (each sequence's new key
-             and value row, FP8-quantised for an e4m3 cache), alone, and the decode
-             step with the append chained in front of it.
+             and value row, quantised for an e4m3 or MXFP4 cache), alone; the decode step
+             with the append chained in front of it; and the same step through
+             mfa_decode_append_run, which appends inside the decode kernel for one new token
+             per sequence.
 
 --impl reference times the oracle itself (the reference arm) on the same
 workload, each step a bounded sample.
@@ -556,6 +558,15 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
         step(i)
 
     ms_step_append, _ = tm.graph_ms(append_and_step, steps)
+
+    # the same step through mfa_decode_append_run: one kernel launch for one new token per
+    # sequence (the CTA that reads a sequence's last page writes its new rows first)
+    def fused_step(i):
+        s = sets[i % nsets]
+        mfa.mfa_decode_append_run(dec.plan, dec.problem, s["q"], s["k"], s["v"], s["ks"], s["vs"], s["table"],
+                                  s["lens"], k_new, v_new, positions, out, lse, dec.workspace, None)
+
+    ms_step_fused, _ = tm.graph_ms(fused_step, steps)
     app_status = mfa.mfa_read_device_status(dec.workspace)
     if app_status != 0:
         raise RuntimeError(f"append + decode steps set device status bits {app_status:#x} on {w.name}")
@@ -575,6 +586,10 @@ def measure_workload(args, case, tm, world: int, steps: int, headline: bool):
         "bound": "latency: one dependent load chain (position, page id, row) per row",
         "ms_per_step_with_append": ms_step_append,
         "added_ms_per_step": ms_step_append - ms_step,
+        "ms_per_step_with_fused_append": ms_step_fused,
+        "added_ms_per_step_fused": ms_step_fused - ms_step,
+        "fused": "mfa_decode_append_run: " + ("one kernel (the append inside the decode)" if T == 1
+                                              else "the append kernel, then the decode"),
         "timing": "append alone: per-launch events behind a GPU sleep; with append: "
                   "K steps of append + decode + combine from one CUDA graph",
         "device_status": app_status}

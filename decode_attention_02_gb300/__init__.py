@@ -51,7 +51,8 @@ PAGE_SIZE = 64
 # Every symbol include/mfa.h declares.
 EXPORTED_SYMBOLS = ("mfa_decode_plan", "mfa_decode_run", "mfa_combine", "mfa_read_device_status",
                     "mfa_status_string", "mfa_abi_version", "mfa_last_cuda_error",
-                    "mfa_decode_run_static_workspace", "mfa_kv_append", "mfa_decode_run_host")
+                    "mfa_decode_run_static_workspace", "mfa_kv_append", "mfa_decode_run_host",
+                    "mfa_decode_append_run")
 
 # Size of the library's own scratch array used by mfa_decode_run_static_workspace.
 MFA_STATIC_WORKSPACE_BYTES = 24 * 1024 * 1024
@@ -121,6 +122,9 @@ def load_library(path: str = LIB_PATH):
     lib.mfa_decode_run_host.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P, P, P,
                                         P, P, P, P, P, P, P, P, P, P, ctypes.c_uint64, P]
     lib.mfa_decode_run_host.restype = ctypes.c_int
+    lib.mfa_decode_append_run.argtypes = [ctypes.POINTER(MfaPlan), ctypes.POINTER(MfaProblem), P, P, P, P, P, P, P,
+                                          P, P, P, P, P, P, ctypes.c_uint64, P]
+    lib.mfa_decode_append_run.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -202,6 +206,20 @@ def mfa_decode_run(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_sc
                             _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(out),
                             _ptr(lse), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "mfa_decode_run")
+
+
+def mfa_decode_append_run(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_scale, v_scale, block_table,
+                          seq_lens, k_new, v_new, positions, out, lse, workspace, stream=None,
+                          workspace_bytes: Optional[int] = None) -> None:
+    """mfa_kv_append then mfa_decode_run in one call (one kernel for one new token per sequence)."""
+    lib = load_library()
+    if workspace_bytes is None:
+        workspace_bytes = _nbytes(workspace)
+    st = lib.mfa_decode_append_run(ctypes.byref(plan), ctypes.byref(problem), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(k_scale), _ptr(v_scale), _ptr(block_table), _ptr(seq_lens), _ptr(k_new),
+                                   _ptr(v_new), _ptr(positions), _ptr(out), _ptr(lse), _ptr(workspace),
+                                   int(workspace_bytes), _stream(stream))
+    _check(st, "mfa_decode_append_run")
 
 
 def mfa_decode_run_static_workspace(plan: MfaPlan, problem: MfaProblem, q, k_cache, v_cache, k_scale, v_scale,

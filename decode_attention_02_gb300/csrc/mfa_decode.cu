@@ -64,6 +64,7 @@
 #include "mfa.h"
 #include "mfa_host.h"
 #include "ptx.cuh"
+#include "mfa_append_row.cuh"
 
 namespace mfa {
 
@@ -277,6 +278,16 @@ struct DecodeParams {
   float scale_log2;   // softmax_scale * log2(e)
   int tokens;         // new query tokens per sequence T
   int units;          // 64-head units per query token U: batch counts the B * T * U units
+  // fused KV append (one new token per sequence, MFA rows; k_new null: none): row b of k_new
+  // and v_new goes to slot positions[b] of sequence b, in the cache's format (kv_fmt)
+  const uint4* k_new;
+  const uint4* v_new;
+  const int32_t* positions;
+  void* k_cache_w;
+  void* v_cache_w;
+  void* k_scale_w;
+  void* v_scale_w;
+  int kv_fmt;
 };
 
 struct CombineParams {
@@ -673,6 +684,26 @@ __device__ __forceinline__ uint32_t sub_phase(uint32_t u, bool is_v) {
   return (is_v ? u / kVSub<kSlots> : u / kKSub) & 1u;
 }
 
+// Fused KV append of sequence b's new row at token t (a warp): the page id, then the K and V
+// rows in the cache's format.  A position past the block table or a page id outside the pool
+// is reported and the row is skipped, as by the append kernel.
+__device__ __noinline__ void fused_append_row(const DecodeParams& p, int b, int t, int lane) {
+  if (t >= p.max_pages * kPage) {
+    if (lane == 0 && p.status) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
+    return;
+  }
+  const int blk = p.block_table[static_cast<size_t>(b) * p.max_pages + t / kPage];
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (lane == 0 && p.status) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
+    return;
+  }
+  const size_t row = static_cast<size_t>(blk) * kPage + (t % kPage);
+  const uint4 xk = p.k_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
+  const uint4 xv = p.v_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
+  append_row_warp(p.kv_fmt, xk, lane, p.k_cache_w, p.k_scale_w, row);
+  append_row_warp(p.kv_fmt, xv, lane, p.v_cache_w, p.v_scale_w, row);
+}
+
 // kFp8: both contractions on e4m3 operands (an e4m3 cache, or an MXFP4 cache converted to
 // e4m3 on chip: kMx).
 template <bool kFp8, int kShp, bool kMx = false>
@@ -907,6 +938,21 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
     }
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
   }
+  // ---------------- fused KV append, rows this CTA reads: a sequence's new row at token t <
+  // its visible length is written by the CTA that owns tile t / 128 (one segment holds it),
+  // before any of that CTA's loads.  Warp w takes segments w, w + warps, ...  The rows are
+  // fenced to the async proxy, which reads them (TMA), and the block barrier below orders
+  // them before the other warps' loads of the per-row scales.  (Rows past the visible length
+  // are read by nobody this step; the PV warp writes those.)
+  if (p.k_new != nullptr && nseg > 0) {
+    grid_dep_wait();   // the new rows (and the cache) may come from the preceding kernel
+    for (int s = warp; s < nseg; s += kThreads / 32) {
+      const int4 sg = seg[s];
+      const int t = p.positions[sg.x];
+      if (t >= 0 && t < sg.w && t >= kTile * sg.y && t < kTile * sg.z) fused_append_row(p, sg.x, t, lane);
+    }
+    fence_proxy_async_global();
+  }
   __syncthreads();
 
   // MXFP4 warpgroup register split (see threads_of), at the top of each role so that the
@@ -1093,6 +1139,17 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
     }
   } else if (warp == 1 || warp == pv_warp<kMx>()) {
     if constexpr (kMx) reg_dealloc<kRegsCtl>();
+    if (warp == pv_warp<kMx>() && p.k_new != nullptr) {
+      // fused KV append, rows nobody reads this step (token at or past the visible length,
+      // including sequences without tokens): sequence b's by CTA b mod G, before its PVs
+      grid_dep_wait();
+      for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+        const int t = p.positions[b];
+        bool dummy = false;
+        if (t >= 0 && t >= vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy))
+          fused_append_row(p, b, t, lane);
+      }
+    }
     // ---------------- MMA issuers: QK^T of tile n, then PV of tile n - 1, so the next tile's
     // scores are computed while the softmax works on the current one.  Warp 1 issues the
     // QK^T stream and warp pv_warp the PV stream (they share no operand, accumulator or
@@ -2625,14 +2682,21 @@ static mfa_status check_run(const mfa_plan* plan, const mfa_problem* pr, const v
   return MFA_OK;
 }
 
-mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
-                          const void* v_cache, const void* k_scale, const void* v_scale,
-                          const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
-                          void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
-  mfa_status st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse,
-                            workspace, workspace_bytes);
-  if (st != MFA_OK || pr->batch == 0) return st;
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+// The fused KV append's arguments (see mfa_decode_append_run); null: a plain decode step.
+struct FusedAppend {
+  const void* k_new;
+  const void* v_new;
+  const int32_t* positions;
+};
+
+// One decode step after validation: the decode kernel (with the fused append, if given), the
+// combine, and the MFA_PLAN_CHECK read-back.  clear_status: clear the status word first (the
+// two-kernel append path clears it before its append kernel instead).
+static mfa_status decode_step(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
+                              const void* v_cache, const void* k_scale, const void* v_scale,
+                              const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
+                              void* workspace, cudaStream_t stream, const FusedAppend* app, bool clear_status) {
+  mfa_status st = MFA_OK;
 
   DecodeParams prm;
   std::memset(&prm, 0, sizeof(prm));
@@ -2656,10 +2720,20 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
   prm.num_blocks = pr->num_blocks;
   prm.scale_log2 = static_cast<float>(static_cast<double>(pr->softmax_scale) * 1.4426950408889634);
   prm.early_metadata = (plan->flags & MFA_PLAN_EARLY_METADATA) ? 1 : 0;
+  if (app != nullptr) {
+    prm.k_new = static_cast<const uint4*>(app->k_new);
+    prm.v_new = static_cast<const uint4*>(app->v_new);
+    prm.positions = app->positions;
+    prm.k_cache_w = const_cast<void*>(k_cache);
+    prm.v_cache_w = const_cast<void*>(v_cache);
+    prm.k_scale_w = const_cast<void*>(k_scale);
+    prm.v_scale_w = const_cast<void*>(v_scale);
+    prm.kv_fmt = pr->kv_dtype;
+  }
 
   const bool check = (plan->flags & MFA_PLAN_CHECK) != 0;
   cudaError_t e = cudaSuccess;
-  if (check && (e = cudaMemsetAsync(ws, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
+  if (check && clear_status && (e = cudaMemsetAsync(ws, 0, 4, stream)) != cudaSuccess) return cuda_fail(e, "memset");
   const int kidx = kernel_index(pr);
   st = ensure_smem_attribute(kidx);
   if (st != MFA_OK) return st;
@@ -2686,6 +2760,48 @@ mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const voi
     if (word != 0) return MFA_ERR_DEVICE_CHECK;
   }
   return MFA_OK;
+}
+
+mfa_status mfa_decode_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, const void* k_cache,
+                          const void* v_cache, const void* k_scale, const void* v_scale,
+                          const int32_t* block_table, const int32_t* seq_lens, void* out, float* lse,
+                          void* workspace, uint64_t workspace_bytes, void* stream_ptr) {
+  mfa_status st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse,
+                            workspace, workspace_bytes);
+  if (st != MFA_OK || pr->batch == 0) return st;
+  return decode_step(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse, workspace,
+                     static_cast<cudaStream_t>(stream_ptr), nullptr, true);
+}
+
+mfa_status mfa_decode_append_run(const mfa_plan* plan, const mfa_problem* pr, const void* q, void* k_cache,
+                                 void* v_cache, void* k_scale, void* v_scale, const int32_t* block_table,
+                                 const int32_t* seq_lens, const void* k_new, const void* v_new,
+                                 const int32_t* positions, void* out, float* lse, void* workspace,
+                                 uint64_t workspace_bytes, void* stream_ptr) {
+  mfa_status st = check_run(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse,
+                            workspace, workspace_bytes);
+  if (st != MFA_OK) return st;
+  if (problem_shape(pr) != kShapeMfa) return MFA_ERR_UNSUPPORTED;   // the append writes MFA rows
+  if (pr->batch == 0) return MFA_OK;
+  if (!k_new || !v_new || !positions || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(positions, 4))
+    return MFA_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (pr->tokens_per_seq == 1) {
+    const FusedAppend app{k_new, v_new, positions};
+    return decode_step(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse, workspace,
+                       stream, &app, true);
+  }
+  // several new tokens per sequence: the rows of one sequence are read by several units (one
+  // per query token) on different CTAs, so the append kernel runs first
+  if ((plan->flags & MFA_PLAN_CHECK) != 0) {
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
+  }
+  st = mfa_kv_append(pr, k_new, v_new, positions, block_table, k_cache, v_cache, k_scale, v_scale,
+                     static_cast<uint32_t*>(workspace), stream_ptr);
+  if (st != MFA_OK) return st;
+  return decode_step(plan, pr, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, lse, workspace,
+                     stream, nullptr, false);
 }
 
 mfa_status mfa_decode_run_host(const mfa_plan* plan, const mfa_problem* pr, const void* q_host,

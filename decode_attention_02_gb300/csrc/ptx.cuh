@@ -175,6 +175,9 @@ __device__ __forceinline__ void bulk_store_s2g(void* gdst, uint32_t ssrc, uint32
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the source of every committed bulk group of this thread has been read.
+// Order this thread's generic-proxy global writes before later async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MFA_ABI_VERSION 4
+#define MFA_ABI_VERSION 5
 
 typedef enum mfa_status {
     MFA_OK = 0,
@@ -343,6 +343,30 @@ mfa_status mfa_kv_append(const mfa_problem* problem, const void* k_new, const vo
                          const int32_t* positions, const int32_t* block_table,
                          void* k_cache, void* v_cache, void* k_scale, void* v_scale,
                          uint32_t* device_status, void* stream);
+
+/*
+ * One decode step with the KV append in front of it: the same result as mfa_kv_append()
+ * (its status bits going to the workspace's status word) followed by mfa_decode_run() on the
+ * same stream, for the MFA shape.  With one new token per sequence it is one kernel launch:
+ * the CTA that reads the page of a sequence's new row writes that row first (the caches are
+ * written in place, in their format, as by mfa_kv_append), and rows whose position is at or
+ * past the sequence's length (read by nobody this step) are written too.  With several new
+ * tokens per sequence the append kernel runs first.
+ *   k_new, v_new : device bf16 [B, T, 256], 16-byte aligned.
+ *   positions    : device int32 [B], 4-byte aligned (as for mfa_kv_append).
+ *   k_cache .. k_scale, v_scale : written in place (the pools of mfa_decode_run).
+ *   Other arguments as for mfa_decode_run.  seq_lens are the lengths after the append (a
+ *   sequence whose new token is at position t has length t + T when it reads it).
+ * Every argument is validated before anything is enqueued; other shapes give
+ * MFA_ERR_UNSUPPORTED.
+ */
+mfa_status mfa_decode_append_run(const mfa_plan* plan, const mfa_problem* problem,
+                                 const void* q, void* k_cache, void* v_cache,
+                                 void* k_scale, void* v_scale,
+                                 const int32_t* block_table, const int32_t* seq_lens,
+                                 const void* k_new, const void* v_new, const int32_t* positions,
+                                 void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                                 void* stream);
 
 /* MFA_ABI_VERSION of the loaded library. */
 int32_t mfa_abi_version(void);

@@ -28,7 +28,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(mfa.EXPORTED_SYMBOLS)
     for n in names:
         assert hasattr(lib, n), f"{n} not exported"
-    assert lib.mfa_abi_version() == 4
+    assert lib.mfa_abi_version() == 5
 
 
 def test_status_strings(lib):
@@ -253,3 +253,26 @@ def test_run_host_validates_before_enqueuing_anything(lib):
     assert call(odd) == mfa.MFA_ERR_INVALID_ARG
     assert call(good, plan.workspace_bytes - 1) == mfa.MFA_ERR_WORKSPACE
     assert call(good, pr=problem(batch=5)) == mfa.MFA_ERR_INVALID_ARG
+
+
+def test_decode_append_run_validates_before_touching_the_device(lib):
+    """The fused append-and-decode entry point refuses bad arguments without enqueueing."""
+    prob = problem()
+    plan = mfa.mfa_decode_plan(prob, [10, 20, 30, 40], num_sms=8)
+    P = ctypes.c_void_p
+    base = [0x1000, 0x2000, 0x3000, None, None, 0x6000, 0x7000]   # q, k, v, ks, vs, table, lens
+    newp = [0xA000, 0xB000, 0xC000]                               # k_new, v_new, positions
+    tail = [0x8000, 0x9000, 0x10000]                               # out, lse, workspace
+
+    def call(pr, pl, b=base, n=newp):
+        return lib.mfa_decode_append_run(ctypes.byref(pl), ctypes.byref(pr), *[P(x) if x else None for x in b],
+                                         *[P(x) if x else None for x in n], P(tail[0]), P(tail[1]), P(tail[2]),
+                                         ctypes.c_uint64(pl.workspace_bytes), None)
+    for i in range(3):
+        bad = list(newp); bad[i] = None
+        assert call(prob, plan, n=bad) == mfa.MFA_ERR_INVALID_ARG
+    assert call(prob, plan, n=[0xA008, 0xB000, 0xC000]) == mfa.MFA_ERR_INVALID_ARG
+    assert call(prob, plan, n=[0xA000, 0xB000, 0xC002]) == mfa.MFA_ERR_INVALID_ARG
+    gqa = problem(head_dim=128, num_kv_heads=4)
+    gplan = mfa.mfa_decode_plan(gqa, [10, 20, 30, 40], num_sms=8)
+    assert call(gqa, gplan) == mfa.MFA_ERR_UNSUPPORTED

@@ -207,3 +207,95 @@ def test_multi_token_append_then_decode(kv_dtype):
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isneginf(lse.cpu().numpy()), np.isneginf(ref_lse))
     assert np.abs(lse.cpu().double().numpy()[fin] - ref_lse[fin]).max() <= 2e-3
+
+
+def _fused_step(case, step, flags=0, force_ctas=0, tokens_per_seq=1, positions=None):
+    """One mfa_decode_append_run on device copies of case: returns (caches, out, lse, dec)."""
+    dev = "cuda"
+    t = dict(q=case.q.to(dev), k=case.k_cache.to(dev), v=case.v_cache.to(dev), table=case.block_table.to(dev),
+             lens=case.seq_lens.to(dev), ks=None if case.k_scale is None else case.k_scale.to(dev),
+             vs=None if case.v_scale is None else case.v_scale.to(dev))
+    dec = mfa.Decoder(case.seq_lens.shape[0], case.max_pages, case.num_blocks, kv_dtype=kv_of(case),
+                      host_seq_lens=case.seq_lens.tolist(), flags=flags, force_ctas=force_ctas,
+                      out_dtype=mfa.MFA_OUT_FP32, tokens_per_seq=tokens_per_seq)
+    rows = case.q.shape[0]
+    out = torch.empty((rows, 64, 256), dtype=torch.float32, device=dev)
+    lse = torch.empty((rows, 64), dtype=torch.float32, device=dev)
+    pos = (step.positions if positions is None else positions).to(dev)
+    mfa.mfa_decode_append_run(dec.plan, dec.problem, t["q"], t["k"], t["v"], t["ks"], t["vs"], t["table"], t["lens"],
+                              step.k_new.to(dev), step.v_new.to(dev), pos, out, lse, dec.workspace)
+    torch.cuda.synchronize()
+    return (t["k"], t["v"], t["ks"], t["vs"]), out, lse, dec
+
+
+def _oracle_after_append(case, step, tokens_per_seq=1, positions=None):
+    kc, vc, ks, vs, mask = oracle_append(case, step, positions=positions, tokens_per_seq=tokens_per_seq)
+    appended = inputs.Case(workload=case.workload, q=case.q,
+                           k_cache=torch.from_numpy(kc).view(case.k_cache.dtype),
+                           v_cache=torch.from_numpy(vc).view(case.v_cache.dtype),
+                           k_scale=None if ks is None else torch.from_numpy(ks),
+                           v_scale=None if vs is None else torch.from_numpy(vs),
+                           block_table=case.block_table, seq_lens=case.seq_lens)
+    return (kc, vc, ks, vs, mask), oracle.decode(appended)
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
+@pytest.mark.parametrize("flags, force_ctas", [(0, 0), (mfa.MFA_PLAN_EARLY_METADATA, 0), (mfa.MFA_PLAN_CHECK, 7)])
+def test_fused_append_decode_matches_the_oracle(kv_dtype, flags, force_ctas):
+    """mfa_decode_append_run with one new token per sequence (one kernel): the caches equal the
+    oracle's append byte for byte, and the decode equals the oracle's over the appended cache.
+    Some sequences append no row (position -1); the others at their last position."""
+    case = inputs.small("fused", len(RAGGED), RAGGED, kv_dtype=kv_dtype, seed=80)
+    step = inputs.append_step(case, seed=81, inactive_every=5, kinds=("normal",))
+    want, (ref_o, ref_lse) = _oracle_after_append(case, step)
+    assert want[4] == 0
+    caches, out, lse, dec = _fused_step(case, step, flags=flags, force_ctas=force_ctas)
+    assert_pools_equal(caches, want)
+    assert mfa.mfa_read_device_status(dec.workspace) == 0
+    got = out.cpu().double().numpy()
+    tol = (1e-2, 5e-3) if kv_dtype == "bf16" else (3e-2, 1.5e-2)
+    assert np.abs(got - ref_o).max() <= tol[0]
+    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= tol[1]
+    assert np.abs(lse.cpu().double().numpy() - ref_lse).max() <= 2e-3
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3", "mxfp4"])
+def test_fused_append_writes_rows_past_the_length_and_reports_bad_ones(kv_dtype):
+    """Rows at or past a sequence's length (read by nobody this step) are written as well; a
+    position past the block table and a page id outside the pool are reported and skipped,
+    exactly as by the append kernel."""
+    case = inputs.small("fused_past", len(RAGGED), RAGGED, kv_dtype=kv_dtype, seed=82)
+    step = inputs.append_step(case, seed=83, kinds=("normal",))
+    pos = step.positions.clone()
+    lens = case.seq_lens
+    for b in (1, 4, 9):           # one past the last token, inside the same page
+        if int(lens[b]) % 64 != 0:
+            pos[b] = int(lens[b])
+    pos[6] = 64 * case.block_table.shape[1]          # past the table: BAD_LENGTH
+    table = case.block_table.clone()
+    table[11, int(pos[11]) // 64] = case.num_blocks   # outside the pool: BAD_BLOCK
+    bad = inputs.Case(workload=case.workload, q=case.q, k_cache=case.k_cache, v_cache=case.v_cache,
+                      k_scale=case.k_scale, v_scale=case.v_scale, block_table=table, seq_lens=case.seq_lens)
+    want, _ = _oracle_after_append(bad, step, positions=pos)
+    assert want[4] == oracle.APPEND_BAD_BLOCK | oracle.APPEND_BAD_POSITION
+    caches, out, lse, dec = _fused_step(bad, step, positions=pos)
+    assert_pools_equal(caches, want)
+    st = mfa.mfa_read_device_status(dec.workspace)
+    assert st & mfa.MFA_DEV_BAD_LENGTH and st & mfa.MFA_DEV_BAD_BLOCK
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_fused_append_with_several_tokens_runs_the_two_kernels(kv_dtype):
+    """T = 2: the append kernel first, then the decode; the same bytes and bits as the two
+    separate calls."""
+    T = 2
+    case = inputs.small("fused_t2", len(RAGGED), RAGGED, kv_dtype=kv_dtype, seed=84, tokens_per_seq=T)
+    step = inputs.append_step(case, seed=85, tokens_per_seq=T, kinds=("normal",))
+    caches, out, lse, dec = _fused_step(case, step, tokens_per_seq=T)
+    kc, vc, ks, vs = gpu_append(case, step, tokens_per_seq=T)
+    assert_pools_equal(caches, tuple(as_bits(x) for x in (kc, vc, ks, vs)) + (0,))
+    dev = "cuda"
+    out2, lse2 = dec(case.q.to(dev), kc, vc, case.block_table.to(dev), case.seq_lens.to(dev), k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int32), out.view(torch.int32))
+    assert torch.equal(lse2, lse)
