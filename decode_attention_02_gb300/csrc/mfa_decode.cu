@@ -161,27 +161,26 @@ constexpr int kOffBar = 212992;                              // mbarriers
 //   bf16: slots of 16 KB (a 64-element chunk of both pages of a tile for K; a 128-element
 //         block of one page for V), kRow / 64 uses per tile for each of K and V;
 //   e4m3: slots of 8 KB (one page's 128-element half row block), four uses each.
-//   MXFP4: the e4m3 ring shrinks to 16 slots, filled by the converter warps; after it, 4
-//          staging slots of 8 KB hold 4-bit pages as TMA writes them ([64 tokens][128 B] of
-//          E2M1 pairs, 128-byte swizzle), and their E8M0 scale bytes (512 B a page) sit past
-//          the metadata (kOffStageScale).  With 16 slots a tile's K and V uses reuse the slots
-//          of the tile two back, so converting V(n) never waits for QK^T(n).
+//   MXFP4: the e4m3 ring shrinks to 12 slots (K 8, V 4), filled by the converter warps; after
+//          it, 8 staging slots of 8 KB hold 4-bit pages as TMA writes them ([64 tokens][128 B]
+//          of E2M1 pairs, 128-byte swizzle), two tiles of loads in flight, and their E8M0 scale
+//          bytes (512 B a page) sit past the metadata (kOffStageScale).
 template <bool kFp8, int kShp, bool kMx = false>
 struct Layout {
   using Sh = ShapeOf<kShp>;
   static constexpr int kOffP = kFp8 ? 32768 : 64 * Sh::kDq * 2;
   static constexpr int kOffRing = kOffP + 16384;
   static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
-  static constexpr int kNumSlots = kMx ? 16 : (kOffBar - kOffRing) / kSlotBytes;
+  static constexpr int kNumSlots = kMx ? 12 : (kOffBar - kOffRing) / kSlotBytes;
   static constexpr int kKU = kFp8 ? 4 : Sh::kRow / 64;   // ring uses per K group and per V group
   static constexpr int kOffStage = kOffRing + kNumSlots * kSlotBytes;   // MXFP4 staging slots
-  static constexpr int kStageSlots = 4;
+  static constexpr int kStageSlots = 8;
   static constexpr int kStageBytes = 8192;
 };
-static_assert(Layout<true, kShapeMfa, true>::kOffStage + 4 * 8192 == kOffBar, "MXFP4 staging fills the ring area");
+static_assert(Layout<true, kShapeMfa, true>::kOffStage + 8 * 8192 == kOffBar, "MXFP4 staging fills the ring area");
 static_assert(Layout<true, kShapeMfa, true>::kNumSlots + Layout<true, kShapeMfa, true>::kStageSlots <= 20,
               "MXFP4: the e4m3 ring and the staging slots share the 20 Full/Empty barrier pairs");
-static_assert(Layout<true, kShapeMfa, true>::kNumSlots % 4 == 0, "MXFP4 e4m3 ring: groups must not wrap");
+static_assert(Layout<true, kShapeMfa, true>::kNumSlots >= 12, "MXFP4: a K sub-ring of 8 and a V sub-ring of 4 or more");
 static_assert(Layout<false, kShapeMfa>::kNumSlots == 10 && Layout<true, kShapeMfa>::kNumSlots == 20 &&
               Layout<false, kShapeGqa>::kNumSlots == 11 && Layout<false, kShapeMla>::kNumSlots == 8, "");
 static_assert(Layout<false, kShapeMla>::kNumSlots >= Layout<false, kShapeMla>::kKU, "a ring holds one group");
@@ -222,11 +221,11 @@ constexpr int kOffSeg = kOffLinv + 512;       // int4[kMaxSeg] {b, first tile, e
 constexpr int kOffSegN0 = kOffSeg + 16 * kMaxSeg;       // int[kMaxSeg] CTA-local index of first tile
 constexpr int kOffTileInfo = kOffSegN0 + 4 * kMaxSeg;   // int4[kMaxTilesPerCta] {page 0, page 1, rows 0, rows 1}
 constexpr int kSmemUsed = kOffTileInfo + 16 * kMaxTilesPerCta;
-constexpr int kOffStageScale = kSmemUsed;   // MXFP4: E8M0 bytes of the 4 staged pages, 512 B each
-constexpr int smem_bytes(bool mx) { return kSmemUsed + (mx ? 4 * 512 : 0) + 1024; }
+constexpr int kOffStageScale = kSmemUsed;   // MXFP4: E8M0 bytes of the 8 staged pages, 512 B each
+constexpr int smem_bytes(bool mx) { return kSmemUsed + (mx ? 8 * 512 : 0) + 1024; }
 static_assert(smem_bytes(true) <= 232448, "shared memory budget");
 
-// MXFP4 uses Full/Empty 0..15 for its e4m3 ring and 16..19 for the staging slots.
+// MXFP4 uses Full/Empty 0..11 for its e4m3 ring and 12..19 for the staging slots.
 enum Bar : int {
   kBarFull = 0,
   kBarEmpty = kBarFull + 20,   // room for the larger ring
