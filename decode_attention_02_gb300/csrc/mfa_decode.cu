@@ -199,20 +199,9 @@ constexpr int kOffMisc = kOffBar + 512;  // int: [0] tmem base [1] abort [2] nse
 // publishes how many tiles of its uses have landed -- cnt[0]: K tiles, by the QK^T issuer
 // after its Full waits; cnt[1], cnt[2]: V tiles (page 0 and page 1, written together), by
 // the PV issuer after its Full waits -- and waits on the other's count where the slot's
-// previous use is not already ordered before it (k_needs_v, v_needs_k: the counts follow from
-// the ring order; a PV of tile m follows K(m) through the softmax's P).
-template <int kKU, int kSlots>
-__device__ __forceinline__ int k_needs_v(int n) {
-  const int hi = (n == 0 ? 0 : 2 * kKU * n - kKU) + kKU - 1 - kSlots;   // last previous use
-  return hi >= 2 * kKU ? (hi - 2 * kKU) / (2 * kKU) + 1 : 0;
-}
-template <int kKU, int kSlots>
-__device__ __forceinline__ int v_needs_k(int m, int ntiles) {
-  const int base = (m + 1 < ntiles) ? 2 * kKU * m + 2 * kKU : 2 * kKU * m + kKU;
-  const int hi = base + kKU - 1 - kSlots;
-  return hi >= 0 ? (hi + kKU) / (2 * kKU) + 1 : 0;
-}
-constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1, spare
+// previous use is not already ordered before it (needs_other: the count is exact -- a larger
+// one could wait on a tile that itself waits for this stream's slots).
+constexpr int kOffCnt = kOffBar + 448;   // int[4]: K tiles, V tiles of page 0 and of page 1 (one ring), K tiles issued (e4m3)
 constexpr int kOffMref = kOffMisc + 128;      // float[64]  reference max per head (log2 domain)
 constexpr int kOffAlpha = kOffMref + 256;     // float[64]  rescale factor per head
 constexpr int kOffRed = kOffAlpha + 256;      // float[2][4][64] cross-warp reduction scratch
@@ -532,37 +521,22 @@ __device__ __forceinline__ uint32_t pack_e4m3_sat(float lo, float hi) {
   return r;
 }
 
-// Value of the e4m3 code in the low byte of b, exactly: the 7 magnitude bits placed at bit 20
-// of an fp32 word are the code's value times 2^-120 (subnormal codes included, as fp32
-// subnormals), so one multiply by 2^120 restores it; the sign bit moves to bit 31.
-__device__ __forceinline__ float e4m3_value(uint32_t b) {
-  return __uint_as_float(((b & 0x7Fu) << 20) | ((b & 0x80u) << 24)) * 0x1p120f;
-}
-
 // Split two scaled q values x into e4m3 pairs hi + lo with hi = e4m3(x) and lo = e4m3(x - hi).
 // x is a bf16 value times a power of two (8 significant bits) and the largest |x| of the
 // sequence lies in [64, 128).  x - hi is exact in fp32 and is k * ulp(x) with |k| <= 8, so
 // it fits e4m3's 4 significant bits: hi + lo = x exactly when ulp(x) >= 2^-9 (the e4m3
 // subnormal step), i.e. for |x| >= 2^-2, which covers every element at least 2^-9 of the
 // largest.  Smaller elements err by at most 2^-10, under 2^-16 of the largest.
-// (The hi part is read back through the f16 conversion rather than e4m3_value: the same
-// bits, but the slower read-back measured faster end to end -- finishing a segment's q split
-// earlier moves the CTAs' load streams into a worse phase.)
+// (The hi part is read back exactly through the f16 conversion.  A bit-placement read-back,
+// the 7 magnitude bits at bit 20 of an fp32 word times 2^120, gives the same bits, but the
+// conversion measured faster end to end -- finishing a segment's q split earlier moves the
+// CTAs' load streams into a worse phase.)
 __device__ __forceinline__ void split_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   hi = pack_e4m3_sat(x0, x1);
   uint32_t back;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(back) : "h"(static_cast<uint16_t>(hi)));
   lo = pack_e4m3_sat(x0 - __half2float(__ushort_as_half(static_cast<unsigned short>(back))),
                      x1 - __half2float(__ushort_as_half(static_cast<unsigned short>(back >> 16))));
-}
-
-// Split two PV weights x >= 0 (below 448) into e4m3 pairs hi + lo: hi = e4m3(x) rounded to
-// nearest, lo = e4m3(x - hi), hi read back exactly from its code.  x - hi is exact in fp32,
-// and hi + lo matches x to 2^-9 of x where lo is a normal e4m3 number (x above about 2^-1),
-// and to 2^-10 absolute below that.
-__device__ __forceinline__ void split_weights_e4m3(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_e4m3_sat(x0, x1);
-  lo = pack_e4m3_sat(x0 - e4m3_value(hi), x1 - e4m3_value(hi >> 8));
 }
 
 // e4m3: per-token scale of box row ri of page pg of tile `ti` ({page 0, page 1, rows 0,
@@ -655,13 +629,32 @@ __device__ __forceinline__ void mx_block_to_e4m3(const uint4 w, int D, uint4& ou
 // Ring use index of the first use of the K (is_v = false) or V group of tile t of a CTA with
 // `ntiles` tiles, kKU uses per group.  The producer issues K(0), then K(t) and V(t-1) for
 // t = 1..N-1, then V(N-1): K(0) = 0.., K(t) = 2 kKU t - kKU.., V(t) = 2 kKU t + 2 kKU.. except
-// the last tile's V, which directly follows its K: V(N-1) = 2 kKU N - kKU...  e4m3 (kKU = 4):
-// every group starts at a multiple of 4 and the ring has 20 slots, so a group never wraps and
-// K's two pages of one d-half sit in adjacent slots, one 128-row MMA operand.
+// the last tile's V, which directly follows its K: V(N-1) = 2 kKU N - kKU...
 template <int kKU>
 __device__ __forceinline__ uint32_t ring_use(int t, int ntiles, bool is_v) {
   constexpr uint32_t U = kKU;
   return is_v ? (t + 1 < ntiles ? 2u * U * t + 2u * U : 2u * U * t + U) : (t == 0 ? 0u : 2u * U * t - U);
+}
+// The inverse: the tile (and whether V) of the g-th group of uses in the producer's order.
+__device__ __forceinline__ int group_owner(int g, int ntiles, bool& is_v) {
+  is_v = (g & 1) == 0 ? g > 0 : (g + 1) / 2 >= ntiles;
+  return !is_v ? (g + 1) / 2 : ((g & 1) == 0 ? g / 2 - 1 : ntiles - 1);
+}
+// How many tiles of the other stream (V if want_v, else K) must have landed before the group
+// at ring use a may be waited on: the highest such tile among the previous uses of its slots,
+// plus one (zero if none).
+template <int kKU, int kSlots>
+__device__ __forceinline__ int needs_other(int a, int ntiles, bool want_v) {
+  const int hi = a + kKU - 1 - kSlots;
+  if (hi < 0) return 0;
+  int need = 0;
+#pragma unroll 1
+  for (int g = max(a - kSlots, 0) / kKU; g <= hi / kKU; ++g) {
+    bool v;
+    const int t = group_owner(g, ntiles, v);
+    if (v == want_v) need = max(need, t + 1);
+  }
+  return need;
 }
 
 // The e4m3 operand slots (e4m3 and MXFP4 caches) form two sub-rings: K in slots 0..7 (two
@@ -1059,6 +1052,13 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           for (int t = 0; t < ntiles && okl; ++t) {
             while (segl + 1 < nseg && seg_n0[segl + 1] <= t) ++segl;
             const uint64_t pol = (reads > 1 && seg[segl].x % reads != reads - 1) ? pol_again : pol_once;
+            // a V lane issues V(t) once lane 0 has issued K(t): at start-up, when every CTA
+            // fills its rings at once, the memory queue then holds K(0), V(0), K(1), V(1)
+            // first rather than three tiles of V ahead of the first K
+            if (is_v && !wait_count(cnt + 3, t + 1, abort_flag)) {
+              okl = false;
+              break;
+            }
             const uint32_t u = 4u * t + cc;
             const uint32_t slot = sub_slot<kNumSlots>(u, is_v);
             okl = wait_bar(bar(kBarEmpty + slot), sub_phase<kNumSlots>(u, is_v) ^ 1, abort_flag);
@@ -1077,6 +1077,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
             mine_bar[nmine % 3] = kBarFull + slot;
             mine_par[nmine % 3] = sub_phase<kNumSlots>(u, is_v);
             ++nmine;
+            if (lane == 0) st_release_cta(cnt + 3, t + 1);   // K(t) issued (lane 0's use)
             if (lane == 0 && sq < nseg && t == seg_n0[sq]) {
               if (sq > 0) okl = wait_bar(bar(kBarQEmpty), (sq - 1) & 1, abort_flag);
               if (okl) {
@@ -1170,7 +1171,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           const bool first = (jk == sg.y), last = (jk == sg.z - 1);
           const uint32_t u0 = kFp8 ? 4u * n : ring_use<kKU>(n, ntiles, false);
           // (one ring) some slots of tile n's K last held an earlier tile's V: it must have landed
-          const int nv = kFp8 ? 0 : k_needs_v<kKU, kNumSlots>(n);
+          const int nv = kFp8 ? 0 : needs_other<kKU, kNumSlots>(static_cast<int>(u0), ntiles, true);
           if (nv > 0) ok = wait_count(cnt + 1, nv, abort_flag) && wait_count(cnt + 2, nv, abort_flag);
           if (ok && first) ok = wait_bar(bar(kFp8 ? kBarQReady : kBarQFull), sk & 1, abort_flag);
           if (ok && n >= 2) ok = wait_bar(bar(kBarSEmpty + (n & 1)), ((n >> 1) - 1) & 1, abort_flag);
@@ -1240,7 +1241,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           if (ok && first && sv >= kOBufs)
             ok = wait_bar(bar(kBarOEmpty + kb), ((sv / kOBufs) - 1) & 1, abort_flag);
           // some slots of tile m's V last held a later tile's K (small rings): it must have landed
-          const int nk = kFp8 ? 0 : v_needs_k<kKU, kNumSlots>(m, ntiles);
+          const int nk = kFp8 ? 0 : needs_other<kKU, kNumSlots>(static_cast<int>(uv), ntiles, false);
           if (ok && nk > m + 1) ok = wait_count(cnt, nk, abort_flag);
           if (!ok) break;
           tc_fence_after();
@@ -1353,14 +1354,13 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         }
         return true;
       };
-      // staging use su = page su & 1 of group su >> 1, the groups in the producer's order: K(0),
-      // then K(t) and V(t - 1) for t = 1..N-1, then V(N-1) (one call site keeps the loop small)
+      // staging use su = page su & 1 of group su >> 1, the groups in the producer's order
+      // (ring_use; one call site keeps the loop small)
       bool ok = true;
 #pragma unroll 1
       for (int su = 0; su < 4 * ntiles; ++su) {
-        const int g = su >> 1;
-        const bool is_v = (g & 1) == 0 ? g > 0 : (g + 1) / 2 >= ntiles;
-        const int t = !is_v ? (g + 1) / 2 : ((g & 1) == 0 ? g / 2 - 1 : ntiles - 1);
+        bool is_v;
+        const int t = group_owner(su >> 1, ntiles, is_v);
         if (!page(is_v, t, su & 1)) {
           ok = false;
           break;
@@ -1725,8 +1725,10 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         //     an e4m3 hi part and an e4m3 lo part (pk[0..7] and pk[8..15], four heads a word)
         uint32_t pk[16];
         float u = 0.f;
+        uint32_t u2 = 0u;   // e4m3: u in both halves of an f16x2
         if constexpr (kFp8) {
           u = svt * __uint_as_float(static_cast<uint32_t>(127 + kPvShift - e_ref) << 23);
+          asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(u2) : "f"(u));
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = 0u;
         }
@@ -1756,16 +1758,35 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           for (int e = 0; e < 8; ++e) {
             const int hl = 2 * e, h = 16 * half + hl;
             const float2 m2 = *reinterpret_cast<const float2*>(m_ref + h0 + h);
-            const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), ck, -m2.x)) : 0.f;
-            const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), ck, -m2.y)) : 0.f;
             if constexpr (kFp8) {
-              uint32_t hi, lo;
-              split_weights_e4m3(p0 * u, p1 * u, hi, lo);
-              pk[4 * half + (e >> 1)] |= hi << (16 * (e & 1));
-              pk[8 + 4 * half + (e >> 1)] |= lo << (16 * (e & 1));
-              lreg[h] += p0;
-              lreg[h + 1] += p1;
+              // the pair's weights in packed f16 arithmetic: two exponentials per ex2.f16x2, then
+              // w = p u split into e4m3 parts hi = e4m3(w) and lo = e4m3(w - hi), with w - hi
+              // exact in f16 (hi is within 2^-4 of w).  The exponent's argument x <= 3 is
+              // rounded to f16 first (an error under 2^-11 |x|), p and w carry f16's 11 bits,
+              // more than hi + lo keep (about 9), and the row sum adds p as rounded.
+              const float x0 = fmaf(__uint_as_float(sv[hl]), ck, -m2.x);
+              const float x1 = fmaf(__uint_as_float(sv[hl + 1]), ck, -m2.y);
+              uint32_t xh, ph;
+              asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(x1), "f"(x0));
+              asm("ex2.approx.f16x2 %0, %1;" : "=r"(ph) : "r"(xh));
+              if (!valid) ph = 0u;
+              float q0, q1;
+              asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+                  : "=f"(q0), "=f"(q1) : "r"(ph));
+              lreg[h] += q0;
+              lreg[h + 1] += q1;
+              uint32_t wh, hb, rh;
+              uint16_t hi16, lo16;
+              asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(wh) : "r"(ph), "r"(u2));
+              asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hi16) : "r"(wh));
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hb) : "h"(hi16));
+              asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rh) : "r"(wh), "r"(hb));
+              asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lo16) : "r"(rh));
+              pk[4 * half + (e >> 1)] |= static_cast<uint32_t>(hi16) << (16 * (e & 1));
+              pk[8 + 4 * half + (e >> 1)] |= static_cast<uint32_t>(lo16) << (16 * (e & 1));
             } else {
+              const float p0 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl]), ck, -m2.x)) : 0.f;
+              const float p1 = valid ? ex2_approx(fmaf(__uint_as_float(sv[hl + 1]), ck, -m2.y)) : 0.f;
               const uint32_t w = pack_bf16(p0, p1);
               pk[8 * half + e] = w;
               // the row sum adds the same bf16-rounded weights the PV MMA uses, so the

@@ -421,18 +421,22 @@ def test_multi_token_decode(T, kv_dtype, force_ctas):
         check_parity(case, out, lse, max_abs=3e-2, rel_l2=1.5e-2)
 
 
-def test_multi_token_decode_full_size():
-    """Two new tokens for each of 32 sequences of 4096: the benchmark's MTP workload, checked
-    on a sample of sequences (the oracle runs per (sequence, token) pair)."""
-    case = inputs.generate(inputs.WORKLOADS["mtp2_b32_l4096_bf16"])
+@pytest.mark.parametrize("name", ["mtp2_b32_l4096_bf16", "mtp2_b32_l4096_fp8"])
+def test_multi_token_decode_full_size(name):
+    """Two new tokens for each of 32 sequences of 4096 (bf16 and e4m3 caches): the multi-token
+    workloads, checked on a sample of sequences (the oracle runs per (sequence, token) pair)
+    plus two sequences from the far end of the batch."""
+    case = inputs.generate(inputs.WORKLOADS[name])
     out, lse, dec = gpu_decode_mtp(case, flags=mfa.MFA_PLAN_CHECK | mfa.MFA_PLAN_EARLY_METADATA)
-    sample = slice(0, 8)   # the first four sequences' two tokens each
-    ref_o, ref_lse = oracle.decode(case, batch_slice=sample)
-    got = out[sample].cpu().double().numpy()
-    err = np.abs(got - ref_o)
-    assert err.max() <= BF16_MAX_ABS
-    assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= BF16_REL_L2
-    assert np.abs(lse[sample].cpu().double().numpy() - ref_lse).max() <= LSE_ABS
+    assert mfa.mfa_read_device_status(dec.workspace) == 0
+    max_abs, rel_l2 = (3e-2, 1.5e-2) if name.endswith("fp8") else (BF16_MAX_ABS, BF16_REL_L2)
+    for sample in (slice(0, 8), slice(60, 64)):   # pairs (sequence, token)
+        ref_o, ref_lse = oracle.decode(case, batch_slice=sample)
+        got = out[sample].cpu().double().numpy()
+        err = np.abs(got - ref_o)
+        assert err.max() <= max_abs
+        assert np.linalg.norm(got - ref_o) / np.linalg.norm(ref_o) <= rel_l2
+        assert np.abs(lse[sample].cpu().double().numpy() - ref_lse).max() <= LSE_ABS
 
 
 @pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
