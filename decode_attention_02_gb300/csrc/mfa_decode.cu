@@ -345,6 +345,22 @@ __device__ __forceinline__ int vlen_from(int L_raw, int T, int U, int x, int cap
   const int L = clamp_len(L_raw, cap, bad);
   return T == 1 ? L : max(0, L - (T - 1 - (x / U) % T));
 }
+// Schedule order.  With R = T U > 1 units reading each sequence's pages, the cost-balanced
+// schedule walks the Bv units reader-major: position pos = r (Bv / R) + b holds unit
+// x = b R + r.  With readers of equal cost, the CTAs that hold readers r and r' of sequence b
+// then sit at the same place in their cost ranges (exactly so for an even split), so a page's
+// readers load it at about the same time and all but the first find it in L2.  Partial slots
+// are numbered by position (pos + CTA).
+__device__ __forceinline__ int unit_at(int pos, int T, int U, int Bv) {
+  const int R = T * U;
+  if (R == 1) return pos;
+  const int Bs = Bv / R;
+  return (pos % Bs) * R + pos / Bs;
+}
+__device__ __forceinline__ int pos_of(int x, int T, int U, int Bv) {
+  const int R = T * U;
+  return R == 1 ? x : (x % R) * (Bv / R) + x / R;
+}
 
 // Bounded wait on an mbarrier phase.  Returns false after kWaitLimitNs, or at
 // once when another role has raised the CTA's abort flag.
@@ -725,10 +741,12 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * static_cast<uint32_t>(i); };
 
+  // the unit at schedule position pos (unit_at)
+  auto unit_of = [&](int pos) { return unit_at(pos, p.tokens, p.units, p.batch); };
   // With early metadata the lengths are read before anything else: the schedule below
   // waits on them and on nothing the set-up does.
-  int L_first = 0;
-  if (p.early_metadata && tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, tid);
+  int L_first = 0;   // raw length of the unit at schedule position tid
+  if (p.early_metadata && tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, unit_of(tid));
 
   // ---------------- set-up: barriers (one per lane of warp 0), tensor memory
   if (warp == 0) {
@@ -770,7 +788,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
   // kernel does not write them); q, K, V and every output wait.
   if (!p.early_metadata) {
     grid_dep_wait();
-    if (tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, tid);
+    if (tid < p.batch) L_first = raw_len(p.seq_lens, p.tokens, p.units, unit_of(tid));
   }
 
   // ---------------- schedule: this CTA's tile range and its per-sequence segments
@@ -789,9 +807,11 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
     auto packed = [](int T) { return static_cast<long long>(T) | (static_cast<long long>(T > 0) << 32); };
     long long loc = 0;
     // L_first (read above) is reused by the segment scan below
-    loc += packed(tiles_of(tid < p.batch ? vlen_from(L_first, p.tokens, p.units, tid, cap, bad) : 0));
-    for (int b = tid + kThreads; b < p.batch; b += kThreads)
-      loc += packed(tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, bad)));
+    loc += packed(tiles_of(tid < p.batch ? vlen_from(L_first, p.tokens, p.units, unit_of(tid), cap, bad) : 0));
+    for (int b = tid + kThreads; b < p.batch; b += kThreads) {
+      const int x = unit_of(b);
+      loc += packed(tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, x), p.tokens, p.units, x, cap, bad)));
+    }
     if (bad) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
     long long tot0 = 0;
     const long long incl0 = block_incl_scan<kThreads, long long>(loc, scratch, tot0);
@@ -825,7 +845,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       // one sequence per thread: its tiles are [S, S + T) of the first scan; the sequences
       // overlapping the CTA are numbered by a ballot count
       bool dummy = false;
-      const int L = (tid < p.batch) ? vlen_from(L_first, p.tokens, p.units, tid, cap, dummy) : 0;
+      const int L = (tid < p.batch) ? vlen_from(L_first, p.tokens, p.units, unit_of(tid), cap, dummy) : 0;
       const int T = tiles_of(L);
       const long long ex = incl0 - packed(T);
       const int S = static_cast<int>(ex & 0xFFFFFFFFll), Nb = static_cast<int>(ex >> 32);
@@ -850,7 +870,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         nseg = 0;
       } else if (f) {
         const int fidx = before + __popc(m & ((1u << lane) - 1u));
-        seg[fidx] = make_int4(tid, k_lo, k_hi, L);
+        seg[fidx] = make_int4(unit_of(tid), k_lo, k_hi, L);
         seg_n0[fidx] = S + k_lo - t0;
       }
     } else {
@@ -860,7 +880,8 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       for (int c0 = 0; c0 < p.batch && cost_of(carry) <= X1; c0 += kThreads) {
         const int b = c0 + tid;
         bool dummy = false;
-        const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy) : 0;
+        const int x = unit_of(b);
+        const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, x), p.tokens, p.units, x, cap, dummy) : 0;
         const int T = tiles_of(L);
         long long tot = 0;
         const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -878,7 +899,8 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         for (int c0 = 0; c0 < p.batch && (carry & 0xFFFFFFFFll) < t1; c0 += kThreads) {
           const int b = c0 + tid;
           bool dummy = false;
-          const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, b), p.tokens, p.units, b, cap, dummy) : 0;
+          const int x = unit_of(b);
+          const int L = (b < p.batch) ? vlen_from(c0 == 0 ? L_first : raw_len(p.seq_lens, p.tokens, p.units, x), p.tokens, p.units, x, cap, dummy) : 0;
           const int T = tiles_of(L);
           long long tot = 0;
           const long long ex = block_incl_scan<kThreads, long long>(packed(T), scratch, tot) + carry - packed(T);
@@ -889,7 +911,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
           int ftot = 0;
           const int fidx = nseg + block_incl_scan<kThreads>(f, misc + 4, ftot) - f;
           if (f) {
-            seg[fidx] = make_int4(b, k_lo, k_hi, L);
+            seg[fidx] = make_int4(x, k_lo, k_hi, L);
             seg_n0[fidx] = S + k_lo - t0;
           }
           carry += tot;
@@ -1598,7 +1620,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       const int4 sg = seg[s];
       const int b = sg.x, L = sg.w, kb = s % kOBufs;
       const bool whole = (sg.y == 0) && (sg.z == tiles_of(L));
-      const int slot_p = b + static_cast<int>(blockIdx.x);
+      const int slot_p = pos_of(b, p.tokens, p.units, p.batch) + static_cast<int>(blockIdx.x);
       const uint32_t o_tmem = tmem + tmem_o<kFp8>() + 64u * kOBlocks * kb + h0 + lane_base;   // + 64 per block
       if (ts < kH) m_ref[ts] = -INFINITY;
       if constexpr (kFp8) {
@@ -1947,13 +1969,15 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int cap = p.max_pages * kPage;
   // tiles (and non-empty sequences) before b and in all: the decode kernel's cost positions
   int before = 0, total = 0, nb = 0, nt = 0;
+  const int pb = pos_of(b, p.tokens, p.units, p.batch);   // b's schedule position
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
     bool dummy = false;
-    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, i), p.tokens, p.units, i, cap, dummy));
+    const int x = unit_at(i, p.tokens, p.units, p.batch);
+    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, x), p.tokens, p.units, x, cap, dummy));
     total += T;
     nt += (T > 0);
-    before += (i < b) ? T : 0;
-    nb += (i < b && T > 0);
+    before += (i < pb) ? T : 0;
+    nb += (i < pb && T > 0);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -2011,7 +2035,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
             live = k_lo < min(k_hi, static_cast<long long>(Tb));
           }
           const unsigned m = __ballot_sync(0xffffffffu, live);
-          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
+          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = pb + g;
           n += __popc(m);
         }
         if (threadIdx.x == 0) nparts_s = n;
@@ -2130,13 +2154,15 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_wide_kernel(const
   const int cap = p.max_pages * kPage;
   // tiles (and non-empty sequences) before b and in all: the decode kernel's cost positions
   int before = 0, total = 0, nb = 0, nt = 0;
+  const int pb = pos_of(b, p.tokens, p.units, p.batch);   // b's schedule position
   for (int i = threadIdx.x; i < p.batch; i += kCombineThreads) {
     bool dummy = false;
-    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, i), p.tokens, p.units, i, cap, dummy));
+    const int x = unit_at(i, p.tokens, p.units, p.batch);
+    const int T = tiles_of(vlen_from(raw_len(p.seq_lens, p.tokens, p.units, x), p.tokens, p.units, x, cap, dummy));
     total += T;
     nt += (T > 0);
-    before += (i < b) ? T : 0;
-    nb += (i < b && T > 0);
+    before += (i < pb) ? T : 0;
+    nb += (i < pb && T > 0);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -2197,7 +2223,7 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_wide_kernel(const
             live = k_lo < min(k_hi, static_cast<long long>(Tb));
           }
           const unsigned m = __ballot_sync(0xffffffffu, live);
-          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = b + g;
+          if (live) slots[n + __popc(m & ((1u << threadIdx.x) - 1))] = pb + g;
           n += __popc(m);
         }
         if (threadIdx.x == 0) nparts_s = n;
@@ -2610,7 +2636,8 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
   const int nt = pr->tokens_per_seq, nu = units_of(pr);
   const long long Bv = vbatch(pr);
   // tiles of each unit (sequence, new token, head set): query token i of a sequence of L
-  // tokens attends to its first L - T + 1 + i
+  // tokens attends to its first L - T + 1 + i.  T is in schedule order: reader r = i nu + u
+  // of sequence b sits at position r B + b (reader-major, as the kernels walk it)
   std::vector<long long> T(static_cast<size_t>(Bv));
   long long W = 0;
   if (host_seq_lens != nullptr) {
@@ -2619,9 +2646,9 @@ mfa_status mfa_decode_plan(const mfa_problem* pr, const int32_t* host_seq_lens, 
       for (int i = 0; i < nt; ++i) {
         const long long L = std::max(0ll, static_cast<long long>(host_seq_lens[b]) - (nt - 1 - i));
         for (int u = 0; u < nu; ++u) {
-          const size_t x = (static_cast<size_t>(b) * nt + i) * nu + u;
-          T[x] = (L + kTile - 1) / kTile;
-          W += T[x];
+          const size_t pos = (static_cast<size_t>(i) * nu + u) * pr->batch + b;
+          T[pos] = (L + kTile - 1) / kTile;
+          W += T[pos];
         }
       }
     }

@@ -157,7 +157,10 @@ typedef struct mfa_plan {
  * sequences: every CTA gets the same share whatever the length mix, a sequence boundary
  * inside a CTA's range (the next sequence's q and one more epilogue) counting as c/4 of a
  * tile, c = 3 for bf16 KV and c = 10 for e4m3 and MXFP4 KV.  A sequence is split once per CTA
- * boundary that falls inside it.  Planned
+ * boundary that falls inside it.  Where several units read one sequence's pages (T > 1 query
+ * tokens, or the shared-latent shape's two head sets: R units a sequence, "readers"), the
+ * units are laid end to end reader-major -- reader r of sequence b at position r B + b -- so
+ * that a page's readers run at the same time on different CTAs and share its L2 lines.  Planned
  * from a length bound (host_seq_lens NULL), the grid keeps every CTA within 128 tiles
  * for any lengths up to the bound.
  */
@@ -196,8 +199,9 @@ mfa_status mfa_decode_plan(const mfa_problem* problem, const int32_t* host_seq_l
  *   workspace    : device buffer of >= plan->workspace_bytes bytes, 256-byte aligned.
  *                  Layout: bytes [0,256) header (uint32 status word at offset 0);
  *                  then partial O fp32 [num_partials, 64, 256]; then partial lse fp32
- *                  [num_partials, 64].  The partial of sequence b from CTA g sits in
- *                  slot b + g.  Contents between calls are scratch, except the status word.
+ *                  [num_partials, 64].  The partial of the unit at position x of the
+ *                  order above (x = b for one reader a sequence) from CTA g sits in slot
+ *                  x + g.  Contents between calls are scratch, except the status word.
  *   stream       : cudaStream_t.
  * Unused slots of a sequence's last page and unused pool pages may hold any bits
  * (NaN included); they never reach the output.
