@@ -1551,7 +1551,9 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
     // hi = e4m3(2^sigma q) and lo = e4m3(2^sigma q - hi), with one power of two 2^sigma per
     // sequence putting its largest |q| in [64, 128): hi + lo reproduces 2^sigma q (see
     // split_e4m3) and the QK^T MMA runs on e4m3 K as stored.  Thread ts converts row
-    // ts & 63 (a head) of bf16 box ts >> 6 (64 d); all reads precede all writes.  Done for
+    // ts & 63 (a head) of bf16 box ts >> 6 (64 d); all reads precede all writes, and each
+    // thread reads its row's 16-byte chunks in logical order, which the 128-byte swizzle
+    // spreads over the banks (eight rows of a warp hit eight different bank groups).  Done for
     // a later segment right after the previous segment's last scores are read, so its
     // first QK^T can overlap that segment's last PV and epilogue.
     auto convert_q = [&](int sidx) {
@@ -1563,7 +1565,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         const uint8_t* src = smem + kOffQ + cq * 8192 + hq * 128;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          w[q] = *reinterpret_cast<const uint4*>(src + 16 * q);
+          w[q] = *reinterpret_cast<const uint4*>(src + 16 * (q ^ (hq & 7)));   // logical chunk q
           const uint32_t* e = reinterpret_cast<const uint32_t*>(&w[q]);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -1586,7 +1588,7 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
         uint8_t* dst = smem + kOffQ + (cq >> 1) * 16384 + hq * 128;   // hi part (rows 0..63); lo rows at +8 KB
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          const int k = q ^ (hq & 7);                       // logical 16-byte chunk of the bf16 row
+          const int k = q;                                  // logical 16-byte chunk of the bf16 row
           const uint32_t* e = reinterpret_cast<const uint32_t*>(&w[q]);
           uint32_t hi[4], lo[4];
 #pragma unroll
