@@ -695,6 +695,14 @@ __device__ __forceinline__ uint32_t sub_phase(uint32_t u, bool is_v) {
 // Fused KV append of sequence b's new row at token t (a warp): the page id, then the K and V
 // rows in the cache's format.  A position past the block table or a page id outside the pool
 // is reported and the row is skipped, as by the append kernel.
+// Sequence b's new K and V rows into slot t % 64 of pool page blk (one warp).
+__device__ __noinline__ void append_row_at(const DecodeParams& p, int b, int t, int blk, int lane) {
+  const size_t row = static_cast<size_t>(blk) * kPage + (t % kPage);
+  const uint4 xk = p.k_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
+  const uint4 xv = p.v_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
+  append_row_warp(p.kv_fmt, xk, lane, p.k_cache_w, p.k_scale_w, row);
+  append_row_warp(p.kv_fmt, xv, lane, p.v_cache_w, p.v_scale_w, row);
+}
 __device__ __noinline__ void fused_append_row(const DecodeParams& p, int b, int t, int lane) {
   if (t >= p.max_pages * kPage) {
     if (lane == 0 && p.status) atomicOr(p.status, MFA_DEV_BAD_LENGTH);
@@ -705,11 +713,7 @@ __device__ __noinline__ void fused_append_row(const DecodeParams& p, int b, int 
     if (lane == 0 && p.status) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
     return;
   }
-  const size_t row = static_cast<size_t>(blk) * kPage + (t % kPage);
-  const uint4 xk = p.k_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
-  const uint4 xv = p.v_new[static_cast<size_t>(b) * (kRowElems / 8) + lane];
-  append_row_warp(p.kv_fmt, xk, lane, p.k_cache_w, p.k_scale_w, row);
-  append_row_warp(p.kv_fmt, xv, lane, p.v_cache_w, p.v_scale_w, row);
+  append_row_at(p, b, t, blk, lane);
 }
 
 // kFp8: both contractions on e4m3 operands (an e4m3 cache, or an MXFP4 cache converted to
@@ -718,6 +722,7 @@ template <bool kFp8, int kShp, bool kMx = false>
 __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const __grid_constant__ DecodeParams p) {
   static_assert(!kFp8 || kShp == kShapeMfa, "the e4m3 cache is built for the MFA shape");
   static_assert(!kMx || kFp8, "the MXFP4 path runs on the e4m3 MMAs");
+  static_assert(threads_of<kMx>() >= kMaxTilesPerCta + kMaxSeg, "page ids and append positions load in one round");
   using Lay = Layout<kFp8, kShp, kMx>;
   using Sh = ShapeOf<kShp>;
   constexpr int kThreads = threads_of<kMx>();
@@ -929,6 +934,8 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
   const uint32_t tmem = static_cast<uint32_t>(misc[0]);
   const int nseg = misc[2];
   const int ntiles = misc[3];
+  int* app_t = reinterpret_cast<int*>(smem + kOffRed);   // [nseg] fused-append positions (scratch
+                                                         // idle until the softmax)
   // ---------------- page ids and valid rows of each of this CTA's tiles (one round of
   // independent loads, one tile per thread).  Rows r of a page: the last page of a sequence
   // has r < 64 (its valid rows land at the end of the box), an absent second page r <= 0.
@@ -951,19 +958,29 @@ __global__ void __launch_bounds__(threads_of<kMx>(), 1) mfa_decode_kernel(const 
       tile_info[n] = make_int4(b0, b1, r0, r1);
     }
     if (bad_blk) atomicOr(p.status, MFA_DEV_BAD_BLOCK);
+    // fused KV append: each segment's new-row position, loaded in the same round by the
+    // threads past the page-id ones (with early metadata, before the dependency wait)
+    if (p.k_new != nullptr && tid >= kMaxTilesPerCta && tid - kMaxTilesPerCta < nseg)
+      app_t[tid - kMaxTilesPerCta] = p.positions[seg[tid - kMaxTilesPerCta].x];
   }
   // ---------------- fused KV append, rows this CTA reads: a sequence's new row at token t <
   // its visible length is written by the CTA that owns tile t / 128 (one segment holds it),
-  // before any of that CTA's loads.  Warp w takes segments w, w + warps, ...  The rows are
-  // fenced to the async proxy, which reads them (TMA), and the block barrier below orders
-  // them before the other warps' loads of the per-row scales.  (Rows past the visible length
-  // are read by nobody this step; the PV warp writes those.)
+  // before any of that CTA's loads, into the page id the tile already holds.  Warp w takes
+  // segments w, w + warps, ...  The rows are fenced to the async proxy, which reads them
+  // (TMA), and the block barrier below orders them before the other warps' loads of the
+  // per-row scales.  (Rows past the visible length are read by nobody this step; the PV
+  // warp writes those.)
   if (p.k_new != nullptr && nseg > 0) {
+    __syncthreads();   // app_t and tile_info
     grid_dep_wait();   // the new rows (and the cache) may come from the preceding kernel
     for (int s = warp; s < nseg; s += kThreads / 32) {
       const int4 sg = seg[s];
-      const int t = p.positions[sg.x];
-      if (t >= 0 && t < sg.w && t >= kTile * sg.y && t < kTile * sg.z) fused_append_row(p, sg.x, t, lane);
+      const int t = app_t[s];
+      if (t >= 0 && t < sg.w && t >= kTile * sg.y && t < kTile * sg.z) {
+        const int4 ti = tile_info[seg_n0[s] + t / kTile - sg.y];
+        const int blk = ((t / kPage) & 1) ? ti.y : ti.x;
+        if (blk >= 0) append_row_at(p, sg.x, t, blk, lane);   // (-1: reported above, page reads as zeros)
+      }
     }
     fence_proxy_async_global();
   }

@@ -89,10 +89,11 @@ typedef enum mfa_out_dtype {
 #define MFA_PLAN_CHECK       0x1u  /* run: clear the status word, then read it back (synchronises) */
 #define MFA_PLAN_NO_COMBINE  0x2u  /* run: launch only the decode kernel; call mfa_combine() yourself */
 /* run: the decode kernel is launched as a programmatic dependent of the preceding
- * kernel on the stream and reads seq_lens and block_table before that kernel has
- * finished.  Set it only if the preceding kernel does not write them (for example,
- * when the host fills them once per decode step).  q, K, V and all outputs are
- * always ordered after the preceding kernel. */
+ * kernel on the stream and reads seq_lens and block_table (and, in
+ * mfa_decode_append_run, positions) before that kernel has finished.  Set it only if
+ * the preceding kernel does not write them (for example, when the host fills them
+ * once per decode step).  q, K, V, the new rows and all outputs are always ordered
+ * after the preceding kernel. */
 #define MFA_PLAN_EARLY_METADATA 0x4u
 
 typedef struct mfa_problem {
