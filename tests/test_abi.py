@@ -92,6 +92,32 @@ def test_plan_tile_counts_follow_the_documented_split(lib, kv, c):
     assert plan.max_tiles_per_cta == max(split_tiles_brute_force(lens, 152, c))
 
 
+@pytest.mark.parametrize("kv, c", [(mfa.MFA_KV_BF16, 3), (mfa.MFA_KV_FP8_E4M3, 10)])
+def test_multi_token_plan_walks_the_units_reader_major(lib, kv, c):
+    """T query tokens a sequence: the units are laid end to end reader-major (every sequence's
+    token 0, then every sequence's token 1, ...), token i of a sequence of L seeing L - T + 1 + i
+    tokens.  The plan's largest CTA share is the documented split over that order, and for
+    some of these ragged mixes it differs from the split over the sequence-major order."""
+    import random
+    rng = random.Random(11)
+    differs = 0
+    for trial in range(30):
+        B, T = rng.randint(1, 24), rng.randint(2, 4)
+        lens = [rng.choice([0, 1, 2, 130, rng.randint(0, 3000)]) for _ in range(B)]
+        vis = lambda b, i: max(0, lens[b] - (T - 1 - i))
+        reader_major = [vis(b, i) for i in range(T) for b in range(B)]
+        seq_major = [vis(b, i) for b in range(B) for i in range(T)]
+        W = sum((L + 127) // 128 for L in reader_major)
+        G = rng.randint(max(1, -(-W // 96)), max(2, -(-W // 96)) + 40)   # room under the 128-tile cap
+        plan = mfa.mfa_decode_plan(problem(batch=B, max_pages_per_seq=64, num_blocks=4096, kv_dtype=kv,
+                                           tokens_per_seq=T), lens, num_sms=152, force_ctas=G)
+        per = split_tiles_brute_force(reader_major, G, c)
+        assert sum(per) == plan.total_tiles
+        assert plan.max_tiles_per_cta == max(per), (lens, T, G)
+        differs += max(split_tiles_brute_force(seq_major, G, c)) != max(per)
+    assert differs > 0
+
+
 def test_plan_fewer_ctas_than_sms_for_short_batches(lib):
     plan = mfa.mfa_decode_plan(problem(batch=1), [512], num_sms=152)
     assert plan.num_ctas == 4 and plan.max_tiles_per_cta == 1
