@@ -1976,9 +1976,9 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   __shared__ int red_b[kCombineThreads / 32], red_t[kCombineThreads / 32];
   __shared__ int red_nb[kCombineThreads / 32], red_nt[kCombineThreads / 32];
   __shared__ int slots[kCombineMaxParts];
-  __shared__ float wts[4][kCombineMaxParts];
+  __shared__ float wts[16][kCombineMaxParts];   // a single pass: every head's weights; else a round's
   __shared__ float4 part_acc[3][64];
-  __shared__ float pass_max[4], pass_sum[4];
+  __shared__ float pass_max[16], pass_sum[16];
   __shared__ int nparts_s;
   const int b = blockIdx.x;
   const int hpc = p.heads_per_cta;
@@ -2033,15 +2033,22 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
   const int hr = quad / groups;               // head of the round owned by this quad
   const int grp = quad % groups;              // partial group within that head
   const int d4 = threadIdx.x & 63;            // float4 column: d = 4*d4 .. 4*d4+3
+  // With all partials in one pass (the usual case) the slots and the weights of all the
+  // CTA's heads are found once, before the first round; otherwise pass by pass, round by round.
+  const bool one_pass = g1 - g0 + 1 <= kCombineMaxParts;
   for (int r = 0; r < rounds; ++r) {
     const int h = blockIdx.y * hpc + r * hpr + hr;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float run_max = -INFINITY, run_sum = 0.f;
+    const bool load_w = r == 0 || !one_pass;
+    const int nh = one_pass ? hpc : hpr;                             // heads whose weights a load takes
+    const int h_first = blockIdx.y * hpc + (one_pass ? 0 : r * hpr);
+    const int hw = (one_pass ? r * hpr : 0) + hr;                    // this quad's row of wts
     // partials come from CTAs g0..g1 (CTAs with an empty tile range hold none)
     for (int gs = g0; gs <= g1; gs += kCombineMaxParts) {
       const int ge = min(g1 + 1, gs + kCombineMaxParts);
       __syncthreads();
-      if (threadIdx.x < 32) {
+      if (threadIdx.x < 32 && load_w) {
         int n = 0;
         for (int g = gs + threadIdx.x; g - static_cast<int>(threadIdx.x) < ge; g += 32) {
           // CTA g holds a tile of b if a tile cost of b lies in its cost range
@@ -2061,15 +2068,16 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
       }
       __syncthreads();
       const int n = nparts_s;
-      for (int k = threadIdx.x; k < n * hpr; k += kCombineThreads) {
-        const int kk = k / hpr, hh = k % hpr;
-        wts[hh][kk] = p.part_lse[static_cast<size_t>(slots[kk]) * kH + blockIdx.y * hpc + r * hpr + hh];
-      }
-      __syncthreads();
-      {
-        // warp w < hpr turns head w's lse values into weights relative to their max
-        const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-        if (w < hpr) {
+      if (load_w) {
+        for (int k = threadIdx.x; k < n * nh; k += kCombineThreads) {
+          const int kk = k / nh, hh = k % nh;
+          wts[hh][kk] = p.part_lse[static_cast<size_t>(slots[kk]) * kH + h_first + hh];
+        }
+        __syncthreads();
+        // warp w turns heads w, w + 8, ... into weights relative to their max
+        const int l = threadIdx.x & 31;
+#pragma unroll 1
+        for (int w = threadIdx.x >> 5; w < nh; w += kCombineThreads / 32) {
           float m = -INFINITY;
           for (int k = l; k < n; k += 32) m = fmaxf(m, wts[w][k]);
 #pragma unroll
@@ -2087,16 +2095,16 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
             pass_sum[w] = sum;
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
       // rescale what earlier passes accumulated to this pass's reference
-      const float m_new = fmaxf(run_max, pass_max[hr]);
+      const float m_new = fmaxf(run_max, pass_max[hw]);
       const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
-      const float a_new = expf(pass_max[hr] - m_new);
+      const float a_new = expf(pass_max[hw] - m_new);
       acc.x *= a_old; acc.y *= a_old; acc.z *= a_old; acc.w *= a_old;
-      run_sum = run_sum * a_old + pass_sum[hr] * a_new;
+      run_sum = run_sum * a_old + pass_sum[hw] * a_new;
       run_max = m_new;
-      const float* wrow = wts[hr];
+      const float* wrow = wts[hw];
       int k = grp;
       for (; k + 3 * groups < n; k += 4 * groups) {
         float4 v[4];
