@@ -2097,6 +2097,49 @@ __global__ void __launch_bounds__(kCombineThreads) mfa_combine_kernel(const __gr
         }
         __syncthreads();
       }
+      if (one_pass && groups == 1 && rounds > 1) {
+        // a single pass with one head per quad: every round's partial loads go out together
+        // (parts outer, rounds inner), so that the CTA waits for memory once rather than once
+        // a round; per head the sums run over the parts in the same order as below
+        float4 accr[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) accr[rr] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+        for (int k = 0; k < n; ++k) {
+          const float* src0 = p.part_o + (static_cast<size_t>(slots[k]) * kH + blockIdx.y * hpc + hr) * kD;
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            if (rr < rounds) {
+              const float4 v = reinterpret_cast<const float4*>(src0 + static_cast<size_t>(rr * hpr) * kD)[d4];
+              const float w = wts[rr * hpr + hr][k];
+              accr[rr].x = fmaf(w, v.x, accr[rr].x); accr[rr].y = fmaf(w, v.y, accr[rr].y);
+              accr[rr].z = fmaf(w, v.z, accr[rr].z); accr[rr].w = fmaf(w, v.w, accr[rr].w);
+            }
+          }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          if (rr < rounds) {
+            const int hw2 = rr * hpr + hr, h2 = blockIdx.y * hpc + hw2;
+            const float4 a = accr[rr];
+            const float inv = 1.f / pass_sum[hw2];
+            const size_t oi = (static_cast<size_t>(b) * kH + h2) * kD + 4 * d4;
+            if (p.out_f32) {
+              reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi)[0] =
+                  make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+            } else {
+              __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+              __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&lo);
+              pk.y = *reinterpret_cast<uint32_t*>(&hi);
+              reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + oi)[0] = pk;
+            }
+            if (d4 == 0 && p.lse != nullptr) p.lse[b * kH + h2] = pass_max[hw2] + logf(pass_sum[hw2]);
+          }
+        }
+        return;
+      }
       // rescale what earlier passes accumulated to this pass's reference
       const float m_new = fmaxf(run_max, pass_max[hw]);
       const float a_old = (run_max == -INFINITY) ? 0.f : expf(run_max - m_new);
