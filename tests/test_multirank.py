@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, results):
 
 def test_two_gloo_ranks_reduce_to_the_slowest_and_shard_the_data():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.start_processes(_rank_main, args=(world, port, results), nprocs=world, start_method="spawn")
         r = dict(results)
