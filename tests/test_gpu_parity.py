@@ -453,6 +453,20 @@ def test_multi_token_decode_beyond_one_thread_per_pair(kv_dtype):
         check_parity(case, out, lse, max_abs=3e-2, rel_l2=1.5e-2)
 
 
+@pytest.mark.parametrize("out_dtype", [mfa.MFA_OUT_FP32, mfa.MFA_OUT_BF16])
+def test_combine_with_sixteen_heads_a_cta(out_dtype):
+    """96 sequences over 152 CTAs: the combine takes 16 heads a CTA in four rounds, and with all
+    of a sequence's partials in one pass it loads every round's partials together.  Lengths
+    from 1 to 1,500 leave sequences whole, split in two and split over several CTAs."""
+    rng = np.random.default_rng(123)
+    lens = [int(x) for x in rng.integers(1, 1500, size=96)]
+    lens[:4] = [1, 128, 129, 1499]
+    case = inputs.small("combine16", len(lens), lens, seed=124)
+    out, lse, dec = gpu_decode(case, force_ctas=152, out_dtype=out_dtype)
+    assert 96 * 64 >= 16 * 2 * 152          # the host picks 16 heads a combine CTA here
+    check_parity(case, out, lse)
+
+
 @pytest.mark.parametrize("kv", ["bf16", "fp8_e4m3"])
 def test_ctas_without_tiles_leave_the_partials_alone(kv):
     """With 16 CTAs over these lengths, CTA 11's cost range holds no tile while sequence 0 is
